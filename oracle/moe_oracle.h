@@ -1,0 +1,70 @@
+/*
+ * CPU oracle of the NVFP4 routed-MoE layer -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg use this code.
+ * It shares no source, header, table or helper with the CUDA library; the two meet only in
+ * the seeded inputs that the `synth` module draws.
+ *
+ * The layer it computes (W4A16 routed mixture of experts with NVFP4 expert weights) is the
+ * one the "long-context cold prefill to SGLang parity" issue of the Atlas project states in
+ * its kernel comparison table (untransposed column: bf16 activations, e2m1 x e4m3 block x
+ * scale2 weights, f32 accumulation, SiLU intermediate, fp32 weighted unpermute/combine) and
+ * in its op-dump list (router logits, top-k ids/weights, token permutation, shared-expert
+ * in/out, routed outputs before combine, combine result).  Routing ties follow the
+ * "handover briefs" page (device-side indexer selection: lower index wins, NaN never wins).
+ *
+ * Every function computes the plain definition: no blocking, no fusion, fp64 arithmetic for
+ * the layer.  The quantizer takes its rounding decisions in fp32, the precision in which the
+ * GPU quantizer takes them, so that both produce the same codes.
+ *
+ * Status: 0 = ok, -1 = invalid argument.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* --- NVFP4 element formats (from their bit definitions) --- */
+double orc_e2m1_value(int code);        /* 4-bit code -> value, -0 for code 8 */
+double orc_e4m3_value(int code);        /* 8-bit E4M3 (no inf) -> value, NaN for 0x7F/0xFF */
+int orc_e2m1_encode(float v);           /* round to nearest, ties to even code, saturate at 6 */
+int orc_e4m3_encode(float v);           /* round to nearest, ties to even code, saturate at 448 */
+
+/* --- NVFP4 quantizer: w fp32 [G, N, K] -> packed [G, N, K/2] (low nibble = even k),
+ *     scales [G, N, K/16] e4m3, scale2 [G] fp32.  K % 16 == 0. --- */
+int orc_quantize(const float* w, int64_t G, int64_t N, int64_t K,
+                 uint8_t* packed, uint8_t* scales, float* scale2);
+/* exact fp64 dequantization of the same layout -> out [G, N, K] */
+int orc_dequantize(const uint8_t* packed, const uint8_t* scales, const float* scale2,
+                   int64_t G, int64_t N, int64_t K, double* out);
+
+/* --- routing: logits fp32 [T, E] -> ids int32 [T, k] (rank order), w fp64 [T, k] --- */
+int orc_route(const float* logits, int T, int E, int k, int32_t* ids, double* w);
+
+/* --- permutation: stable counting sort of slots s = t*k + j by expert --- */
+int orc_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                int32_t* sorted_slot, int32_t* slot_pos);
+
+/* --- layer forward in fp64.
+ * x: bf16 bit patterns [T, H]; logits fp32 [T, E].
+ * gate_up: packed [G, 2I, H/2], scales [G, 2I, H/16], scale2 [G]; rows 0..I-1 gate, I..2I-1 up.
+ * down:    packed [G, H, I/2],  scales [G, H, I/16],  scale2 [G].
+ * G = E + has_shared (the shared expert is group E).
+ * tokens: the n_tok token indices to evaluate (NULL = all T, in order).
+ * out fp64 [n_tok, H].  Optional dumps (may be NULL), per evaluated token i and rank j
+ * (j = k is the shared expert):  h fp64 [n_tok, k+1, I],  y fp64 [n_tok, k+1, H].
+ * n_threads <= 0 uses every hardware thread. --- */
+int orc_moe_forward(const uint16_t* x, const float* logits,
+                    const uint8_t* gu_packed, const uint8_t* gu_scales, const float* gu_scale2,
+                    const uint8_t* dn_packed, const uint8_t* dn_scales, const float* dn_scale2,
+                    int T, int H, int I, int E, int k, int has_shared,
+                    const int32_t* tokens, int n_tok, double* out, double* h, double* y,
+                    int n_threads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
