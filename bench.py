@@ -1,0 +1,460 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 routed-MoE layer (moe_forward) on GB300.
+
+Metric: MoE-layer tokens/s (token-layers per second for stacked workloads), with the
+dominant kernel's roofline fraction (HBM GB/s for the decode arm, bf16 tensor TFLOP/s for the
+prefill arm) against the measured peaks, the CPU oracle timed beside it, and an end-to-end
+number through host buffers.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|batched|prefill|long|tiny]
+    python bench.py --impl reference ...      # the CPU oracle as the reference arm
+
+One step = one pass of the whole layer over one batch of every layer of the workload (decode:
+four layers with T = 1, 2, 4, 8; long: four layers of T = 32768).  Inputs are synthetic
+(seeded, see synth/), weights random-init NVFP4, resident in HBM before timing.  Each step uses
+the next of P distinct input batches, so the experts touched change from step to step; every
+layer's weights (907 MB each) exceed L2.  The steps are replayed as CUDA graphs.  N > 1 runs N
+independent replicas (one per GPU, no collective on the data path); value = all ranks' tokens /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+GU_BYTES_PER_EXPERT = None  # filled from the shape
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="decode", choices=list(synth.WORKLOADS))
+    p.add_argument("--pool", type=int, default=None, help="distinct input batches cycled through")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+DEFAULTS = {  # steps, warmup, pool
+    "tiny": (2000, 50, 16), "decode": (2000, 50, 16), "batched": (500, 20, 8),
+    "prefill": (50, 5, 4), "long": (8, 3, 2),
+}
+
+
+def workload_entries(name):
+    """(T, seed) of every layer one step runs."""
+    w = synth.WORKLOADS[name]
+    if w.layers > 1:
+        return [(w.Ts[0], synth.layer_seed(w, w.seeds[0], l)) for l in range(w.layers)]
+    return list(zip(w.Ts, w.seeds))
+
+
+def describe(name):
+    w = synth.WORKLOADS[name]
+    return {"workload": w.description, "T": list(w.Ts), "H": w.H, "E": w.E, "k": w.k, "I": w.I,
+            "shared_expert": True, "layers_per_step": len(workload_entries(name)),
+            "seeds": [s for _, s in workload_entries(name)], "logit_bias": w.logit_bias,
+            "outlier_frac": w.outlier_frac, "weights": "NVFP4 (e2m1 x e4m3/16 x fp32 scale2)"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def stored_traffic(workload, kernel, src_files):
+    """DRAM bytes per launch from the committed ncu summary, or None when absent or when the
+    kernel's source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in src_files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    sha = h.hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == workload and parts[1] == kernel:
+            return float(parts[2]) if parts[3] == sha else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples of this process's GPU while running."""
+    Q = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", "")).lower()
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            if self.uuid and self.uuid.replace("gpu-", "") not in f[0].lower():
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle legs
+
+def oracle_sample(name, gen_device, reps_budget_s=10.0, max_reps=8, n_steps=None):
+    """Time the CPU oracle on one token of every layer of the workload (its first input batch).
+    Quantizing the needed experts with the oracle's quantizer is setup, not timed."""
+    import concurrent.futures as cf
+
+    import oracle
+    w = synth.WORKLOADS[name]
+    prepared = []
+    for T, seed in workload_entries(name):
+        shape = w.shape(T)
+        x = synth.activations(T, w.H, seed, 0, w.outlier_frac, device=gen_device).cpu()
+        lg = synth.router_logits(T, w.E, seed, 0, w.logit_bias, device=gen_device).cpu()
+        ids, _ = oracle.route(lg, w.k)
+        groups = sorted(set(ids[0].tolist()) | {w.E})
+        G = w.E + 1
+        packs = []
+        for proj, (N, K) in (("gate_up", (2 * w.I, w.H)), ("down", (w.H, w.I))):
+            P_ = np.zeros((G, N, K // 2), np.uint8)
+            S_ = np.zeros((G, N, K // 16), np.uint8)
+            Z_ = np.zeros((G,), np.float32)
+
+            def one(g):
+                return g, oracle.quantize(synth.projection_weights(shape, seed, 0, proj, [g], device=gen_device).cpu().numpy())
+            with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+                for g, (p, s, z) in ex.map(one, groups):
+                    P_[g], S_[g], Z_[g] = p[0], s[0], z[0]
+            packs.append((P_, S_, Z_))
+        prepared.append((x, lg, packs[0], packs[1]))
+
+    def run_once():
+        for x, lg, gu, dn in prepared:
+            oracle.moe_forward(x, lg, gu, dn, w.k, tokens=[0])
+        return len(prepared)
+
+    if n_steps is not None:
+        return prepared, run_once
+    run_once()  # warm
+    t0 = time.perf_counter()
+    toks, reps = 0, 0
+    while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < reps_budget_s):
+        toks += run_once()
+        reps += 1
+    dt = time.perf_counter() - t0
+    return {"value": toks / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{toks} tokens: token 0 of each of the {len(prepared)} layer(s) of the workload, "
+                      f"{reps} repetition(s); fp64 C++ oracle with std::thread over experts"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return 0
+    name = args.workload
+    steps = args.steps if args.steps is not None else 20
+    warmup = args.warmup if args.warmup is not None else 3
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    _, run_once = oracle_sample(name, gen, n_steps=steps)
+    for _ in range(warmup):
+        run_once()
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(steps):
+        toks += run_once()
+    dt = time.perf_counter() - t0
+    value = toks / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": 1e3 * dt / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": describe(name),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": "each step: token 0 of each layer of the workload through the fp64 oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_layer(moe, w, T, seed, pool, device):
+    shape = w.shape(T)
+    ms = moe.Shape(T=T, H=w.H, I=w.I, E=w.E, k=w.k, has_shared=1)
+    G = w.E + 1
+    weights = []
+    for proj, (N, K) in (("gate_up", (2 * w.I, w.H)), ("down", (w.H, w.I))):
+        packed = torch.empty(G, N, K // 2, dtype=torch.uint8, device=device)
+        scales = torch.empty(G, N, K // 16, dtype=torch.uint8, device=device)
+        scale2 = torch.empty(G, dtype=torch.float32, device=device)
+        for g0 in range(0, G, 32):
+            gs = list(range(g0, min(G, g0 + 32)))
+            q = moe.quantize_nvfp4(synth.projection_weights(shape, seed, 0, proj, gs, device=device))
+            packed[g0:g0 + len(gs)], scales[g0:g0 + len(gs)], scale2[g0:g0 + len(gs)] = q.packed, q.scales, q.scale2
+        weights.append(moe.NVFP4Weights(packed, scales, scale2))
+    xs = [synth.activations(T, w.H, seed, p, w.outlier_frac, device=device) for p in range(pool)]
+    lgs = [synth.router_logits(T, w.E, seed, p, w.logit_bias, device=device) for p in range(pool)]
+    ws = moe.workspace(ms, device=device)
+    out = torch.empty(T, w.H, dtype=torch.bfloat16, device=device)
+    # distinct routed experts of every input batch, from the library's own route/permute
+    uniq = []
+    for p in range(pool):
+        ids, _ = moe.route_topk(lgs[p], ms)
+        counts, *_ = moe.permute(ids, ms, ws)
+        uniq.append(int((counts > 0).sum().item()))
+    return dict(T=T, ms=ms, gu=weights[0], dn=weights[1], xs=xs, lgs=lgs, ws=ws, out=out, uniq=uniq)
+
+
+def run_ours(args):
+    import quantized_moe_expert_nvfp4_gb300 as moe
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    name = args.workload
+    w = synth.WORKLOADS[name]
+    d_steps, d_warm, d_pool = DEFAULTS[name]
+    steps = args.steps if args.steps is not None else d_steps
+    warmup = max(3, args.warmup if args.warmup is not None else d_warm)
+    pool = args.pool or d_pool
+    moe.load()
+    layers = [build_layer(moe, w, T, seed, pool, device) for T, seed in workload_entries(name)]
+    tokens_per_step = sum(L["T"] for L in layers)
+    decode_arm = all(L["T"] <= moe.DECODE_MAX_T for L in layers)
+    launches_per_forward = 3 if decode_arm else 8
+    stream = torch.cuda.Stream(device)
+
+    # graphs[b][p]: one step on input batch p, recording event set b
+    def new_events():
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in layers]
+    events = [[new_events() for _ in range(pool)] for _ in range(2)]
+    graphs = [[None] * pool for _ in range(2)]
+    with torch.cuda.stream(stream):
+        for p in range(pool):  # one eager pass per batch before capture
+            for L in layers:
+                moe.forward(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+    stream.synchronize()
+    for b in range(2):
+        for p in range(pool):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for li, L in enumerate(layers):
+                    moe.forward_profiled(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"],
+                                         L["out"], events[b][p][li])
+            graphs[b][p] = g
+
+    stage_ms = [[0.0] * 4 for _ in layers]
+    gate_up_bytes = 0.0
+    gate_up_flops = 0.0
+    fwd_bytes = 0.0
+    H, I, E = w.H, w.I, w.E
+    gu_expert = 2 * I * H // 2 + 2 * I * H // 16 + 4
+    dn_expert = H * I // 2 + H * I // 16 + 4
+
+    def collect(b, batch_steps):
+        nonlocal gate_up_bytes, gate_up_flops, fwd_bytes
+        for p in batch_steps:
+            evs = events[b][p]
+            evs[-1][4].synchronize()
+            for li, L in enumerate(layers):
+                e = evs[li]
+                for s in range(4):
+                    stage_ms[li][s] += e[s].elapsed_time(e[s + 1])
+                T, U = L["T"], L["uniq"][p] + 1
+                S = T * w.k
+                gate_up_bytes += U * gu_expert + T * H * 2 + (S + T) * I * 2
+                gate_up_flops += 2.0 * (2 * I) * H * (S + T)
+                fwd_bytes += U * (gu_expert + dn_expert) + T * H * 2 + T * E * 4 + T * H * 2
+
+    def run_steps(n, timed):
+        pending = None
+        for i in range(n):
+            b, p = (i // pool) % 2, i % pool
+            graphs[b][p].replay()
+            if timed and (p == pool - 1 or i == n - 1):
+                batch = (b, list(range(0, p + 1)))
+                if pending is not None:
+                    collect(*pending)
+                pending = batch
+        return pending
+
+    with ClockSampler(device) as clk:
+        with torch.cuda.stream(stream):
+            t_w = time.perf_counter()
+            i = 0
+            while i < warmup or time.perf_counter() - t_w < 2.0:   # >= W steps and >= 2 s under load
+                run_steps(pool, timed=False)
+                i += pool
+            stream.synchronize()
+            if dist:
+                dist.barrier()
+            stream.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            pending = run_steps(steps, timed=True)
+            t1.record(stream)
+        t1.synchronize()
+        if pending is not None:
+            collect(*pending)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    max_ms = elapsed_ms
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        max_ms = float(tt.item())
+    value = world * steps * tokens_per_step / (max_ms / 1e3)
+
+    # dominant kernel (largest summed stage time): gate_up on both arms so far
+    tot_stage = [sum(stage_ms[li][s] for li in range(len(layers))) for s in range(4)]
+    dom = max(range(4), key=lambda s: tot_stage[s])
+    stage_names = ["route+permute", "gate_up", "down" if not decode_arm else "down+combine", "combine"]
+    gu_ms = tot_stage[1]
+    n_launch = steps * len(layers)
+    if decode_arm:
+        achieved = gate_up_bytes / (gu_ms / 1e3) / 1e9
+        pk = peaks()
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                    "frac": achieved / pk["hbm"], "peak_source": pk["source"],
+                    "kernel": "grouped_simt_kernel<gate_up> (decode GEMV)",
+                    "algorithmic_bytes_per_launch": gate_up_bytes / n_launch,
+                    "avg_launch_us": 1e3 * gu_ms / n_launch,
+                    "traffic": stored_traffic(name, "gate_up", ["quantized_moe_expert_nvfp4_gb300/csrc/grouped_simt.cu"])}
+    else:
+        achieved = gate_up_flops / (gu_ms / 1e3) / 1e12
+        pk = peaks()
+        peak = pk["bf16_sustained"] if name == "long" else pk["bf16"]
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "peak_source": pk["source"],
+                    "kernel": "grouped gate_up GEMM", "algorithmic_flops_per_launch": gate_up_flops / n_launch,
+                    "avg_launch_us": 1e3 * gu_ms / n_launch,
+                    "traffic": stored_traffic(name, "gate_up", ["quantized_moe_expert_nvfp4_gb300/csrc/grouped_simt.cu"])}
+
+    # end to end through host buffers: H2D of x and logits from pinned memory, the C-ABI call,
+    # D2H of the output, every step.
+    e2e_steps = min(steps, 200)
+    hx = [[L["xs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
+    hl = [[L["lgs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
+    ho = [torch.empty(L["T"], H, dtype=torch.bfloat16).pin_memory() for L in layers]
+    dx = [torch.empty_like(L["xs"][0]) for L in layers]
+    dl = [torch.empty_like(L["lgs"][0]) for L in layers]
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        e0.record(stream)
+        for i in range(e2e_steps):
+            p = i % pool
+            for li, L in enumerate(layers):
+                dx[li].copy_(hx[li][p], non_blocking=True)
+                dl[li].copy_(hl[li][p], non_blocking=True)
+                moe.forward(dx[li], dl[li], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+                ho[li].copy_(L["out"], non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    h2d = sum(L["T"] * H * 2 + L["T"] * E * 4 for L in layers)
+    d2h = sum(L["T"] * H * 2 for L in layers)
+    e2e = {"value": world * e2e_steps * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    status = [moe.device_status(L["ws"]) for L in layers]
+    if any(status):
+        raise RuntimeError(f"device status {status}")
+
+    if rank == 0:
+        cfg = describe(name)
+        cfg.update({"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh "
+                          f"input batch each step ({pool} batches cycled), experts differ per step",
+                    "cuda_graphs": True, "parallelism": f"replicas x{world}", "arm": "decode (grouped GEMV)"
+                    if decode_arm else "prefill (grouped GEMM)"})
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+                "warmup": warmup, "ms_per_step": max_ms / steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "nvfp4 x bf16 -> f32 accumulate", "data": "synthetic",
+                "config": cfg, "roofline": roofline, "e2e": e2e,
+                "gpu_launches": steps * len(layers) * launches_per_forward,
+                "clocks": clk.summary(),
+                "stages_ms_per_step": {stage_names[s]: tot_stage[s] / steps for s in range(4)},
+                "forward_hbm_gbs": fwd_bytes / (sum(tot_stage) / 1e3) / 1e9,
+                "distinct_experts_mean": [float(np.mean(L["uniq"])) for L in layers]}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_sample(name, device)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,169 @@
+/*
+ * moe_nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 routed mixture-of-experts layer.
+ *
+ * The layer is the one the Atlas project's "long-context cold prefill to SGLang parity" issue
+ * states for NVFP4 checkpoints (kernel comparison table, untransposed W4A16 column):
+ *   bf16 activations; expert weights stored as e2m1 values x one e4m3 scale per 16-element
+ *   K block x one fp32 per-tensor scale2; f32 accumulation; SiLU(gate)*up intermediate in
+ *   bf16; an fp32 weighted unpermute/combine; an always-on shared expert.
+ * Its stages are the tensors the same issue's op-dump list names (router logits, top-k ids and
+ * weights, the token permutation, shared-expert in/out, routed outputs before combine, the
+ * combine result), and each stage is one call below.  `moe_forward` runs them all.
+ *
+ * Conventions for every call
+ *  - Memory: every tensor argument is DEVICE memory owned by the caller.  The library never
+ *    allocates or frees.  Scratch comes from the caller's workspace `ws` (size from
+ *    moe_workspace_size), which the call may overwrite; 256-byte alignment is required for
+ *    `ws` and 16-byte alignment for every other device pointer.
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
+ *    enqueue work; none synchronizes the host, none copies device data to the host (the
+ *    route and permutation results stay on the device, so no host round trip breaks stream
+ *    capture, as the "handover briefs" page requires of its device-side selection), so a
+ *    call sequence can be captured in a CUDA graph.
+ *  - Errors: argument and shape errors are returned before anything is enqueued.  A failed
+ *    launch returns MOE_ERR_CUDA.  Errors detected on the device (a bounded wait that ran
+ *    out) are written to a status word in `ws`; read it with moe_get_device_status.
+ *  - Sizes: T >= 0 tokens (T = 0 enqueues nothing); H % 128 == 0, 128 <= H <= 16384;
+ *    I % 128 == 0, 128 <= I <= 8192; 1 <= E <= 1024; 1 <= k <= min(E, 16);
+ *    T * (k + 1) < 2^31.  The shared expert, when present, has the routed experts' I.
+ *  - Data types: bf16 tensors are passed as their 16-bit patterns (uint16_t).
+ *
+ * Weight layout (one projection, all groups), chosen as the resident "[N, K/2]" layout the
+ * issue prices ("no dequant, no transpose"):
+ *    packed [G, N, K/2] bytes, element k of row n in byte k/2, even k in the low nibble;
+ *    scales [G, N, K/16] e4m3 bytes, one per 16 consecutive k of a row;
+ *    scale2 [G] fp32, one per group and projection;
+ *    G = E + has_shared groups, the shared expert is group E.
+ *  gate_up: N = 2I, K = H (rows 0..I-1 are gate, rows I..2I-1 are up).  down: N = H, K = I.
+ *
+ * Row conventions of the staged tensors: S = T*k slots, slot s = t*k + j for rank j of
+ * token t.  h [S+T, I] and y [S+T, H] hold the routed slots in permuted order (row p is slot
+ * sorted_slot[p]) followed by one shared-expert row per token (row S + t).
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,          /* null/misaligned pointer, inconsistent struct */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2,    /* sizes outside the supported ranges above */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -3,  /* ws_bytes < moe_workspace_size(shape) */
+  MOE_ERR_ARCH = -4,                 /* current device is not compute capability 10.3 */
+  MOE_ERR_CUDA = -5,                 /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = -6        /* a device-side bounded wait ran out */
+} moe_status_t;
+
+/* Sizes of one MoE layer. */
+typedef struct {
+  int32_t T;           /* tokens (rows of x) */
+  int32_t H;           /* hidden size */
+  int32_t I;           /* expert intermediate size (routed and shared) */
+  int32_t E;           /* routed experts */
+  int32_t k;           /* experts per token */
+  int32_t has_shared;  /* 1: an always-on shared expert is group E; 0: none */
+} moe_shape_t;
+
+/* One NVFP4 projection of every group (device pointers, caller-owned; layout above). */
+typedef struct {
+  const uint8_t* packed;
+  const uint8_t* scales;
+  const float* scale2;
+  int32_t G, N, K;
+} moe_nvfp4_weights_t;
+
+/* Bytes of workspace every call below needs for this shape (0 on an unsupported shape). */
+size_t moe_workspace_size(const moe_shape_t* shape);
+
+/* Router top-k ("router/gating GEMM and top-k" of the issue's list of logit-changing ops; the
+ * tie rule is the handover briefs' device selection: lower index wins, NaN never wins).
+ *   logits   fp32 [T, E]
+ *   topk_ids int32 [T, k]: experts ordered by (logit descending, index ascending), NaN as -inf
+ *   topk_w   fp32 [T, k]: softmax over all E, restricted to the k picks and renormalised to
+ *            sum 1 (= a softmax over the k selected logits).  A token whose logits are all
+ *            -inf/NaN gets weights 0; +inf logits share the mass equally. */
+moe_status_t moe_route_topk(const float* logits, const moe_shape_t* shape, int32_t* topk_ids,
+                            float* topk_w, void* stream);
+
+/* Token permutation by expert (the issue's "token permutation" dump), built on the device.
+ *   topk_ids    int32 [T, k] (values in [0, E))
+ *   counts      int32 [E]     slots routed to each expert
+ *   offsets     int32 [E + 1] exclusive prefix sum of counts (offsets[E] = S)
+ *   sorted_slot int32 [S]     slot ids sorted by expert, ascending slot id within an expert
+ *   slot_pos    int32 [S]     inverse: sorted_slot[slot_pos[s]] == s
+ * Bit-exact and deterministic. */
+moe_status_t moe_permute(const int32_t* topk_ids, const moe_shape_t* shape, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* Grouped gate_up GEMM with SiLU(gate)*up fused (the issue's fused gate_up kernel, W4A16):
+ * for routed row p (expert e with offsets[e] <= p < offsets[e+1]) and x row t = sorted_slot[p]/k,
+ *   g = scale2_e * (x_t . deq(W_e[r]))   for gate rows r < I,  u likewise for up rows I + r,
+ *   h[p, r] = bf16(SiLU(g) * u), accumulated in fp32;
+ * and the shared expert (group E) for h rows S + t over every token t.
+ *   x [T, H] bf16; h [S + T, I] bf16 (shared rows written only when has_shared). */
+moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
+                                 const int32_t* offsets, const moe_nvfp4_weights_t* gate_up,
+                                 const moe_shape_t* shape, uint16_t* h, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* Grouped down GEMM (the issue's pointer-table grouped GEMM): y[p] = bf16(scale2 * (h[p] .
+ * deq(Wd_e)^T)) in fp32 for every routed row p of expert e and, for the shared expert, rows
+ * S + t.   h [S + T, I] bf16 -> y [S + T, H] bf16. */
+moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
+                              const moe_nvfp4_weights_t* down, const moe_shape_t* shape,
+                              uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+
+/* fp32 weighted unpermute/combine ("fp32 weighted sum" of the issue's table; fixed summation
+ * order as in the expert-parallel discussion of the TensorFold sm_120 issue):
+ *   out[t] = (sum_{j=0..k-1} topk_w[t, j] * y[slot_pos[t*k + j]]) + y[S + t]
+ * summed in fp32 in exactly that order, then written as bf16 (out_is_fp32 = 0) or fp32. */
+moe_status_t moe_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w,
+                         const moe_shape_t* shape, void* out, int out_is_fp32, void* stream);
+
+/* The whole layer: route, permute, grouped gate_up(+SiLU), grouped down, combine, with the
+ * shared expert.  Picks the decode arm (grouped GEMV streaming only the selected experts'
+ * bytes) for T <= 64 and the prefill arm (grouped GEMM) above.  Same numerics contract as the
+ * stage calls; out is [T, H] bf16 or fp32. */
+moe_status_t moe_forward(const uint16_t* x, const float* logits,
+                         const moe_nvfp4_weights_t* gate_up, const moe_nvfp4_weights_t* down,
+                         const moe_shape_t* shape, void* out, int out_is_fp32, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* moe_forward with per-stage timing (the per-stage microsecond hooks of the handover briefs'
+ * measure-first steps, as CUDA events).  stage_events, when not NULL, points to 5 cudaEvent_t
+ * (created with timing enabled) that are recorded on `stream`: [0] before routing, [1] after
+ * the permutation and work list, [2] after gate_up, [3] after down, [4] after combine.  On the
+ * decode arm down and combine are one kernel, so [3] and [4] are recorded together.  With
+ * stage_events == NULL this is moe_forward. */
+moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
+                                  const moe_nvfp4_weights_t* gate_up,
+                                  const moe_nvfp4_weights_t* down, const moe_shape_t* shape,
+                                  void* out, int out_is_fp32, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* stage_events);
+
+/* Load-time NVFP4 quantizer of fp32 weights [G, N, K] (K % 16 == 0, finite values) into the
+ * layout above, with the recipe of the benchmark configurations: scale2 = amax / (448 * 6);
+ * block scale = e4m3_rne_satfinite(block_amax / 6 / scale2); code = e2m1_rne_satfinite(
+ * w / (e4m3(scale) * scale2)); every step one fp32 operation; a block whose scale decodes to 0
+ * stores code 0.  Not on the hot path (weights are quantized once, at load). */
+moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,
+                                uint8_t* scales, float* scale2, void* stream);
+
+/* Reads (and clears) the device status word of a workspace: *status receives MOE_OK or the
+ * first device-side error recorded since the last read.  Synchronizes `stream`. */
+moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,255 @@
+"""Python binding of `libmoe_nvfp4.so`, the GB300 (sm_103a) NVFP4 routed-MoE layer.
+
+Argument marshalling only: each function checks dtypes, shapes and devices of torch tensors,
+passes their device pointers and the current CUDA stream to the C ABI declared in
+`include/moe_nvfp4.h`, and raises `MoeError` on a non-zero status.  Every step of the layer runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and importing a function
+that needs the library fails loudly when `libmoe_nvfp4.so` has not been built
+(`python -c "import __graft_entry__ as g; g.build()"`).
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_nvfp4.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE",
+                -3: "MOE_ERR_WORKSPACE_TOO_SMALL", -4: "MOE_ERR_ARCH", -5: "MOE_ERR_CUDA",
+                -6: "MOE_ERR_DEVICE_TIMEOUT"}
+DECODE_MAX_T = 64   # moe_forward takes the grouped-GEMV (decode) arm up to this many tokens
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}: "
+                         f"{load().moe_status_string(status).decode()}")
+
+
+class MoeShape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("has_shared", ctypes.c_int32)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("scale2", ctypes.c_void_p),
+                ("G", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libmoe_nvfp4.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build the CUDA library first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(LIB_PATH)
+            _declare(lib)
+            _lib = lib
+    return _lib
+
+
+def _declare(L):
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    SH, W = ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights)
+    sigs = {
+        "moe_workspace_size": ([SH], SZ),
+        "moe_route_topk": ([P, SH, P, P, P], I32),
+        "moe_permute": ([P, SH, P, P, P, P, P, SZ, P], I32),
+        "moe_grouped_gate_up": ([P, P, P, W, SH, P, P, SZ, P], I32),
+        "moe_grouped_down": ([P, P, W, SH, P, P, SZ, P], I32),
+        "moe_combine": ([P, P, P, SH, P, I32, P], I32),
+        "moe_forward": ([P, P, W, W, SH, P, I32, P, SZ, P], I32),
+        "moe_forward_profiled": ([P, P, W, W, SH, P, I32, P, SZ, P, P], I32),
+        "moe_quantize_nvfp4": ([P, I64, I64, I64, P, P, P, P], I32),
+        "moe_get_device_status": ([P, ctypes.POINTER(I32), P], I32),
+        "moe_status_string": ([I32], ctypes.c_char_p),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes, fn.restype = args, res
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor") -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@dataclass
+class Shape:
+    T: int
+    H: int
+    I: int
+    E: int
+    k: int
+    has_shared: int = 1
+
+    @property
+    def S(self) -> int:
+        return self.T * self.k
+
+    def c(self) -> MoeShape:
+        return MoeShape(self.T, self.H, self.I, self.E, self.k, self.has_shared)
+
+
+@dataclass
+class NVFP4Weights:
+    """One projection of every group: packed u8 [G, N, K/2], scales u8 [G, N, K/16] (e4m3
+    bytes), scale2 fp32 [G]; all on the device."""
+    packed: torch.Tensor
+    scales: torch.Tensor
+    scale2: torch.Tensor
+
+    def c(self) -> MoeWeights:
+        G, N, K2 = self.packed.shape
+        for name, t, dt in (("packed", self.packed, torch.uint8), ("scales", self.scales, torch.uint8),
+                            ("scale2", self.scale2, torch.float32)):
+            _ptr(t, dt, name)
+        return MoeWeights(self.packed.data_ptr(), self.scales.data_ptr(), self.scale2.data_ptr(),
+                          G, N, 2 * K2)
+
+
+def workspace_size(shape: Shape) -> int:
+    n = load().moe_workspace_size(ctypes.byref(shape.c()))
+    if n == 0:
+        raise MoeError("moe_workspace_size", -2)
+    return n
+
+
+def workspace(shape: Shape, device="cuda") -> torch.Tensor:
+    """A workspace buffer for `shape` (uint8, 256-byte aligned as torch allocates)."""
+    return torch.empty(workspace_size(shape), dtype=torch.uint8, device=device)
+
+
+def quantize_nvfp4(w: torch.Tensor, stream=None) -> NVFP4Weights:
+    """Load-time NVFP4 quantization of fp32 weights [G, N, K] on the GPU."""
+    G, N, K = w.shape
+    dev = w.device
+    packed = torch.empty(G, N, K // 2, dtype=torch.uint8, device=dev)
+    scales = torch.empty(G, N, K // 16, dtype=torch.uint8, device=dev)
+    scale2 = torch.empty(G, dtype=torch.float32, device=dev)
+    _check("moe_quantize_nvfp4", load().moe_quantize_nvfp4(
+        _ptr(w, torch.float32, "w"), G, N, K, _ptr(packed), _ptr(scales), _ptr(scale2), _stream(stream)))
+    return NVFP4Weights(packed, scales, scale2)
+
+
+def route_topk(logits: torch.Tensor, shape: Shape, topk_ids=None, topk_w=None, stream=None):
+    dev = logits.device
+    ids = topk_ids if topk_ids is not None else torch.empty(shape.T, shape.k, dtype=torch.int32, device=dev)
+    w = topk_w if topk_w is not None else torch.empty(shape.T, shape.k, dtype=torch.float32, device=dev)
+    _check("moe_route_topk", load().moe_route_topk(
+        _ptr(logits, torch.float32, "logits"), ctypes.byref(shape.c()), _ptr(ids, torch.int32, "topk_ids"),
+        _ptr(w, torch.float32, "topk_w"), _stream(stream)))
+    return ids, w
+
+
+def permute(topk_ids: torch.Tensor, shape: Shape, ws: torch.Tensor, stream=None):
+    dev = topk_ids.device
+    counts = torch.empty(shape.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(shape.E + 1, dtype=torch.int32, device=dev)
+    sorted_slot = torch.empty(max(shape.S, 1), dtype=torch.int32, device=dev)
+    slot_pos = torch.empty(max(shape.S, 1), dtype=torch.int32, device=dev)
+    _check("moe_permute", load().moe_permute(
+        _ptr(topk_ids, torch.int32, "topk_ids"), ctypes.byref(shape.c()), _ptr(counts), _ptr(offsets),
+        _ptr(sorted_slot), _ptr(slot_pos), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return counts, offsets, sorted_slot[:shape.S], slot_pos[:shape.S]
+
+
+def grouped_gate_up(x, sorted_slot, offsets, gate_up: NVFP4Weights, shape: Shape, ws, h=None, stream=None):
+    h = h if h is not None else torch.empty(shape.S + shape.T, shape.I, dtype=torch.bfloat16, device=x.device)
+    _check("moe_grouped_gate_up", load().moe_grouped_gate_up(
+        _ptr(x, torch.bfloat16, "x"), _ptr(sorted_slot, torch.int32, "sorted_slot"),
+        _ptr(offsets, torch.int32, "offsets"), ctypes.byref(gate_up.c()), ctypes.byref(shape.c()),
+        _ptr(h, torch.bfloat16, "h"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return h
+
+
+def grouped_down(h, offsets, down: NVFP4Weights, shape: Shape, ws, y=None, stream=None):
+    y = y if y is not None else torch.empty(shape.S + shape.T, shape.H, dtype=torch.bfloat16, device=h.device)
+    _check("moe_grouped_down", load().moe_grouped_down(
+        _ptr(h, torch.bfloat16, "h"), _ptr(offsets, torch.int32, "offsets"), ctypes.byref(down.c()),
+        ctypes.byref(shape.c()), _ptr(y, torch.bfloat16, "y"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _stream(stream)))
+    return y
+
+
+def combine(y, slot_pos, topk_w, shape: Shape, out=None, out_fp32: bool = False, stream=None):
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    out = out if out is not None else torch.empty(shape.T, shape.H, dtype=dt, device=y.device)
+    _check("moe_combine", load().moe_combine(
+        _ptr(y, torch.bfloat16, "y"), _ptr(slot_pos, torch.int32, "slot_pos"), _ptr(topk_w, torch.float32, "topk_w"),
+        ctypes.byref(shape.c()), _ptr(out, dt, "out"), int(out_fp32), _stream(stream)))
+    return out
+
+
+def forward(x, logits, gate_up: NVFP4Weights, down: NVFP4Weights, shape: Shape, ws, out=None,
+            out_fp32: bool = False, stream=None):
+    """The whole layer (route, permute, grouped gate_up+SiLU, grouped down, combine, shared)."""
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    out = out if out is not None else torch.empty(shape.T, shape.H, dtype=dt, device=x.device)
+    _check("moe_forward", load().moe_forward(
+        _ptr(x, torch.bfloat16, "x"), _ptr(logits, torch.float32, "logits"), ctypes.byref(gate_up.c()),
+        ctypes.byref(down.c()), ctypes.byref(shape.c()), _ptr(out, dt, "out"), int(out_fp32),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return out
+
+
+def forward_profiled(x, logits, gate_up: NVFP4Weights, down: NVFP4Weights, shape: Shape, ws, out,
+                     stage_events, out_fp32: bool = False, stream=None):
+    """forward() that also records 5 torch.cuda.Event (timing enabled) at the stage
+    boundaries: before routing, after permute, after gate_up, after down, after combine."""
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(ev.cuda_event) for ev in stage_events])
+    _check("moe_forward_profiled", load().moe_forward_profiled(
+        _ptr(x, torch.bfloat16, "x"), _ptr(logits, torch.float32, "logits"), ctypes.byref(gate_up.c()),
+        ctypes.byref(down.c()), ctypes.byref(shape.c()), _ptr(out, dt, "out"), int(out_fp32),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream), arr))
+    return out
+
+
+def device_status(ws: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_int32(0)
+    _check("moe_get_device_status", load().moe_get_device_status(
+        _ptr(ws, torch.uint8, "ws"), ctypes.byref(v), _stream(stream)))
+    return v.value
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+__all__ = ["Shape", "NVFP4Weights", "MoeError", "load", "workspace_size", "workspace",
+           "quantize_nvfp4", "route_topk", "permute", "grouped_gate_up", "grouped_down", "combine",
+           "forward", "forward_profiled", "device_status", "status_string", "DECODE_MAX_T", "LIB_PATH"]

@@ -1,0 +1,381 @@
+// C ABI of the NVFP4 routed-MoE library: argument validation, workspace layout and the
+// choice of arm.  Host code only; every stage runs in the kernels of the other files.
+#include <algorithm>
+#include <atomic>
+
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_shape(const moe_shape_t* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->H < 128 || s->H > 16384 || s->H % 128 || s->I < 128 || s->I > 8192 ||
+      s->I % 128 || s->E < 1 || s->E > kMaxE || s->k < 1 || s->k > kMaxK || s->k > s->E ||
+      (s->has_shared != 0 && s->has_shared != 1))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<int64_t>(s->T) * (s->k + 1) >= (int64_t{1} << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status_t check_weights(const moe_nvfp4_weights_t* w, const moe_shape_t& s, bool gate_up) {
+  if (!w || !aligned16(w->packed) || !aligned16(w->scales) || !aligned16(w->scale2))
+    return MOE_ERR_INVALID_ARG;
+  const int N = gate_up ? 2 * s.I : s.H, K = gate_up ? s.H : s.I;
+  if (w->G != s.E + s.has_shared || w->N != N || w->K != K) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const void* ws, size_t ws_bytes, const moe_shape_t& s) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < ws_layout(s).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+// The current device must be compute capability 10.3 (GB300).  Cached per device.
+moe_status_t check_arch() {
+  static std::atomic<int> cache[64];  // 0 unknown, 1 ok, 2 wrong arch
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c == 1) return MOE_OK;
+    if (c == 2) return MOE_ERR_ARCH;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
+  return ok ? MOE_OK : MOE_ERR_ARCH;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct Ws {
+  int32_t* status;
+  int32_t* meta;
+  int32_t* ids;
+  float* w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_slot;
+  int32_t* slot_pos;
+  int4* tiles;
+  int32_t* hist;
+  uint16_t* h;
+  uint16_t* y;
+  WsLayout L;
+};
+
+Ws carve(void* ws, const moe_shape_t& s) {
+  Ws r;
+  r.L = ws_layout(s);
+  char* b = static_cast<char*>(ws);
+  r.status = reinterpret_cast<int32_t*>(b + r.L.status);
+  r.meta = reinterpret_cast<int32_t*>(b + r.L.meta);
+  r.ids = reinterpret_cast<int32_t*>(b + r.L.ids);
+  r.w = reinterpret_cast<float*>(b + r.L.w);
+  r.counts = reinterpret_cast<int32_t*>(b + r.L.counts);
+  r.offsets = reinterpret_cast<int32_t*>(b + r.L.offsets);
+  r.sorted_slot = reinterpret_cast<int32_t*>(b + r.L.sorted_slot);
+  r.slot_pos = reinterpret_cast<int32_t*>(b + r.L.slot_pos);
+  r.tiles = reinterpret_cast<int4*>(b + r.L.tiles);
+  r.hist = reinterpret_cast<int32_t*>(b + r.L.hist);
+  r.h = reinterpret_cast<uint16_t*>(b + r.L.h);
+  r.y = reinterpret_cast<uint16_t*>(b + r.L.y);
+  return r;
+}
+
+int tile_rows_for(const moe_shape_t& s) { return s.T <= kDecodeMaxT ? kDecodeMaxT : kSimtTileRows; }
+
+GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, const uint16_t* act,
+                         const int32_t* sorted_slot, const Ws& ws, uint16_t* out) {
+  GroupedArgs a;
+  a.packed = w.packed;
+  a.scales = w.scales;
+  a.scale2 = w.scale2;
+  a.N = w.N;
+  a.K = w.K;
+  a.act = act;
+  a.sorted_slot = sorted_slot;
+  a.T = s.T;
+  a.k = s.k;
+  a.S = s.T * s.k;
+  a.E = s.E;
+  a.tiles = ws.tiles;
+  a.meta = ws.meta;
+  a.max_tiles = max_tiles_for(s, tile_rows_for(s));
+  a.out = out;
+  return a;
+}
+
+}  // namespace
+
+int64_t max_tiles_for(const moe_shape_t& s, int tile_rows) {
+  const int64_t S = static_cast<int64_t>(s.T) * s.k;
+  int64_t routed = S / tile_rows + s.E;
+  if (tile_rows >= s.T) routed = std::min<int64_t>(routed, std::min<int64_t>(S, s.E));
+  const int64_t shared = s.has_shared ? (s.T + tile_rows - 1) / tile_rows : 0;
+  return std::max<int64_t>(1, routed + shared);
+}
+
+WsLayout ws_layout(const moe_shape_t& s) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const int64_t S = static_cast<int64_t>(s.T) * s.k;
+  const int64_t R = S + s.T;
+  L.status = take(256);
+  L.meta = take(256);
+  L.ids = take(4 * S);
+  L.w = take(4 * S);
+  L.counts = take(4 * static_cast<size_t>(s.E));
+  L.offsets = take(4 * static_cast<size_t>(s.E + 1));
+  L.sorted_slot = take(4 * S);
+  L.slot_pos = take(4 * S);
+  L.max_tiles = std::max(max_tiles_for(s, kSimtTileRows), max_tiles_for(s, kDecodeMaxT));
+  L.tiles = take(16 * static_cast<size_t>(L.max_tiles));
+  L.n_chunks = (S + kScatterChunk - 1) / kScatterChunk;
+  L.hist = take(4 * static_cast<size_t>(std::max<int64_t>(1, L.n_chunks)) * s.E);
+  L.h = take(2 * static_cast<size_t>(R) * s.I);
+  L.y = take(2 * static_cast<size_t>(R) * s.H);
+  L.total = off;
+  return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_shape_t* shape) {
+  if (check_shape(shape) != MOE_OK) return 0;
+  return ws_layout(*shape).total;
+}
+
+moe_status_t moe_route_topk(const float* logits, const moe_shape_t* shape, int32_t* topk_ids,
+                            float* topk_w, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_arch()) != MOE_OK) return st;
+  return cuda_status(launch_route_topk(logits, shape->T, shape->E, shape->k, topk_ids, topk_w,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, const moe_shape_t* shape, int32_t* counts,
+                         int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos, void* ws,
+                         size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(topk_ids) || !aligned16(counts) || !aligned16(offsets) ||
+      !aligned16(sorted_slot) || !aligned16(slot_pos))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if ((st = check_arch()) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const moe_shape_t& s = *shape;
+  if (s.T == 0) {  // offsets of an empty batch are all zero
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * s.E, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (s.E + 1), cs);
+    return cuda_status(e);
+  }
+  Ws w = carve(ws, s);
+  if (s.T <= kDecodeMaxT)
+    return cuda_status(launch_route_permute_small(nullptr, topk_ids, s.T, s.E, s.k, s.has_shared,
+                                                  nullptr, nullptr, counts, offsets, sorted_slot,
+                                                  slot_pos, w.tiles, w.meta, kDecodeMaxT, cs));
+  return cuda_status(launch_permute_large(topk_ids, s.T, s.E, s.k, counts, offsets, sorted_slot,
+                                          slot_pos, w.hist, w.L.n_chunks, cs));
+}
+
+moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
+                                 const int32_t* offsets, const moe_nvfp4_weights_t* gate_up,
+                                 const moe_shape_t* shape, uint16_t* h, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(sorted_slot) || !aligned16(offsets) || !aligned16(h))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_weights(gate_up, *shape, true)) != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_arch()) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const moe_shape_t& s = *shape;
+  Ws w = carve(ws, s);
+  cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
+                                     w.tiles, w.meta, cs);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_gate_up_simt(grouped_args(*gate_up, s, x, sorted_slot, w, h), cs));
+}
+
+moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
+                              const moe_nvfp4_weights_t* down, const moe_shape_t* shape,
+                              uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(h) || !aligned16(offsets) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_weights(down, *shape, false)) != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_arch()) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const moe_shape_t& s = *shape;
+  Ws w = carve(ws, s);
+  cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
+                                     w.tiles, w.meta, cs);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_down_simt(grouped_args(*down, s, h, nullptr, w, y), cs));
+}
+
+moe_status_t moe_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w,
+                         const moe_shape_t* shape, void* out, int out_is_fp32, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(y) || !aligned16(slot_pos) || !aligned16(topk_w) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if (out_is_fp32 != 0 && out_is_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_arch()) != MOE_OK) return st;
+  return cuda_status(launch_combine(y, slot_pos, topk_w, shape->T, shape->H, shape->k,
+                                    shape->has_shared, out, out_is_fp32,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_forward(const uint16_t* x, const float* logits,
+                         const moe_nvfp4_weights_t* gate_up, const moe_nvfp4_weights_t* down,
+                         const moe_shape_t* shape, void* out, int out_is_fp32, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return moe_forward_profiled(x, logits, gate_up, down, shape, out, out_is_fp32, ws, ws_bytes,
+                              stream, nullptr);
+}
+
+moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
+                                  const moe_nvfp4_weights_t* gate_up,
+                                  const moe_nvfp4_weights_t* down, const moe_shape_t* shape,
+                                  void* out, int out_is_fp32, void* ws, size_t ws_bytes,
+                                  void* stream, void* const* stage_events) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(logits) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (out_is_fp32 != 0 && out_is_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if ((st = check_weights(gate_up, *shape, true)) != MOE_OK) return st;
+  if ((st = check_weights(down, *shape, false)) != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_arch()) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const moe_shape_t& s = *shape;
+  Ws w = carve(ws, s);
+  auto mark = [&](int i) -> cudaError_t {
+    return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), cs,
+                                                   cudaEventRecordExternal)
+                        : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (s.T <= kDecodeMaxT) {
+    // decode arm: 1) route + permute + work list, 2) gate_up GEMV (+SiLU*up) of every active
+    // group incl. the shared expert, 3) down GEMV + fixed-order combine.
+    e = launch_route_permute_small(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w,
+                                   w.counts, w.offsets, w.sorted_slot, w.slot_pos, w.tiles, w.meta,
+                                   kDecodeMaxT, cs);
+    if (e == cudaSuccess) e = mark(1);
+    if (e == cudaSuccess) e = launch_gate_up_simt(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), cs);
+    if (e == cudaSuccess) e = mark(2);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    DownCombineArgs d;
+    d.packed = down->packed;
+    d.scales = down->scales;
+    d.scale2 = down->scale2;
+    d.H = s.H;
+    d.I = s.I;
+    d.T = s.T;
+    d.k = s.k;
+    d.S = s.T * s.k;
+    d.E = s.E;
+    d.h = w.h;
+    d.slot_pos = w.slot_pos;
+    d.topk_w = w.w;
+    d.tiles = w.tiles;
+    d.meta = w.meta;
+    d.max_tiles = max_tiles_for(s, kDecodeMaxT);
+    d.has_shared = s.has_shared;
+    d.out = out;
+    d.out_is_fp32 = out_is_fp32;
+    e = launch_down_combine_gemv(d, cs);
+    if (e == cudaSuccess) e = mark(3);
+    if (e == cudaSuccess) e = mark(4);
+    return cuda_status(e);
+  }
+  // prefill arm
+  e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, cs);
+  if (e == cudaSuccess)
+    e = launch_permute_large(w.ids, s.T, s.E, s.k, w.counts, w.offsets, w.sorted_slot, w.slot_pos,
+                             w.hist, w.L.n_chunks, cs);
+  if (e == cudaSuccess)
+    e = launch_build_tiles(w.offsets, s.T, s.E, s.k, s.has_shared, kSimtTileRows, w.tiles, w.meta,
+                           cs);
+  if (e == cudaSuccess) e = mark(1);
+  if (e == cudaSuccess)
+    e = launch_gate_up_simt(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), cs);
+  if (e == cudaSuccess) e = mark(2);
+  if (e == cudaSuccess) e = launch_down_simt(grouped_args(*down, s, w.h, nullptr, w, w.y), cs);
+  if (e == cudaSuccess) e = mark(3);
+  if (e == cudaSuccess)
+    e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, cs);
+  if (e == cudaSuccess) e = mark(4);
+  return cuda_status(e);
+}
+
+moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,
+                                uint8_t* scales, float* scale2, void* stream) {
+  if (!aligned16(w) || !aligned16(packed) || !aligned16(scales) || !aligned16(scale2))
+    return MOE_ERR_INVALID_ARG;
+  if (G < 1 || G > 65535 || N < 1 || K < 16 || K % 16 || N * K > (int64_t{1} << 40))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status_t st = check_arch();
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_quantize(w, G, N, K, packed, scales, scale2,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream) {
+  if (!ws || !status || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID_ARG;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), cs);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer or inconsistent struct)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_ARCH: return "current device is not compute capability 10.3 (sm_103)";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side bounded wait timed out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// fp32 weighted unpermute/combine of the staged path: out[t] = sum_j w[t, j] * y[slot_pos[t*k+j]]
+// + y[S + t], accumulated in fp32 in rank order then the shared expert (the "fp32 weighted sum"
+// of the "long-context cold prefill to SGLang parity" issue's kernel table; the fixed order is
+// the one-rank reduction order the TensorFold sm_120 issue requires of expert parallelism).
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// One thread per (token, 8 consecutive hidden columns).
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y,
+                                                      const int32_t* __restrict__ slot_pos,
+                                                      const float* __restrict__ topk_w, int T,
+                                                      int H, int k, int has_shared, void* out,
+                                                      int out_is_fp32) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int cpr = H / 8;
+  if (idx >= static_cast<int64_t>(T) * cpr) return;
+  const int t = static_cast<int>(idx / cpr);
+  const int c = static_cast<int>(idx % cpr) * 8;
+  const int64_t S = static_cast<int64_t>(T) * k;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const int64_t p = __ldg(slot_pos + static_cast<int64_t>(t) * k + j);
+    const float wj = __ldg(topk_w + static_cast<int64_t>(t) * k + j);
+    float v[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(y + p * H + c)), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+  }
+  if (has_shared) {
+    float v[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(y + (S + t) * H + c)), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+  }
+  const int64_t o = static_cast<int64_t>(t) * H + c;
+  if (out_is_fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * i])) |
+             (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w, int T,
+                           int H, int k, int has_shared, void* out, int out_is_fp32,
+                           cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(T) * (H / 8);
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  combine_kernel<<<blocks, 256, 0, st>>>(y, slot_pos, topk_w, T, H, k, has_shared, out,
+                                         out_is_fp32);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

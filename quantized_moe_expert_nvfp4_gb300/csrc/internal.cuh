@@ -1,0 +1,142 @@
+// Internal declarations of the NVFP4 routed-MoE library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "moe_nvfp4.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ limits and arm choice
+constexpr int kMaxK = 16;
+constexpr int kMaxE = 1024;
+constexpr int kDecodeMaxT = 64;        // moe_forward uses the grouped-GEMV arm up to this T
+constexpr int kSimtTileRows = 64;      // rows per work item of the SIMT grouped GEMM
+constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutation
+
+// ------------------------------------------------------------------ workspace layout
+// All offsets are in bytes from the workspace base and 256-byte aligned.
+struct WsLayout {
+  size_t status;       // int32 device status word (+ padding)
+  size_t meta;         // int32 meta[8]: [0] = number of work tiles
+  size_t ids;          // int32 [S]
+  size_t w;            // fp32  [S]
+  size_t counts;       // int32 [E]
+  size_t offsets;      // int32 [E + 1]
+  size_t sorted_slot;  // int32 [S]
+  size_t slot_pos;     // int32 [S]
+  size_t tiles;        // int4  [max_tiles] work items {group, row_begin, rows, 0}
+  size_t hist;         // int32 [n_chunks, E] per-chunk expert histogram / bases
+  size_t h;            // bf16  [S + T, I]
+  size_t y;            // bf16  [S + T, H]
+  size_t total;
+  int64_t max_tiles;
+  int64_t n_chunks;
+};
+
+WsLayout ws_layout(const moe_shape_t& s);
+int64_t max_tiles_for(const moe_shape_t& s, int tile_rows);
+
+enum DeviceError : int32_t { kDevOk = 0, kDevTimeout = MOE_ERR_DEVICE_TIMEOUT };
+
+// ------------------------------------------------------------------ device helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Four e2m1 codes packed in the low 16 bits ... eight codes in a 32-bit word (element i in
+// bits 4i..4i+3) -> eight exact fp32 values, via the hardware e2m1x2 -> f16x2 conversion.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&v)[8]) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ void report_device_error(int32_t* status, int32_t code) {
+  atomicCAS(status, 0, code);
+}
+
+// ------------------------------------------------------------------ launchers
+// Each returns cudaGetLastError() of its launches.
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                              cudaStream_t st);
+// Single-CTA routing + permutation + work list for small T (decode arm).
+cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_in, int T, int E,
+                                       int k, int has_shared, int32_t* ids, float* w,
+                                       int32_t* counts, int32_t* offsets, int32_t* sorted_slot,
+                                       int32_t* slot_pos, int4* tiles, int32_t* meta,
+                                       int tile_rows, cudaStream_t st);
+// Multi-CTA permutation for any T.
+cudaError_t launch_permute_large(const int32_t* ids, int T, int E, int k, int32_t* counts,
+                                 int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
+                                 int32_t* hist, int64_t n_chunks, cudaStream_t st);
+// Work list from offsets: one item per (group, run of <= tile_rows rows).
+cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,
+                               int tile_rows, int4* tiles, int32_t* meta, cudaStream_t st);
+
+struct GroupedArgs {
+  const uint8_t* packed;
+  const uint8_t* scales;
+  const float* scale2;
+  int N, K;                     // weight rows and reduction length
+  const uint16_t* act;          // x [T, H] (gate_up) or h [S + T, I] (down)
+  const int32_t* sorted_slot;   // gate_up: routed row -> slot (token = slot / k)
+  int T, k, S, E;
+  const int4* tiles;
+  const int32_t* meta;
+  int64_t max_tiles;
+  uint16_t* out;                // h [S + T, I] or y [S + T, H]
+};
+cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
+cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
+
+struct DownCombineArgs {
+  const uint8_t* packed;
+  const uint8_t* scales;
+  const float* scale2;
+  int H, I, T, k, S, E;
+  const uint16_t* h;            // [S + T, I]
+  const int32_t* slot_pos;
+  const float* topk_w;
+  const int4* tiles;
+  const int32_t* meta;
+  int64_t max_tiles;
+  int has_shared;
+  void* out;
+  int out_is_fp32;
+};
+cudaError_t launch_down_combine_gemv(const DownCombineArgs& a, cudaStream_t st);
+
+cudaError_t launch_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w, int T,
+                           int H, int k, int has_shared, void* out, int out_is_fp32,
+                           cudaStream_t st);
+
+cudaError_t launch_quantize(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,
+                            uint8_t* scales, float* scale2, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,367 @@
+// Router top-k and token permutation, built entirely on the device.
+//
+// Routing follows the layer statement of the "long-context cold prefill to SGLang parity"
+// issue (router top-k ids and weights among the op-dump tensors) with the selection rule of
+// the "handover briefs" page's device-side indexer selection: rank an entry by (value desc,
+// index asc), a NaN never wins.  The permutation is the issue's "token permutation": slots
+// grouped by expert, stable in slot order, with counts and exclusive prefix offsets, computed
+// here by warp-level match/scan so that nothing returns to the host.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Order-preserving 32-bit key of a logit: larger key = preferred.  NaN counts as -inf and
+// -0 equals +0, so equal logits tie and the lower index wins.
+__device__ __forceinline__ uint32_t logit_key(float x) {
+  if (isnan(x)) x = -INFINITY;
+  if (x == 0.0f) x = 0.0f;
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp ranks one row of E logits (lane l holds entries l, l+32, ...).  Lane j < k receives
+// the rank-j winner and its routing weight: the renormalised softmax over the k winners,
+// w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), the sum taken in rank order.  A row with no
+// finite or +inf logit gets weights 0; +inf winners share the mass equally.
+template <int EPL>
+__device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, int k, int lane,
+                                          int& my_id, float& my_w) {
+  uint32_t key[EPL];
+  uint32_t taken = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = (e < E) ? logit_key(__ldg(row + e)) : 0u;
+    if (e >= E) taken |= 1u << i;
+  }
+  my_id = -1;
+  float my_val = -INFINITY;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (!((taken >> i) & 1u) && key[i] > bk) {  // within a lane indices increase with i
+        bk = key[i];
+        be = lane + 32 * i;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const uint32_t ok = __shfl_xor_sync(kFull, bk, off);
+      const int oe = __shfl_xor_sync(kFull, be, off);
+      if (ok > bk || (ok == bk && oe < be)) {
+        bk = ok;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_id = be;
+      my_val = key_value(bk);
+    }
+  }
+  const float m = __shfl_sync(kFull, my_val, 0);
+  const bool live = lane < k;
+  float ev;
+  if (m == -INFINITY) {
+    ev = 0.0f;
+  } else if (m == INFINITY) {
+    ev = (live && my_val == INFINITY) ? 1.0f : 0.0f;
+  } else {
+    ev = live ? expf(my_val - m) : 0.0f;
+  }
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(kFull, ev, j);
+  my_w = (sum > 0.0f) ? ev / sum : 0.0f;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  int my_id;
+  float my_w;
+  warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w);
+  if (lane < k) {
+    ids[static_cast<int64_t>(t) * k + lane] = my_id;
+    w[static_cast<int64_t>(t) * k + lane] = my_w;
+  }
+}
+
+// Exclusive scan over blockDim.x (<= 1024, multiple of 32) values, one per thread.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = (lane < nw) ? s_warp[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, s, off);
+      if (lane >= off) s += y;
+    }
+    if (lane < nw) s_warp[lane] = s;  // inclusive warp prefix
+  }
+  __syncthreads();
+  const int base = (warp > 0) ? s_warp[warp - 1] : 0;
+  const int tot = s_warp[nw - 1];
+  __syncthreads();
+  if (total) *total = tot;
+  return base + x - v;
+}
+
+// Work list: for each group with rows, ceil(rows / tile_rows) items {g, row_begin, rows, 0};
+// routed groups first (ascending expert), then the shared group (rows S .. S+T-1).  Called by
+// one whole block of >= E threads; cnt(e) / off(e) come from the caller.
+__device__ void write_tiles_block(int E, int S, int T, int has_shared, int tile_rows,
+                                  const int* cnt_of, const int* off_of, int4* tiles,
+                                  int32_t* meta, int* s_warp) {
+  const int e = threadIdx.x;
+  const int c = (e < E) ? cnt_of[e] : 0;
+  const int n = (c + tile_rows - 1) / tile_rows;
+  int total = 0;
+  const int base = block_exclusive_scan(n, s_warp, &total);
+  if (e < E) {
+    for (int i = 0; i < n; ++i) {
+      const int r0 = i * tile_rows;
+      tiles[base + i] = make_int4(e, off_of[e] + r0, min(tile_rows, c - r0), 0);
+    }
+  }
+  const int n_shared = has_shared ? (T + tile_rows - 1) / tile_rows : 0;
+  for (int i = threadIdx.x; i < n_shared; i += blockDim.x) {
+    const int r0 = i * tile_rows;
+    tiles[total + i] = make_int4(E, S + r0, min(tile_rows, T - r0), 0);
+  }
+  if (threadIdx.x == 0) meta[0] = total + n_shared;
+}
+
+// Stable placement of n consecutive slots [s0, s0 + n) by one warp: every slot gets
+// cursor[e] + (number of earlier slots of the same expert in this run); the cursors advance.
+__device__ __forceinline__ void warp_stable_scatter(const int32_t* ids, int s0, int n, int E,
+                                                    int* cursor, int32_t* sorted_slot,
+                                                    int32_t* slot_pos) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int b = 0; b < n; b += 32) {
+    const int s = s0 + b + lane;
+    const bool live = (b + lane) < n;
+    int e = live ? ids[s] : -1;
+    if (e >= E) e = -2;  // out-of-range ids are ignored (the caller validated them)
+    const unsigned grp = __match_any_sync(kFull, e);
+    const int rank = __popc(grp & lt);
+    if (e >= 0) {
+      const int pos = cursor[e] + rank;
+      sorted_slot[pos] = s;
+      slot_pos[s] = pos;
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) cursor[e] += __popc(grp);
+    __syncwarp();
+  }
+}
+
+// Decode arm: routing (or given ids), counts, offsets, stable permutation and the work list of
+// a small batch in a single CTA of 1024 threads.
+template <int EPL>
+__global__ void __launch_bounds__(1024) route_permute_small_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ ids_in, int T, int E, int k,
+    int has_shared, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot,
+    int32_t* __restrict__ slot_pos, int4* __restrict__ tiles, int32_t* __restrict__ meta,
+    int tile_rows) {
+  __shared__ int s_ids[kDecodeMaxT * kMaxK];
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE];
+  __shared__ int s_cur[kMaxE];
+  __shared__ int s_warp[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int S = T * k;
+
+  if (logits) {
+    for (int t = warp; t < T; t += 32) {
+      int my_id;
+      float my_w;
+      warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w);
+      if (lane < k) {
+        ids[t * k + lane] = my_id;
+        w[t * k + lane] = my_w;
+        s_ids[t * k + lane] = my_id;
+      }
+    }
+  } else {
+    for (int s = threadIdx.x; s < S; s += blockDim.x) s_ids[s] = ids_in[s];
+  }
+  for (int e = threadIdx.x; e < kMaxE; e += blockDim.x) {
+    s_cnt[e] = 0;
+    s_cur[e] = 0;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const int e = s_ids[s];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  const int my = (threadIdx.x < E) ? s_cnt[threadIdx.x] : 0;
+  const int off = block_exclusive_scan(my, s_warp, nullptr);
+  if (threadIdx.x < E) {
+    s_off[threadIdx.x] = off;
+    s_cur[threadIdx.x] = off;
+    counts[threadIdx.x] = my;
+    offsets[threadIdx.x] = off;
+  }
+  if (threadIdx.x == 0) offsets[E] = S;
+  __syncthreads();
+  if (warp == 0) warp_stable_scatter(s_ids, 0, S, E, s_cur, sorted_slot, slot_pos);
+  write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+}
+
+// Large T, pass 1: per-chunk expert histogram.
+__global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __restrict__ ids, int S,
+                                                           int E, int32_t* __restrict__ hist) {
+  __shared__ int s_cnt[kMaxE];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kScatterChunk;
+  const int n = static_cast<int>(min(static_cast<int64_t>(kScatterChunk), static_cast<int64_t>(S) - s0));
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = ids[s0 + i];
+    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[static_cast<int64_t>(blockIdx.x) * E + e] = s_cnt[e];
+}
+
+// Large T, pass 2 (one CTA of 1024 threads): counts, offsets, and per-chunk bases
+// hist[c, e] <- offsets[e] + sum_{c' < c} hist[c', e].
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist,
+                                                            int64_t n_chunks, int E, int S,
+                                                            int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int64_t c = 0; c < n_chunks; ++c) {
+      const int v = hist[c * E + e];
+      hist[c * E + e] = run;
+      run += v;
+    }
+  }
+  const int off = block_exclusive_scan(run, s_warp, nullptr);
+  if (e < E) {
+    counts[e] = run;
+    offsets[e] = off;
+    for (int64_t c = 0; c < n_chunks; ++c) hist[c * E + e] += off;
+  }
+  if (e == 0) offsets[E] = S;
+}
+
+// Large T, pass 3: stable scatter.  Warp w of the CTA places the w-th eighth of the chunk.
+__global__ void __launch_bounds__(256) permute_scatter_kernel(const int32_t* __restrict__ ids,
+                                                              int S, int E,
+                                                              const int32_t* __restrict__ hist,
+                                                              int32_t* __restrict__ sorted_slot,
+                                                              int32_t* __restrict__ slot_pos) {
+  constexpr int kWarps = 8;
+  constexpr int kSub = kScatterChunk / kWarps;
+  __shared__ int s_cur[kWarps][kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kWarps * kMaxE; i += blockDim.x) (&s_cur[0][0])[i] = 0;
+  __syncthreads();
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kScatterChunk;
+  const int64_t w0 = c0 + static_cast<int64_t>(warp) * kSub;
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(kSub), static_cast<int64_t>(S) - w0)));
+  for (int i = lane; i < n; i += 32) {
+    const int e = ids[w0 + i];
+    if (e >= 0 && e < E) atomicAdd(&s_cur[warp][e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = hist[static_cast<int64_t>(blockIdx.x) * E + e];
+    for (int q = 0; q < kWarps; ++q) {
+      const int v = s_cur[q][e];
+      s_cur[q][e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  warp_stable_scatter(ids, static_cast<int>(w0), n, E, s_cur[warp], sorted_slot, slot_pos);
+}
+
+__global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
+                                                           int T, int E, int k, int has_shared,
+                                                           int tile_rows, int4* __restrict__ tiles,
+                                                           int32_t* __restrict__ meta) {
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE];
+  __shared__ int s_warp[32];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    s_off[e] = offsets[e];
+    s_cnt[e] = offsets[e + 1] - offsets[e];
+  }
+  __syncthreads();
+  write_tiles_block(E, T * k, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                              cudaStream_t st) {
+  const int blocks = (T + 7) / 8;
+  if (E <= 256)
+    route_topk_kernel<8><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else if (E <= 512)
+    route_topk_kernel<16><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  else
+    route_topk_kernel<32><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_in, int T, int E,
+                                       int k, int has_shared, int32_t* ids, float* w,
+                                       int32_t* counts, int32_t* offsets, int32_t* sorted_slot,
+                                       int32_t* slot_pos, int4* tiles, int32_t* meta,
+                                       int tile_rows, cudaStream_t st) {
+  auto kern = (E <= 256) ? route_permute_small_kernel<8>
+             : (E <= 512) ? route_permute_small_kernel<16> : route_permute_small_kernel<32>;
+  kern<<<1, 1024, 0, st>>>(logits, ids_in, T, E, k, has_shared, ids, w, counts, offsets,
+                           sorted_slot, slot_pos, tiles, meta, tile_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_large(const int32_t* ids, int T, int E, int k, int32_t* counts,
+                                 int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
+                                 int32_t* hist, int64_t n_chunks, cudaStream_t st) {
+  const int S = T * k;
+  permute_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, 0, st>>>(ids, S, E, hist);
+  permute_scan_kernel<<<1, 1024, 0, st>>>(hist, n_chunks, E, S, counts, offsets);
+  permute_scatter_kernel<<<static_cast<unsigned>(n_chunks), 256, 0, st>>>(ids, S, E, hist,
+                                                                          sorted_slot, slot_pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,
+                               int tile_rows, int4* tiles, int32_t* meta, cudaStream_t st) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, T, E, k, has_shared, tile_rows, tiles, meta);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

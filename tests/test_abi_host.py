@@ -1,0 +1,76 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every function that
+include/moe_nvfp4.h declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_moe_expert_nvfp4_gb300 import build
+    build.build()
+    import quantized_moe_expert_nvfp4_gb300 as moe
+    return moe, moe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    moe, L = lib
+    names = declared_functions()
+    assert "moe_forward" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def _shape(moe, **kw):
+    base = dict(T=8, H=2048, I=512, E=512, k=10, has_shared=1)
+    base.update(kw)
+    return moe.Shape(**base).c()
+
+
+def test_workspace_size_and_unsupported_shapes(lib):
+    moe, L = lib
+    ok = _shape(moe)
+    assert L.moe_workspace_size(ctypes.byref(ok)) > 0
+    for bad in (dict(H=100), dict(H=64), dict(I=96), dict(E=0), dict(E=2048), dict(k=0), dict(k=17),
+                dict(E=4, k=5), dict(T=-1), dict(has_shared=2), dict(T=1 << 30)):
+        assert L.moe_workspace_size(ctypes.byref(_shape(moe, **bad))) == 0, bad
+
+
+def test_host_validation_errors(lib):
+    moe, L = lib
+    P = ctypes.c_void_p
+    shape = _shape(moe)
+    ws_need = L.moe_workspace_size(ctypes.byref(shape))
+    fake = P(0x100000)      # aligned, never dereferenced: validation fails before any CUDA call
+    mis = P(0x100008)       # misaligned
+    w_gu = moe.MoeWeights(0x200000, 0x300000, 0x400000, 513, 1024, 2048)
+    w_dn = moe.MoeWeights(0x200000, 0x300000, 0x400000, 513, 2048, 512)
+    call = lambda **o: L.moe_forward(o.get("x", fake), o.get("lg", fake), ctypes.byref(o.get("gu", w_gu)),
+                                     ctypes.byref(o.get("dn", w_dn)), ctypes.byref(o.get("shape", shape)),
+                                     o.get("out", fake), o.get("fp32", 0), o.get("ws", fake),
+                                     o.get("ws_bytes", ws_need), None)
+    assert call(x=P(0)) == -1
+    assert call(out=mis) == -1
+    assert call(fp32=2) == -1
+    assert call(gu=moe.MoeWeights(0x200000, 0x300000, 0x400000, 512, 1024, 2048)) == -1
+    assert call(dn=moe.MoeWeights(0x200000, 0x300000, 0x400000, 513, 1024, 512)) == -1
+    assert call(shape=_shape(moe, H=100)) == -2
+    assert call(ws_bytes=ws_need - 1) == -3
+    assert call(ws=P(0x100010)) == -1   # workspace must be 256-byte aligned
+    assert L.moe_route_topk(fake, ctypes.byref(shape), P(0), fake, None) == -1
+    assert L.moe_combine(fake, fake, fake, ctypes.byref(shape), fake, 3, None) == -1
+    assert L.moe_quantize_nvfp4(fake, 1, 16, 20, fake, fake, fake, None) == -2
+    assert L.moe_quantize_nvfp4(mis, 1, 16, 32, fake, fake, fake, None) == -1
+    for code in range(-6, 1):
+        assert L.moe_status_string(code)

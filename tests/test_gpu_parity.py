@@ -1,0 +1,199 @@
+"""GPU parity of every stage and of moe_forward against the CPU oracle (needs a GB300).
+
+Integer results (top-k ids, counts, offsets, permutation, quantized bytes) must be bit-exact;
+floating-point results must satisfy the layer tolerance (max |err| <= 2e-2 * row RMS and mean
+relative error <= 3e-3) against the oracle's fp64 values.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from moe_cases import Layer, check_layer_close, moe_shape, to_np
+
+pytestmark = pytest.mark.gpu
+
+# (T, H, E, k, I, has_shared, logit bias, seed): the tiny workload itself, both arms, the arm
+# boundary (T = 64 / 65), k = 16, no shared expert, E = 1024, ragged tails everywhere.
+SMALL = [
+    (4, 256, 16, 2, 128, 1, "none", 0),
+    (1, 256, 16, 2, 128, 1, "none", 101),
+    (7, 384, 24, 3, 256, 1, "normal", 102),
+    (64, 256, 32, 4, 128, 1, "zipf", 103),
+    (65, 256, 32, 4, 128, 1, "zipf", 104),
+    (200, 512, 40, 6, 256, 1, "zipf", 105),
+    (300, 256, 16, 16, 128, 0, "none", 106),
+    (3000, 256, 64, 8, 128, 1, "normal", 107),
+    (16, 128, 1024, 16, 128, 1, "none", 108),
+]
+
+
+def _small_layer(case):
+    T, H, E, k, I, sh, bias, seed = case
+    return Layer(synth.Shape(T=T, H=H, E=E, k=k, I=I, has_shared=sh), seed, logit_bias=bias)
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_I{c[4]}_sh{c[5]}")
+def test_small_layers_all_stages(cuda_lib, case):
+    moe = cuda_lib
+    L = _small_layer(case)
+    s = L.shape
+    ms = moe_shape(moe, s)
+    gu, dn = L.gpu_weights(moe)
+    ogu, odn = L.oracle_weights()
+    # quantizer: identical bytes
+    for q, o in ((gu, ogu), (dn, odn)):
+        assert np.array_equal(q.packed.cpu().numpy(), o[0])
+        assert np.array_equal(q.scales.cpu().numpy(), o[1])
+        assert np.array_equal(q.scale2.cpu().numpy(), o[2])
+    x, logits = L.x.cuda(), L.logits.cuda()
+    ws = moe.workspace(ms)
+    # route
+    ids, w = moe.route_topk(logits, ms)
+    oids, ow = oracle.route(L.logits, s.k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+    # permute
+    counts, offsets, sorted_slot, slot_pos = moe.permute(ids, ms, ws)
+    oc, oo, oss, osp = oracle.permute(oids, s.E)
+    assert np.array_equal(counts.cpu().numpy(), oc)
+    assert np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(sorted_slot.cpu().numpy(), oss)
+    assert np.array_equal(slot_pos.cpu().numpy(), osp)
+    # stages vs the oracle's dumps
+    out_ref, h_ref, y_ref = oracle.moe_forward(L.x, L.logits, ogu, odn, s.k, s.has_shared, dumps=True)
+    h = moe.grouped_gate_up(x, sorted_slot, offsets, gu, ms, ws)
+    y = moe.grouped_down(h, offsets, dn, ms, ws)
+    S = s.T * s.k
+    slot_of_row = oss  # routed row p holds slot oss[p] = t*k + j
+    t_of, j_of = slot_of_row // s.k, slot_of_row % s.k
+    check_layer_close(to_np(h[:S]), h_ref[t_of, j_of], "h routed")
+    check_layer_close(to_np(y[:S]), y_ref[t_of, j_of], "y routed")
+    if s.has_shared:
+        check_layer_close(to_np(h[S:]), h_ref[:, s.k], "h shared")
+        check_layer_close(to_np(y[S:]), y_ref[:, s.k], "y shared")
+    for fp32 in (False, True):
+        out = moe.combine(y, slot_pos, w, ms, out_fp32=fp32)
+        check_layer_close(to_np(out), out_ref, f"combine fp32={fp32}")
+    # the fused forward, both output types
+    for fp32 in (False, True):
+        out = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=fp32)
+        check_layer_close(to_np(out), out_ref, f"forward fp32={fp32}")
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+
+
+def test_forward_deterministic_and_matches_stages(cuda_lib):
+    moe = cuda_lib
+    for case in (SMALL[2], SMALL[5]):
+        L = _small_layer(case)
+        ms = moe_shape(moe, L.shape)
+        gu, dn = L.gpu_weights(moe)
+        x, logits = L.x.cuda(), L.logits.cuda()
+        ws = moe.workspace(ms)
+        a = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
+        b = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
+        assert torch.equal(a, b)
+
+
+def test_route_edge_rows(cuda_lib):
+    moe = cuda_lib
+    E, k = 16, 4
+    l = np.random.default_rng(3).standard_normal((9, E)).astype(np.float32)
+    l[0] = 1.0                                  # all tied: lowest indices win
+    l[1] = np.nan                               # all NaN: weights 0
+    l[2] = -np.inf
+    l[3, ::2] = np.nan                          # NaN never wins
+    l[4, [3, 9]] = np.inf                       # two +inf share the mass
+    l[5, :] = 0.0
+    l[5, 7] = -0.0                              # -0 ties +0
+    l[6, :] = np.float32(2.0)
+    l[6, 5] = np.float32(2.0000002)             # one ulp above the tie
+    l[7, :k] = -np.inf                          # -inf are ranked last among finite
+    l[8] = np.arange(E)[::-1].astype(np.float32)
+    ms = moe.Shape(T=9, H=128, I=128, E=E, k=k)
+    ids, w = moe.route_topk(torch.from_numpy(l).cuda(), ms)
+    oids, ow = oracle.route(l, k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+
+
+def test_empty_batch_is_a_noop(cuda_lib):
+    moe = cuda_lib
+    L = _small_layer(SMALL[0])
+    gu, dn = L.gpu_weights(moe)
+    ms = moe.Shape(T=0, H=256, I=128, E=16, k=2)
+    ws = moe.workspace(moe.Shape(T=1, H=256, I=128, E=16, k=2))
+    x = torch.zeros(1, 256, dtype=torch.bfloat16, device="cuda")
+    lg = torch.zeros(1, 16, device="cuda")
+    out = torch.full((1, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe.forward(x, lg, gu, dn, ms, ws, out=out)
+    torch.cuda.synchronize()
+    assert (out == 7.0).all()
+
+
+# --------------------------------------------------------------------------- full sizes
+
+def _full_case(w: synth.Workload, T, seed, layer=0, n_sample=None, rng_seed=0):
+    shape = w.shape(T)
+    L = Layer(shape, synth.layer_seed(w, seed, layer), layer=0, logit_bias=w.logit_bias,
+              outlier_frac=w.outlier_frac, gen_device="cuda")
+    return L
+
+
+def _check_full(moe, L, tokens):
+    s = L.shape
+    ms = moe_shape(moe, s)
+    gu, dn = L.gpu_weights(moe)
+    x, logits = L.x, L.logits
+    ws = moe.workspace(ms)
+    out = moe.forward(x, logits, gu, dn, ms, ws)
+    ids, w = moe.route_topk(logits, ms)
+    oids, ow = oracle.route(logits.cpu(), s.k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+    counts, offsets, sorted_slot, slot_pos = moe.permute(ids, ms, ws)
+    oc, oo, oss, osp = oracle.permute(oids, s.E)
+    assert np.array_equal(counts.cpu().numpy(), oc)
+    assert np.array_equal(offsets.cpu().numpy(), oo)
+    assert np.array_equal(sorted_slot.cpu().numpy(), oss)
+    assert np.array_equal(slot_pos.cpu().numpy(), osp)
+    groups = L.used_groups(tokens)
+    ogu, odn = L.oracle_weights(groups)
+    for q, o in ((gu, ogu), (dn, odn)):
+        gi = torch.tensor(groups, device="cuda")
+        assert np.array_equal(q.packed[gi].cpu().numpy(), o[0][groups])
+        assert np.array_equal(q.scales[gi].cpu().numpy(), o[1][groups])
+        assert np.array_equal(q.scale2[gi].cpu().numpy(), o[2][groups])
+    ref = oracle.moe_forward(x.cpu(), logits.cpu(), ogu, odn, s.k, s.has_shared, tokens=tokens)
+    check_layer_close(to_np(out[torch.tensor(tokens, device="cuda")]), ref, "forward sampled rows")
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+
+
+@pytest.mark.parametrize("T,seed", list(zip(synth.WORKLOADS["decode"].Ts, synth.WORKLOADS["decode"].seeds)))
+def test_decode_sweep_full_size(cuda_lib, T, seed):
+    L = _full_case(synth.WORKLOADS["decode"], T, seed)
+    _check_full(cuda_lib, L, list(range(T)))
+
+
+def test_batched_decode_full_size(cuda_lib):
+    w = synth.WORKLOADS["batched"]
+    L = _full_case(w, 64, w.seeds[0])
+    _check_full(cuda_lib, L, [0, 5, 17, 31, 40, 63])
+
+
+def test_prefill_chunk_full_size(cuda_lib):
+    w = synth.WORKLOADS["prefill"]
+    L = _full_case(w, 4096, w.seeds[0])
+    outliers = torch.nonzero(L.x.float().abs().amax(1) > 8).flatten().tolist()
+    assert len(outliers) >= 30
+    _check_full(cuda_lib, L, [0, 1, 2047, 4095] + outliers[:3])
+
+
+@pytest.mark.parametrize("layer", [0, 3])
+def test_long_prefill_full_size(cuda_lib, layer):
+    w = synth.WORKLOADS["long"]
+    L = _full_case(w, 32768, w.seeds[0], layer=layer)
+    _check_full(cuda_lib, L, [0, 12345, 32767])
