@@ -149,8 +149,9 @@ def workspace_size(shape: Shape) -> int:
 
 
 def workspace(shape: Shape, device="cuda") -> torch.Tensor:
-    """A workspace buffer for `shape` (uint8, 256-byte aligned as torch allocates)."""
-    return torch.empty(workspace_size(shape), dtype=torch.uint8, device=device)
+    """A zero-filled workspace buffer for `shape` (uint8, 256-byte aligned as torch allocates).
+    Zero-filling clears the device status word the library keeps in its first bytes."""
+    return torch.zeros(workspace_size(shape), dtype=torch.uint8, device=device)
 
 
 def quantize_nvfp4(w: torch.Tensor, stream=None) -> NVFP4Weights:

@@ -92,7 +92,30 @@ Ws carve(void* ws, const moe_shape_t& s) {
   return r;
 }
 
-int tile_rows_for(const moe_shape_t& s) { return s.T <= kDecodeMaxT ? kDecodeMaxT : kSimtTileRows; }
+// Arm of a shape: the grouped-GEMV decode arm for small T; above it the tcgen05 grouped GEMM
+// when H and I are multiples of 256, else the CUDA-core grouped GEMM.
+enum class Arm { kDecode, kTc, kSimt };
+
+Arm arm_for(const moe_shape_t& s) {
+  if (s.T <= kDecodeMaxT) return Arm::kDecode;
+  return tc_supported(s) ? Arm::kTc : Arm::kSimt;
+}
+
+int tile_rows_for(const moe_shape_t& s) {
+  switch (arm_for(s)) {
+    case Arm::kDecode: return kDecodeMaxT;
+    case Arm::kTc: return kTcTileRows;
+    default: return kSimtTileRows;
+  }
+}
+
+cudaError_t launch_gate_up(const GroupedArgs& a, const moe_shape_t& s, cudaStream_t cs) {
+  return arm_for(s) == Arm::kTc ? launch_gate_up_tc(a, cs) : launch_gate_up_simt(a, cs);
+}
+
+cudaError_t launch_down(const GroupedArgs& a, const moe_shape_t& s, cudaStream_t cs) {
+  return arm_for(s) == Arm::kTc ? launch_down_tc(a, cs) : launch_down_simt(a, cs);
+}
 
 GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, const uint16_t* act,
                          const int32_t* sorted_slot, const Ws& ws, uint16_t* out) {
@@ -112,15 +135,17 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   a.meta = ws.meta;
   a.max_tiles = max_tiles_for(s, tile_rows_for(s));
   a.out = out;
+  a.status = ws.status;
   return a;
 }
 
 }  // namespace
 
+// Work items of a shape: sum_e ceil(c_e / R) <= S / R + (number of non-empty experts), and the
+// shared expert adds ceil(T / R).
 int64_t max_tiles_for(const moe_shape_t& s, int tile_rows) {
   const int64_t S = static_cast<int64_t>(s.T) * s.k;
-  int64_t routed = S / tile_rows + s.E;
-  if (tile_rows >= s.T) routed = std::min<int64_t>(routed, std::min<int64_t>(S, s.E));
+  const int64_t routed = S / tile_rows + std::min<int64_t>(S, s.E);
   const int64_t shared = s.has_shared ? (s.T + tile_rows - 1) / tile_rows : 0;
   return std::max<int64_t>(1, routed + shared);
 }
@@ -217,9 +242,9 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
   const moe_shape_t& s = *shape;
   Ws w = carve(ws, s);
   cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
-                                     w.tiles, w.meta, cs);
+                                     w.tiles, w.meta, w.status, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_gate_up_simt(grouped_args(*gate_up, s, x, sorted_slot, w, h), cs));
+  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, cs));
 }
 
 moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
@@ -236,9 +261,9 @@ moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
   const moe_shape_t& s = *shape;
   Ws w = carve(ws, s);
   cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
-                                     w.tiles, w.meta, cs);
+                                     w.tiles, w.meta, w.status, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_down_simt(grouped_args(*down, s, h, nullptr, w, y), cs));
+  return cuda_status(launch_down(grouped_args(*down, s, h, nullptr, w, y), s, cs));
 }
 
 moe_status_t moe_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w,
@@ -251,7 +276,7 @@ moe_status_t moe_combine(const uint16_t* y, const int32_t* slot_pos, const float
   if (shape->T == 0) return MOE_OK;
   if ((st = check_arch()) != MOE_OK) return st;
   return cuda_status(launch_combine(y, slot_pos, topk_w, shape->T, shape->H, shape->k,
-                                    shape->has_shared, out, out_is_fp32,
+                                    shape->has_shared, out, out_is_fp32, nullptr,
                                     static_cast<cudaStream_t>(stream)));
 }
 
@@ -316,6 +341,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     d.has_shared = s.has_shared;
     d.out = out;
     d.out_is_fp32 = out_is_fp32;
+    d.status = w.status;
     e = launch_down_combine_gemv(d, cs);
     if (e == cudaSuccess) e = mark(3);
     if (e == cudaSuccess) e = mark(4);
@@ -327,16 +353,17 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     e = launch_permute_large(w.ids, s.T, s.E, s.k, w.counts, w.offsets, w.sorted_slot, w.slot_pos,
                              w.hist, w.L.n_chunks, cs);
   if (e == cudaSuccess)
-    e = launch_build_tiles(w.offsets, s.T, s.E, s.k, s.has_shared, kSimtTileRows, w.tiles, w.meta,
-                           cs);
+    e = launch_build_tiles(w.offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s), w.tiles,
+                           w.meta, w.status, cs);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
-    e = launch_gate_up_simt(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), cs);
+    e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, cs);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess) e = launch_down_simt(grouped_args(*down, s, w.h, nullptr, w, w.y), cs);
+  if (e == cudaSuccess) e = launch_down(grouped_args(*down, s, w.h, nullptr, w, w.y), s, cs);
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
-    e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, cs);
+    e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32,
+                       w.status, cs);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }

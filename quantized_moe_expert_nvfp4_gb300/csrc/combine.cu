@@ -21,7 +21,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const int32_t* __restrict__ slot_pos,
                                                       const float* __restrict__ topk_w, int T,
                                                       int H, int k, int has_shared, void* out,
-                                                      int out_is_fp32) {
+                                                      int out_is_fp32, int32_t* status) {
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int cpr = H / 8;
   if (idx >= static_cast<int64_t>(T) * cpr) return;
@@ -32,7 +32,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
   for (int j = 0; j < k; ++j) {
-    const int64_t p = __ldg(slot_pos + static_cast<int64_t>(t) * k + j);
+    int64_t p = __ldg(slot_pos + static_cast<int64_t>(t) * k + j);
+    if (p < 0 || p >= S) {  // caller-provided index
+      if (status) report_device_error(status, kDevBadIndex);
+      p = 0;
+    }
     const float wj = __ldg(topk_w + static_cast<int64_t>(t) * k + j);
     float v[8];
     unpack8(__ldg(reinterpret_cast<const uint4*>(y + p * H + c)), v);
@@ -64,11 +68,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
-                           cudaStream_t st) {
+                           int32_t* status, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(T) * (H / 8);
   const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
   combine_kernel<<<blocks, 256, 0, st>>>(y, slot_pos, topk_w, T, H, k, has_shared, out,
-                                         out_is_fp32);
+                                         out_is_fp32, status);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,559 @@
+// Grouped NVFP4 x bf16 GEMM on the fifth-generation tensor cores (tcgen05) -- the prefill arm.
+//
+// W4A16 as in the untransposed column of the "long-context cold prefill to SGLang parity"
+// issue's kernel table (bf16 MMA, f32 accumulation, scale2 and SiLU(gate)*up in an fp32
+// epilogue), computed over the resident [N, K/2] weight layout the same issue prices ("MoE FP4
+// MMA over the resident decode layout, no dequant pass, no transpose").
+//
+// Swap-AB: the MMA's M dimension is 128 weight rows of one expert, N is up to 128 of that
+// expert's tokens, so a small expert group still fills M.  Per CTA (one per SM, persistent):
+//   warp 0      TMA producer: packed e2m1 tiles (and, for down, the bf16 activation tile)
+//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, A from TMEM, B from SMEM
+//   warps 2-5   dequant: one weight row per thread, e2m1 x e4m3 -> bf16 exactly (every
+//               product fits bf16), written to TMEM with tcgen05.st as the A operand
+//   warps 6-9   gate_up only: gather of the expert's token rows of x into 128B-swizzled SMEM
+//   warps 10-13 epilogue: tcgen05.ld of the fp32 accumulator, x scale2, SiLU(gate)*up (gate_up)
+// The accumulator is double-buffered in TMEM so the epilogue of one tile overlaps the next
+// tile's main loop.  Dequantizing into TMEM rather than SMEM leaves the shared-memory bandwidth
+// to the B operand.  Every mbarrier wait is bounded; on timeout the kernel records
+// MOE_ERR_DEVICE_TIMEOUT in the workspace status word and winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;                      // weight rows per tile (MMA M)
+constexpr int kBN = kTcTileRows;              // tokens per tile (MMA N, rounded up to 16)
+constexpr int kBK = 64;                       // K per stage
+constexpr int kStages = 6;
+constexpr int kAStageBytes = kBM * kBK / 2;   // packed e2m1 tile: 128 rows x 32 B
+constexpr int kBStageBytes = kBN * kBK * 2;   // bf16 tile: 128 rows x 128 B (128B swizzle)
+constexpr int kTmemCols = 512;
+constexpr int kDCol = 0;                      // accumulators: 2 x 128 columns
+constexpr int kACol = 2 * kBN;                // A stages: kStages x 32 columns
+static_assert(kACol + kStages * (kBK / 2) <= kTmemCols, "TMEM budget");
+
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpGather = 6, kWarpEpi = 10;
+constexpr int kThreads = 14 * 32;
+constexpr uint32_t kSpinLimit = 1u << 24;      // drain loops only
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: no legitimate wait comes close
+
+struct TcArgs {
+  const uint8_t* scales;
+  const float* scale2;
+  int Nw, K;                    // weight rows per group, reduction length
+  const uint16_t* act;          // x [T, H] (gate_up gather source)
+  const int32_t* sorted_slot;
+  int T, k, S;
+  const int4* tiles;
+  const int32_t* meta;
+  uint16_t* out;                // h [S + T, I] or y [S + T, H]
+  int out_ld;
+  int32_t* status;
+};
+
+struct Smem {
+  uint64_t a_tma_full[kStages];
+  uint64_t a_full[kStages];
+  uint64_t b_full[kStages];
+  uint64_t stage_free[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the CTA is aborting (another role timed out) or this wait timed out.
+// The warp_ variant gives every lane of the warp the same answer, as the .sync.aligned tcgen05
+// instructions that follow it need the whole warp converged.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Smem* sm, int32_t* status) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitTimeoutNs) {
+        report_device_error(status, kDevTimeout);
+        *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, Smem* sm, int32_t* status) {
+  const bool ok = mbar_wait(b, parity, sm, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(b))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// K-major bf16 operand in SMEM, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor: D f32, A bf16, B bf16, both K-major, M = 128, N.
+__device__ __forceinline__ uint32_t make_idesc(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+#define TC_ST32(taddr, r)                                                                          \
+  asm volatile(                                                                                    \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),           \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),      \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), \
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),          \
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),          \
+      "r"(r[30]), "r"(r[31])                                                                       \
+      : "memory")
+
+#define TC_LD16(taddr, v)                                                                          \
+  asm volatile(                                                                                    \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}," \
+      " [%16];"                                                                                    \
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),       \
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),   \
+        "=r"(v[14]), "=r"(v[15])                                                                   \
+      : "r"(taddr)                                                                                 \
+      : "memory")
+
+// Eight e2m1 codes (one 32-bit word, element i in bits 4i..4i+3) times the block scale ->
+// four bf16x2 words.  e2m1 -> f16 is the hardware conversion, the product with the e4m3 scale
+// is exact in f16 (at most 6 significant bits, |v| in [2^-10, 2688]), and the f16 -> bf16 step
+// is exact for such values.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t scale_f16x2, uint32_t* o) {
+  uint32_t h[4];
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+  const __half2 s = *reinterpret_cast<const __half2*>(&scale_f16x2);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&h[i]), s);
+    const __nv_bfloat162 b = __float22bfloat162_rn(__half22float2(p));
+    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+}
+
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_splat(uint32_t byte) {
+  const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3);
+  const uint32_t h = hr.x;
+  return h | (h << 16);
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           TcArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;                                  // kStages x 4 KB
+  uint8_t* sB = base + kStages * kAStageBytes;         // kStages x 16 KB (1024-aligned)
+  Smem* sm = reinterpret_cast<Smem*>(sB + kStages * kBStageBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int MB = a.Nw / kBM;                           // m-blocks per group
+  const int KS = a.K / kBK;                            // K stages per item
+  const int n_items = __ldg(a.meta) * MB;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm->a_tma_full[s], 1);
+      mbar_init(&sm->a_full[s], 128);
+      mbar_init(&sm->b_full[s], kGateUp ? 128 : 1);
+      mbar_init(&sm->stage_free[s], 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&sm->acc_full[d], 1);
+      mbar_init(&sm->acc_empty[d], 128);
+    }
+    mbar_init(&sm->drain, 1);
+    sm->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kWarpTma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sm->tmem_base)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm->tmem_base;
+
+  if (warp == kWarpTma) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int4 td = __ldg(a.tiles + item / MB);
+        const int mb = item % MB;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int st = it % kStages;
+          if (!(ok = mbar_wait(&sm->stage_free[st], ((it / kStages) & 1) ^ 1, sm, a.status))) break;
+          uint8_t* dA = sA + st * kAStageBytes;
+          mbar_expect_tx(&sm->a_tma_full[st], kAStageBytes);
+          if (kGateUp) {
+            const int I = a.Nw / 2;
+            const int r0 = td.x * a.Nw + mb * 64;
+            tma_load_2d(dA, &tmA, ks * (kBK / 2), r0, &sm->a_tma_full[st]);
+            tma_load_2d(dA + 64 * (kBK / 2), &tmA, ks * (kBK / 2), r0 + I, &sm->a_tma_full[st]);
+          } else {
+            tma_load_2d(dA, &tmA, ks * (kBK / 2), td.x * a.Nw + mb * kBM, &sm->a_tma_full[st]);
+            mbar_expect_tx(&sm->b_full[st], kBStageBytes);
+            tma_load_2d(sB + st * kBStageBytes, &tmB, ks * kBK, td.y, &sm->b_full[st]);
+          }
+        }
+      }
+      if (!ok) {  // let copies already issued land before the CTA winds down
+        for (int j = 0; j < kStages && it > 0; ++j, --it) {
+          const uint32_t q = it - 1;
+          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->a_tma_full[q % kStages], (q / kStages) & 1); ++i) {
+          }
+        }
+      }
+    }
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      uint32_t it = 0, ic = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+        const int4 td = __ldg(a.tiles + item / MB);
+        const int n = (td.z + 15) & ~15;
+        const uint32_t idesc = make_idesc(n);
+        const int d = ic & 1;
+        if (!(ok = mbar_wait(&sm->acc_empty[d], ((ic >> 1) & 1) ^ 1, sm, a.status))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + kDCol + d * kBN;
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int st = it % kStages;
+          const uint32_t par = (it / kStages) & 1;
+          if (!(ok = mbar_wait(&sm->a_full[st], par, sm, a.status))) break;
+          if (!(ok = mbar_wait(&sm->b_full[st], par, sm, a.status))) break;
+          tc_fence_after();
+          const uint32_t b_addr = smem_u32(sB + st * kBStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma(d_tmem, tmem + kACol + st * (kBK / 2) + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
+                   (ks | kk) != 0);
+          tc_commit(&sm->stage_free[st]);
+        }
+        if (ok) tc_commit(&sm->acc_full[d]);
+      }
+      // every MMA issued must have completed before TMEM is released (bounded)
+      tc_commit(&sm->drain);
+      for (uint32_t i = 0; i < kSpinLimit && !mbar_try(&sm->drain, 0); ++i) {
+      }
+    }
+  } else if (warp >= kWarpDeq && warp < kWarpDeq + 4) {
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int r = q * 32 + lane;            // tile row == TMEM lane
+    int srow;                               // SMEM row of the packed tile
+    int wrow_off;                           // weight row within the group, relative to the m-block
+    if (kGateUp) {
+      const int half = lane >> 4, j = q * 16 + (lane & 15);
+      srow = half * 64 + j;
+      wrow_off = j + half * (a.Nw / 2);
+    } else {
+      srow = r;
+      wrow_off = r;
+    }
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const int4 td = __ldg(a.tiles + item / MB);
+      const int mb = item % MB;
+      const int64_t wrow = static_cast<int64_t>(td.x) * a.Nw + (kGateUp ? mb * 64 : mb * kBM) + wrow_off;
+      const uint8_t* srow_scales = a.scales + wrow * (a.K / 16);
+      uint4 sc = make_uint4(0, 0, 0, 0);
+      for (int ks = 0; ks < KS; ++ks, ++it) {
+        const int st = it % kStages;
+        if ((ks & 3) == 0) sc = __ldg(reinterpret_cast<const uint4*>(srow_scales + (ks >> 2) * 16));
+        if (!(ok = warp_wait(&sm->a_tma_full[st], (it / kStages) & 1, sm, a.status))) break;
+        const uint8_t* rowp = sA + st * kAStageBytes + srow * 32;
+        const int sw = (srow >> 2) & 1;     // 32-byte swizzle: 16-byte chunk index ^= row bit 2
+        const uint4 p0 = *reinterpret_cast<const uint4*>(rowp + ((0 ^ sw) << 4));
+        const uint4 p1 = *reinterpret_cast<const uint4*>(rowp + ((1 ^ sw) << 4));
+        const uint32_t scw = (&sc.x)[ks & 3];   // 4 scale bytes: blocks of 16 k of this stage
+        uint32_t o[32];
+        const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint32_t s2 = e4m3_to_f16x2_splat((scw >> (8 * b)) & 0xffu);
+          dequant8(pw[2 * b], s2, o + 8 * b);
+          dequant8(pw[2 * b + 1], s2, o + 8 * b + 4);
+        }
+        __syncwarp();
+        TC_ST32(t_lane + kACol + st * (kBK / 2), o);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        mbar_arrive(&sm->a_full[st]);
+      }
+    }
+  } else if (warp >= kWarpGather && warp < kWarpGather + 4) {
+    if (kGateUp) {
+      const int t = threadIdx.x - kWarpGather * 32;   // 0..127
+      const int c = t & 7;                            // 16-byte chunk of a 128-byte row
+      uint32_t it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int4 td = __ldg(a.tiles + item / MB);
+        int64_t src[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int row = (t >> 3) + 16 * i;
+          src[i] = -1;
+          if (row < td.z) {
+            const int p = td.y + row;
+            int tok;
+            if (p < a.S) {
+              int slot = __ldg(a.sorted_slot + p);
+              if (static_cast<unsigned>(slot) >= static_cast<unsigned>(a.S)) {
+                report_device_error(a.status, kDevBadIndex);
+                slot = 0;
+              }
+              tok = slot / a.k;
+            } else {
+              tok = p - a.S;
+            }
+            src[i] = static_cast<int64_t>(tok) * a.K + c * 8;
+          }
+        }
+        for (int ks = 0; ks < KS; ++ks, ++it) {
+          const int st = it % kStages;
+          if (!(ok = mbar_wait(&sm->stage_free[st], ((it / kStages) & 1) ^ 1, sm, a.status))) break;
+          uint8_t* dB = sB + st * kBStageBytes;
+          uint4 v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            v[i] = (src[i] >= 0) ? __ldg(reinterpret_cast<const uint4*>(a.act + src[i] + ks * kBK))
+                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = (t >> 3) + 16 * i;
+            *reinterpret_cast<uint4*>(dB + row * 128 + ((c ^ (row & 7)) << 4)) = v[i];
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&sm->b_full[st]);
+        }
+      }
+    }
+  } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+    const int q = warp & 3;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t ic = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+      const int4 td = __ldg(a.tiles + item / MB);
+      const int mb = item % MB;
+      const int d = ic & 1;
+      if (!(ok = warp_wait(&sm->acc_full[d], (ic >> 1) & 1, sm, a.status))) break;
+      tc_fence_after();
+      const float s2 = __ldg(a.scale2 + td.x);
+      const int n = (td.z + 15) & ~15;
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        TC_LD16(t_lane + kDCol + d * kBN + c0, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (kGateUp) {
+          // lanes 0-15: gate rows j, lanes 16-31: up rows j (j = mb*64 + 16q + lane%16)
+          uint32_t pv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pv[i] = __shfl_xor_sync(0xffffffffu, v[i], 16);
+          const bool is_gate = lane < 16;
+          const int j = mb * 64 + q * 16 + (lane & 15);
+          const int cbase = c0 + (is_gate ? 0 : 8);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int ci = is_gate ? i : 8 + i;
+            const float g = __uint_as_float(is_gate ? v[ci] : pv[ci]) * s2;
+            const float u = __uint_as_float(is_gate ? pv[ci] : v[ci]) * s2;
+            const int col = cbase + i;
+            if (col < td.z)
+              a.out[static_cast<int64_t>(td.y + col) * a.out_ld + j] = f32_to_bf16_bits(silu_f32(g) * u);
+          }
+        } else {
+          const int nrow = mb * kBM + q * 32 + lane;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int col = c0 + i;
+            if (col < td.z)
+              a.out[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =
+                  f32_to_bf16_bits(__uint_as_float(v[i]) * s2);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm->acc_empty[d]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpTma) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr, uint64_t inner,
+                 uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * elem_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + sizeof(Smem);
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <bool kGateUp>
+cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int G = g.E + 1;
+  CUtensorMap tmA, tmB;
+  if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.packed, g.K / 2, static_cast<uint64_t>(G) * g.N,
+                   kBK / 2, kGateUp ? 64 : kBM, CU_TENSOR_MAP_SWIZZLE_32B))
+    return cudaErrorInvalidValue;
+  if (kGateUp) {
+    tmB = tmA;
+  } else if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.act, g.K,
+                          static_cast<uint64_t>(g.S) + g.T, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) {
+    return cudaErrorInvalidValue;
+  }
+  TcArgs a;
+  a.scales = g.scales;
+  a.scale2 = g.scale2;
+  a.Nw = g.N;
+  a.K = g.K;
+  a.act = g.act;
+  a.sorted_slot = g.sorted_slot;
+  a.T = g.T;
+  a.k = g.k;
+  a.S = g.S;
+  a.tiles = g.tiles;
+  a.meta = g.meta;
+  a.out = g.out;
+  a.out_ld = kGateUp ? g.N / 2 : g.N;
+  a.status = g.status;
+  const int64_t items_max = g.max_tiles * (g.N / kBM);
+  const int grid = static_cast<int>(std::min<int64_t>(items_max, sm_count()));
+  grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supported(const moe_shape_t& s) { return s.H % 256 == 0 && s.I % 256 == 0 && s.H <= 16384; }
+
+cudaError_t launch_gate_up_tc(const GroupedArgs& a, cudaStream_t st) { return launch_tc<true>(a, st); }
+cudaError_t launch_down_tc(const GroupedArgs& a, cudaStream_t st) { return launch_tc<false>(a, st); }
+
+}  // namespace moe

@@ -64,7 +64,13 @@ __device__ __forceinline__ void warp_allreduce(float (&acc)[R][TB]) {
 // (shared); down reads h[p].
 __device__ __forceinline__ int64_t act_row(const GroupedArgs& a, bool gate_up, int p) {
   if (!gate_up) return p;
-  return (p < a.S) ? (a.sorted_slot[p] / a.k) : (p - a.S);
+  if (p >= a.S) return p - a.S;
+  int slot = __ldg(a.sorted_slot + p);
+  if (static_cast<unsigned>(slot) >= static_cast<unsigned>(a.S)) {  // caller-provided index
+    report_device_error(a.status, kDevBadIndex);
+    slot = 0;
+  }
+  return slot / a.k;
 }
 
 // R weight rows (wrow) x TB permuted rows starting at p0 (nt of them live) for one warp.
@@ -218,7 +224,11 @@ __global__ void __launch_bounds__(256) down_combine_gemv_kernel(DownCombineArgs 
     const int t = idx / kDcRows, r = idx % kDcRows;
     float s = 0.0f;
     for (int j = 0; j < a.k; ++j) {
-      const int p = __ldg(a.slot_pos + t * a.k + j);
+      int p = __ldg(a.slot_pos + t * a.k + j);
+      if (static_cast<unsigned>(p) >= static_cast<unsigned>(a.S)) {
+        report_device_error(a.status, kDevBadIndex);
+        p = 0;
+      }
       s = fmaf(__ldg(a.topk_w + t * a.k + j), ybuf[p * kDcRows + r], s);
     }
     if (a.has_shared) s += ybuf[(a.S + t) * kDcRows + r];

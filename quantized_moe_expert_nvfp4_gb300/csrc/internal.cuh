@@ -17,6 +17,7 @@ constexpr int kMaxE = 1024;
 constexpr int kDecodeMaxT = 64;        // moe_forward uses the grouped-GEMV arm up to this T
 constexpr int kSimtTileRows = 64;      // rows per work item of the SIMT grouped GEMM
 constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutation
+constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 grouped GEMM
 
 // ------------------------------------------------------------------ workspace layout
 // All offsets are in bytes from the workspace base and 256-byte aligned.
@@ -41,7 +42,12 @@ struct WsLayout {
 WsLayout ws_layout(const moe_shape_t& s);
 int64_t max_tiles_for(const moe_shape_t& s, int tile_rows);
 
-enum DeviceError : int32_t { kDevOk = 0, kDevTimeout = MOE_ERR_DEVICE_TIMEOUT };
+// Codes a kernel writes into the workspace status word (first error wins).
+enum DeviceError : int32_t {
+  kDevOk = 0,
+  kDevBadIndex = MOE_ERR_INVALID_ARG,   // an index array (offsets, sorted_slot, slot_pos) out of range
+  kDevTimeout = MOE_ERR_DEVICE_TIMEOUT
+};
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
@@ -96,8 +102,11 @@ cudaError_t launch_permute_large(const int32_t* ids, int T, int E, int k, int32_
                                  int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
                                  int32_t* hist, int64_t n_chunks, cudaStream_t st);
 // Work list from offsets: one item per (group, run of <= tile_rows rows).
+// Offsets that are not a valid exclusive prefix (offsets[0] = 0, non-decreasing, offsets[E] = S)
+// produce no routed work and record kDevBadIndex.
 cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,
-                               int tile_rows, int4* tiles, int32_t* meta, cudaStream_t st);
+                               int tile_rows, int4* tiles, int32_t* meta, int32_t* status,
+                               cudaStream_t st);
 
 struct GroupedArgs {
   const uint8_t* packed;
@@ -111,9 +120,14 @@ struct GroupedArgs {
   const int32_t* meta;
   int64_t max_tiles;
   uint16_t* out;                // h [S + T, I] or y [S + T, H]
+  int32_t* status;              // device status word (bad indices are clamped and reported)
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
+// tcgen05 grouped GEMM (work items from a tile list built with kTcTileRows rows).
+bool tc_supported(const moe_shape_t& s);
+cudaError_t launch_gate_up_tc(const GroupedArgs& a, cudaStream_t st);
+cudaError_t launch_down_tc(const GroupedArgs& a, cudaStream_t st);
 
 struct DownCombineArgs {
   const uint8_t* packed;
@@ -129,12 +143,14 @@ struct DownCombineArgs {
   int has_shared;
   void* out;
   int out_is_fp32;
+  int32_t* status;
 };
 cudaError_t launch_down_combine_gemv(const DownCombineArgs& a, cudaStream_t st);
 
+// status may be NULL (bad slot positions are then clamped silently).
 cudaError_t launch_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
-                           cudaStream_t st);
+                           int32_t* status, cudaStream_t st);
 
 cudaError_t launch_quantize(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,
                             uint8_t* scales, float* scale2, cudaStream_t st);

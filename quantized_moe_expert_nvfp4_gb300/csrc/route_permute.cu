@@ -309,16 +309,27 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const int32_t* __r
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
                                                            int T, int E, int k, int has_shared,
                                                            int tile_rows, int4* __restrict__ tiles,
-                                                           int32_t* __restrict__ meta) {
+                                                           int32_t* __restrict__ meta,
+                                                           int32_t* __restrict__ status) {
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE];
   __shared__ int s_warp[32];
+  __shared__ int s_bad;
+  const int S = T * k;
+  if (threadIdx.x == 0) s_bad = (offsets[0] != 0 || offsets[E] != S);
+  __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     s_off[e] = offsets[e];
     s_cnt[e] = offsets[e + 1] - offsets[e];
+    if (s_cnt[e] < 0) s_bad = 1;
   }
   __syncthreads();
-  write_tiles_block(E, T * k, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+  if (s_bad) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
+    if (threadIdx.x == 0) report_device_error(status, kDevBadIndex);
+  }
+  __syncthreads();
+  write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
 }
 
 }  // namespace
@@ -359,8 +370,10 @@ cudaError_t launch_permute_large(const int32_t* ids, int T, int E, int k, int32_
 }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,
-                               int tile_rows, int4* tiles, int32_t* meta, cudaStream_t st) {
-  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, T, E, k, has_shared, tile_rows, tiles, meta);
+                               int tile_rows, int4* tiles, int32_t* meta, int32_t* status,
+                               cudaStream_t st) {
+  build_tiles_kernel<<<1, 1024, 0, st>>>(offsets, T, E, k, has_shared, tile_rows, tiles, meta,
+                                         status);
   return cudaGetLastError();
 }
 

@@ -26,6 +26,11 @@ SMALL = [
     (300, 256, 16, 16, 128, 0, "none", 106),
     (3000, 256, 64, 8, 128, 1, "normal", 107),
     (16, 128, 1024, 16, 128, 1, "none", 108),
+    # tcgen05 arm (T > 64, H and I multiples of 256): ragged token tiles, several tiles per
+    # expert, no shared expert, the N tail of a single 16-column step
+    (129, 256, 8, 2, 256, 0, "none", 109),
+    (1000, 512, 64, 8, 256, 1, "zipf", 110),
+    (700, 1024, 32, 6, 512, 1, "normal", 111),
 ]
 
 
