@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--workload", default="decode", choices=list(synth.WORKLOADS))
     p.add_argument("--pool", type=int, default=None, help="distinct input batches cycled through")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--warmup-seconds", type=float, default=2.0,
+                   help="keep warming up (whole steps) at least this long, for steady clocks")
     return p.parse_args()
 
 
@@ -289,6 +291,10 @@ def run_ours(args):
     def new_events():
         return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in layers]
     events = [[new_events() for _ in range(pool)] for _ in range(2)]
+    with torch.cuda.stream(stream):   # torch creates an event's handle on its first record
+        for ev in (e for b in events for p in b for L_ in p for e in L_):
+            ev.record(stream)
+    stream.synchronize()
     graphs = [[None] * pool for _ in range(2)]
     with torch.cuda.stream(stream):
         for p in range(pool):  # one eager pass per batch before capture
@@ -343,7 +349,7 @@ def run_ours(args):
         with torch.cuda.stream(stream):
             t_w = time.perf_counter()
             i = 0
-            while i < warmup or time.perf_counter() - t_w < 2.0:   # >= W steps and >= 2 s under load
+            while i < warmup or time.perf_counter() - t_w < args.warmup_seconds:
                 run_steps(pool, timed=False)
                 i += pool
             stream.synchronize()
@@ -439,6 +445,8 @@ def run_ours(args):
                 "gpu_launches": steps * len(layers) * launches_per_forward,
                 "clocks": clk.summary(),
                 "stages_ms_per_step": {stage_names[s]: tot_stage[s] / steps for s in range(4)},
+                "stages_us_per_forward": {f"T={L['T']}": [round(1e3 * stage_ms[li][s] / steps, 2) for s in range(4)]
+                                          for li, L in enumerate(layers)},
                 "forward_hbm_gbs": fwd_bytes / (sum(tot_stage) / 1e3) / 1e9,
                 "distinct_experts_mean": [float(np.mean(L["uniq"])) for L in layers]}
         if world == 1 and not args.no_cpu_baseline:

@@ -38,8 +38,11 @@
  *  gate_up: N = 2I, K = H (rows 0..I-1 are gate, rows I..2I-1 are up).  down: N = H, K = I.
  *
  * Row conventions of the staged tensors: S = T*k slots, slot s = t*k + j for rank j of
- * token t.  h [S+T, I] and y [S+T, H] hold the routed slots in permuted order (row p is slot
- * sorted_slot[p]) followed by one shared-expert row per token (row S + t).
+ * token t.  h [S+T, I] (bf16) and y [S+T, H] (fp32) hold the routed slots in permuted order
+ * (row p is slot sorted_slot[p]) followed by one shared-expert row per token (row S + t).
+ * h is bf16 because the issue's table fixes the SiLU intermediate as bf16; the expert outputs y
+ * feed an fp32 weighted sum and are kept in fp32 (rounding them to bf16 before the combine
+ * costs up to ~2.5% of a row's RMS in the worst element).
  */
 #ifndef MOE_NVFP4_H
 #define MOE_NVFP4_H
@@ -114,18 +117,18 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
                                  const moe_shape_t* shape, uint16_t* h, void* ws, size_t ws_bytes,
                                  void* stream);
 
-/* Grouped down GEMM (the issue's pointer-table grouped GEMM): y[p] = bf16(scale2 * (h[p] .
- * deq(Wd_e)^T)) in fp32 for every routed row p of expert e and, for the shared expert, rows
- * S + t.   h [S + T, I] bf16 -> y [S + T, H] bf16. */
+/* Grouped down GEMM (the issue's pointer-table grouped GEMM): y[p] = scale2 * (h[p] .
+ * deq(Wd_e)^T) accumulated in fp32 for every routed row p of expert e and, for the shared
+ * expert, rows S + t.   h [S + T, I] bf16 -> y [S + T, H] fp32. */
 moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
                               const moe_nvfp4_weights_t* down, const moe_shape_t* shape,
-                              uint16_t* y, void* ws, size_t ws_bytes, void* stream);
+                              float* y, void* ws, size_t ws_bytes, void* stream);
 
 /* fp32 weighted unpermute/combine ("fp32 weighted sum" of the issue's table; fixed summation
  * order as in the expert-parallel discussion of the TensorFold sm_120 issue):
  *   out[t] = (sum_{j=0..k-1} topk_w[t, j] * y[slot_pos[t*k + j]]) + y[S + t]
  * summed in fp32 in exactly that order, then written as bf16 (out_is_fp32 = 0) or fp32. */
-moe_status_t moe_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w,
+moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* topk_w,
                          const moe_shape_t* shape, void* out, int out_is_fp32, void* stream);
 
 /* The whole layer: route, permute, grouped gate_up(+SiLU), grouped down, combine, with the

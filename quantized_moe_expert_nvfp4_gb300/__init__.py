@@ -198,10 +198,10 @@ def grouped_gate_up(x, sorted_slot, offsets, gate_up: NVFP4Weights, shape: Shape
 
 
 def grouped_down(h, offsets, down: NVFP4Weights, shape: Shape, ws, y=None, stream=None):
-    y = y if y is not None else torch.empty(shape.S + shape.T, shape.H, dtype=torch.bfloat16, device=h.device)
+    y = y if y is not None else torch.empty(shape.S + shape.T, shape.H, dtype=torch.float32, device=h.device)
     _check("moe_grouped_down", load().moe_grouped_down(
         _ptr(h, torch.bfloat16, "h"), _ptr(offsets, torch.int32, "offsets"), ctypes.byref(down.c()),
-        ctypes.byref(shape.c()), _ptr(y, torch.bfloat16, "y"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        ctypes.byref(shape.c()), _ptr(y, torch.float32, "y"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
         _stream(stream)))
     return y
 
@@ -210,7 +210,7 @@ def combine(y, slot_pos, topk_w, shape: Shape, out=None, out_fp32: bool = False,
     dt = torch.float32 if out_fp32 else torch.bfloat16
     out = out if out is not None else torch.empty(shape.T, shape.H, dtype=dt, device=y.device)
     _check("moe_combine", load().moe_combine(
-        _ptr(y, torch.bfloat16, "y"), _ptr(slot_pos, torch.int32, "slot_pos"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(y, torch.float32, "y"), _ptr(slot_pos, torch.int32, "slot_pos"), _ptr(topk_w, torch.float32, "topk_w"),
         ctypes.byref(shape.c()), _ptr(out, dt, "out"), int(out_fp32), _stream(stream)))
     return out
 

@@ -69,7 +69,7 @@ struct Ws {
   int4* tiles;
   int32_t* hist;
   uint16_t* h;
-  uint16_t* y;
+  float* y;
   WsLayout L;
 };
 
@@ -88,7 +88,7 @@ Ws carve(void* ws, const moe_shape_t& s) {
   r.tiles = reinterpret_cast<int4*>(b + r.L.tiles);
   r.hist = reinterpret_cast<int32_t*>(b + r.L.hist);
   r.h = reinterpret_cast<uint16_t*>(b + r.L.h);
-  r.y = reinterpret_cast<uint16_t*>(b + r.L.y);
+  r.y = reinterpret_cast<float*>(b + r.L.y);
   return r;
 }
 
@@ -118,7 +118,7 @@ cudaError_t launch_down(const GroupedArgs& a, const moe_shape_t& s, cudaStream_t
 }
 
 GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, const uint16_t* act,
-                         const int32_t* sorted_slot, const Ws& ws, uint16_t* out) {
+                         const int32_t* sorted_slot, const Ws& ws, void* out) {
   GroupedArgs a;
   a.packed = w.packed;
   a.scales = w.scales;
@@ -173,7 +173,7 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.n_chunks = (S + kScatterChunk - 1) / kScatterChunk;
   L.hist = take(4 * static_cast<size_t>(std::max<int64_t>(1, L.n_chunks)) * s.E);
   L.h = take(2 * static_cast<size_t>(R) * s.I);
-  L.y = take(2 * static_cast<size_t>(R) * s.H);
+  L.y = take(4 * static_cast<size_t>(R) * s.H);
   L.total = off;
   return L;
 }
@@ -249,7 +249,7 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
 
 moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
                               const moe_nvfp4_weights_t* down, const moe_shape_t* shape,
-                              uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
+                              float* y, void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (!aligned16(h) || !aligned16(offsets) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
@@ -266,7 +266,7 @@ moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
   return cuda_status(launch_down(grouped_args(*down, s, h, nullptr, w, y), s, cs));
 }
 
-moe_status_t moe_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w,
+moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* topk_w,
                          const moe_shape_t* shape, void* out, int out_is_fp32, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;

@@ -1,4 +1,5 @@
-// fp32 weighted unpermute/combine of the staged path: out[t] = sum_j w[t, j] * y[slot_pos[t*k+j]]
+// fp32 weighted unpermute/combine of the staged path (fp32 expert outputs y):
+// out[t] = sum_j w[t, j] * y[slot_pos[t*k+j]]
 // + y[S + t], accumulated in fp32 in rank order then the shared expert (the "fp32 weighted sum"
 // of the "long-context cold prefill to SGLang parity" issue's kernel table; the fixed order is
 // the one-rank reduction order the TensorFold sm_120 issue requires of expert parallelism).
@@ -7,17 +8,15 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
 // One thread per (token, 8 consecutive hidden columns).
-__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y,
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
                                                       const int32_t* __restrict__ slot_pos,
                                                       const float* __restrict__ topk_w, int T,
                                                       int H, int k, int has_shared, void* out,
@@ -39,13 +38,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     }
     const float wj = __ldg(topk_w + static_cast<int64_t>(t) * k + j);
     float v[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(y + p * H + c)), v);
+    load8(y + p * H + c, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
   }
   if (has_shared) {
     float v[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(y + (S + t) * H + c)), v);
+    load8(y + (S + t) * H + c, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] += v[i];
   }
@@ -66,7 +65,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w, int T,
+cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
                            int32_t* status, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(T) * (H / 8);

@@ -52,7 +52,7 @@ struct TcArgs {
   int T, k, S;
   const int4* tiles;
   const int32_t* meta;
-  uint16_t* out;                // h [S + T, I] or y [S + T, H]
+  void* out;                    // h [S + T, I] bf16 or y [S + T, H] fp32
   int out_ld;
   int32_t* status;
 };
@@ -441,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float u = __uint_as_float(is_gate ? pv[ci] : v[ci]) * s2;
             const int col = cbase + i;
             if (col < td.z)
-              a.out[static_cast<int64_t>(td.y + col) * a.out_ld + j] = f32_to_bf16_bits(silu_f32(g) * u);
+              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + j] =
+                  f32_to_bf16_bits(silu_f32(g) * u);
           }
         } else {
           const int nrow = mb * kBM + q * 32 + lane;
@@ -449,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
             if (col < td.z)
-              a.out[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =
-                  f32_to_bf16_bits(__uint_as_float(v[i]) * s2);
+              static_cast<float*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =
+                  __uint_as_float(v[i]) * s2;
           }
         }
       }

@@ -123,7 +123,8 @@ __device__ __forceinline__ void store_rows(const GroupedArgs& a, const float (&a
       for (int i = 0; i < 4; ++i)
         if (lane == i + 4 * t && t < nt) {
           const float g = acc[i][t] * s2, u = acc[4 + i][t] * s2;
-          a.out[static_cast<int64_t>(p0 + t) * I + wbase + i] = f32_to_bf16_bits(silu_f32(g) * u);
+          static_cast<uint16_t*>(a.out)[static_cast<int64_t>(p0 + t) * I + wbase + i] =
+              f32_to_bf16_bits(silu_f32(g) * u);
         }
   } else {
 #pragma unroll
@@ -131,7 +132,7 @@ __device__ __forceinline__ void store_rows(const GroupedArgs& a, const float (&a
 #pragma unroll
       for (int r = 0; r < 8; ++r)
         if (lane == r + 8 * (t & 3) && t < nt)
-          a.out[static_cast<int64_t>(p0 + t) * a.N + wbase + r] = f32_to_bf16_bits(acc[r][t] * s2);
+          static_cast<float*>(a.out)[static_cast<int64_t>(p0 + t) * a.N + wbase + r] = acc[r][t] * s2;
   }
 }
 

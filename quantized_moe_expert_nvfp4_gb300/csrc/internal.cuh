@@ -33,7 +33,7 @@ struct WsLayout {
   size_t tiles;        // int4  [max_tiles] work items {group, row_begin, rows, 0}
   size_t hist;         // int32 [n_chunks, E] per-chunk expert histogram / bases
   size_t h;            // bf16  [S + T, I]
-  size_t y;            // bf16  [S + T, H]
+  size_t y;            // fp32  [S + T, H]
   size_t total;
   int64_t max_tiles;
   int64_t n_chunks;
@@ -119,7 +119,7 @@ struct GroupedArgs {
   const int4* tiles;
   const int32_t* meta;
   int64_t max_tiles;
-  uint16_t* out;                // h [S + T, I] or y [S + T, H]
+  void* out;                    // h [S + T, I] bf16 (gate_up) or y [S + T, H] fp32 (down)
   int32_t* status;              // device status word (bad indices are clamped and reported)
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
@@ -148,7 +148,7 @@ struct DownCombineArgs {
 cudaError_t launch_down_combine_gemv(const DownCombineArgs& a, cudaStream_t st);
 
 // status may be NULL (bad slot positions are then clamped silently).
-cudaError_t launch_combine(const uint16_t* y, const int32_t* slot_pos, const float* topk_w, int T,
+cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
                            int32_t* status, cudaStream_t st);
 

@@ -36,6 +36,25 @@ def check_layer_close(got, ref, what="output"):
     return float(ratio.max()), float(rel)
 
 
+def check_bf16_stage_close(got, ref, what="stage"):
+    """Bound for a bf16-rounded intermediate (h = SiLU(g)*u): one round-to-nearest bf16 step
+    (relative error <= 2^-9, taken as 2^-8 for the fp32 work before it) plus 1e-3 of the row RMS
+    for the fp32 accumulation-order differences.  The layer tolerance itself is checked on the
+    layer output; this bound is per element and so catches any wrong element."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
+    err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-3 * rms
+    worst = (err / np.maximum(bound, 1e-300)).max()
+    assert (err <= bound).all(), f"{what}: worst err/bound = {worst:.3e}"
+    rel = err.sum() / max(np.abs(ref).sum(), 1e-300)
+    assert rel <= MEAN_REL_TOL, f"{what}: mean relative error {rel:.3e}"
+    return float(worst)
+
+
 def to_np(t):
     if t.dtype == torch.bfloat16:
         return t.float().cpu().numpy()

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from moe_cases import Layer, check_layer_close, moe_shape, to_np
+from moe_cases import Layer, check_bf16_stage_close, check_layer_close, moe_shape, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -73,10 +73,10 @@ def test_small_layers_all_stages(cuda_lib, case):
     S = s.T * s.k
     slot_of_row = oss  # routed row p holds slot oss[p] = t*k + j
     t_of, j_of = slot_of_row // s.k, slot_of_row % s.k
-    check_layer_close(to_np(h[:S]), h_ref[t_of, j_of], "h routed")
+    check_bf16_stage_close(to_np(h[:S]), h_ref[t_of, j_of], "h routed")
     check_layer_close(to_np(y[:S]), y_ref[t_of, j_of], "y routed")
     if s.has_shared:
-        check_layer_close(to_np(h[S:]), h_ref[:, s.k], "h shared")
+        check_bf16_stage_close(to_np(h[S:]), h_ref[:, s.k], "h shared")
         check_layer_close(to_np(y[S:]), y_ref[:, s.k], "y shared")
     for fp32 in (False, True):
         out = moe.combine(y, slot_pos, w, ms, out_fp32=fp32)
