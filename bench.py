@@ -283,8 +283,9 @@ def run_ours(args):
     moe.load()
     layers = [build_layer(moe, w, T, seed, pool, device) for T, seed in workload_entries(name)]
     tokens_per_step = sum(L["T"] for L in layers)
-    decode_arm = all(L["T"] <= moe.DECODE_MAX_T for L in layers)
-    launches_per_forward = 3 if decode_arm else 8
+    arms = [moe.forward_arm(L["ms"]) for L in layers]
+    decode_arm = all(a in (0, 1) for a in arms)
+    launches = sum({0: 1, 1: 3, 2: 8, 3: 8}[a] for a in arms)
     stream = torch.cuda.Stream(device)
 
     # graphs[b][p]: one step on input batch p, recording event set b
@@ -312,6 +313,7 @@ def run_ours(args):
 
     stage_ms = [[0.0] * 4 for _ in layers]
     gate_up_bytes = 0.0
+    down_bytes = 0.0
     gate_up_flops = 0.0
     fwd_bytes = 0.0
     H, I, E = w.H, w.I, w.E
@@ -319,7 +321,7 @@ def run_ours(args):
     dn_expert = H * I // 2 + H * I // 16 + 4
 
     def collect(b, batch_steps):
-        nonlocal gate_up_bytes, gate_up_flops, fwd_bytes
+        nonlocal gate_up_bytes, down_bytes, gate_up_flops, fwd_bytes
         for p in batch_steps:
             evs = events[b][p]
             evs[-1][4].synchronize()
@@ -330,6 +332,7 @@ def run_ours(args):
                 T, U = L["T"], L["uniq"][p] + 1
                 S = T * w.k
                 gate_up_bytes += U * gu_expert + T * H * 2 + (S + T) * I * 2
+                down_bytes += U * dn_expert + (S + T) * I * 2 + T * H * 2 + S * 8
                 gate_up_flops += 2.0 * (2 * I) * H * (S + T)
                 fwd_bytes += U * (gu_expert + dn_expert) + T * H * 2 + T * E * 4 + T * H * 2
 
@@ -375,30 +378,38 @@ def run_ours(args):
         max_ms = float(tt.item())
     value = world * steps * tokens_per_step / (max_ms / 1e3)
 
-    # dominant kernel (largest summed stage time): gate_up on both arms so far
+    # dominant kernel: the whole-layer kernel on the one-launch decode arm, otherwise the stage
+    # with the largest summed time
     tot_stage = [sum(stage_ms[li][s] for li in range(len(layers))) for s in range(4)]
-    dom = max(range(4), key=lambda s: tot_stage[s])
     stage_names = ["route+permute", "gate_up", "down" if not decode_arm else "down+combine", "combine"]
-    gu_ms = tot_stage[1]
     n_launch = steps * len(layers)
+    pk = peaks()
+    src = "quantized_moe_expert_nvfp4_gb300/csrc/"
+    if all(a == 0 for a in arms):
+        stage_names[0] = "whole layer (one launch)"
+        t_ms, alg = tot_stage[0], fwd_bytes
+        kname, kfile = "decode_fused_kernel (route+gate_up+down+combine)", ["decode_fused.cu"]
+    elif decode_arm:
+        dom = 1 if tot_stage[1] >= tot_stage[2] else 2
+        t_ms, alg = tot_stage[dom], (gate_up_bytes if dom == 1 else down_bytes)
+        kname = "grouped_simt_kernel<gate_up>" if dom == 1 else "down_combine_gemv_kernel"
+        kfile = ["grouped_simt.cu"]
     if decode_arm:
-        achieved = gate_up_bytes / (gu_ms / 1e3) / 1e9
-        pk = peaks()
+        achieved = alg / (t_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                    "frac": achieved / pk["hbm"], "peak_source": pk["source"],
-                    "kernel": "grouped_simt_kernel<gate_up> (decode GEMV)",
-                    "algorithmic_bytes_per_launch": gate_up_bytes / n_launch,
-                    "avg_launch_us": 1e3 * gu_ms / n_launch,
-                    "traffic": stored_traffic(name, "gate_up", ["quantized_moe_expert_nvfp4_gb300/csrc/grouped_simt.cu"])}
+                    "frac": achieved / pk["hbm"], "peak_source": pk["source"], "kernel": kname,
+                    "algorithmic_bytes_per_launch": alg / n_launch, "avg_launch_us": 1e3 * t_ms / n_launch,
+                    "traffic": stored_traffic(name, kname.split(" ")[0], [src + f for f in kfile])}
     else:
+        gu_ms = tot_stage[1]
         achieved = gate_up_flops / (gu_ms / 1e3) / 1e12
-        pk = peaks()
         peak = pk["bf16_sustained"] if name == "long" else pk["bf16"]
+        kname = "grouped_gemm_tc_kernel<gate_up>" if all(a == 2 for a in arms) else "grouped_simt_kernel<gate_up>"
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_source": pk["source"],
-                    "kernel": "grouped gate_up GEMM", "algorithmic_flops_per_launch": gate_up_flops / n_launch,
+                    "frac": achieved / peak, "peak_source": pk["source"], "kernel": kname,
+                    "algorithmic_flops_per_launch": gate_up_flops / n_launch,
                     "avg_launch_us": 1e3 * gu_ms / n_launch,
-                    "traffic": stored_traffic(name, "gate_up", ["quantized_moe_expert_nvfp4_gb300/csrc/grouped_simt.cu"])}
+                    "traffic": stored_traffic(name, kname, [src + "gemm_tc.cu"])}
 
     # end to end through host buffers: H2D of x and logits from pinned memory, the C-ABI call,
     # D2H of the output, every step.
@@ -436,13 +447,13 @@ def run_ours(args):
         cfg = describe(name)
         cfg.update({"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh "
                           f"input batch each step ({pool} batches cycled), experts differ per step",
-                    "cuda_graphs": True, "parallelism": f"replicas x{world}", "arm": "decode (grouped GEMV)"
-                    if decode_arm else "prefill (grouped GEMM)"})
+                    "cuda_graphs": True, "parallelism": f"replicas x{world}",
+                    "arm": sorted({moe.ARM_NAMES[a] for a in arms})})
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
                 "warmup": warmup, "ms_per_step": max_ms / steps, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "nvfp4 x bf16 -> f32 accumulate", "data": "synthetic",
                 "config": cfg, "roofline": roofline, "e2e": e2e,
-                "gpu_launches": steps * len(layers) * launches_per_forward,
+                "gpu_launches": steps * launches,
                 "clocks": clk.summary(),
                 "stages_ms_per_step": {stage_names[s]: tot_stage[s] / steps for s in range(4)},
                 "stages_us_per_forward": {f"T={L['T']}": [round(1e3 * stage_ms[li][s] / steps, 2) for s in range(4)]

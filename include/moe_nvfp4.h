@@ -132,9 +132,10 @@ moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* t
                          const moe_shape_t* shape, void* out, int out_is_fp32, void* stream);
 
 /* The whole layer: route, permute, grouped gate_up(+SiLU), grouped down, combine, with the
- * shared expert.  Picks the decode arm (grouped GEMV streaming only the selected experts'
- * bytes) for T <= 64 and the prefill arm (grouped GEMM) above.  Same numerics contract as the
- * stage calls; out is [T, H] bf16 or fp32. */
+ * shared expert.  Same numerics contract as the stage calls; out is [T, H] bf16 or fp32.  The
+ * arm depends on the shape (see moe_forward_arm): decode/verify batches stream only the
+ * selected experts' bytes through grouped GEMVs, prefill batches run the grouped GEMM on the
+ * tensor cores. */
 moe_status_t moe_forward(const uint16_t* x, const float* logits,
                          const moe_nvfp4_weights_t* gate_up, const moe_nvfp4_weights_t* down,
                          const moe_shape_t* shape, void* out, int out_is_fp32, void* ws,
@@ -144,7 +145,8 @@ moe_status_t moe_forward(const uint16_t* x, const float* logits,
  * measure-first steps, as CUDA events).  stage_events, when not NULL, points to 5 cudaEvent_t
  * (created with timing enabled) that are recorded on `stream`: [0] before routing, [1] after
  * the permutation and work list, [2] after gate_up, [3] after down, [4] after combine.  On the
- * decode arm down and combine are one kernel, so [3] and [4] are recorded together.  With
+ * decode arm down and combine are one kernel, so [3] and [4] are recorded together; on arm 0
+ * (see moe_forward_arm) the whole layer is one kernel and [1]..[4] follow it.  With
  * stage_events == NULL this is moe_forward. */
 moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                                   const moe_nvfp4_weights_t* gate_up,
@@ -163,6 +165,14 @@ moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K,
 /* Reads (and clears) the device status word of a workspace: *status receives MOE_OK or the
  * first device-side error recorded since the last read.  Synchronizes `stream`. */
 moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream);
+
+/* Which kernels moe_forward runs for a shape (-1 for an unsupported shape):
+ *   0  T <= 8 (H % 512 == 0, H <= 4096, I <= 1024): one cooperative launch that routes,
+ *      streams the active experts' weights with TMA bulk copies and combines (grouped GEMV);
+ *   1  T <= 64 otherwise: three launches (route+permute, gate_up GEMV, down GEMV + combine);
+ *   2  T > 64, H and I multiples of 256: tcgen05 grouped GEMMs (prefill arm);
+ *   3  T > 64 otherwise: CUDA-core grouped GEMMs. */
+int moe_forward_arm(const moe_shape_t* shape);
 
 /* Static description of a status code. */
 const char* moe_status_string(moe_status_t status);

@@ -78,6 +78,7 @@ def _declare(L):
         "moe_quantize_nvfp4": ([P, I64, I64, I64, P, P, P, P], I32),
         "moe_get_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "moe_status_string": ([I32], ctypes.c_char_p),
+        "moe_forward_arm": ([SH], I32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -247,10 +248,20 @@ def device_status(ws: torch.Tensor, stream=None) -> int:
     return v.value
 
 
+ARM_NAMES = {0: "decode, one cooperative launch (grouped GEMV)",
+             1: "decode, three launches (grouped GEMV)",
+             2: "prefill, tcgen05 grouped GEMM", 3: "prefill, CUDA-core grouped GEMM"}
+
+
+def forward_arm(shape: Shape) -> int:
+    """Which kernels moe_forward runs for this shape (see moe_forward_arm in the header)."""
+    return load().moe_forward_arm(ctypes.byref(shape.c()))
+
+
 def status_string(status: int) -> str:
     return load().moe_status_string(status).decode()
 
 
 __all__ = ["Shape", "NVFP4Weights", "MoeError", "load", "workspace_size", "workspace",
            "quantize_nvfp4", "route_topk", "permute", "grouped_gate_up", "grouped_down", "combine",
-           "forward", "forward_profiled", "device_status", "status_string", "DECODE_MAX_T", "LIB_PATH"]
+           "forward", "forward_profiled", "forward_arm", "ARM_NAMES", "device_status", "status_string", "DECODE_MAX_T", "LIB_PATH"]

@@ -101,6 +101,12 @@ Arm arm_for(const moe_shape_t& s) {
   return tc_supported(s) ? Arm::kTc : Arm::kSimt;
 }
 
+// Which kernels moe_forward runs for a shape (the value moe_forward_arm reports).
+int forward_arm(const moe_shape_t& s) {
+  if (s.T <= kDecodeMaxT) return decode_fused_supported(s) ? 0 : 1;
+  return arm_for(s) == Arm::kTc ? 2 : 3;
+}
+
 int tile_rows_for(const moe_shape_t& s) {
   switch (arm_for(s)) {
     case Arm::kDecode: return kDecodeMaxT;
@@ -312,9 +318,33 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
   };
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (forward_arm(s) == 0) {
+    // decode arm, one cooperative launch: route, permute, gate_up, down, combine
+    DecodeFusedArgs f;
+    f.x = x;
+    f.logits = logits;
+    f.gate_up = *gate_up;
+    f.down = *down;
+    f.shape = s;
+    f.ids = w.ids;
+    f.topk_w = w.w;
+    f.counts = w.counts;
+    f.offsets = w.offsets;
+    f.sorted_slot = w.sorted_slot;
+    f.slot_pos = w.slot_pos;
+    f.h = w.h;
+    f.y = w.y;
+    f.out = out;
+    f.out_is_fp32 = out_is_fp32;
+    f.grid_bar = reinterpret_cast<unsigned*>(w.meta + 2);
+    f.status = w.status;
+    e = launch_decode_fused(f, cs);
+    for (int i = 1; i <= 4 && e == cudaSuccess; ++i) e = mark(i);
+    return cuda_status(e);
+  }
   if (s.T <= kDecodeMaxT) {
-    // decode arm: 1) route + permute + work list, 2) gate_up GEMV (+SiLU*up) of every active
-    // group incl. the shared expert, 3) down GEMV + fixed-order combine.
+    // decode arm for larger batches: 1) route + permute + work list, 2) gate_up GEMV (+SiLU*up)
+    // of every active group incl. the shared expert, 3) down GEMV + fixed-order combine.
     e = launch_route_permute_small(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w,
                                    w.counts, w.offsets, w.sorted_slot, w.slot_pos, w.tiles, w.meta,
                                    kDecodeMaxT, cs);
@@ -390,6 +420,11 @@ moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream) {
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   *status = v;
   return MOE_OK;
+}
+
+int moe_forward_arm(const moe_shape_t* shape) {
+  if (check_shape(shape) != MOE_OK) return -1;
+  return forward_arm(*shape);
 }
 
 const char* moe_status_string(moe_status_t status) {

@@ -1,0 +1,547 @@
+// Decode/verify arm (T <= 8 rows): the whole layer in one persistent cooperative kernel.
+//
+// The "handover briefs" page asks of the decode arm: a vectorised NVFP4 GEMV that streams only
+// the selected experts' bytes (bandwidth floor = bytes of the active experts / stream bandwidth,
+// done when within 1.3x of it), the routed top-k and the shared expert in one launch per
+// projection, gate+up fused and silu+down fused, and no host round trip.  Here one launch does
+// all of it:
+//   phase A  every CTA routes the T tokens itself (same result everywhere, no launch boundary
+//            between routing and the weight stream) and builds the permutation in SMEM;
+//   phase B  gate_up units (8 gate + 8 up rows of one active expert): h = SiLU(g) * u in bf16;
+//   grid barrier (h complete);
+//   phase C  down units (64 output rows of one active expert): y in fp32;
+//   grid barrier (y complete);
+//   phase D  fixed-order fp32 combine  out[t] = sum_j w[t,j] y[slot(t,j)] + y[shared t].
+// A producer warp streams each CTA's units (phase B then C, without waiting for the barrier)
+// into a ring of SMEM slots with TMA bulk copies; 8 compute warps dequantize (e2m1 x e4m3,
+// exact) and accumulate in fp32.  Units are dealt round-robin to the CTAs, one CTA per SM.
+// Every wait is bounded: an mbarrier or grid-barrier wait that runs past 1 s records
+// MOE_ERR_DEVICE_TIMEOUT in the status word and the kernel winds down.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "topk.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kFdComputeWarps = 8;
+constexpr int kFdThreads = (kFdComputeWarps + 1) * 32;
+constexpr int kFdProducer = kFdComputeWarps;   // warp index of the producer
+constexpr int kFdGuPairs = 8;                  // gate_up unit: 8 gate rows + the 8 up rows
+constexpr int kFdDnRows = 64;                  // down unit rows
+constexpr int kFdMaxSlots = 16;
+constexpr int kFdMaxS = kFdMaxT * kMaxK;
+constexpr int kFdSmemLimit = 227 * 1024;
+constexpr uint64_t kFdTimeoutNs = 1000000000ull;
+
+struct FdArgs {
+  const uint16_t* x;
+  const float* logits;
+  const uint8_t* gu_packed;
+  const uint8_t* gu_scales;
+  const float* gu_scale2;
+  const uint8_t* dn_packed;
+  const uint8_t* dn_scales;
+  const float* dn_scale2;
+  int T, H, I, E, k, has_shared;
+  int32_t* ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_slot;
+  int32_t* slot_pos;
+  uint16_t* h;          // [S + T, I]
+  float* y;             // [S + T, H]
+  void* out;
+  int out_is_fp32;
+  unsigned* grid_bar;   // {count, generation}
+  int32_t* status;
+  int x_bytes, smem_off, ring_off, slot_bytes, n_slots;
+};
+
+struct FdSmem {
+  uint64_t full[kFdMaxSlots];
+  uint64_t empty[kFdMaxSlots];
+  int32_t ids[kFdMaxS];
+  float w[kFdMaxS];
+  int32_t sorted[kFdMaxS];
+  int32_t slot_pos[kFdMaxS];
+  int32_t act[kFdMaxS + 1];
+  int32_t act_row[kFdMaxS + 1];
+  int32_t act_cnt[kFdMaxS + 1];
+  int32_t cnt[kMaxE];
+  int n_act;
+  int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool fd_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ bool fd_wait(uint64_t* b, uint32_t parity, FdSmem* sm, int32_t* status) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (fd_try(b, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return false;
+      const uint64_t t = now_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kFdTimeoutNs) {
+        report_device_error(status, kDevTimeout);
+        *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void compute_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFdComputeWarps * 32) : "memory");
+}
+
+// Grid-wide barrier of a cooperative launch (one thread per CTA): arrive on the counter, the
+// last CTA resets it and bumps the generation; others wait for the generation to move.
+__device__ bool grid_barrier(unsigned* bar, FdSmem* sm, int32_t* status) {
+  volatile unsigned* vgen = bar + 1;
+  const unsigned gen = *vgen;
+  __threadfence();
+  if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+    atomicExch(bar, 0u);
+    __threadfence();
+    atomicAdd(bar + 1, 1u);
+    return true;
+  }
+  uint64_t t0 = now_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (*vgen != gen) break;
+    if ((i & 1023u) == 1023u && now_ns() - t0 > kFdTimeoutNs) {
+      report_device_error(status, kDevTimeout);
+      sm->abort_flag = 1;
+      return false;
+    }
+  }
+  __threadfence();
+  return true;
+}
+
+// sum over one 16-element NVFP4 block of e2m1(q_i) * x_i, times the block's e4m3 scale.
+__device__ __forceinline__ float block_dot(uint2 q, uint32_t scale_byte, const float (&x)[16]) {
+  float v[8];
+  float d = 0.0f;
+  e2m1x8_to_f32(q.x, v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d = fmaf(v[i], x[i], d);
+  e2m1x8_to_f32(q.y, v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) d = fmaf(v[i], x[8 + i], d);
+  return d * e4m3_to_f32(scale_byte);
+}
+
+__device__ __forceinline__ void bf16x16_to_f32(const uint16_t* p, float (&x)[16], bool coherent) {
+  uint4 a, b;
+  if (coherent) {   // data written by other CTAs earlier in this kernel: bypass L1
+    a = __ldcg(reinterpret_cast<const uint4*>(p));
+    b = __ldcg(reinterpret_cast<const uint4*>(p) + 1);
+  } else {
+    a = *reinterpret_cast<const uint4*>(p);
+    b = *(reinterpret_cast<const uint4*>(p) + 1);
+  }
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
+  extern __shared__ __align__(1024) uint8_t fd_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fd_raw) + 1023) & ~uintptr_t(1023));
+  uint16_t* xs = reinterpret_cast<uint16_t*>(base);
+  FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.smem_off);
+  uint8_t* ring = base + a.ring_off;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = T * k;
+  const int NS = a.n_slots;
+
+  // ------------------------------------------------------------ phase A: route + permute
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm->full[s])));
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm->empty[s])),
+                   "r"(kFdComputeWarps));
+    }
+    sm->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+  }
+  if (warp < T) {
+    int my_id;
+    float my_w;
+    warp_topk<EPL>(a.logits + static_cast<int64_t>(warp) * E, E, k, lane, my_id, my_w);
+    if (lane < k) {
+      sm->ids[warp * k + lane] = my_id;
+      sm->w[warp * k + lane] = my_w;
+      if (blockIdx.x == 0) {
+        a.ids[warp * k + lane] = my_id;
+        a.topk_w[warp * k + lane] = my_w;
+      }
+    }
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&sm->cnt[sm->ids[s]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scan of the expert counts (each lane a contiguous run of experts), the
+    // active-expert list in ascending order, then the stable scatter of the slots
+    const int per = (E + 31) / 32;
+    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+    int sum = 0, nz = 0;
+    for (int e = e0; e < e1; ++e) {
+      sum += sm->cnt[e];
+      nz += sm->cnt[e] > 0;
+    }
+    int is = sum, in = nz;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int ys = __shfl_up_sync(0xffffffffu, is, off);
+      const int yn = __shfl_up_sync(0xffffffffu, in, off);
+      if (lane >= off) {
+        is += ys;
+        in += yn;
+      }
+    }
+    int run = is - sum, pos = in - nz;
+    for (int e = e0; e < e1; ++e) {
+      const int c = sm->cnt[e];
+      if (blockIdx.x == 0) {
+        a.counts[e] = c;
+        a.offsets[e] = run;
+      }
+      if (c > 0) {
+        sm->act[pos] = e;
+        sm->act_row[pos] = run;
+        sm->act_cnt[pos] = c;
+        ++pos;
+      }
+      sm->cnt[e] = run;  // becomes the scatter cursor
+      run += c;
+    }
+    const int n_routed = __shfl_sync(0xffffffffu, in, 31);
+    if (lane == 0) {
+      if (a.has_shared) {
+        sm->act[n_routed] = E;
+        sm->act_row[n_routed] = S;
+        sm->act_cnt[n_routed] = T;
+      }
+      sm->n_act = n_routed + a.has_shared;
+      if (blockIdx.x == 0) a.offsets[E] = S;
+    }
+    __syncwarp();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b = 0; b < S; b += 32) {
+      const int s = b + lane;
+      const int e = (s < S) ? sm->ids[s] : -1;
+      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(grp & lt);
+      if (e >= 0) {
+        const int p = sm->cnt[e] + rank;
+        sm->sorted[p] = s;
+        sm->slot_pos[s] = p;
+        if (blockIdx.x == 0) {
+          a.sorted_slot[p] = s;
+          a.slot_pos[s] = p;
+        }
+      }
+      __syncwarp();
+      if (e >= 0 && rank == 0) sm->cnt[e] += __popc(grp);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+
+  const int n_act = sm->n_act;
+  const int gu_per_group = I / kFdGuPairs;
+  const int dn_per_group = H / kFdDnRows;
+  const int nB = n_act * gu_per_group;
+  const int nC = n_act * dn_per_group;
+
+  if (warp == kFdProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < nB + nC; u += gridDim.x, ++it) {
+        const int slot = it % NS;
+        if (!(ok = fd_wait(&sm->empty[slot], ((it / NS) & 1) ^ 1, sm, a.status))) break;
+        uint8_t* dst = ring + slot * a.slot_bytes;
+        if (u < nB) {
+          const int g = sm->act[u / gu_per_group];
+          const int j0 = (u % gu_per_group) * kFdGuPairs;
+          const int64_t rg = static_cast<int64_t>(g) * 2 * I + j0;   // first gate row
+          const int64_t ru = rg + I;                                   // first up row
+          const uint32_t pb = kFdGuPairs * (H / 2), sb = kFdGuPairs * (H / 16);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm->full[slot])),
+                       "r"(2 * pb + 2 * sb)
+                       : "memory");
+          bulk_g2s(dst, a.gu_packed + rg * (H / 2), pb, &sm->full[slot]);
+          bulk_g2s(dst + pb, a.gu_packed + ru * (H / 2), pb, &sm->full[slot]);
+          bulk_g2s(dst + 2 * pb, a.gu_scales + rg * (H / 16), sb, &sm->full[slot]);
+          bulk_g2s(dst + 2 * pb + sb, a.gu_scales + ru * (H / 16), sb, &sm->full[slot]);
+        } else {
+          const int v = u - nB;
+          const int g = sm->act[v / dn_per_group];
+          const int64_t r0 = static_cast<int64_t>(g) * H + (v % dn_per_group) * kFdDnRows;
+          const uint32_t pb = kFdDnRows * (I / 2), sb = kFdDnRows * (I / 16);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm->full[slot])),
+                       "r"(pb + sb)
+                       : "memory");
+          bulk_g2s(dst, a.dn_packed + r0 * (I / 2), pb, &sm->full[slot]);
+          bulk_g2s(dst + pb, a.dn_scales + r0 * (I / 16), sb, &sm->full[slot]);
+        }
+      }
+      if (!ok) {  // let copies already issued land before the CTA exits (bounded)
+        for (uint32_t j = 0; j < static_cast<uint32_t>(NS) && j < it; ++j) {
+          const uint32_t q = it - 1 - j;
+          for (uint32_t i = 0; i < (1u << 20) && !fd_try(&sm->full[q % NS], (q / NS) & 1); ++i) {
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ compute warps
+  uint32_t it = 0;
+  bool ok = true;
+  const int hb = H / 16;   // 16-element blocks per gate_up row
+  // phase B: gate_up units; warp w owns gate row j0 + w and up row j0 + w of the unit
+  for (int u = blockIdx.x; u < nB; u += gridDim.x, ++it) {
+    const int slot = it % NS;
+    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, sm, a.status));
+    if (ok) {
+      const int gi = u / gu_per_group;
+      const int g = sm->act[gi];
+      const int j = (u % gu_per_group) * kFdGuPairs + warp;
+      const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
+      const uint8_t* sl = ring + slot * a.slot_bytes;
+      const uint8_t* pg = sl + warp * (H / 2);
+      const uint8_t* pu = sl + (kFdGuPairs + warp) * (H / 2);
+      const uint8_t* sg = sl + 2 * kFdGuPairs * (H / 2) + warp * (H / 16);
+      const uint8_t* su = sg + kFdGuPairs * (H / 16);
+      const float s2 = __ldg(a.gu_scale2 + g);
+      for (int te = 0; te < nt; ++te) {
+        const int p = row0 + te;
+        const int t = (g == E) ? te : sm->sorted[p] / k;
+        const uint16_t* xt = xs + t * H;
+        float ag = 0.0f, au = 0.0f;
+        for (int b = lane; b < hb; b += 32) {
+          float xv[16];
+          bf16x16_to_f32(xt + b * 16, xv, false);
+          ag += block_dot(*reinterpret_cast<const uint2*>(pg + b * 8), sg[b], xv);
+          au += block_dot(*reinterpret_cast<const uint2*>(pu + b * 8), su[b], xv);
+        }
+        ag = warp_sum(ag);
+        au = warp_sum(au);
+        if (lane == 0) a.h[static_cast<int64_t>(p) * I + j] = f32_to_bf16_bits(silu_f32(ag * s2) * (au * s2));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+  }
+  compute_sync();
+  if (threadIdx.x == 0 && ok && !sm->abort_flag) grid_barrier(a.grid_bar, sm, a.status);
+  compute_sync();
+  ok = ok && !*reinterpret_cast<volatile int*>(&sm->abort_flag);
+
+  // phase C: down units; warp w owns output rows n0 + 8w .. n0 + 8w + 7
+  const int ib = I / 16;
+  for (int u = blockIdx.x; u < nC; u += gridDim.x, ++it) {
+    const int slot = it % NS;
+    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, sm, a.status));
+    if (ok) {
+      const int gi = u / dn_per_group;
+      const int g = sm->act[gi];
+      const int n0 = (u % dn_per_group) * kFdDnRows + warp * 8;
+      const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
+      const uint8_t* sl = ring + slot * a.slot_bytes;
+      const uint8_t* pr = sl + warp * 8 * (I / 2);
+      const uint8_t* sr = sl + kFdDnRows * (I / 2) + warp * 8 * (I / 16);
+      const float s2 = __ldg(a.dn_scale2 + g);
+      for (int te = 0; te < nt; ++te) {
+        const int p = row0 + te;
+        const uint16_t* hp = a.h + static_cast<int64_t>(p) * I;
+        float acc[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r] = 0.0f;
+        for (int b = lane; b < ib; b += 32) {
+          float hv[16];
+          bf16x16_to_f32(hp + b * 16, hv, true);
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            acc[r] += block_dot(*reinterpret_cast<const uint2*>(pr + r * (I / 2) + b * 8), sr[r * (I / 16) + b], hv);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) acc[r] = warp_sum(acc[r]);
+        if (lane < 8) {
+          float v = acc[0];
+#pragma unroll
+          for (int r = 1; r < 8; ++r) v = (lane == r) ? acc[r] : v;
+          a.y[static_cast<int64_t>(p) * H + n0 + lane] = v * s2;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+  }
+  compute_sync();
+  if (threadIdx.x == 0 && ok && !sm->abort_flag) grid_barrier(a.grid_bar, sm, a.status);
+  compute_sync();
+  if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return;
+
+  // phase D: out[t, n] = sum_j w[t, j] * y[slot_pos[t*k + j], n] + y[S + t, n], in that order
+  const int nthr = kFdComputeWarps * 32;
+  for (int idx = blockIdx.x * nthr + threadIdx.x; idx < T * H; idx += gridDim.x * nthr) {
+    const int t = idx / H, n = idx - t * H;
+    float s = 0.0f;
+    for (int j = 0; j < k; ++j)
+      s = fmaf(sm->w[t * k + j], __ldcg(a.y + static_cast<int64_t>(sm->slot_pos[t * k + j]) * H + n), s);
+    if (a.has_shared) s += __ldcg(a.y + static_cast<int64_t>(S + t) * H + n);
+    if (a.out_is_fp32)
+      static_cast<float*>(a.out)[idx] = s;
+    else
+      static_cast<uint16_t*>(a.out)[idx] = f32_to_bf16_bits(s);
+  }
+}
+
+struct FdPlan {
+  int x_bytes, smem_off, ring_off, slot_bytes, n_slots;
+  size_t smem_total;
+};
+
+bool fd_plan(const moe_shape_t& s, FdPlan* p) {
+  if (s.T < 1 || s.T > kFdMaxT || s.H % 512 || s.H > 4096 || s.I > 1024 || s.I % kFdGuPairs) return false;
+  p->x_bytes = ((s.T * s.H * 2 + 127) / 128) * 128;
+  p->smem_off = p->x_bytes;
+  p->ring_off = ((p->smem_off + static_cast<int>(sizeof(FdSmem)) + 1023) / 1024) * 1024;
+  const int gu_unit = 2 * kFdGuPairs * (s.H / 2 + s.H / 16);
+  const int dn_unit = kFdDnRows * (s.I / 2 + s.I / 16);
+  p->slot_bytes = ((std::max(gu_unit, dn_unit) + 127) / 128) * 128;
+  const int avail = kFdSmemLimit - 1024 - p->ring_off;
+  p->n_slots = std::min(kFdMaxSlots, avail / p->slot_bytes);
+  p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * p->slot_bytes;
+  return p->n_slots >= 3;
+}
+
+template <int EPL>
+cudaError_t launch_fd(const FdArgs& args, const FdPlan& plan, cudaStream_t st) {
+  static int configured_smem = 0;
+  const auto kern = decode_fused_kernel<EPL>;
+  if (configured_smem < static_cast<int>(plan.smem_total)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(plan.smem_total));
+    if (e != cudaSuccess) return e;
+    configured_smem = static_cast<int>(plan.smem_total);
+  }
+  int dev = 0, n_sm = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFdThreads, plan.smem_total);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_sm);
+  cfg.blockDim = dim3(kFdThreads);
+  cfg.dynamicSmemBytes = plan.smem_total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
+}  // namespace
+
+bool decode_fused_supported(const moe_shape_t& s) {
+  FdPlan p;
+  return fd_plan(s, &p);
+}
+
+cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
+  const moe_shape_t& s = d.shape;
+  FdPlan plan;
+  if (!fd_plan(s, &plan)) return cudaErrorInvalidValue;
+  FdArgs a;
+  a.x = d.x;
+  a.logits = d.logits;
+  a.gu_packed = d.gate_up.packed;
+  a.gu_scales = d.gate_up.scales;
+  a.gu_scale2 = d.gate_up.scale2;
+  a.dn_packed = d.down.packed;
+  a.dn_scales = d.down.scales;
+  a.dn_scale2 = d.down.scale2;
+  a.T = s.T;
+  a.H = s.H;
+  a.I = s.I;
+  a.E = s.E;
+  a.k = s.k;
+  a.has_shared = s.has_shared;
+  a.ids = d.ids;
+  a.topk_w = d.topk_w;
+  a.counts = d.counts;
+  a.offsets = d.offsets;
+  a.sorted_slot = d.sorted_slot;
+  a.slot_pos = d.slot_pos;
+  a.h = d.h;
+  a.y = d.y;
+  a.out = d.out;
+  a.out_is_fp32 = d.out_is_fp32;
+  a.grid_bar = d.grid_bar;
+  a.status = d.status;
+  a.x_bytes = plan.x_bytes;
+  a.smem_off = plan.smem_off;
+  a.ring_off = plan.ring_off;
+  a.slot_bytes = plan.slot_bytes;
+  a.n_slots = plan.n_slots;
+  if (s.E <= 256) return launch_fd<8>(a, plan, st);
+  if (s.E <= 512) return launch_fd<16>(a, plan, st);
+  return launch_fd<32>(a, plan, st);
+}
+
+}  // namespace moe

@@ -18,12 +18,13 @@ constexpr int kDecodeMaxT = 64;        // moe_forward uses the grouped-GEMV arm 
 constexpr int kSimtTileRows = 64;      // rows per work item of the SIMT grouped GEMM
 constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutation
 constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 grouped GEMM
+constexpr int kFdMaxT = 8;             // the fused single-launch decode kernel handles T <= 8
 
 // ------------------------------------------------------------------ workspace layout
 // All offsets are in bytes from the workspace base and 256-byte aligned.
 struct WsLayout {
   size_t status;       // int32 device status word (+ padding)
-  size_t meta;         // int32 meta[8]: [0] = number of work tiles
+  size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] grid barrier
   size_t ids;          // int32 [S]
   size_t w;            // fp32  [S]
   size_t counts;       // int32 [E]
@@ -148,6 +149,28 @@ struct DownCombineArgs {
 cudaError_t launch_down_combine_gemv(const DownCombineArgs& a, cudaStream_t st);
 
 // status may be NULL (bad slot positions are then clamped silently).
+// Single-launch decode arm (route + gate_up + down + combine, cooperative, T <= kFdMaxT).
+struct DecodeFusedArgs {
+  const uint16_t* x;
+  const float* logits;
+  moe_nvfp4_weights_t gate_up, down;
+  moe_shape_t shape;
+  int32_t* ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_slot;
+  int32_t* slot_pos;
+  uint16_t* h;
+  float* y;
+  void* out;
+  int out_is_fp32;
+  unsigned* grid_bar;
+  int32_t* status;
+};
+bool decode_fused_supported(const moe_shape_t& s);
+cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st);
+
 cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
                            int32_t* status, cudaStream_t st);

@@ -26,6 +26,12 @@ SMALL = [
     (300, 256, 16, 16, 128, 0, "none", 106),
     (3000, 256, 64, 8, 128, 1, "normal", 107),
     (16, 128, 1024, 16, 128, 1, "none", 108),
+    # one-launch decode arm (T <= 8, H % 512 == 0): E = 1024 with k = 16 and no shared expert,
+    # a skewed batch where experts are shared by several tokens, I = 1024
+    (3, 512, 16, 4, 128, 1, "none", 112),
+    (8, 1024, 64, 8, 256, 1, "zipf", 113),
+    (5, 512, 1024, 16, 128, 0, "none", 114),
+    (2, 512, 32, 2, 1024, 1, "normal", 115),
     # tcgen05 arm (T > 64, H and I multiples of 256): ragged token tiles, several tiles per
     # expert, no shared expert, the N tail of a single 16-column step
     (129, 256, 8, 2, 256, 0, "none", 109),
@@ -87,6 +93,16 @@ def test_small_layers_all_stages(cuda_lib, case):
         check_layer_close(to_np(out), out_ref, f"forward fp32={fp32}")
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
+
+
+def test_forward_arm_selection(cuda_lib):
+    moe = cuda_lib
+    arm = lambda **kw: moe.forward_arm(moe.Shape(**{**dict(T=1, H=2048, I=512, E=512, k=10), **kw}))
+    assert arm(T=1) == 0 and arm(T=8) == 0
+    assert arm(T=9) == 1 and arm(T=64) == 1 and arm(T=4, H=256) == 1
+    assert arm(T=65) == 2 and arm(T=4096) == 2
+    assert arm(T=65, I=128) == 3
+    assert arm(H=100) == -1
 
 
 def test_forward_deterministic_and_matches_stages(cuda_lib):
