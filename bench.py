@@ -302,6 +302,9 @@ def run_ours(args):
             for L in layers:
                 moe.forward(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
     stream.synchronize()
+    bad = [moe.device_status(L["ws"]) for L in layers]
+    if any(bad):
+        raise RuntimeError(f"device status after the first pass: {bad}")
     for b in range(2):
         for p in range(pool):
             g = torch.cuda.CUDAGraph()

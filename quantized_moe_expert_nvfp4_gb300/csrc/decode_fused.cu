@@ -346,11 +346,15 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   }
 
   // ------------------------------------------------------------ compute warps
+  // Units u = blockIdx.x, blockIdx.x + gridDim.x, ... over [0, nB + nC): the producer walks the
+  // same sequence, so the two sides agree on every slot.  u < nB are gate_up units, the rest
+  // down units (v = u - nB).
   uint32_t it = 0;
   bool ok = true;
   const int hb = H / 16;   // 16-element blocks per gate_up row
+  int u = blockIdx.x;
   // phase B: gate_up units; warp w owns gate row j0 + w and up row j0 + w of the unit
-  for (int u = blockIdx.x; u < nB; u += gridDim.x, ++it) {
+  for (; u < nB; u += gridDim.x, ++it) {
     const int slot = it % NS;
     if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, sm, a.status));
     if (ok) {
@@ -390,13 +394,14 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
 
   // phase C: down units; warp w owns output rows n0 + 8w .. n0 + 8w + 7
   const int ib = I / 16;
-  for (int u = blockIdx.x; u < nC; u += gridDim.x, ++it) {
+  for (; u < nB + nC; u += gridDim.x, ++it) {
     const int slot = it % NS;
     if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, sm, a.status));
     if (ok) {
-      const int gi = u / dn_per_group;
+      const int v = u - nB;
+      const int gi = v / dn_per_group;
       const int g = sm->act[gi];
-      const int n0 = (u % dn_per_group) * kFdDnRows + warp * 8;
+      const int n0 = (v % dn_per_group) * kFdDnRows + warp * 8;
       const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
       const uint8_t* sl = ring + slot * a.slot_bytes;
       const uint8_t* pr = sl + warp * 8 * (I / 2);

@@ -89,10 +89,12 @@ def test_small_layers_all_stages(cuda_lib, case):
         check_layer_close(to_np(out), out_ref, f"combine fp32={fp32}")
     # the fused forward, both output types
     for fp32 in (False, True):
-        out = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=fp32)
-        check_layer_close(to_np(out), out_ref, f"forward fp32={fp32}")
-    torch.cuda.synchronize()
-    assert moe.device_status(ws) == 0
+        out = torch.full((s.T, s.H), float("nan"), device="cuda",
+                         dtype=torch.float32 if fp32 else torch.bfloat16)
+        moe.forward(x, logits, gu, dn, ms, ws, out=out, out_fp32=fp32)
+        torch.cuda.synchronize()
+        assert moe.device_status(ws) == 0
+        check_layer_close(to_np(out), out_ref, f"forward fp32={fp32} arm={moe.forward_arm(ms)}")
 
 
 def test_forward_arm_selection(cuda_lib):
@@ -169,7 +171,10 @@ def _check_full(moe, L, tokens):
     gu, dn = L.gpu_weights(moe)
     x, logits = L.x, L.logits
     ws = moe.workspace(ms)
-    out = moe.forward(x, logits, gu, dn, ms, ws)
+    out = torch.full((s.T, s.H), float("nan"), device="cuda", dtype=torch.bfloat16)
+    moe.forward(x, logits, gu, dn, ms, ws, out=out)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
     ids, w = moe.route_topk(logits, ms)
     oids, ow = oracle.route(logits.cpu(), s.k)
     assert np.array_equal(ids.cpu().numpy(), oids)
