@@ -25,11 +25,13 @@
 namespace moe {
 namespace {
 
-constexpr int kFdComputeWarps = 8;
+constexpr int kFdGroups = 2;                   // compute warp groups, alternate units
+constexpr int kFdGroupWarps = 8;
+constexpr int kFdComputeWarps = kFdGroups * kFdGroupWarps;
 constexpr int kFdThreads = (kFdComputeWarps + 1) * 32;
 constexpr int kFdProducer = kFdComputeWarps;   // warp index of the producer
 constexpr int kFdGuPairs = 8;                  // gate_up unit: 8 gate rows + the 8 up rows
-constexpr int kFdDnRows = 64;                  // down unit rows
+constexpr int kFdDnRows = 64;                  // down unit rows (8 per warp of a group)
 constexpr int kFdMaxSlots = 16;
 constexpr int kFdMaxS = kFdMaxT * kMaxK;
 constexpr int kFdSmemLimit = 227 * 1024;
@@ -63,6 +65,7 @@ struct FdArgs {
 struct FdSmem {
   uint64_t full[kFdMaxSlots];
   uint64_t empty[kFdMaxSlots];
+  unsigned long long win[kFdMaxT][kMaxK];   // routing winners: (logit key << 32) | ~index
   int32_t ids[kFdMaxS];
   float w[kFdMaxS];
   int32_t sorted[kFdMaxS];
@@ -146,17 +149,21 @@ __device__ bool grid_barrier(unsigned* bar, FdSmem* sm, int32_t* status) {
   return true;
 }
 
-// sum over one 16-element NVFP4 block of e2m1(q_i) * x_i, times the block's e4m3 scale.
+// sum over one 16-element NVFP4 block of e2m1(q_i) * x_i (two interleaved fp32 chains), times
+// the block's e4m3 scale.
 __device__ __forceinline__ float block_dot(uint2 q, uint32_t scale_byte, const float (&x)[16]) {
-  float v[8];
-  float d = 0.0f;
+  float v[8], w[8];
   e2m1x8_to_f32(q.x, v);
+  e2m1x8_to_f32(q.y, w);
+  float d0 = v[0] * x[0], d1 = v[1] * x[1], d2 = w[0] * x[8], d3 = w[1] * x[9];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) d = fmaf(v[i], x[i], d);
-  e2m1x8_to_f32(q.y, v);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) d = fmaf(v[i], x[8 + i], d);
-  return d * e4m3_to_f32(scale_byte);
+  for (int i = 2; i < 8; i += 2) {
+    d0 = fmaf(v[i], x[i], d0);
+    d1 = fmaf(v[i + 1], x[i + 1], d1);
+    d2 = fmaf(w[i], x[8 + i], d2);
+    d3 = fmaf(w[i + 1], x[9 + i], d3);
+  }
+  return ((d0 + d1) + (d2 + d3)) * e4m3_to_f32(scale_byte);
 }
 
 __device__ __forceinline__ void bf16x16_to_f32(const uint16_t* p, float (&x)[16], bool coherent) {
@@ -176,10 +183,51 @@ __device__ __forceinline__ void bf16x16_to_f32(const uint16_t* p, float (&x)[16]
   }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Warp reduction of N values at once by recursive halving: after it, lane l holds the full
+// sum of value ((l >> 2) & (N - 1)) for N = 8 (value (l >> 4) & 1 for N = 2).
+template <int N>
+__device__ __forceinline__ float warp_reduce_multi(float (&v)[N], int lane) {
+  int n = N;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+  for (int m = 16; m >= 1; m >>= 1) {
+    if (n > 1) {
+      const bool up = (lane & m) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < n / 2) {
+          const float send = up ? v[i] : v[i + n / 2];
+          const float keep = up ? v[i + n / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      n >>= 1;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+    }
+  }
+  return v[0];
+}
+
+__device__ __forceinline__ unsigned long long expert_key(const float* row, int e, int E) {
+  if (e >= E) return 0ull;
+  return (static_cast<unsigned long long>(logit_key(__ldg(row + e))) << 32) |
+         static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e));
+}
+
+// Descending bitonic sort of one 64-bit key per lane across the warp.
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long key, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
+      const bool desc = ((lane & size) == 0);          // direction of this bitonic subsequence
+      const bool lower = ((lane & stride) == 0);       // this lane holds the first element
+      const bool take_max = (desc == lower);
+      key = take_max ? (other > key ? other : key) : (other < key ? other : key);
+    }
+  }
+  return key;
 }
 
 template <int EPL>
@@ -189,19 +237,62 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   uint16_t* xs = reinterpret_cast<uint16_t*>(base);
   FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.smem_off);
   uint8_t* ring = base + a.ring_off;
+  // routing candidates live in ring slots 1.. (idle until routing is done; slot 0 may already
+  // be receiving the shared expert's first unit)
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(ring + a.slot_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = T * k;
   const int NS = a.n_slots;
+  const int gu_per_group = I / kFdGuPairs;
+  const int dn_per_group = H / kFdDnRows;
+  const uint32_t gu_pb = kFdGuPairs * (H / 2), gu_sb = kFdGuPairs * (H / 16);
+  const uint32_t dn_pb = kFdDnRows * (I / 2), dn_sb = kFdDnRows * (I / 16);
+
+  // The producer issues one unit: u < nB is a gate_up unit of active group u / gu_per_group,
+  // otherwise a down unit.  The shared expert is active group 0, so this CTA's first unit is
+  // known before routing when blockIdx.x < gu_per_group.
+  auto issue = [&](int u, int nB, uint32_t it) {
+    const int slot = it % NS;
+    uint8_t* dst = ring + slot * a.slot_bytes;
+    uint64_t* bar = &sm->full[slot];
+    if (u < nB) {
+      const int g = (u < gu_per_group && a.has_shared) ? E : sm->act[u / gu_per_group];
+      const int j0 = (u % gu_per_group) * kFdGuPairs;
+      const int64_t rg = static_cast<int64_t>(g) * 2 * I + j0;
+      const int64_t ru = rg + I;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                   "r"(2 * gu_pb + 2 * gu_sb)
+                   : "memory");
+      bulk_g2s(dst, a.gu_packed + rg * (H / 2), gu_pb, bar);
+      bulk_g2s(dst + gu_pb, a.gu_packed + ru * (H / 2), gu_pb, bar);
+      bulk_g2s(dst + 2 * gu_pb, a.gu_scales + rg * (H / 16), gu_sb, bar);
+      bulk_g2s(dst + 2 * gu_pb + gu_sb, a.gu_scales + ru * (H / 16), gu_sb, bar);
+    } else {
+      const int v = u - nB;
+      const int g = sm->act[v / dn_per_group];
+      const int64_t r0 = static_cast<int64_t>(g) * H + (v % dn_per_group) * kFdDnRows;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                   "r"(dn_pb + dn_sb)
+                   : "memory");
+      bulk_g2s(dst, a.dn_packed + r0 * (I / 2), dn_pb, bar);
+      bulk_g2s(dst + dn_pb, a.dn_scales + r0 * (I / 16), dn_sb, bar);
+    }
+  };
 
   // ------------------------------------------------------------ phase A: route + permute
-  if (threadIdx.x == 0) {
+  bool early = false;
+  if (warp == kFdProducer && lane == 0) {
     for (int s = 0; s < NS; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm->full[s])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm->empty[s])),
-                   "r"(kFdComputeWarps));
+                   "r"(kFdGroupWarps));
     }
     sm->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (a.has_shared && blockIdx.x < gu_per_group) {   // first unit: shared expert, gate_up
+      issue(blockIdx.x, 1 << 30, 0);
+      early = true;
+    }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
   {
@@ -209,13 +300,55 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
     uint4* dst = reinterpret_cast<uint4*>(xs);
     for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
   }
-  if (warp < T) {
-    int my_id;
-    float my_w;
-    warp_topk<EPL>(a.logits + static_cast<int64_t>(warp) * E, E, k, lane, my_id, my_w);
+  // routing step 1: the top-k of every 32-expert slice of every token, by a warp bitonic sort
+  const int n_slices = (E + 31) / 32;
+  const int kk = min(k, 32);
+  if (warp < kFdComputeWarps) {
+    for (int task = warp; task < T * n_slices; task += kFdComputeWarps) {
+      const int t = task / n_slices, sl = task % n_slices;
+      const unsigned long long key = warp_sort_desc(expert_key(a.logits + static_cast<int64_t>(t) * E, sl * 32 + lane, E), lane);
+      if (lane < kk) cand[t * n_slices * kk + sl * kk + lane] = key;
+    }
+  }
+  __syncthreads();
+  // routing step 2: rank of every candidate among its token's candidates; rank < k wins
+  {
+    const int nc = n_slices * kk;
+    for (int task = threadIdx.x; task < T * nc; task += blockDim.x) {
+      const int t = task / nc, c = task % nc;
+      const unsigned long long* ct = cand + t * nc;
+      const unsigned long long key = ct[c];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += ct[j] > key;
+      if (rank < k && key != 0ull) sm->win[t][rank] = key;
+    }
+  }
+  __syncthreads();
+  if (warp < T) {  // weights: renormalised softmax over the k winners, summed in rank order
+    float my_val = -INFINITY;
+    int my_id = 0;
+    if (lane < k) {
+      const unsigned long long key = sm->win[warp][lane];
+      my_id = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull));
+      my_val = key_value(static_cast<uint32_t>(key >> 32));
+    }
+    const float m = __shfl_sync(0xffffffffu, my_val, 0);
+    const bool live = lane < k;
+    float ev;
+    if (m == -INFINITY) {
+      ev = 0.0f;
+    } else if (m == INFINITY) {
+      ev = (live && my_val == INFINITY) ? 1.0f : 0.0f;
+    } else {
+      ev = live ? expf(my_val - m) : 0.0f;
+    }
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ev, j);
+    const float my_w = (sum > 0.0f) ? ev / sum : 0.0f;
     if (lane < k) {
       sm->ids[warp * k + lane] = my_id;
       sm->w[warp * k + lane] = my_w;
+      atomicAdd(&sm->cnt[my_id], 1);
       if (blockIdx.x == 0) {
         a.ids[warp * k + lane] = my_id;
         a.topk_w[warp * k + lane] = my_w;
@@ -223,11 +356,10 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
     }
   }
   __syncthreads();
-  for (int s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&sm->cnt[sm->ids[s]], 1);
-  __syncthreads();
   if (warp == 0) {
-    // exclusive scan of the expert counts (each lane a contiguous run of experts), the
-    // active-expert list in ascending order, then the stable scatter of the slots
+    // exclusive scan of the expert counts (each lane a contiguous run of experts), the active
+    // list (shared expert first, then routed experts ascending), then the stable scatter
+    const int sh = a.has_shared;
     const int per = (E + 31) / 32;
     const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
     int sum = 0, nz = 0;
@@ -245,7 +377,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
         in += yn;
       }
     }
-    int run = is - sum, pos = in - nz;
+    int run = is - sum, pos = in - nz + sh;
     for (int e = e0; e < e1; ++e) {
       const int c = sm->cnt[e];
       if (blockIdx.x == 0) {
@@ -263,12 +395,12 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
     }
     const int n_routed = __shfl_sync(0xffffffffu, in, 31);
     if (lane == 0) {
-      if (a.has_shared) {
-        sm->act[n_routed] = E;
-        sm->act_row[n_routed] = S;
-        sm->act_cnt[n_routed] = T;
+      if (sh) {
+        sm->act[0] = E;
+        sm->act_row[0] = S;
+        sm->act_cnt[0] = T;
       }
-      sm->n_act = n_routed + a.has_shared;
+      sm->n_act = n_routed + sh;
       if (blockIdx.x == 0) a.offsets[E] = S;
     }
     __syncwarp();
@@ -295,44 +427,18 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   __syncthreads();
 
   const int n_act = sm->n_act;
-  const int gu_per_group = I / kFdGuPairs;
-  const int dn_per_group = H / kFdDnRows;
   const int nB = n_act * gu_per_group;
   const int nC = n_act * dn_per_group;
 
   if (warp == kFdProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = early ? 1 : 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < nB + nC; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x + static_cast<int>(it) * gridDim.x; u < nB + nC; u += gridDim.x, ++it) {
         const int slot = it % NS;
         if (!(ok = fd_wait(&sm->empty[slot], ((it / NS) & 1) ^ 1, sm, a.status))) break;
-        uint8_t* dst = ring + slot * a.slot_bytes;
-        if (u < nB) {
-          const int g = sm->act[u / gu_per_group];
-          const int j0 = (u % gu_per_group) * kFdGuPairs;
-          const int64_t rg = static_cast<int64_t>(g) * 2 * I + j0;   // first gate row
-          const int64_t ru = rg + I;                                   // first up row
-          const uint32_t pb = kFdGuPairs * (H / 2), sb = kFdGuPairs * (H / 16);
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm->full[slot])),
-                       "r"(2 * pb + 2 * sb)
-                       : "memory");
-          bulk_g2s(dst, a.gu_packed + rg * (H / 2), pb, &sm->full[slot]);
-          bulk_g2s(dst + pb, a.gu_packed + ru * (H / 2), pb, &sm->full[slot]);
-          bulk_g2s(dst + 2 * pb, a.gu_scales + rg * (H / 16), sb, &sm->full[slot]);
-          bulk_g2s(dst + 2 * pb + sb, a.gu_scales + ru * (H / 16), sb, &sm->full[slot]);
-        } else {
-          const int v = u - nB;
-          const int g = sm->act[v / dn_per_group];
-          const int64_t r0 = static_cast<int64_t>(g) * H + (v % dn_per_group) * kFdDnRows;
-          const uint32_t pb = kFdDnRows * (I / 2), sb = kFdDnRows * (I / 16);
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(&sm->full[slot])),
-                       "r"(pb + sb)
-                       : "memory");
-          bulk_g2s(dst, a.dn_packed + r0 * (I / 2), pb, &sm->full[slot]);
-          bulk_g2s(dst + pb, a.dn_scales + r0 * (I / 16), sb, &sm->full[slot]);
-        }
+        issue(u, nB, it);
       }
       if (!ok) {  // let copies already issued land before the CTA exits (bounded)
         for (uint32_t j = 0; j < static_cast<uint32_t>(NS) && j < it; ++j) {
@@ -346,42 +452,44 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   }
 
   // ------------------------------------------------------------ compute warps
-  // Units u = blockIdx.x, blockIdx.x + gridDim.x, ... over [0, nB + nC): the producer walks the
-  // same sequence, so the two sides agree on every slot.  u < nB are gate_up units, the rest
-  // down units (v = u - nB).
-  uint32_t it = 0;
+  // This CTA's units are u = blockIdx.x + i * gridDim.x, i = 0, 1, ... over [0, nB + nC), in
+  // the producer's order; warp group wg takes i = wg, wg + 2, ...  (slot i % NS).
+  const int wg = warp / kFdGroupWarps, gw = warp % kFdGroupWarps;
   bool ok = true;
   const int hb = H / 16;   // 16-element blocks per gate_up row
-  int u = blockIdx.x;
-  // phase B: gate_up units; warp w owns gate row j0 + w and up row j0 + w of the unit
-  for (; u < nB; u += gridDim.x, ++it) {
-    const int slot = it % NS;
-    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, sm, a.status));
+  const int nB_cta = (blockIdx.x < nB) ? (nB - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int n_cta = (blockIdx.x < nB + nC) ? (nB + nC - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // phase B: gate_up units; warp gw owns gate row j0 + gw and up row j0 + gw of the unit
+  for (int i = wg; i < nB_cta; i += kFdGroups) {
+    const int u = blockIdx.x + i * gridDim.x;
+    const int slot = i % NS;
+    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (i / NS) & 1, sm, a.status));
     if (ok) {
       const int gi = u / gu_per_group;
       const int g = sm->act[gi];
-      const int j = (u % gu_per_group) * kFdGuPairs + warp;
+      const int j = (u % gu_per_group) * kFdGuPairs + gw;
       const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
       const uint8_t* sl = ring + slot * a.slot_bytes;
-      const uint8_t* pg = sl + warp * (H / 2);
-      const uint8_t* pu = sl + (kFdGuPairs + warp) * (H / 2);
-      const uint8_t* sg = sl + 2 * kFdGuPairs * (H / 2) + warp * (H / 16);
+      const uint8_t* pg = sl + gw * (H / 2);
+      const uint8_t* pu = sl + (kFdGuPairs + gw) * (H / 2);
+      const uint8_t* sg = sl + 2 * kFdGuPairs * (H / 2) + gw * (H / 16);
       const uint8_t* su = sg + kFdGuPairs * (H / 16);
       const float s2 = __ldg(a.gu_scale2 + g);
       for (int te = 0; te < nt; ++te) {
         const int p = row0 + te;
         const int t = (g == E) ? te : sm->sorted[p] / k;
         const uint16_t* xt = xs + t * H;
-        float ag = 0.0f, au = 0.0f;
+        float acc[2] = {0.0f, 0.0f};
+#pragma unroll 4
         for (int b = lane; b < hb; b += 32) {
           float xv[16];
           bf16x16_to_f32(xt + b * 16, xv, false);
-          ag += block_dot(*reinterpret_cast<const uint2*>(pg + b * 8), sg[b], xv);
-          au += block_dot(*reinterpret_cast<const uint2*>(pu + b * 8), su[b], xv);
+          acc[0] += block_dot(*reinterpret_cast<const uint2*>(pg + b * 8), sg[b], xv);
+          acc[1] += block_dot(*reinterpret_cast<const uint2*>(pu + b * 8), su[b], xv);
         }
-        ag = warp_sum(ag);
-        au = warp_sum(au);
-        if (lane == 0) a.h[static_cast<int64_t>(p) * I + j] = f32_to_bf16_bits(silu_f32(ag * s2) * (au * s2));
+        const float r = warp_reduce_multi<2>(acc, lane);   // lanes 0-15: gate, 16-31: up
+        const float uval = __shfl_sync(0xffffffffu, r, 16);
+        if (lane == 0) a.h[static_cast<int64_t>(p) * I + j] = f32_to_bf16_bits(silu_f32(r * s2) * (uval * s2));
       }
     }
     __syncwarp();
@@ -392,20 +500,22 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   compute_sync();
   ok = ok && !*reinterpret_cast<volatile int*>(&sm->abort_flag);
 
-  // phase C: down units; warp w owns output rows n0 + 8w .. n0 + 8w + 7
+  // phase C: down units; warp gw owns output rows n0 + 8 gw .. n0 + 8 gw + 7
   const int ib = I / 16;
-  for (; u < nB + nC; u += gridDim.x, ++it) {
-    const int slot = it % NS;
-    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, sm, a.status));
+  const int i0 = nB_cta + ((wg - nB_cta) % kFdGroups + kFdGroups) % kFdGroups;   // first i >= nB_cta with i % 2 == wg
+  for (int i = i0; i < n_cta; i += kFdGroups) {
+    const int u = blockIdx.x + i * gridDim.x;
+    const int slot = i % NS;
+    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (i / NS) & 1, sm, a.status));
     if (ok) {
       const int v = u - nB;
       const int gi = v / dn_per_group;
       const int g = sm->act[gi];
-      const int n0 = (v % dn_per_group) * kFdDnRows + warp * 8;
+      const int n0 = (v % dn_per_group) * kFdDnRows + gw * 8;
       const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
       const uint8_t* sl = ring + slot * a.slot_bytes;
-      const uint8_t* pr = sl + warp * 8 * (I / 2);
-      const uint8_t* sr = sl + kFdDnRows * (I / 2) + warp * 8 * (I / 16);
+      const uint8_t* pr = sl + gw * 8 * (I / 2);
+      const uint8_t* sr = sl + kFdDnRows * (I / 2) + gw * 8 * (I / 16);
       const float s2 = __ldg(a.dn_scale2 + g);
       for (int te = 0; te < nt; ++te) {
         const int p = row0 + te;
@@ -420,14 +530,8 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
           for (int r = 0; r < 8; ++r)
             acc[r] += block_dot(*reinterpret_cast<const uint2*>(pr + r * (I / 2) + b * 8), sr[r * (I / 16) + b], hv);
         }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) acc[r] = warp_sum(acc[r]);
-        if (lane < 8) {
-          float v = acc[0];
-#pragma unroll
-          for (int r = 1; r < 8; ++r) v = (lane == r) ? acc[r] : v;
-          a.y[static_cast<int64_t>(p) * H + n0 + lane] = v * s2;
-        }
+        const float r = warp_reduce_multi<8>(acc, lane);   // lane l: row (l >> 2) & 7
+        if ((lane & 3) == 0) a.y[static_cast<int64_t>(p) * H + n0 + (lane >> 2)] = r * s2;
       }
     }
     __syncwarp();
@@ -469,7 +573,8 @@ bool fd_plan(const moe_shape_t& s, FdPlan* p) {
   const int avail = kFdSmemLimit - 1024 - p->ring_off;
   p->n_slots = std::min(kFdMaxSlots, avail / p->slot_bytes);
   p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * p->slot_bytes;
-  return p->n_slots >= 3;
+  const int cand_bytes = s.T * ((s.E + 31) / 32) * std::min(s.k, 32) * 8;
+  return p->n_slots >= 3 && (p->n_slots - 1) * p->slot_bytes >= cand_bytes;
 }
 
 template <int EPL>
