@@ -7,16 +7,20 @@
 //
 // Swap-AB: the MMA's M dimension is 128 weight rows of one expert, N is up to 128 of that
 // expert's tokens, so a small expert group still fills M.  Per CTA (one per SM, persistent):
-//   warp 0      TMA producer: packed e2m1 tiles (and, for down, the bf16 activation tile)
-//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, A from TMEM, B from SMEM
-//   warps 2-5   dequant: one weight row per thread, e2m1 x e4m3 -> bf16 exactly (every
-//               product fits bf16), written to TMEM with tcgen05.st as the A operand
-//   warps 6-9   gate_up only: gather of the expert's token rows of x into 128B-swizzled SMEM
-//   warps 10-13 epilogue: tcgen05.ld of the fp32 accumulator, x scale2, SiLU(gate)*up (gate_up)
-// The accumulator is double-buffered in TMEM so the epilogue of one tile overlaps the next
-// tile's main loop.  Dequantizing into TMEM rather than SMEM leaves the shared-memory bandwidth
-// to the B operand.  Every mbarrier wait is bounded; on timeout the kernel records
-// MOE_ERR_DEVICE_TIMEOUT in the workspace status word and winds down.
+//   warp 0       TMA producer: packed e2m1 + e4m3 scale tiles (K = 256 per stage) and, for
+//                down, the bf16 activation tiles (K = 64 per stage)
+//   warp 1       MMA issuer (one thread): tcgen05.mma kind::f16, A from TMEM, B from SMEM
+//   warps 2-9    dequant: one weight row per thread (two warps per TMEM lane quarter, taking
+//                alternate 64-wide K chunks), e2m1 x e4m3 -> bf16 exactly (every product fits
+//                bf16), written to TMEM with tcgen05.st as the A operand
+//   warps 10-13  gate_up only: gather of the expert's token rows of x into 128B-swizzled SMEM
+//   warps 14-17  epilogue: tcgen05.ld of the fp32 accumulator, x scale2, SiLU(gate)*up (gate_up)
+// Three rings decouple the producers: packed weights (SMEM, K = 256 per stage, deep enough to
+// cover an HBM round trip), dequantized A (TMEM, K = 64 per stage) and activations (SMEM,
+// K = 64 per stage).  The accumulator is double-buffered in TMEM so the epilogue of one tile
+// overlaps the next tile's main loop.  Dequantizing into TMEM rather than SMEM leaves the
+// shared-memory bandwidth to the B operand.  Every mbarrier wait is bounded; on timeout the
+// kernel records MOE_ERR_DEVICE_TIMEOUT in the workspace status word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -29,17 +33,24 @@ namespace {
 
 constexpr int kBM = 128;                      // weight rows per tile (MMA M)
 constexpr int kBN = kTcTileRows;              // tokens per tile (MMA N, rounded up to 16)
-constexpr int kBK = 64;                       // K per stage
-constexpr int kStages = 6;
-constexpr int kAStageBytes = kBM * kBK / 2;   // packed e2m1 tile: 128 rows x 32 B
+constexpr int kBK = 64;                       // K per MMA stage (TMEM A stage, B stage)
+constexpr int kAK = 256;                      // K per packed-weight stage
+constexpr int kAStages = 4;                   // packed-weight ring (SMEM)
+constexpr int kTStages = 4;                   // dequantized-A ring (TMEM)
+constexpr int kBStages = 6;                   // activation ring (SMEM)
+constexpr int kAPackedBytes = kBM * kAK / 2;  // 16 KB: 128 rows x 128 B, 128B swizzle
+constexpr int kAScaleBytes = kBM * kAK / 16;  // 2 KB: 128 rows x 16 B
+constexpr int kAStageBytes = kAPackedBytes + kAScaleBytes;
 constexpr int kBStageBytes = kBN * kBK * 2;   // bf16 tile: 128 rows x 128 B (128B swizzle)
 constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                      // accumulators: 2 x 128 columns
-constexpr int kACol = 2 * kBN;                // A stages: kStages x 32 columns
-static_assert(kACol + kStages * (kBK / 2) <= kTmemCols, "TMEM budget");
+constexpr int kACol = 2 * kBN;                // A stages: kTStages x 32 columns
+static_assert(kACol + kTStages * (kBK / 2) <= kTmemCols, "TMEM budget");
+static_assert(kAK / kBK == 4 && kTStages == 4, "dequant halves own TMEM slots {h, h+2}");
 
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpGather = 6, kWarpEpi = 10;
-constexpr int kThreads = 14 * 32;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpGather = 10, kWarpEpi = 14;
+constexpr int kDeqWarps = 8;
+constexpr int kThreads = 18 * 32;
 constexpr uint32_t kSpinLimit = 1u << 24;      // drain loops only
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: no legitimate wait comes close
 
@@ -58,10 +69,12 @@ struct TcArgs {
 };
 
 struct Smem {
-  uint64_t a_tma_full[kStages];
-  uint64_t a_full[kStages];
-  uint64_t b_full[kStages];
-  uint64_t stage_free[kStages];
+  uint64_t a_full[kAStages];     // packed tile + scales landed (TMA transaction)
+  uint64_t a_free[kAStages];     // every dequant warp is done reading the stage
+  uint64_t t_full[kTStages];     // dequantized A written to TMEM (128 threads)
+  uint64_t t_free[kTStages];     // the MMAs reading that TMEM stage completed
+  uint64_t b_full[kBStages];     // activation tile ready (gather threads or TMA)
+  uint64_t b_free[kBStages];     // the MMAs reading that activation tile completed
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -212,25 +225,33 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_splat(uint32_t byte) {
 
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                           TcArgs a) {
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
+                           const __grid_constant__ CUtensorMap tmB, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = base;                                  // kStages x 4 KB
-  uint8_t* sB = base + kStages * kAStageBytes;         // kStages x 16 KB (1024-aligned)
-  Smem* sm = reinterpret_cast<Smem*>(sB + kStages * kBStageBytes);
+  uint8_t* sB = base;                                   // kBStages x 16 KB (1024-aligned)
+  uint8_t* sA = base + kBStages * kBStageBytes;         // kAStages x 18 KB (1024-aligned)
+  Smem* sm = reinterpret_cast<Smem*>(sA + kAStages * kAStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MB = a.Nw / kBM;                           // m-blocks per group
-  const int KS = a.K / kBK;                            // K stages per item
+  const int KS = a.K / kBK;                            // MMA stages per item
+  const int KA = a.K / kAK;                            // packed-weight stages per item
   const int n_items = __ldg(a.meta) * MB;
+  const int half_rows = kGateUp ? kBM / 2 : kBM;       // rows per TMA box
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm->a_tma_full[s], 1);
-      mbar_init(&sm->a_full[s], 128);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&sm->a_full[s], 1);
+      mbar_init(&sm->a_free[s], kDeqWarps);
+    }
+    for (int s = 0; s < kTStages; ++s) {
+      mbar_init(&sm->t_full[s], 128);
+      mbar_init(&sm->t_free[s], 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
       mbar_init(&sm->b_full[s], kGateUp ? 128 : 1);
-      mbar_init(&sm->stage_free[s], 1);
+      mbar_init(&sm->b_free[s], 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm->acc_full[d], 1);
@@ -252,32 +273,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     if (lane == 0) {
-      uint32_t it = 0;
+      // Issue order: packed stage ka, then (down) its four activation stages.  The producer only
+      // ever waits for resources freed by work it has already issued, so the order cannot stall.
+      uint32_t ia = 0, ib = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const int4 td = __ldg(a.tiles + item / MB);
         const int mb = item % MB;
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int st = it % kStages;
-          if (!(ok = mbar_wait(&sm->stage_free[st], ((it / kStages) & 1) ^ 1, sm, a.status))) break;
+        const int r0 = td.x * a.Nw + (kGateUp ? mb * (kBM / 2) : mb * kBM);
+        for (int ka = 0; ok && ka < KA; ++ka, ++ia) {
+          const int st = ia % kAStages;
+          if (!(ok = mbar_wait(&sm->a_free[st], ((ia / kAStages) & 1) ^ 1, sm, a.status))) break;
           uint8_t* dA = sA + st * kAStageBytes;
-          mbar_expect_tx(&sm->a_tma_full[st], kAStageBytes);
-          if (kGateUp) {
-            const int I = a.Nw / 2;
-            const int r0 = td.x * a.Nw + mb * 64;
-            tma_load_2d(dA, &tmA, ks * (kBK / 2), r0, &sm->a_tma_full[st]);
-            tma_load_2d(dA + 64 * (kBK / 2), &tmA, ks * (kBK / 2), r0 + I, &sm->a_tma_full[st]);
+          mbar_expect_tx(&sm->a_full[st], kAStageBytes);
+          tma_load_2d(dA, &tmA, ka * (kAK / 2), r0, &sm->a_full[st]);
+          tma_load_2d(dA + kAPackedBytes, &tmS, ka * (kAK / 16), r0, &sm->a_full[st]);
+          if (kGateUp) {   // the matching up rows: I rows further down the group
+            tma_load_2d(dA + half_rows * (kAK / 2), &tmA, ka * (kAK / 2), r0 + a.Nw / 2, &sm->a_full[st]);
+            tma_load_2d(dA + kAPackedBytes + half_rows * (kAK / 16), &tmS, ka * (kAK / 16), r0 + a.Nw / 2,
+                        &sm->a_full[st]);
           } else {
-            tma_load_2d(dA, &tmA, ks * (kBK / 2), td.x * a.Nw + mb * kBM, &sm->a_tma_full[st]);
-            mbar_expect_tx(&sm->b_full[st], kBStageBytes);
-            tma_load_2d(sB + st * kBStageBytes, &tmB, ks * kBK, td.y, &sm->b_full[st]);
+            for (int kb = 0; kb < kAK / kBK; ++kb, ++ib) {
+              const int sb = ib % kBStages;
+              if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
+              mbar_expect_tx(&sm->b_full[sb], kBStageBytes);
+              tma_load_2d(sB + sb * kBStageBytes, &tmB, (ka * (kAK / kBK) + kb) * kBK, td.y, &sm->b_full[sb]);
+            }
           }
         }
       }
-      if (!ok) {  // let copies already issued land before the CTA winds down
-        for (int j = 0; j < kStages && it > 0; ++j, --it) {
-          const uint32_t q = it - 1;
-          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->a_tma_full[q % kStages], (q / kStages) & 1); ++i) {
+      if (!ok) {  // let copies already issued land before the CTA winds down (bounded)
+        for (int j = 0; j < kAStages && ia > 0; ++j, --ia) {
+          const uint32_t q = ia - 1;
+          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->a_full[q % kAStages], (q / kAStages) & 1); ++i) {
+          }
+        }
+        for (int j = 0; j < kBStages && ib > 0; ++j, --ib) {
+          const uint32_t q = ib - 1;
+          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->b_full[q % kBStages], (q / kBStages) & 1); ++i) {
           }
         }
       }
@@ -295,17 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + kDCol + d * kBN;
         for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int st = it % kStages;
-          const uint32_t par = (it / kStages) & 1;
-          if (!(ok = mbar_wait(&sm->a_full[st], par, sm, a.status))) break;
-          if (!(ok = mbar_wait(&sm->b_full[st], par, sm, a.status))) break;
+          const int ts = it % kTStages, bs = it % kBStages;
+          if (!(ok = mbar_wait(&sm->t_full[ts], (it / kTStages) & 1, sm, a.status))) break;
+          if (!(ok = mbar_wait(&sm->b_full[bs], (it / kBStages) & 1, sm, a.status))) break;
           tc_fence_after();
-          const uint32_t b_addr = smem_u32(sB + st * kBStageBytes);
+          const uint32_t b_addr = smem_u32(sB + bs * kBStageBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma(d_tmem, tmem + kACol + st * (kBK / 2) + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
+            tc_mma(d_tmem, tmem + kACol + ts * (kBK / 2) + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
                    (ks | kk) != 0);
-          tc_commit(&sm->stage_free[st]);
+          tc_commit(&sm->t_free[ts]);
+          tc_commit(&sm->b_free[bs]);
         }
         if (ok) tc_commit(&sm->acc_full[d]);
       }
@@ -314,57 +347,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t i = 0; i < kSpinLimit && !mbar_try(&sm->drain, 0); ++i) {
       }
     }
-  } else if (warp >= kWarpDeq && warp < kWarpDeq + 4) {
+  } else if (warp >= kWarpDeq && warp < kWarpDeq + kDeqWarps) {
     const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int r = q * 32 + lane;            // tile row == TMEM lane
-    int srow;                               // SMEM row of the packed tile
-    int wrow_off;                           // weight row within the group, relative to the m-block
+    const int hsel = (warp - kWarpDeq) >> 2;   // which two of the four 64-wide K chunks
+    int srow;                               // SMEM row of the packed tile (== weight row offset)
     if (kGateUp) {
       const int half = lane >> 4, j = q * 16 + (lane & 15);
-      srow = half * 64 + j;
-      wrow_off = j + half * (a.Nw / 2);
+      srow = half * (kBM / 2) + j;          // lanes 0-15 gate rows, 16-31 the matching up rows
     } else {
-      srow = r;
-      wrow_off = r;
+      srow = q * 32 + lane;
     }
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t it = 0;
+    uint32_t ia = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const int4 td = __ldg(a.tiles + item / MB);
-      const int mb = item % MB;
-      const int64_t wrow = static_cast<int64_t>(td.x) * a.Nw + (kGateUp ? mb * 64 : mb * kBM) + wrow_off;
-      const uint8_t* srow_scales = a.scales + wrow * (a.K / 16);
-      uint4 sc = make_uint4(0, 0, 0, 0);
-      for (int ks = 0; ks < KS; ++ks, ++it) {
-        const int st = it % kStages;
-        if ((ks & 3) == 0) sc = __ldg(reinterpret_cast<const uint4*>(srow_scales + (ks >> 2) * 16));
-        if (!(ok = warp_wait(&sm->a_tma_full[st], (it / kStages) & 1, sm, a.status))) break;
-        const uint8_t* rowp = sA + st * kAStageBytes + srow * 32;
-        const int sw = (srow >> 2) & 1;     // 32-byte swizzle: 16-byte chunk index ^= row bit 2
-        const uint4 p0 = *reinterpret_cast<const uint4*>(rowp + ((0 ^ sw) << 4));
-        const uint4 p1 = *reinterpret_cast<const uint4*>(rowp + ((1 ^ sw) << 4));
-        const uint32_t scw = (&sc.x)[ks & 3];   // 4 scale bytes: blocks of 16 k of this stage
-        uint32_t o[32];
-        const uint32_t pw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      for (int ka = 0; ka < KA; ++ka, ++ia) {
+        const int st = ia % kAStages;
+        if (!(ok = warp_wait(&sm->a_full[st], (ia / kAStages) & 1, sm, a.status))) break;
+        const uint8_t* stage = sA + st * kAStageBytes;
+        const uint8_t* rowp = stage + srow * (kAK / 2);
+        const uint4 sc = *reinterpret_cast<const uint4*>(stage + kAPackedBytes + srow * (kAK / 16));
+        uint4 pk[2][2];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const uint32_t s2 = e4m3_to_f16x2_splat((scw >> (8 * b)) & 0xffu);
-          dequant8(pw[2 * b], s2, o + 8 * b);
-          dequant8(pw[2 * b + 1], s2, o + 8 * b + 4);
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int ss = hsel + 2 * h2;     // 64-wide chunk of this 256-wide stage
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = 2 * ss + c2;      // 16-byte chunk, 128B swizzle: chunk ^= row & 7
+            pk[h2][c2] = *reinterpret_cast<const uint4*>(rowp + ((c ^ (srow & 7)) << 4));
+          }
         }
         __syncwarp();
-        TC_ST32(t_lane + kACol + st * (kBK / 2), o);
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        mbar_arrive(&sm->a_full[st]);
+        if (lane == 0) mbar_arrive(&sm->a_free[st]);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int ss = hsel + 2 * h2;
+          const uint32_t it = ia * 4 + ss;
+          const int ts = it % kTStages;
+          const uint32_t scw = (&sc.x)[ss];
+          uint32_t o[32];
+          const uint32_t pw[8] = {pk[h2][0].x, pk[h2][0].y, pk[h2][0].z, pk[h2][0].w,
+                                  pk[h2][1].x, pk[h2][1].y, pk[h2][1].z, pk[h2][1].w};
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const uint32_t s2 = e4m3_to_f16x2_splat((scw >> (8 * b)) & 0xffu);
+            dequant8(pw[2 * b], s2, o + 8 * b);
+            dequant8(pw[2 * b + 1], s2, o + 8 * b + 4);
+          }
+          if (!(ok = warp_wait(&sm->t_free[ts], ((it / kTStages) & 1) ^ 1, sm, a.status))) break;
+          tc_fence_after();
+          __syncwarp();
+          TC_ST32(t_lane + kACol + ts * (kBK / 2), o);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          mbar_arrive(&sm->t_full[ts]);
+        }
       }
     }
   } else if (warp >= kWarpGather && warp < kWarpGather + 4) {
     if (kGateUp) {
       const int t = threadIdx.x - kWarpGather * 32;   // 0..127
       const int c = t & 7;                            // 16-byte chunk of a 128-byte row
-      uint32_t it = 0;
+      uint32_t ib = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const int4 td = __ldg(a.tiles + item / MB);
@@ -389,10 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             src[i] = static_cast<int64_t>(tok) * a.K + c * 8;
           }
         }
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int st = it % kStages;
-          if (!(ok = mbar_wait(&sm->stage_free[st], ((it / kStages) & 1) ^ 1, sm, a.status))) break;
-          uint8_t* dB = sB + st * kBStageBytes;
+        for (int ks = 0; ks < KS; ++ks, ++ib) {
+          const int sb = ib % kBStages;
+          if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
+          uint8_t* dB = sB + sb * kBStageBytes;
           uint4 v[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -404,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(dB + row * 128 + ((c ^ (row & 7)) << 4)) = v[i];
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(&sm->b_full[st]);
+          mbar_arrive(&sm->b_full[sb]);
         }
       }
     }
@@ -496,7 +540,7 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + sizeof(Smem);
+constexpr size_t kSmemBytes = 1024 + kBStages * kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
 
 int sm_count() {
   static int n = 0;
@@ -519,9 +563,13 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
     attr_set = true;
   }
   const int G = g.E + 1;
-  CUtensorMap tmA, tmB;
+  const int box_rows = kGateUp ? kBM / 2 : kBM;
+  CUtensorMap tmA, tmS, tmB;
   if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.packed, g.K / 2, static_cast<uint64_t>(G) * g.N,
-                   kBK / 2, kGateUp ? 64 : kBM, CU_TENSOR_MAP_SWIZZLE_32B))
+                   kAK / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.scales, g.K / 16, static_cast<uint64_t>(G) * g.N,
+                   kAK / 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (kGateUp) {
     tmB = tmA;
@@ -546,7 +594,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.status = g.status;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, sm_count()));
-  grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmB, a);
+  grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmS, tmB, a);
   return cudaGetLastError();
 }
 
