@@ -331,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ts = it % kTStages, bs = it % kBStages;
           if (!(ok = mbar_wait(&sm->t_full[ts], (it / kTStages) & 1, sm, a.status))) break;
           if (!(ok = mbar_wait(&sm->b_full[bs], (it / kBStages) & 1, sm, a.status))) break;
+          if (kGateUp)  // the gathered tile was written by cp.async (generic proxy); the MMA reads it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // through the async proxy
           tc_fence_after();
           const uint32_t b_addr = smem_u32(sB + bs * kBStageBytes);
 #pragma unroll
@@ -436,19 +438,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < KS; ++ks, ++ib) {
           const int sb = ib % kBStages;
           if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
-          uint8_t* dB = sB + sb * kBStageBytes;
-          uint4 v[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            v[i] = (src[i] >= 0) ? __ldg(reinterpret_cast<const uint4*>(a.act + src[i] + ks * kBK))
-                                 : make_uint4(0, 0, 0, 0);
+          const uint32_t dB = smem_u32(sB + sb * kBStageBytes);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int row = (t >> 3) + 16 * i;
-            *reinterpret_cast<uint4*>(dB + row * 128 + ((c ^ (row & 7)) << 4)) = v[i];
+            // 16-byte async copy into the 128B-swizzled slot; padding rows are zero-filled
+            const bool live = src[i] >= 0;
+            const uint16_t* gsrc = a.act + (live ? src[i] + ks * kBK : 0);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dB + row * 128 + ((c ^ (row & 7)) << 4)),
+                         "l"(gsrc), "r"(live ? 16 : 0)
+                         : "memory");
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(&sm->b_full[sb]);
+          // the barrier gets this thread's arrival once its copies above have landed
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sm->b_full[sb]))
+                       : "memory");
         }
       }
     }
