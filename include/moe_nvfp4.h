@@ -154,6 +154,29 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                                   void* out, int out_is_fp32, void* ws, size_t ws_bytes,
                                   void* stream, void* const* stage_events);
 
+/* The one-launch decode forward (moe_forward_arm == 0 shapes: T <= 8, H % 512 == 0, H <= 4096,
+ * I <= 1024) for callers that cannot allocate device memory -- code running where cudaMalloc is
+ * not allowed or not available, such as inside a framework's memory-planning phase, a host
+ * callback, or a plugin whose host application owns every device allocation and only passes in
+ * tensor pointers.  No workspace argument: the scratch (routing results, permutation, h, y, the
+ * status word and grid-barrier counters) lives in one 4 MiB array in device global memory that
+ * the library declares at file scope; every GPU that loads the library holds it until the
+ * library is unloaded.  The pages have no counterpart to this call; it is a deployment aid.
+ *   - Inputs, weights and out are as for moe_forward; nothing is allocated or freed.
+ *   - Shapes whose scratch exceeds 4 MiB, and shapes outside arm 0, return
+ *     MOE_ERR_UNSUPPORTED_SHAPE.
+ *   - All calls on a device share the array: calls that overlap on the GPU (other streams or
+ *     threads) race and corrupt each other; serialize them.
+ *   - The first call on a device looks up the array's device address; make it outside any CUDA
+ *     stream capture.
+ *   - Each call first clears the status and barrier words on `stream` (an asynchronous memset).
+ *     Device-side timeouts are not reported back by this call. */
+moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, const float* logits,
+                                               const moe_nvfp4_weights_t* gate_up,
+                                               const moe_nvfp4_weights_t* down,
+                                               const moe_shape_t* shape, void* out,
+                                               int out_is_fp32, void* stream);
+
 /* Load-time NVFP4 quantizer of fp32 weights [G, N, K] (K % 16 == 0, finite values) into the
  * layout above, with the recipe of the benchmark configurations: scale2 = amax / (448 * 6);
  * block scale = e4m3_rne_satfinite(block_amax / 6 / scale2); code = e2m1_rne_satfinite(
