@@ -70,6 +70,10 @@ struct Ws {
   int32_t* hist;
   uint16_t* h;
   float* y;
+  uint16_t* xf;
+  int32_t* xe;
+  uint16_t* hf;
+  int32_t* he;
   WsLayout L;
 };
 
@@ -89,6 +93,10 @@ Ws carve(void* ws, const moe_shape_t& s) {
   r.hist = reinterpret_cast<int32_t*>(b + r.L.hist);
   r.h = reinterpret_cast<uint16_t*>(b + r.L.h);
   r.y = reinterpret_cast<float*>(b + r.L.y);
+  r.xf = reinterpret_cast<uint16_t*>(b + r.L.xf);
+  r.xe = reinterpret_cast<int32_t*>(b + r.L.xe);
+  r.hf = reinterpret_cast<uint16_t*>(b + r.L.hf);
+  r.he = reinterpret_cast<int32_t*>(b + r.L.he);
   return r;
 }
 
@@ -115,12 +123,24 @@ int tile_rows_for(const moe_shape_t& s) {
   }
 }
 
-cudaError_t launch_gate_up(const GroupedArgs& a, const moe_shape_t& s, cudaStream_t cs) {
-  return arm_for(s) == Arm::kTc ? launch_gate_up_tc(a, cs) : launch_gate_up_simt(a, cs);
+// The tensor-core arm takes its activations as f16 rows with power-of-two row exponents: x (or
+// h) is converted into the workspace first.
+cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaStream_t cs) {
+  if (arm_for(s) != Arm::kTc) return launch_gate_up_simt(a, cs);
+  cudaError_t e = launch_act_to_f16(a.act, ws.xf, ws.xe, s.T, s.H, cs);
+  if (e != cudaSuccess) return e;
+  a.act = ws.xf;
+  a.act_exp = ws.xe;
+  return launch_gate_up_tc(a, cs);
 }
 
-cudaError_t launch_down(const GroupedArgs& a, const moe_shape_t& s, cudaStream_t cs) {
-  return arm_for(s) == Arm::kTc ? launch_down_tc(a, cs) : launch_down_simt(a, cs);
+cudaError_t launch_down(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaStream_t cs) {
+  if (arm_for(s) != Arm::kTc) return launch_down_simt(a, cs);
+  cudaError_t e = launch_act_to_f16(a.act, ws.hf, ws.he, static_cast<int64_t>(s.T) * s.k + s.T, s.I, cs);
+  if (e != cudaSuccess) return e;
+  a.act = ws.hf;
+  a.act_exp = ws.he;
+  return launch_down_tc(a, cs);
 }
 
 GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, const uint16_t* act,
@@ -142,6 +162,7 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   a.max_tiles = max_tiles_for(s, tile_rows_for(s));
   a.out = out;
   a.status = ws.status;
+  a.act_exp = nullptr;
   return a;
 }
 
@@ -180,6 +201,10 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.hist = take(4 * static_cast<size_t>(std::max<int64_t>(1, L.n_chunks)) * s.E);
   L.h = take(2 * static_cast<size_t>(R) * s.I);
   L.y = take(4 * static_cast<size_t>(R) * s.H);
+  L.xf = take(2 * static_cast<size_t>(s.T) * s.H);
+  L.xe = take(4 * static_cast<size_t>(s.T));
+  L.hf = take(2 * static_cast<size_t>(R) * s.I);
+  L.he = take(4 * static_cast<size_t>(R));
   L.total = off;
   return L;
 }
@@ -250,7 +275,7 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
   cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
                                      w.tiles, w.meta, w.status, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, cs));
+  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, w, cs));
 }
 
 moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
@@ -269,7 +294,7 @@ moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
   cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
                                      w.tiles, w.meta, w.status, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_down(grouped_args(*down, s, h, nullptr, w, y), s, cs));
+  return cuda_status(launch_down(grouped_args(*down, s, h, nullptr, w, y), s, w, cs));
 }
 
 moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* topk_w,
@@ -387,9 +412,9 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                            w.meta, w.status, cs);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
-    e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, cs);
+    e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, w, cs);
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess) e = launch_down(grouped_args(*down, s, w.h, nullptr, w, w.y), s, cs);
+  if (e == cudaSuccess) e = launch_down(grouped_args(*down, s, w.h, nullptr, w, w.y), s, w, cs);
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
     e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32,

@@ -1,0 +1,63 @@
+// bf16 activation rows -> f16 rows with a per-row power-of-two scale, for the f16 tensor-core
+// GEMMs of the prefill arm.
+//
+// Row r is written as f16(x[r] * 2^-e[r]) with e[r] = floor(log2(max |x[r]|)) - 14, so the row's
+// largest element lands in [2^14, 2^15), well inside f16's range.  A bf16 value has 8 significant
+// bits and f16 11, so every element of at least 2^-31 of the row maximum converts exactly; only
+// smaller ones (below f16's subnormal grid) are rounded.  The GEMM epilogue multiplies the fp32
+// accumulator by 2^e[r] again, so the products are the bf16 activations' own.
+#include "internal.cuh"
+
+namespace moe {
+namespace {
+
+// One warp per row; K % 256 == 0 (eight bf16 per lane per step).
+__global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restrict__ src,
+                                                         uint16_t* __restrict__ dst,
+                                                         int32_t* __restrict__ exps, int64_t rows,
+                                                         int K) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (r >= rows) return;
+  const uint4* s = reinterpret_cast<const uint4*>(src + r * K);
+  float m = 0.0f;
+  for (int c = lane; c < K / 8; c += 32) {
+    const uint4 v = __ldg(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const int e = (m > 0.0f && m <= 3.4e38f) ? ilogbf(m) - 14 : 0;
+  if (lane == 0) exps[r] = e;
+  uint4* d = reinterpret_cast<uint4*>(dst + r * K);
+  for (int c = lane; c < K / 8; c += 32) {
+    const uint4 v = __ldg(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = ldexpf(__uint_as_float(w[i] << 16), -e);
+      const float hi = ldexpf(__uint_as_float(w[i] & 0xffff0000u), -e);
+      const __half2 h = __floats2half2_rn(lo, hi);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    d[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, int32_t* exps, int64_t rows, int K,
+                              cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, dst, exps, rows, K);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

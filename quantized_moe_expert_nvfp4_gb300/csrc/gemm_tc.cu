@@ -11,10 +11,16 @@
 //                down, the bf16 activation tiles (K = 64 per stage)
 //   warp 1       MMA issuer (one thread): tcgen05.mma kind::f16, A from TMEM, B from SMEM
 //   warps 2-9    dequant: one weight row per thread (two warps per TMEM lane quarter, taking
-//                alternate 64-wide K chunks), e2m1 x e4m3 -> bf16 exactly (every product fits
-//                bf16), written to TMEM with tcgen05.st as the A operand
+//                alternate 64-wide K chunks), e2m1 x e4m3 -> f16 exactly (every product has at
+//                most 6 significant bits and lies in [2^-10, 2688]), written to TMEM with
+//                tcgen05.st as the A operand
 //   warps 10-13  gate_up only: gather of the expert's token rows of x into 128B-swizzled SMEM
-//   warps 14-17  epilogue: tcgen05.ld of the fp32 accumulator, x scale2, SiLU(gate)*up (gate_up)
+//   warps 14-17  epilogue: tcgen05.ld of the fp32 accumulator, x scale2 x 2^e (the activation
+//                row's exponent), SiLU(gate)*up (gate_up)
+// The MMA is kind::f16 with f16 operands: the activations arrive as f16 rows scaled by a power
+// of two per row (exact for every element above 2^-31 of the row maximum), so the dequantization
+// is one conversion and one packed multiply per pair of weights instead of the five a bf16
+// operand needs, and the products and the fp32 accumulation are those of the bf16 activations.
 // Three rings decouple the producers: packed weights (SMEM, K = 256 per stage, deep enough to
 // cover an HBM round trip), dequantized A (TMEM, K = 64 per stage) and activations (SMEM,
 // K = 64 per stage).  The accumulator is double-buffered in TMEM so the epilogue of one tile
@@ -65,6 +71,7 @@ struct TcArgs {
   const int32_t* meta;
   void* out;                    // h [S + T, I] bf16 or y [S + T, H] fp32
   int out_ld;
+  const int32_t* act_exp;       // power-of-two exponent of each f16 activation row
   int32_t* status;
 };
 
@@ -170,10 +177,9 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
-// Instruction descriptor: D f32, A bf16, B bf16, both K-major, M = 128, N.
+// Instruction descriptor: D f32, A f16, B f16, both K-major, M = 128, N.
 __device__ __forceinline__ uint32_t make_idesc(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(kBM >> 4) << 24);
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
 }
 
 #define TC_ST32(taddr, r)                                                                          \
@@ -198,9 +204,8 @@ __device__ __forceinline__ uint32_t make_idesc(int n) {
       : "memory")
 
 // Eight e2m1 codes (one 32-bit word, element i in bits 4i..4i+3) times the block scale ->
-// four bf16x2 words.  e2m1 -> f16 is the hardware conversion, the product with the e4m3 scale
-// is exact in f16 (at most 6 significant bits, |v| in [2^-10, 2688]), and the f16 -> bf16 step
-// is exact for such values.
+// four f16x2 words.  e2m1 -> f16 is the hardware conversion and the product with the e4m3
+// scale is exact in f16 (at most 6 significant bits, |v| in [2^-10, 2688]).
 __device__ __forceinline__ void dequant8(uint32_t w, uint32_t scale_f16x2, uint32_t* o) {
   uint32_t h[4];
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
@@ -212,8 +217,7 @@ __device__ __forceinline__ void dequant8(uint32_t w, uint32_t scale_f16x2, uint3
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&h[i]), s);
-    const __nv_bfloat162 b = __float22bfloat162_rn(__half22float2(p));
-    o[i] = *reinterpret_cast<const uint32_t*>(&b);
+    o[i] = *reinterpret_cast<const uint32_t*>(&p);
   }
 }
 
@@ -484,21 +488,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int ci = is_gate ? i : 8 + i;
-            const float g = __uint_as_float(is_gate ? v[ci] : pv[ci]) * s2;
-            const float u = __uint_as_float(is_gate ? pv[ci] : v[ci]) * s2;
             const int col = cbase + i;
-            if (col < td.z)
-              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + j] =
+            if (col < td.z) {
+              const int p = td.y + col;
+              int tok = p - a.S;
+              if (p < a.S) {
+                const int slot = __ldg(a.sorted_slot + p);   // range reported by the gather
+                tok = (static_cast<unsigned>(slot) < static_cast<unsigned>(a.S)) ? slot / a.k : 0;
+              }
+              const float sc = ldexpf(s2, __ldg(a.act_exp + tok));   // scale2 * 2^e(token)
+              const float g = __uint_as_float(is_gate ? v[ci] : pv[ci]) * sc;
+              const float u = __uint_as_float(is_gate ? pv[ci] : v[ci]) * sc;
+              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(p) * a.out_ld + j] =
                   f32_to_bf16_bits(silu_f32(g) * u);
+            }
           }
         } else {
           const int nrow = mb * kBM + q * 32 + lane;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int col = c0 + i;
-            if (col < td.z)
-              static_cast<float*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =
-                  __uint_as_float(v[i]) * s2;
+            if (col < td.z) {
+              const int p = td.y + col;
+              static_cast<float*>(a.out)[static_cast<int64_t>(p) * a.out_ld + nrow] =
+                  __uint_as_float(v[i]) * ldexpf(s2, __ldg(a.act_exp + p));
+            }
           }
         }
       }
@@ -576,7 +590,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
     return cudaErrorInvalidValue;
   if (kGateUp) {
     tmB = tmA;
-  } else if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.act, g.K,
+  } else if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, g.K,
                           static_cast<uint64_t>(g.S) + g.T, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) {
     return cudaErrorInvalidValue;
   }
@@ -594,6 +608,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.meta = g.meta;
   a.out = g.out;
   a.out_ld = kGateUp ? g.N / 2 : g.N;
+  a.act_exp = g.act_exp;
   a.status = g.status;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, sm_count()));
