@@ -71,9 +71,9 @@ struct Ws {
   uint16_t* h;
   float* y;
   uint16_t* xf;
-  int32_t* xe;
+  float* xe;
   uint16_t* hf;
-  int32_t* he;
+  float* he;
   WsLayout L;
 };
 
@@ -94,9 +94,9 @@ Ws carve(void* ws, const moe_shape_t& s) {
   r.h = reinterpret_cast<uint16_t*>(b + r.L.h);
   r.y = reinterpret_cast<float*>(b + r.L.y);
   r.xf = reinterpret_cast<uint16_t*>(b + r.L.xf);
-  r.xe = reinterpret_cast<int32_t*>(b + r.L.xe);
+  r.xe = reinterpret_cast<float*>(b + r.L.xe);
   r.hf = reinterpret_cast<uint16_t*>(b + r.L.hf);
-  r.he = reinterpret_cast<int32_t*>(b + r.L.he);
+  r.he = reinterpret_cast<float*>(b + r.L.he);
   return r;
 }
 
@@ -130,7 +130,7 @@ cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cu
   cudaError_t e = launch_act_to_f16(a.act, ws.xf, ws.xe, s.T, s.H, cs);
   if (e != cudaSuccess) return e;
   a.act = ws.xf;
-  a.act_exp = ws.xe;
+  a.act_factor = ws.xe;
   return launch_gate_up_tc(a, cs);
 }
 
@@ -139,7 +139,7 @@ cudaError_t launch_down(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaS
   cudaError_t e = launch_act_to_f16(a.act, ws.hf, ws.he, static_cast<int64_t>(s.T) * s.k + s.T, s.I, cs);
   if (e != cudaSuccess) return e;
   a.act = ws.hf;
-  a.act_exp = ws.he;
+  a.act_factor = ws.he;
   return launch_down_tc(a, cs);
 }
 
@@ -162,7 +162,7 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   a.max_tiles = max_tiles_for(s, tile_rows_for(s));
   a.out = out;
   a.status = ws.status;
-  a.act_exp = nullptr;
+  a.act_factor = nullptr;
   return a;
 }
 

@@ -1,7 +1,8 @@
 // bf16 activation rows -> f16 rows with a per-row power-of-two scale, for the f16 tensor-core
 // GEMMs of the prefill arm.
 //
-// Row r is written as f16(x[r] * 2^-e[r]) with e[r] = floor(log2(max |x[r]|)) - 14, so the row's
+// Row r is written as f16(x[r] * 2^-e[r]) with e[r] = floor(log2(max |x[r]|)) - 14 (and the factor
+// 2^e[r] as a float for the GEMM epilogue), so the row's
 // largest element lands in [2^14, 2^15), well inside f16's range.  A bf16 value has 8 significant
 // bits and f16 11, so every element of at least 2^-31 of the row maximum converts exactly; only
 // smaller ones (below f16's subnormal grid) are rounded.  The GEMM epilogue multiplies the fp32
@@ -14,7 +15,7 @@ namespace {
 // One warp per row; K % 256 == 0 (eight bf16 per lane per step).
 __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restrict__ src,
                                                          uint16_t* __restrict__ dst,
-                                                         int32_t* __restrict__ exps, int64_t rows,
+                                                         float* __restrict__ factor, int64_t rows,
                                                          int K) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -33,7 +34,7 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   const int e = (m > 0.0f && m <= 3.4e38f) ? ilogbf(m) - 14 : 0;
-  if (lane == 0) exps[r] = e;
+  if (lane == 0) factor[r] = ldexpf(1.0f, e);   // the epilogue's 2^e
   uint4* d = reinterpret_cast<uint4*>(dst + r * K);
   for (int c = lane; c < K / 8; c += 32) {
     const uint4 v = __ldg(s + c);
@@ -52,11 +53,11 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
 
 }  // namespace
 
-cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, int32_t* exps, int64_t rows, int K,
+cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K,
                               cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
-  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, dst, exps, rows, K);
+  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, dst, factor, rows, K);
   return cudaGetLastError();
 }
 

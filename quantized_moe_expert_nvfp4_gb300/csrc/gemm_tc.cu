@@ -42,8 +42,8 @@ constexpr int kBN = kTcTileRows;              // tokens per tile (MMA N, rounded
 constexpr int kBK = 64;                       // K per MMA stage (TMEM A stage, B stage)
 constexpr int kAK = 256;                      // K per packed-weight stage
 constexpr int kAStages = 4;                   // packed-weight ring (SMEM)
-constexpr int kTStages = 4;                   // dequantized-A ring (TMEM)
-constexpr int kBStages = 6;                   // activation ring (SMEM)
+constexpr int kTStages = 8;                   // dequantized-A ring (TMEM)
+constexpr int kBStages = 8;                   // activation ring (SMEM)
 constexpr int kAPackedBytes = kBM * kAK / 2;  // 16 KB: 128 rows x 128 B, 128B swizzle
 constexpr int kAScaleBytes = kBM * kAK / 16;  // 2 KB: 128 rows x 16 B
 constexpr int kAStageBytes = kAPackedBytes + kAScaleBytes;
@@ -52,7 +52,7 @@ constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                      // accumulators: 2 x 128 columns
 constexpr int kACol = 2 * kBN;                // A stages: kTStages x 32 columns
 static_assert(kACol + kTStages * (kBK / 2) <= kTmemCols, "TMEM budget");
-static_assert(kAK / kBK == 4 && kTStages == 4, "dequant halves own TMEM slots {h, h+2}");
+static_assert(kAK / kBK == 4 && kTStages % 4 == 0, "each A stage fills four consecutive TMEM stages");
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpGather = 10, kWarpEpi = 14;
 constexpr int kDeqWarps = 8;
@@ -71,7 +71,7 @@ struct TcArgs {
   const int32_t* meta;
   void* out;                    // h [S + T, I] bf16 or y [S + T, H] fp32
   int out_ld;
-  const int32_t* act_exp;       // power-of-two exponent of each f16 activation row
+  const float* act_factor;      // 2^e of each f16 activation row
   int32_t* status;
 };
 
@@ -477,6 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         TC_LD16(t_lane + kDCol + d * kBN + c0, v);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        // scale of column c0 + i (lane i < 16 looks it up): scale2 * 2^e of its activation row
+        float colf = 0.0f;
+        if (lane < 16 && c0 + lane < td.z) {
+          const int p = td.y + c0 + lane;
+          int r = p;
+          if (kGateUp) {
+            r = p - a.S;
+            if (p < a.S) {
+              const int slot = __ldg(a.sorted_slot + p);   // range reported by the gather
+              r = (static_cast<unsigned>(slot) < static_cast<unsigned>(a.S)) ? slot / a.k : 0;
+            }
+          }
+          colf = s2 * __ldg(a.act_factor + r);
+        }
         if (kGateUp) {
           // lanes 0-15: gate rows j, lanes 16-31: up rows j (j = mb*64 + 16q + lane%16)
           uint32_t pv[16];
@@ -484,22 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 16; ++i) pv[i] = __shfl_xor_sync(0xffffffffu, v[i], 16);
           const bool is_gate = lane < 16;
           const int j = mb * 64 + q * 16 + (lane & 15);
-          const int cbase = c0 + (is_gate ? 0 : 8);
+          const int cb = is_gate ? 0 : 8;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int ci = is_gate ? i : 8 + i;
-            const int col = cbase + i;
+            const float sc = __shfl_sync(0xffffffffu, colf, cb + i);
+            const int col = c0 + cb + i;
             if (col < td.z) {
-              const int p = td.y + col;
-              int tok = p - a.S;
-              if (p < a.S) {
-                const int slot = __ldg(a.sorted_slot + p);   // range reported by the gather
-                tok = (static_cast<unsigned>(slot) < static_cast<unsigned>(a.S)) ? slot / a.k : 0;
-              }
-              const float sc = ldexpf(s2, __ldg(a.act_exp + tok));   // scale2 * 2^e(token)
-              const float g = __uint_as_float(is_gate ? v[ci] : pv[ci]) * sc;
-              const float u = __uint_as_float(is_gate ? pv[ci] : v[ci]) * sc;
-              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(p) * a.out_ld + j] =
+              const float g = __uint_as_float(is_gate ? v[cb + i] : pv[cb + i]) * sc;
+              const float u = __uint_as_float(is_gate ? pv[cb + i] : v[cb + i]) * sc;
+              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + j] =
                   f32_to_bf16_bits(silu_f32(g) * u);
             }
           }
@@ -507,12 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nrow = mb * kBM + q * 32 + lane;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
+            const float sc = __shfl_sync(0xffffffffu, colf, i);
             const int col = c0 + i;
-            if (col < td.z) {
-              const int p = td.y + col;
-              static_cast<float*>(a.out)[static_cast<int64_t>(p) * a.out_ld + nrow] =
-                  __uint_as_float(v[i]) * ldexpf(s2, __ldg(a.act_exp + p));
-            }
+            if (col < td.z)
+              static_cast<float*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =
+                  __uint_as_float(v[i]) * sc;
           }
         }
       }
@@ -608,7 +614,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.meta = g.meta;
   a.out = g.out;
   a.out_ld = kGateUp ? g.N / 2 : g.N;
-  a.act_exp = g.act_exp;
+  a.act_factor = g.act_factor;
   a.status = g.status;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, sm_count()));

@@ -36,9 +36,9 @@ struct WsLayout {
   size_t h;            // bf16  [S + T, I]
   size_t y;            // fp32  [S + T, H]
   size_t xf;           // f16   [T, H]      tensor-core arm: scaled copy of x, and its row exponents
-  size_t xe;           // int32 [T]
+  size_t xe;           // fp32  [T]        2^e of each row of xf
   size_t hf;           // f16   [S + T, I]  tensor-core arm: scaled copy of h, and its row exponents
-  size_t he;           // int32 [S + T]
+  size_t he;           // fp32  [S + T]    2^e of each row of hf
   size_t total;
   int64_t max_tiles;
   int64_t n_chunks;
@@ -126,15 +126,15 @@ struct GroupedArgs {
   int64_t max_tiles;
   void* out;                    // h [S + T, I] bf16 (gate_up) or y [S + T, H] fp32 (down)
   int32_t* status;              // device status word (bad indices are clamped and reported)
-  const int32_t* act_exp;       // tensor-core arm: power-of-two exponent of each act row (f16 act)
+  const float* act_factor;      // tensor-core arm: 2^e of each f16 act row
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
 // bf16 rows -> f16 rows scaled by 2^-e[row] (e = floor(log2 max|row|) - 14), for the f16 MMAs.
-cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, int32_t* exps, int64_t rows, int K,
+cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K,
                               cudaStream_t st);
 // tcgen05 grouped GEMM (work items from a tile list built with kTcTileRows rows); act is the
-// f16 copy from launch_act_to_f16 and act_exp its row exponents.
+// f16 copy from launch_act_to_f16 and act_factor its row factors 2^e.
 bool tc_supported(const moe_shape_t& s);
 cudaError_t launch_gate_up_tc(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedArgs& a, cudaStream_t st);
