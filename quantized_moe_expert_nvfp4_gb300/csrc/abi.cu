@@ -123,11 +123,11 @@ int tile_rows_for(const moe_shape_t& s) {
   }
 }
 
-// The tensor-core arm takes its activations as f16 rows with power-of-two row exponents: x (or
-// h) is converted into the workspace first.
+// The tensor-core arm takes its activations as f16 rows with power-of-two row exponents, in
+// expert order: x is gathered and converted into the workspace first (h already is in order).
 cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaStream_t cs) {
   if (arm_for(s) != Arm::kTc) return launch_gate_up_simt(a, cs);
-  cudaError_t e = launch_act_to_f16(a.act, ws.xf, ws.xe, s.T, s.H, cs);
+  cudaError_t e = launch_act_gather_f16(a.act, a.sorted_slot, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs);
   if (e != cudaSuccess) return e;
   a.act = ws.xf;
   a.act_factor = ws.xe;
@@ -201,10 +201,11 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.hist = take(4 * static_cast<size_t>(std::max<int64_t>(1, L.n_chunks)) * s.E);
   L.h = take(2 * static_cast<size_t>(R) * s.I);
   L.y = take(4 * static_cast<size_t>(R) * s.H);
-  L.xf = take(2 * static_cast<size_t>(s.T) * s.H);
-  L.xe = take(4 * static_cast<size_t>(s.T));
-  L.hf = take(2 * static_cast<size_t>(R) * s.I);
-  L.he = take(4 * static_cast<size_t>(R));
+  const size_t tc_rows = arm_for(s) == Arm::kTc ? static_cast<size_t>(R) : 0;   // tensor-core arm only
+  L.xf = take(2 * tc_rows * s.H);
+  L.xe = take(4 * tc_rows);
+  L.hf = take(2 * tc_rows * s.I);
+  L.he = take(4 * tc_rows);
   L.total = off;
   return L;
 }
@@ -336,9 +337,13 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const moe_shape_t& s = *shape;
   Ws w = carve(ws, s);
+  // Under stream capture the records become external event nodes of the graph; otherwise they
+  // are plain records (the external flag is refused on the legacy default stream).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (stage_events && cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return MOE_ERR_CUDA;
+  const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
   auto mark = [&](int i) -> cudaError_t {
-    return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), cs,
-                                                   cudaEventRecordExternal)
+    return stage_events ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), cs, rec_flags)
                         : cudaSuccess;
   };
   cudaError_t e = mark(0);

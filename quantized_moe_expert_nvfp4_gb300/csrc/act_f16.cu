@@ -12,15 +12,31 @@
 namespace moe {
 namespace {
 
-// One warp per row; K % 256 == 0 (eight bf16 per lane per step).
+// One warp per output row; K % 256 == 0 (eight bf16 per lane per step).  With sorted_slot set,
+// output row p < S is the token sorted_slot[p] / k of the source (the routed rows in expert
+// order) and row S + t is token t (the shared expert's rows); without it row p is source row p.
 __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restrict__ src,
-                                                         uint16_t* __restrict__ dst,
+                                                         const int32_t* __restrict__ sorted_slot,
+                                                         int S, int k, uint16_t* __restrict__ dst,
                                                          float* __restrict__ factor, int64_t rows,
-                                                         int K) {
+                                                         int K, int32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (r >= rows) return;
-  const uint4* s = reinterpret_cast<const uint4*>(src + r * K);
+  int64_t srow = r;
+  if (sorted_slot) {
+    if (r < S) {
+      int slot = __ldg(sorted_slot + r);
+      if (static_cast<unsigned>(slot) >= static_cast<unsigned>(S)) {
+        if (lane == 0) report_device_error(status, kDevBadIndex);
+        slot = 0;
+      }
+      srow = slot / k;
+    } else {
+      srow = r - S;
+    }
+  }
+  const uint4* s = reinterpret_cast<const uint4*>(src + srow * K);
   float m = 0.0f;
   for (int c = lane; c < K / 8; c += 32) {
     const uint4 v = __ldg(s + c);
@@ -57,7 +73,19 @@ cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor,
                               cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
-  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, dst, factor, rows, K);
+  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, nullptr, 0, 1, dst, factor, rows, K,
+                                                                     nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_gather_f16(const uint16_t* x, const int32_t* sorted_slot, int T, int k, int K,
+                                  uint16_t* dst, float* factor, int32_t* status, cudaStream_t st) {
+  const int S = T * k;
+  const int64_t rows = static_cast<int64_t>(S) + T;
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(x, sorted_slot, S, k, dst, factor, rows, K,
+                                                                     status);
   return cudaGetLastError();
 }
 

@@ -1,32 +1,32 @@
 // Grouped NVFP4 x bf16 GEMM on the fifth-generation tensor cores (tcgen05) -- the prefill arm.
 //
 // W4A16 as in the untransposed column of the "long-context cold prefill to SGLang parity"
-// issue's kernel table (bf16 MMA, f32 accumulation, scale2 and SiLU(gate)*up in an fp32
+// issue's kernel table (16-bit MMA, f32 accumulation, scale2 and SiLU(gate)*up in an fp32
 // epilogue), computed over the resident [N, K/2] weight layout the same issue prices ("MoE FP4
 // MMA over the resident decode layout, no dequant pass, no transpose").
 //
 // Swap-AB: the MMA's M dimension is 128 weight rows of one expert, N is up to 128 of that
 // expert's tokens, so a small expert group still fills M.  Per CTA (one per SM, persistent):
-//   warp 0       TMA producer: packed e2m1 + e4m3 scale tiles (K = 256 per stage) and, for
-//                down, the bf16 activation tiles (K = 64 per stage)
-//   warp 1       MMA issuer (one thread): tcgen05.mma kind::f16, A from TMEM, B from SMEM
+//   warp 0       TMA producer of the packed e2m1 + e4m3 scale tiles (K = 256 per stage)
+//   warp 1       MMA issuer: the whole warp waits, one elected lane issues tcgen05.mma kind::f16
+//                with A from TMEM and B from SMEM
 //   warps 2-9    dequant: one weight row per thread (two warps per TMEM lane quarter, taking
 //                alternate 64-wide K chunks), e2m1 x e4m3 -> f16 exactly (every product has at
 //                most 6 significant bits and lies in [2^-10, 2688]), written to TMEM with
 //                tcgen05.st as the A operand
-//   warps 10-13  gate_up only: gather of the expert's token rows of x into 128B-swizzled SMEM
-//   warps 14-17  epilogue: tcgen05.ld of the fp32 accumulator, x scale2 x 2^e (the activation
+//   warp 10      TMA producer of the activation tiles (K = 128 per stage)
+//   warps 11-14  epilogue: tcgen05.ld of the fp32 accumulator, x scale2 x 2^e (the activation
 //                row's exponent), SiLU(gate)*up (gate_up)
-// The MMA is kind::f16 with f16 operands: the activations arrive as f16 rows scaled by a power
-// of two per row (exact for every element above 2^-31 of the row maximum), so the dequantization
-// is one conversion and one packed multiply per pair of weights instead of the five a bf16
-// operand needs, and the products and the fp32 accumulation are those of the bf16 activations.
-// Three rings decouple the producers: packed weights (SMEM, K = 256 per stage, deep enough to
-// cover an HBM round trip), dequantized A (TMEM, K = 64 per stage) and activations (SMEM,
-// K = 64 per stage).  The accumulator is double-buffered in TMEM so the epilogue of one tile
-// overlaps the next tile's main loop.  Dequantizing into TMEM rather than SMEM leaves the
-// shared-memory bandwidth to the B operand.  Every mbarrier wait is bounded; on timeout the
-// kernel records MOE_ERR_DEVICE_TIMEOUT in the workspace status word and winds down.
+// The MMA is kind::f16 with f16 operands: the activations arrive as f16 rows in expert order,
+// scaled by a power of two per row (exact for every element above 2^-31 of the row maximum), so
+// the dequantization is one conversion and one packed multiply per pair of weights, and the
+// products and the fp32 accumulation are those of the bf16 activations.
+// The pipeline advances in groups of K = 256 (16 MMAs): one packed-weight stage, one TMEM stage
+// and two activation stages per group.  Each readiness check of the MMA warp idles the tensor
+// pipe for about 200 cycles at N <= 128 (measured on GB300), so the MMA warp checks once per
+// group, not once per 64-wide slice.  The accumulator is double-buffered in TMEM so the
+// epilogue of one tile overlaps the next tile's main loop.  Every mbarrier wait is bounded; on
+// timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the workspace status word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,52 +38,52 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;                      // weight rows per tile (MMA M)
-constexpr int kBN = kTcTileRows;              // tokens per tile (MMA N, rounded up to 16)
-constexpr int kBK = 64;                       // K per MMA stage (TMEM A stage, B stage)
-constexpr int kAK = 256;                      // K per packed-weight stage
-constexpr int kAStages = 4;                   // packed-weight ring (SMEM)
-constexpr int kTStages = 8;                   // dequantized-A ring (TMEM)
-constexpr int kBStages = 8;                   // activation ring (SMEM)
-constexpr int kAPackedBytes = kBM * kAK / 2;  // 16 KB: 128 rows x 128 B, 128B swizzle
-constexpr int kAScaleBytes = kBM * kAK / 16;  // 2 KB: 128 rows x 16 B
+constexpr int kBN = kTcTileRows;              // tokens per tile at most (MMA N, rounded up to 16)
+constexpr int kBK = 64;                       // K per 128-byte swizzled operand row
+constexpr int kGK = 256;                      // K per pipeline group
+constexpr int kAStages = 4;                   // packed-weight ring (SMEM), one group per stage
+constexpr int kTStages = 2;                   // dequantized-A ring (TMEM), one group per stage
+constexpr int kBStageK = 128;                 // K per activation stage (two 64-wide sub-tiles)
+constexpr int kBStages = 4;                   // activation ring (SMEM)
+constexpr int kAPackedBytes = kBM * kGK / 2;  // 16 KB: 128 rows x 128 B, 128B swizzle
+constexpr int kAScaleBytes = kBM * kGK / 16;  // 2 KB: 128 rows x 16 B
 constexpr int kAStageBytes = kAPackedBytes + kAScaleBytes;
-constexpr int kBStageBytes = kBN * kBK * 2;   // bf16 tile: 128 rows x 128 B (128B swizzle)
+constexpr int kBSubBytes = kBN * kBK * 2;     // 16 KB: 128 rows x 128 B, 128B swizzle
+constexpr int kBStageBytes = (kBStageK / kBK) * kBSubBytes;
+constexpr int kBBoxRows = 32;                 // activation rows per TMA box
 constexpr int kTmemCols = 512;
-constexpr int kDCol = 0;                      // accumulators: 2 x 128 columns
-constexpr int kACol = 2 * kBN;                // A stages: kTStages x 32 columns
-static_assert(kACol + kTStages * (kBK / 2) <= kTmemCols, "TMEM budget");
-static_assert(kAK / kBK == 4 && kTStages % 4 == 0, "each A stage fills four consecutive TMEM stages");
+constexpr int kDCol = 0;                      // accumulators: 2 x kBN columns
+constexpr int kACol = 2 * kBN;                // A stages: kTStages x kGK / 2 columns
+static_assert(kACol + kTStages * (kGK / 2) <= kTmemCols, "TMEM budget");
+static_assert(kGK == 2 * kBStageK && kGK / kBK == 4, "a group is four 64-wide chunks, two activation stages");
 
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpGather = 10, kWarpEpi = 14;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpTmaB = 10, kWarpEpi = 11;
 constexpr int kDeqWarps = 8;
-constexpr int kThreads = 18 * 32;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 15 * 32;
 constexpr uint32_t kSpinLimit = 1u << 24;      // drain loops only
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: no legitimate wait comes close
 
 struct TcArgs {
-  const uint8_t* scales;
   const float* scale2;
   int Nw, K;                    // weight rows per group, reduction length
-  const uint16_t* act;          // x [T, H] (gate_up gather source)
-  const int32_t* sorted_slot;
-  int T, k, S;
   const int4* tiles;
   const int32_t* meta;
   void* out;                    // h [S + T, I] bf16 or y [S + T, H] fp32
   int out_ld;
-  const float* act_factor;      // 2^e of each f16 activation row
+  const float* act_factor;      // 2^e of each f16 activation row (expert order)
   int32_t* status;
 };
 
 struct Smem {
   uint64_t a_full[kAStages];     // packed tile + scales landed (TMA transaction)
   uint64_t a_free[kAStages];     // every dequant warp is done reading the stage
-  uint64_t t_full[kTStages];     // dequantized A written to TMEM (128 threads)
+  uint64_t t_full[kTStages];     // dequantized A written to TMEM (one arrival per dequant warp)
   uint64_t t_free[kTStages];     // the MMAs reading that TMEM stage completed
-  uint64_t b_full[kBStages];     // activation tile ready (gather threads or TMA)
-  uint64_t b_free[kBStages];     // the MMAs reading that activation tile completed
+  uint64_t b_full[kBStages];     // activation stage landed (TMA transaction)
+  uint64_t b_free[kBStages];     // the MMAs reading that activation stage completed
   uint64_t acc_full[2];
-  uint64_t acc_empty[2];
+  uint64_t acc_empty[2];         // one arrival per epilogue warp
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -227,22 +227,34 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_splat(uint32_t byte) {
   return h | (h << 16);
 }
 
+__device__ __forceinline__ void tc_mma_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc),
+               "r"(idesc)
+               : "memory");
+}
+
+// One lane of a converged warp (the MMA issue is cheaper from a converged warp than from a lane
+// branched off on its own).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p != 0;
+}
+
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
                            const __grid_constant__ CUtensorMap tmB, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = base;                                   // kBStages x 16 KB (1024-aligned)
+  uint8_t* sB = base;                                   // kBStages x 32 KB (1024-aligned)
   uint8_t* sA = base + kBStages * kBStageBytes;         // kAStages x 18 KB (1024-aligned)
   Smem* sm = reinterpret_cast<Smem*>(sA + kAStages * kAStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MB = a.Nw / kBM;                           // m-blocks per group
-  const int KS = a.K / kBK;                            // MMA stages per item
-  const int KA = a.K / kAK;                            // packed-weight stages per item
+  const int KG = a.K / kGK;                            // pipeline groups per item
   const int n_items = __ldg(a.meta) * MB;
-  const int half_rows = kGateUp ? kBM / 2 : kBM;       // rows per TMA box
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -250,16 +262,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->a_free[s], kDeqWarps);
     }
     for (int s = 0; s < kTStages; ++s) {
-      mbar_init(&sm->t_full[s], 128);
+      mbar_init(&sm->t_full[s], kDeqWarps);
       mbar_init(&sm->t_free[s], 1);
     }
     for (int s = 0; s < kBStages; ++s) {
-      mbar_init(&sm->b_full[s], kGateUp ? 128 : 1);
+      mbar_init(&sm->b_full[s], 1);
       mbar_init(&sm->b_free[s], 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm->acc_full[d], 1);
-      mbar_init(&sm->acc_empty[d], 128);
+      mbar_init(&sm->acc_empty[d], kEpiWarps);
     }
     mbar_init(&sm->drain, 1);
     sm->abort_flag = 0;
@@ -277,32 +289,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     if (lane == 0) {
-      // Issue order: packed stage ka, then (down) its four activation stages.  The producer only
-      // ever waits for resources freed by work it has already issued, so the order cannot stall.
-      uint32_t ia = 0, ib = 0;
+      // packed weights and scales, one group per stage; gate_up takes the gate rows and the
+      // matching up rows (I rows further down the group) as two 64-row boxes
+      const int box_rows = kGateUp ? kBM / 2 : kBM;
+      uint32_t ia = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const int4 td = __ldg(a.tiles + item / MB);
         const int mb = item % MB;
-        const int r0 = td.x * a.Nw + (kGateUp ? mb * (kBM / 2) : mb * kBM);
-        for (int ka = 0; ok && ka < KA; ++ka, ++ia) {
+        const int r0 = td.x * a.Nw + mb * box_rows;
+        for (int g = 0; g < KG; ++g, ++ia) {
           const int st = ia % kAStages;
           if (!(ok = mbar_wait(&sm->a_free[st], ((ia / kAStages) & 1) ^ 1, sm, a.status))) break;
           uint8_t* dA = sA + st * kAStageBytes;
           mbar_expect_tx(&sm->a_full[st], kAStageBytes);
-          tma_load_2d(dA, &tmA, ka * (kAK / 2), r0, &sm->a_full[st]);
-          tma_load_2d(dA + kAPackedBytes, &tmS, ka * (kAK / 16), r0, &sm->a_full[st]);
-          if (kGateUp) {   // the matching up rows: I rows further down the group
-            tma_load_2d(dA + half_rows * (kAK / 2), &tmA, ka * (kAK / 2), r0 + a.Nw / 2, &sm->a_full[st]);
-            tma_load_2d(dA + kAPackedBytes + half_rows * (kAK / 16), &tmS, ka * (kAK / 16), r0 + a.Nw / 2,
+          tma_load_2d(dA, &tmA, g * (kGK / 2), r0, &sm->a_full[st]);
+          tma_load_2d(dA + kAPackedBytes, &tmS, g * (kGK / 16), r0, &sm->a_full[st]);
+          if (kGateUp) {
+            tma_load_2d(dA + box_rows * (kGK / 2), &tmA, g * (kGK / 2), r0 + a.Nw / 2, &sm->a_full[st]);
+            tma_load_2d(dA + kAPackedBytes + box_rows * (kGK / 16), &tmS, g * (kGK / 16), r0 + a.Nw / 2,
                         &sm->a_full[st]);
-          } else {
-            for (int kb = 0; kb < kAK / kBK; ++kb, ++ib) {
-              const int sb = ib % kBStages;
-              if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
-              mbar_expect_tx(&sm->b_full[sb], kBStageBytes);
-              tma_load_2d(sB + sb * kBStageBytes, &tmB, (ka * (kAK / kBK) + kb) * kBK, td.y, &sm->b_full[sb]);
-            }
           }
         }
       }
@@ -312,6 +318,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->a_full[q % kAStages], (q / kAStages) & 1); ++i) {
           }
         }
+      }
+    }
+  } else if (warp == kWarpTmaB) {
+    if (lane == 0) {
+      // activation rows [td.y, td.y + 32 * nbox) of the expert-ordered f16 operand, two 64-wide
+      // sub-tiles per stage; rows past the tile's own belong to the next tiles (or lie beyond
+      // the tensor and read as zero) and only feed accumulator columns the epilogue skips
+      uint32_t ib = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int4 td = __ldg(a.tiles + item / MB);
+        const int nbox = (td.z + kBBoxRows - 1) / kBBoxRows;
+        for (int kb = 0; kb < a.K / kBStageK; ++kb, ++ib) {
+          const int sb = ib % kBStages;
+          if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
+          uint8_t* dB = sB + sb * kBStageBytes;
+          mbar_expect_tx(&sm->b_full[sb], (kBStageK / kBK) * nbox * kBBoxRows * kBK * 2);
+          for (int sub = 0; sub < kBStageK / kBK; ++sub)
+            for (int bx = 0; bx < nbox; ++bx)
+              tma_load_2d(dB + sub * kBSubBytes + bx * kBBoxRows * kBK * 2, &tmB, kb * kBStageK + sub * kBK,
+                          td.y + bx * kBBoxRows, &sm->b_full[sb]);
+        }
+      }
+      if (!ok) {
         for (int j = 0; j < kBStages && ib > 0; ++j, --ib) {
           const uint32_t q = ib - 1;
           for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->b_full[q % kBStages], (q / kBStages) & 1); ++i) {
@@ -320,46 +350,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kWarpMma) {
-    if (lane == 0) {
-      uint32_t it = 0, ic = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
-        const int4 td = __ldg(a.tiles + item / MB);
-        const int n = (td.z + 15) & ~15;
-        const uint32_t idesc = make_idesc(n);
-        const int d = ic & 1;
-        if (!(ok = mbar_wait(&sm->acc_empty[d], ((ic >> 1) & 1) ^ 1, sm, a.status))) break;
+    // The whole warp waits (converged); one elected lane issues the 16 MMAs of a group and the
+    // commits that release its TMEM stage and its two activation stages.
+    uint32_t ig = 0, ib = 0, ic = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+      const int4 td = __ldg(a.tiles + item / MB);
+      const int n = (td.z + 15) & ~15;
+      const uint32_t idesc = make_idesc(n);
+      const int d = ic & 1;
+      if (!(ok = warp_wait(&sm->acc_empty[d], ((ic >> 1) & 1) ^ 1, sm, a.status))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + kDCol + d * kBN;
+      for (int g = 0; g < KG; ++g, ++ig, ib += 2) {
+        const int ts = ig % kTStages;
+        const int sb0 = ib % kBStages, sb1 = (ib + 1) % kBStages;
+        ok = warp_wait(&sm->t_full[ts], (ig / kTStages) & 1, sm, a.status) &&
+             warp_wait(&sm->b_full[sb0], (ib / kBStages) & 1, sm, a.status) &&
+             warp_wait(&sm->b_full[sb1], ((ib + 1) / kBStages) & 1, sm, a.status);
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + kDCol + d * kBN;
-        for (int ks = 0; ks < KS; ++ks, ++it) {
-          const int ts = it % kTStages, bs = it % kBStages;
-          if (!(ok = mbar_wait(&sm->t_full[ts], (it / kTStages) & 1, sm, a.status))) break;
-          if (!(ok = mbar_wait(&sm->b_full[bs], (it / kBStages) & 1, sm, a.status))) break;
-          if (kGateUp)  // the gathered tile was written by cp.async (generic proxy); the MMA reads it
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // through the async proxy
-          tc_fence_after();
-          const uint32_t b_addr = smem_u32(sB + bs * kBStageBytes);
+        if (elect_one()) {
+          const uint32_t a_tmem = tmem + kACol + ts * (kGK / 2);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            tc_mma(d_tmem, tmem + kACol + ts * (kBK / 2) + kk * 8, smem_desc_sw128(b_addr + kk * 32), idesc,
-                   (ks | kk) != 0);
+          for (int c = 0; c < kGK / kBK; ++c) {       // 64-wide chunk c of the group
+            const uint32_t b_addr = smem_u32(sB + ((c >> 1) ? sb1 : sb0) * kBStageBytes + (c & 1) * kBSubBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint32_t at = a_tmem + c * (kBK / 2) + kk * 8;
+              const uint64_t bd = smem_desc_sw128(b_addr + kk * 32);
+              if (c == 0 && kk == 0)
+                tc_mma(d_tmem, at, bd, idesc, g != 0);
+              else
+                tc_mma_acc(d_tmem, at, bd, idesc);
+            }
+          }
           tc_commit(&sm->t_free[ts]);
-          tc_commit(&sm->b_free[bs]);
+          tc_commit(&sm->b_free[sb0]);
+          tc_commit(&sm->b_free[sb1]);
         }
-        if (ok) tc_commit(&sm->acc_full[d]);
+        __syncwarp();
       }
-      // every MMA issued must have completed before TMEM is released (bounded)
+      if (ok) {
+        if (elect_one()) tc_commit(&sm->acc_full[d]);
+        __syncwarp();
+      }
+    }
+    // every MMA issued must have completed before TMEM is released (bounded)
+    if (elect_one()) {
       tc_commit(&sm->drain);
       for (uint32_t i = 0; i < kSpinLimit && !mbar_try(&sm->drain, 0); ++i) {
       }
     }
+    __syncwarp();
   } else if (warp >= kWarpDeq && warp < kWarpDeq + kDeqWarps) {
-    const int q = warp & 3;                 // TMEM lane quarter of this warp
-    const int hsel = (warp - kWarpDeq) >> 2;   // which two of the four 64-wide K chunks
-    int srow;                               // SMEM row of the packed tile (== weight row offset)
+    const int q = warp & 3;                    // TMEM lane quarter of this warp
+    const int hsel = (warp - kWarpDeq) >> 2;   // chunks hsel and hsel + 2 of each group
+    int srow;                                  // SMEM row of the packed tile (== weight row offset)
     if (kGateUp) {
       const int half = lane >> 4, j = q * 16 + (lane & 15);
-      srow = half * (kBM / 2) + j;          // lanes 0-15 gate rows, 16-31 the matching up rows
+      srow = half * (kBM / 2) + j;             // lanes 0-15 gate rows, 16-31 the matching up rows
     } else {
       srow = q * 32 + lane;
     }
@@ -367,30 +417,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ia = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      for (int ka = 0; ka < KA; ++ka, ++ia) {
-        const int st = ia % kAStages;
+      for (int g = 0; g < KG; ++g, ++ia) {
+        const int st = ia % kAStages, ts = ia % kTStages;
         if (!(ok = warp_wait(&sm->a_full[st], (ia / kAStages) & 1, sm, a.status))) break;
         const uint8_t* stage = sA + st * kAStageBytes;
-        const uint8_t* rowp = stage + srow * (kAK / 2);
-        const uint4 sc = *reinterpret_cast<const uint4*>(stage + kAPackedBytes + srow * (kAK / 16));
+        const uint8_t* rowp = stage + srow * (kGK / 2);
+        const uint4 sc = *reinterpret_cast<const uint4*>(stage + kAPackedBytes + srow * (kGK / 16));
         uint4 pk[2][2];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          const int ss = hsel + 2 * h2;     // 64-wide chunk of this 256-wide stage
+          const int ss = hsel + 2 * h2;        // 64-wide chunk of this group
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
-            const int c = 2 * ss + c2;      // 16-byte chunk, 128B swizzle: chunk ^= row & 7
+            const int c = 2 * ss + c2;         // 16-byte chunk, 128B swizzle: chunk ^= row & 7
             pk[h2][c2] = *reinterpret_cast<const uint4*>(rowp + ((c ^ (srow & 7)) << 4));
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->a_free[st]);
+        if (!(ok = warp_wait(&sm->t_free[ts], ((ia / kTStages) & 1) ^ 1, sm, a.status))) break;
+        tc_fence_after();
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int ss = hsel + 2 * h2;
-          const uint32_t it = ia * 4 + ss;
-          const int ts = it % kTStages;
-          const uint32_t scw = (&sc.x)[ss];
+          const uint32_t scw = h2 ? (hsel ? sc.w : sc.z) : (hsel ? sc.y : sc.x);   // scales of chunk ss
           uint32_t o[32];
           const uint32_t pw[8] = {pk[h2][0].x, pk[h2][0].y, pk[h2][0].z, pk[h2][0].w,
                                   pk[h2][1].x, pk[h2][1].y, pk[h2][1].z, pk[h2][1].w};
@@ -400,66 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             dequant8(pw[2 * b], s2, o + 8 * b);
             dequant8(pw[2 * b + 1], s2, o + 8 * b + 4);
           }
-          if (!(ok = warp_wait(&sm->t_free[ts], ((it / kTStages) & 1) ^ 1, sm, a.status))) break;
-          tc_fence_after();
           __syncwarp();
-          TC_ST32(t_lane + kACol + ts * (kBK / 2), o);
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          tc_fence_before();
-          mbar_arrive(&sm->t_full[ts]);
+          TC_ST32(t_lane + kACol + ts * (kGK / 2) + ss * (kBK / 2), o);
         }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->t_full[ts]);
       }
     }
-  } else if (warp >= kWarpGather && warp < kWarpGather + 4) {
-    if (kGateUp) {
-      const int t = threadIdx.x - kWarpGather * 32;   // 0..127
-      const int c = t & 7;                            // 16-byte chunk of a 128-byte row
-      uint32_t ib = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int4 td = __ldg(a.tiles + item / MB);
-        int64_t src[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int row = (t >> 3) + 16 * i;
-          src[i] = -1;
-          if (row < td.z) {
-            const int p = td.y + row;
-            int tok;
-            if (p < a.S) {
-              int slot = __ldg(a.sorted_slot + p);
-              if (static_cast<unsigned>(slot) >= static_cast<unsigned>(a.S)) {
-                report_device_error(a.status, kDevBadIndex);
-                slot = 0;
-              }
-              tok = slot / a.k;
-            } else {
-              tok = p - a.S;
-            }
-            src[i] = static_cast<int64_t>(tok) * a.K + c * 8;
-          }
-        }
-        for (int ks = 0; ks < KS; ++ks, ++ib) {
-          const int sb = ib % kBStages;
-          if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
-          const uint32_t dB = smem_u32(sB + sb * kBStageBytes);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = (t >> 3) + 16 * i;
-            // 16-byte async copy into the 128B-swizzled slot; padding rows are zero-filled
-            const bool live = src[i] >= 0;
-            const uint16_t* gsrc = a.act + (live ? src[i] + ks * kBK : 0);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dB + row * 128 + ((c ^ (row & 7)) << 4)),
-                         "l"(gsrc), "r"(live ? 16 : 0)
-                         : "memory");
-          }
-          // the barrier gets this thread's arrival once its copies above have landed
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sm->b_full[sb]))
-                       : "memory");
-        }
-      }
-    }
-  } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+  } else if (warp >= kWarpEpi && warp < kWarpEpi + kEpiWarps) {
     const int q = warp & 3;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t ic = 0;
@@ -479,33 +479,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         // scale of column c0 + i (lane i < 16 looks it up): scale2 * 2^e of its activation row
         float colf = 0.0f;
-        if (lane < 16 && c0 + lane < td.z) {
-          const int p = td.y + c0 + lane;
-          int r = p;
-          if (kGateUp) {
-            r = p - a.S;
-            if (p < a.S) {
-              const int slot = __ldg(a.sorted_slot + p);   // range reported by the gather
-              r = (static_cast<unsigned>(slot) < static_cast<unsigned>(a.S)) ? slot / a.k : 0;
-            }
-          }
-          colf = s2 * __ldg(a.act_factor + r);
-        }
+        if (lane < 16 && c0 + lane < td.z) colf = s2 * __ldg(a.act_factor + td.y + c0 + lane);
         if (kGateUp) {
-          // lanes 0-15: gate rows j, lanes 16-31: up rows j (j = mb*64 + 16q + lane%16)
-          uint32_t pv[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pv[i] = __shfl_xor_sync(0xffffffffu, v[i], 16);
+          // lanes 0-15 hold gate rows j, lanes 16-31 the up rows j (j = mb*64 + 16q + lane%16);
+          // a gate lane finishes columns c0..c0+7 and its up partner (lane ^ 16) c0+8..c0+15,
+          // each receiving the other half of its pair by one exchange
           const bool is_gate = lane < 16;
           const int j = mb * 64 + q * 16 + (lane & 15);
           const int cb = is_gate ? 0 : 8;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, is_gate ? v[8 + i] : v[i], 16);
             const float sc = __shfl_sync(0xffffffffu, colf, cb + i);
             const int col = c0 + cb + i;
             if (col < td.z) {
-              const float g = __uint_as_float(is_gate ? v[cb + i] : pv[cb + i]) * sc;
-              const float u = __uint_as_float(is_gate ? pv[cb + i] : v[cb + i]) * sc;
+              const float g = __uint_as_float(is_gate ? v[i] : other) * sc;
+              const float u = __uint_as_float(is_gate ? other : v[8 + i]) * sc;
               static_cast<uint16_t*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + j] =
                   f32_to_bf16_bits(silu_f32(g) * u);
             }
@@ -523,7 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&sm->acc_empty[d]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->acc_empty[d]);
     }
   }
 
@@ -564,6 +554,7 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
 }
 
 constexpr size_t kSmemBytes = 1024 + kBStages * kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 int sm_count() {
   static int n = 0;
@@ -587,29 +578,21 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   }
   const int G = g.E + 1;
   const int box_rows = kGateUp ? kBM / 2 : kBM;
+  const uint64_t act_rows = static_cast<uint64_t>(g.S) + g.T;
   CUtensorMap tmA, tmS, tmB;
   if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.packed, g.K / 2, static_cast<uint64_t>(G) * g.N,
-                   kAK / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
+                   kGK / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.scales, g.K / 16, static_cast<uint64_t>(G) * g.N,
-                   kAK / 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   kGK / 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (kGateUp) {
-    tmB = tmA;
-  } else if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, g.K,
-                          static_cast<uint64_t>(g.S) + g.T, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B)) {
+  if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, g.K, act_rows, kBK, kBBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  }
   TcArgs a;
-  a.scales = g.scales;
   a.scale2 = g.scale2;
   a.Nw = g.N;
   a.K = g.K;
-  a.act = g.act;
-  a.sorted_slot = g.sorted_slot;
-  a.T = g.T;
-  a.k = g.k;
-  a.S = g.S;
   a.tiles = g.tiles;
   a.meta = g.meta;
   a.out = g.out;

@@ -35,8 +35,8 @@ struct WsLayout {
   size_t hist;         // int32 [n_chunks, E] per-chunk expert histogram / bases
   size_t h;            // bf16  [S + T, I]
   size_t y;            // fp32  [S + T, H]
-  size_t xf;           // f16   [T, H]      tensor-core arm: scaled copy of x, and its row exponents
-  size_t xe;           // fp32  [T]        2^e of each row of xf
+  size_t xf;           // f16   [S + T, H]  tensor-core arm: scaled rows of x in expert order
+  size_t xe;           // fp32  [S + T]    2^e of each row of xf
   size_t hf;           // f16   [S + T, I]  tensor-core arm: scaled copy of h, and its row exponents
   size_t he;           // fp32  [S + T]    2^e of each row of hf
   size_t total;
@@ -133,8 +133,13 @@ cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
 // bf16 rows -> f16 rows scaled by 2^-e[row] (e = floor(log2 max|row|) - 14), for the f16 MMAs.
 cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K,
                               cudaStream_t st);
+// The same for the gate_up operand, gathered into expert order: row p < S of dst is token
+// sorted_slot[p] / k of x, row S + t is token t (out-of-range slots are reported as kDevBadIndex).
+cudaError_t launch_act_gather_f16(const uint16_t* x, const int32_t* sorted_slot, int T, int k, int K,
+                                  uint16_t* dst, float* factor, int32_t* status, cudaStream_t st);
 // tcgen05 grouped GEMM (work items from a tile list built with kTcTileRows rows); act is the
-// f16 copy from launch_act_to_f16 and act_factor its row factors 2^e.
+// expert-ordered f16 operand [S + T, K] (launch_act_gather_f16 for gate_up, launch_act_to_f16
+// of h for down) and act_factor its row factors 2^e.
 bool tc_supported(const moe_shape_t& s);
 cudaError_t launch_gate_up_tc(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedArgs& a, cudaStream_t st);

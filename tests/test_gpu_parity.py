@@ -120,6 +120,28 @@ def test_forward_deterministic_and_matches_stages(cuda_lib):
         assert torch.equal(a, b)
 
 
+def test_forward_profiled_matches_forward(cuda_lib):
+    """forward_profiled on the default stream (no capture) gives forward's bytes and five
+    ordered stage events, for every arm."""
+    moe = cuda_lib
+    for case in (SMALL[0], SMALL[2], SMALL[5]):
+        L = _small_layer(case)
+        ms = moe_shape(moe, L.shape)
+        gu, dn = L.gpu_weights(moe)
+        x, logits = L.x.cuda(), L.logits.cuda()
+        ws = moe.workspace(ms)
+        a = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in ev:
+            e.record()
+        b = torch.full_like(a, float("nan"))
+        moe.forward_profiled(x, logits, gu, dn, ms, ws, b, ev, out_fp32=True)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+        assert all(ev[i].elapsed_time(ev[i + 1]) >= 0.0 for i in range(4))
+        assert moe.device_status(ws) == 0
+
+
 def test_route_edge_rows(cuda_lib):
     moe = cuda_lib
     E, k = 16, 4
