@@ -192,8 +192,9 @@ moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream);
 /* Which kernels moe_forward runs for a shape (-1 for an unsupported shape):
  *   0  T <= 8 (H % 512 == 0, H <= 4096, I <= 1024): one cooperative launch that routes,
  *      streams the active experts' weights with TMA bulk copies and combines (grouped GEMV);
- *   1  T <= 64 otherwise: three launches (route+permute, gate_up GEMV, down GEMV + combine);
- *   2  T > 64, H and I multiples of 256: tcgen05 grouped GEMMs (prefill arm);
+ *   1  T <= 8 otherwise, and 8 < T <= 64 when H or I is not a multiple of 256: three launches
+ *      (route+permute, gate_up GEMV, down GEMV + combine);
+ *   2  T > 8, H and I multiples of 256: tcgen05 grouped GEMMs (batched decode and prefill);
  *   3  T > 64 otherwise: CUDA-core grouped GEMMs. */
 int moe_forward_arm(const moe_shape_t* shape);
 

@@ -25,7 +25,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE",
                 -3: "MOE_ERR_WORKSPACE_TOO_SMALL", -4: "MOE_ERR_ARCH", -5: "MOE_ERR_CUDA",
                 -6: "MOE_ERR_DEVICE_TIMEOUT"}
-DECODE_MAX_T = 64   # moe_forward takes the grouped-GEMV (decode) arm up to this many tokens
+DECODE_MAX_T = 64   # largest batch the CUDA-core grouped-GEMV arm (1) takes, for shapes arm 2 cannot
 
 
 class MoeError(RuntimeError):
@@ -250,7 +250,7 @@ def device_status(ws: torch.Tensor, stream=None) -> int:
 
 ARM_NAMES = {0: "decode, one cooperative launch (grouped GEMV)",
              1: "decode, three launches (grouped GEMV)",
-             2: "prefill, tcgen05 grouped GEMM", 3: "prefill, CUDA-core grouped GEMM"}
+             2: "batched decode / prefill, tcgen05 grouped GEMM", 3: "prefill, CUDA-core grouped GEMM"}
 
 
 def forward_arm(shape: Shape) -> int:

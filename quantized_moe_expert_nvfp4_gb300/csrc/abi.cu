@@ -100,19 +100,25 @@ Ws carve(void* ws, const moe_shape_t& s) {
   return r;
 }
 
-// Arm of a shape: the grouped-GEMV decode arm for small T; above it the tcgen05 grouped GEMM
-// when H and I are multiples of 256, else the CUDA-core grouped GEMM.
+// Arm of a shape: the grouped-GEMV decode arms for up to kFdMaxT tokens; above that the tcgen05
+// grouped GEMM when H and I are multiples of 256 (it streams the selected experts' weights at
+// least as fast as the GEMV arm once an expert sees more than a few tokens), else the CUDA-core
+// GEMV arm up to kDecodeMaxT tokens and the CUDA-core grouped GEMM beyond.
 enum class Arm { kDecode, kTc, kSimt };
 
 Arm arm_for(const moe_shape_t& s) {
-  if (s.T <= kDecodeMaxT) return Arm::kDecode;
-  return tc_supported(s) ? Arm::kTc : Arm::kSimt;
+  if (s.T <= kFdMaxT) return Arm::kDecode;
+  if (tc_supported(s)) return Arm::kTc;
+  return s.T <= kDecodeMaxT ? Arm::kDecode : Arm::kSimt;
 }
 
 // Which kernels moe_forward runs for a shape (the value moe_forward_arm reports).
 int forward_arm(const moe_shape_t& s) {
-  if (s.T <= kDecodeMaxT) return decode_fused_supported(s) ? 0 : 1;
-  return arm_for(s) == Arm::kTc ? 2 : 3;
+  switch (arm_for(s)) {
+    case Arm::kDecode: return (s.T <= kFdMaxT && decode_fused_supported(s)) ? 0 : 1;
+    case Arm::kTc: return 2;
+    default: return 3;
+  }
 }
 
 int tile_rows_for(const moe_shape_t& s) {
@@ -372,7 +378,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     for (int i = 1; i <= 4 && e == cudaSuccess; ++i) e = mark(i);
     return cuda_status(e);
   }
-  if (s.T <= kDecodeMaxT) {
+  if (arm_for(s) == Arm::kDecode) {
     // decode arm for larger batches: 1) route + permute + work list, 2) gate_up GEMV (+SiLU*up)
     // of every active group incl. the shared expert, 3) down GEMV + fixed-order combine.
     e = launch_route_permute_small(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w,

@@ -55,6 +55,7 @@ constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                      // accumulators: 2 x kBN columns
 constexpr int kACol = 2 * kBN;                // A stages: kTStages x kGK / 2 columns
 static_assert(kACol + kTStages * (kGK / 2) <= kTmemCols, "TMEM budget");
+static_assert(kBN == 128, "the epilogue holds four 32-column groups of row factors");
 static_assert(kGK == 2 * kBStageK && kGK / kBK == 4, "a group is four 64-wide chunks, two activation stages");
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpTmaB = 10, kWarpEpi = 11;
@@ -468,18 +469,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int4 td = __ldg(a.tiles + item / MB);
       const int mb = item % MB;
       const int d = ic & 1;
+      // the tile's column scales (scale2 x 2^e of each activation row; lane l holds columns
+      // l, l + 32, l + 64, l + 96) are fetched before the wait, so their latency hides behind it
+      const float s2 = __ldg(a.scale2 + td.x);
+      float cf[kBN / 32];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i)
+        cf[i] = (32 * i + lane < td.z) ? __ldg(a.act_factor + td.y + 32 * i + lane) : 0.0f;
       if (!(ok = warp_wait(&sm->acc_full[d], (ic >> 1) & 1, sm, a.status))) break;
       tc_fence_after();
-      const float s2 = __ldg(a.scale2 + td.x);
       const int n = (td.z + 15) & ~15;
       for (int c0 = 0; c0 < n; c0 += 16) {
         uint32_t v[16];
         __syncwarp();
         TC_LD16(t_lane + kDCol + d * kBN + c0, v);
+        // scale of column c0 + i: lane (c0 & 31) + i of register c0 / 32
+        const int cr = c0 >> 5;
+        const float colf = s2 * (cr == 0 ? cf[0] : cr == 1 ? cf[1] : cr == 2 ? cf[2] : cf[3]);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        // scale of column c0 + i (lane i < 16 looks it up): scale2 * 2^e of its activation row
-        float colf = 0.0f;
-        if (lane < 16 && c0 + lane < td.z) colf = s2 * __ldg(a.act_factor + td.y + c0 + lane);
         if (kGateUp) {
           // lanes 0-15 hold gate rows j, lanes 16-31 the up rows j (j = mb*64 + 16q + lane%16);
           // a gate lane finishes columns c0..c0+7 and its up partner (lane ^ 16) c0+8..c0+15,
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t other = __shfl_xor_sync(0xffffffffu, is_gate ? v[8 + i] : v[i], 16);
-            const float sc = __shfl_sync(0xffffffffu, colf, cb + i);
+            const float sc = __shfl_sync(0xffffffffu, colf, (c0 & 31) + cb + i);
             const int col = c0 + cb + i;
             if (col < td.z) {
               const float g = __uint_as_float(is_gate ? v[i] : other) * sc;
@@ -503,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nrow = mb * kBM + q * 32 + lane;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float sc = __shfl_sync(0xffffffffu, colf, i);
+            const float sc = __shfl_sync(0xffffffffu, colf, (c0 & 31) + i);
             const int col = c0 + i;
             if (col < td.z)
               static_cast<float*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =

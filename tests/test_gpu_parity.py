@@ -14,8 +14,8 @@ from moe_cases import Layer, check_bf16_stage_close, check_layer_close, moe_shap
 
 pytestmark = pytest.mark.gpu
 
-# (T, H, E, k, I, has_shared, logit bias, seed): the tiny workload itself, both arms, the arm
-# boundary (T = 64 / 65), k = 16, no shared expert, E = 1024, ragged tails everywhere.
+# (T, H, E, k, I, has_shared, logit bias, seed): the tiny workload itself, every arm, the arm
+# boundaries (T = 8 / 9, 64 / 65), k = 16, no shared expert, E = 1024, ragged tails everywhere.
 SMALL = [
     (4, 256, 16, 2, 128, 1, "none", 0),
     (1, 256, 16, 2, 128, 1, "none", 101),
@@ -32,8 +32,10 @@ SMALL = [
     (8, 1024, 64, 8, 256, 1, "zipf", 113),
     (5, 512, 1024, 16, 128, 0, "none", 114),
     (2, 512, 32, 2, 1024, 1, "normal", 115),
-    # tcgen05 arm (T > 64, H and I multiples of 256): ragged token tiles, several tiles per
-    # expert, no shared expert, the N tail of a single 16-column step
+    # tcgen05 arm (T > 8, H and I multiples of 256): ragged token tiles, several tiles per
+    # expert, no shared expert, the N tail of a single 16-column step, single-token experts
+    (9, 256, 16, 2, 256, 1, "none", 116),
+    (48, 512, 32, 4, 256, 1, "zipf", 117),
     (129, 256, 8, 2, 256, 0, "none", 109),
     (1000, 512, 64, 8, 256, 1, "zipf", 110),
     (700, 1024, 32, 6, 512, 1, "normal", 111),
@@ -101,8 +103,8 @@ def test_forward_arm_selection(cuda_lib):
     moe = cuda_lib
     arm = lambda **kw: moe.forward_arm(moe.Shape(**{**dict(T=1, H=2048, I=512, E=512, k=10), **kw}))
     assert arm(T=1) == 0 and arm(T=8) == 0
-    assert arm(T=9) == 1 and arm(T=64) == 1 and arm(T=4, H=256) == 1
-    assert arm(T=65) == 2 and arm(T=4096) == 2
+    assert arm(T=4, H=256) == 1 and arm(T=9, I=128) == 1 and arm(T=64, I=128) == 1
+    assert arm(T=9) == 2 and arm(T=64) == 2 and arm(T=65) == 2 and arm(T=4096) == 2
     assert arm(T=65, I=128) == 3
     assert arm(H=100) == -1
 
