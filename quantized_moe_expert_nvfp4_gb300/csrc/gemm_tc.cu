@@ -242,6 +242,12 @@ __device__ __forceinline__ bool elect_one() {
   return p != 0;
 }
 
+// Tile descriptor of a work item (zeros past the end).  Every role loads the next item's
+// descriptor one item ahead, so its latency hides behind the current item.
+__device__ __forceinline__ int4 load_tile(const TcArgs& a, int item, int n_items, int MB) {
+  return item < n_items ? __ldg(a.tiles + item / MB) : make_int4(0, 0, 0, 0);
+}
+
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
@@ -295,8 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int box_rows = kGateUp ? kBM / 2 : kBM;
       uint32_t ia = 0;
       bool ok = true;
+      int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int4 td = __ldg(a.tiles + item / MB);
+        const int4 td = td_next;
+        td_next = load_tile(a, item + gridDim.x, n_items, MB);
         const int mb = item % MB;
         const int r0 = td.x * a.Nw + mb * box_rows;
         for (int g = 0; g < KG; ++g, ++ia) {
@@ -328,8 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the tensor and read as zero) and only feed accumulator columns the epilogue skips
       uint32_t ib = 0;
       bool ok = true;
+      int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int4 td = __ldg(a.tiles + item / MB);
+        const int4 td = td_next;
+        td_next = load_tile(a, item + gridDim.x, n_items, MB);
         const int nbox = (td.z + kBBoxRows - 1) / kBBoxRows;
         for (int kb = 0; kb < a.K / kBStageK; ++kb, ++ib) {
           const int sb = ib % kBStages;
@@ -355,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // commits that release its TMEM stage and its two activation stages.
     uint32_t ig = 0, ib = 0, ic = 0;
     bool ok = true;
+    int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
-      const int4 td = __ldg(a.tiles + item / MB);
+      const int4 td = td_next;
+      td_next = load_tile(a, item + gridDim.x, n_items, MB);
       const int n = (td.z + 15) & ~15;
       const uint32_t idesc = make_idesc(n);
       const int d = ic & 1;
@@ -465,17 +477,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t ic = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
-      const int4 td = __ldg(a.tiles + item / MB);
-      const int mb = item % MB;
-      const int d = ic & 1;
-      // the tile's column scales (scale2 x 2^e of each activation row; lane l holds columns
-      // l, l + 32, l + 64, l + 96) are fetched before the wait, so their latency hides behind it
-      const float s2 = __ldg(a.scale2 + td.x);
-      float cf[kBN / 32];
+    // column scales of an item: scale2 of its group and 2^e of each activation row (lane l holds
+    // columns l, l + 32, l + 64, l + 96); those of the next item are fetched while this one's
+    // accumulator is awaited and stored
+    float s2_next = 0.0f, cf_next[kBN / 32];
+    auto fetch_scales = [&](const int4& t) {
+      s2_next = __ldg(a.scale2 + t.x);
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i)
-        cf[i] = (32 * i + lane < td.z) ? __ldg(a.act_factor + td.y + 32 * i + lane) : 0.0f;
+        cf_next[i] = (32 * i + lane < t.z) ? __ldg(a.act_factor + t.y + 32 * i + lane) : 0.0f;
+    };
+    int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
+    if (blockIdx.x < n_items) fetch_scales(td_next);
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+      const int4 td = td_next;
+      td_next = load_tile(a, item + gridDim.x, n_items, MB);
+      const float s2 = s2_next;
+      float cf[kBN / 32];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) cf[i] = cf_next[i];
+      const int mb = item % MB;
+      const int d = ic & 1;
       if (!(ok = warp_wait(&sm->acc_full[d], (ic >> 1) & 1, sm, a.status))) break;
       tc_fence_after();
       const int n = (td.z + 15) & ~15;
@@ -507,20 +529,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-          const int nrow = mb * kBM + q * 32 + lane;
+          float* yrow = static_cast<float*>(a.out) + static_cast<int64_t>(td.y + c0) * a.out_ld + mb * kBM +
+                        q * 32 + lane;
+          float sc[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float sc = __shfl_sync(0xffffffffu, colf, (c0 & 31) + i);
-            const int col = c0 + i;
-            if (col < td.z)
-              static_cast<float*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + nrow] =
-                  __uint_as_float(v[i]) * sc;
+          for (int i = 0; i < 16; ++i) sc[i] = __shfl_sync(0xffffffffu, colf, (c0 & 31) + i);
+          if (c0 + 16 <= td.z) {   // a full chunk: no per-column checks
+#pragma unroll
+            for (int i = 0; i < 16; ++i) yrow[static_cast<int64_t>(i) * a.out_ld] = __uint_as_float(v[i]) * sc[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c0 + i < td.z) yrow[static_cast<int64_t>(i) * a.out_ld] = __uint_as_float(v[i]) * sc[i];
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->acc_empty[d]);
+      if (item + static_cast<int>(gridDim.x) < n_items) fetch_scales(td_next);
     }
   }
 
