@@ -50,7 +50,6 @@ constexpr int kAScaleBytes = kBM * kGK / 16;  // 2 KB: 128 rows x 16 B
 constexpr int kAStageBytes = kAPackedBytes + kAScaleBytes;
 constexpr int kBSubBytes = kBN * kBK * 2;     // 16 KB: 128 rows x 128 B, 128B swizzle
 constexpr int kBStageBytes = (kBStageK / kBK) * kBSubBytes;
-constexpr int kBBoxRows = 32;                 // activation rows per TMA box
 constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                      // accumulators: 2 x kBN columns
 constexpr int kACol = 2 * kBN;                // A stages: kTStages x kGK / 2 columns
@@ -64,6 +63,17 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = 15 * 32;
 constexpr uint32_t kSpinLimit = 1u << 24;      // drain loops only
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: no legitimate wait comes close
+
+// Tensor maps of one launch.  Weights: gate_up reads a tile's 64 gate rows and the matching 64 up
+// rows (I rows further down the group) as one 3D box {K bytes, 64 rows, 2 halves}; down reads
+// 128 consecutive rows.  Activations: one 3D box {64 columns, rows, 2 sub-tiles} per 128-wide K
+// stage lands as two [rows][128 B] swizzled sub-tiles; b[i] has a box of 16 (i + 1) rows, so a
+// tile loads its own rows rounded up to 16.
+struct TcMaps {
+  CUtensorMap a;                // packed e2m1
+  CUtensorMap s;                // e4m3 scales
+  CUtensorMap b[kBN / 16];      // f16 activations
+};
 
 struct TcArgs {
   const float* scale2;
@@ -151,6 +161,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -250,8 +268,7 @@ __device__ __forceinline__ int4 load_tile(const TcArgs& a, int item, int n_items
 
 template <bool kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmS,
-                           const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+    grouped_gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sB = base;                                   // kBStages x 32 KB (1024-aligned)
@@ -312,12 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&sm->a_free[st], ((ia / kAStages) & 1) ^ 1, sm, a.status))) break;
           uint8_t* dA = sA + st * kAStageBytes;
           mbar_expect_tx(&sm->a_full[st], kAStageBytes);
-          tma_load_2d(dA, &tmA, g * (kGK / 2), r0, &sm->a_full[st]);
-          tma_load_2d(dA + kAPackedBytes, &tmS, g * (kGK / 16), r0, &sm->a_full[st]);
           if (kGateUp) {
-            tma_load_2d(dA + box_rows * (kGK / 2), &tmA, g * (kGK / 2), r0 + a.Nw / 2, &sm->a_full[st]);
-            tma_load_2d(dA + kAPackedBytes + box_rows * (kGK / 16), &tmS, g * (kGK / 16), r0 + a.Nw / 2,
-                        &sm->a_full[st]);
+            tma_load_3d(dA, &maps.a, g * (kGK / 2), r0, 0, &sm->a_full[st]);
+            tma_load_3d(dA + kAPackedBytes, &maps.s, g * (kGK / 16), r0, 0, &sm->a_full[st]);
+          } else {
+            tma_load_2d(dA, &maps.a, g * (kGK / 2), r0, &sm->a_full[st]);
+            tma_load_2d(dA + kAPackedBytes, &maps.s, g * (kGK / 16), r0, &sm->a_full[st]);
           }
         }
       }
@@ -331,25 +348,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpTmaB) {
     if (lane == 0) {
-      // activation rows [td.y, td.y + 32 * nbox) of the expert-ordered f16 operand, two 64-wide
-      // sub-tiles per stage; rows past the tile's own belong to the next tiles (or lie beyond
-      // the tensor and read as zero) and only feed accumulator columns the epilogue skips
+      // activation rows [td.y, td.y + n16) of the expert-ordered f16 operand (n16 = the tile's
+      // rows rounded up to 16), both 64-wide sub-tiles of a stage in one box; rows past the
+      // tile's own belong to the next tiles (or lie beyond the tensor and read as zero) and only
+      // feed accumulator columns the epilogue skips
       uint32_t ib = 0;
       bool ok = true;
       int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const int4 td = td_next;
         td_next = load_tile(a, item + gridDim.x, n_items, MB);
-        const int nbox = (td.z + kBBoxRows - 1) / kBBoxRows;
+        const int n16 = (td.z + 15) >> 4;                 // 16-row blocks of the tile
+        const CUtensorMap* mb_map = &maps.b[n16 - 1];
         for (int kb = 0; kb < a.K / kBStageK; ++kb, ++ib) {
           const int sb = ib % kBStages;
           if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
-          uint8_t* dB = sB + sb * kBStageBytes;
-          mbar_expect_tx(&sm->b_full[sb], (kBStageK / kBK) * nbox * kBBoxRows * kBK * 2);
-          for (int sub = 0; sub < kBStageK / kBK; ++sub)
-            for (int bx = 0; bx < nbox; ++bx)
-              tma_load_2d(dB + sub * kBSubBytes + bx * kBBoxRows * kBK * 2, &tmB, kb * kBStageK + sub * kBK,
-                          td.y + bx * kBBoxRows, &sm->b_full[sb]);
+          mbar_expect_tx(&sm->b_full[sb], (kBStageK / kBK) * n16 * 16 * kBK * 2);
+          tma_load_3d(sB + sb * kBStageBytes, mb_map, 0, td.y, kb * (kBStageK / kBK), &sm->b_full[sb]);
         }
       }
       if (!ok) {
@@ -387,7 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_tmem = tmem + kACol + ts * (kGK / 2);
 #pragma unroll
           for (int c = 0; c < kGK / kBK; ++c) {       // 64-wide chunk c of the group
-            const uint32_t b_addr = smem_u32(sB + ((c >> 1) ? sb1 : sb0) * kBStageBytes + (c & 1) * kBSubBytes);
+            // sub-tile c & 1 of the stage starts n rows (n * 128 B, a multiple of 2 KB) in
+            const uint32_t b_addr = smem_u32(sB + ((c >> 1) ? sb1 : sb0) * kBStageBytes + (c & 1) * n * (kBK * 2));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t at = a_tmem + c * (kBK / 2) + kk * 8;
@@ -575,6 +591,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr, uint64_t d0, uint64_t d1,
+                 uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1, uint32_t b2,
+                 CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  (void)elem_bytes;
+  return fn(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr, uint64_t inner,
                  uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   auto fn = encode_fn();
@@ -611,18 +641,30 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
     attr_set = true;
   }
   const int G = g.E + 1;
-  const int box_rows = kGateUp ? kBM / 2 : kBM;
+  const uint64_t rows = static_cast<uint64_t>(G) * g.N;
   const uint64_t act_rows = static_cast<uint64_t>(g.S) + g.T;
-  CUtensorMap tmA, tmS, tmB;
-  if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.packed, g.K / 2, static_cast<uint64_t>(G) * g.N,
-                   kGK / 2, box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  if (!make_map_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.scales, g.K / 16, static_cast<uint64_t>(G) * g.N,
-                   kGK / 16, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
-  if (!make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, g.K, act_rows, kBK, kBBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  TcMaps maps;
+  bool ok = true;
+  if (kGateUp) {
+    // rows y of the gate half and y + N/2 of the up half; y < rows - N/2 keeps every box of a
+    // valid gate row inside the tensor
+    const uint64_t half = static_cast<uint64_t>(g.N / 2);
+    ok = ok && make_map_3d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.packed, g.K / 2, rows - half, 2, g.K / 2,
+                           half * (g.K / 2), kGK / 2, kBM / 2, 2, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map_3d(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.scales, g.K / 16, rows - half, 2, g.K / 16,
+                           half * (g.K / 16), kGK / 16, kBM / 2, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+  } else {
+    ok = ok && make_map_2d(&maps.a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.packed, g.K / 2, rows, kGK / 2, kBM,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_map_2d(&maps.s, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.scales, g.K / 16, rows, kGK / 16, kBM,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  // activations viewed as {64 columns, rows, K / 64 chunks}: chunk z of row y at y * 2K + 128 z bytes
+  for (int i = 0; ok && i < kBN / 16; ++i)
+    ok = make_map_3d(&maps.b[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, kBK, act_rows, g.K / kBK,
+                     static_cast<uint64_t>(g.K) * 2, kBK * 2, kBK, 16 * (i + 1), kBStageK / kBK,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
   TcArgs a;
   a.scale2 = g.scale2;
   a.Nw = g.N;
@@ -635,7 +677,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.status = g.status;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, sm_count()));
-  grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(tmA, tmS, tmB, a);
+  grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(maps, a);
   return cudaGetLastError();
 }
 
