@@ -14,19 +14,20 @@
 //                alternate 64-wide K chunks), e2m1 x e4m3 -> f16 exactly (every product has at
 //                most 6 significant bits and lies in [2^-10, 2688]), written to TMEM with
 //                tcgen05.st as the A operand
-//   warp 10      TMA producer of the activation tiles (K = 128 per stage)
+//   warp 10      TMA producer of the activation tiles (K = 256 per stage)
 //   warps 11-14  epilogue: tcgen05.ld of the fp32 accumulator, x scale2 x 2^e (the activation
 //                row's exponent), SiLU(gate)*up (gate_up)
 // The MMA is kind::f16 with f16 operands: the activations arrive as f16 rows in expert order,
 // scaled by a power of two per row (exact for every element above 2^-31 of the row maximum), so
 // the dequantization is one conversion and one packed multiply per pair of weights, and the
 // products and the fp32 accumulation are those of the bf16 activations.
-// The pipeline advances in groups of K = 256 (16 MMAs): one packed-weight stage, one TMEM stage
-// and two activation stages per group.  Each readiness check of the MMA warp idles the tensor
-// pipe for about 200 cycles at N <= 128 (measured on GB300), so the MMA warp checks once per
-// group, not once per 64-wide slice.  The accumulator is double-buffered in TMEM so the
-// epilogue of one tile overlaps the next tile's main loop.  Every mbarrier wait is bounded; on
-// timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the workspace status word and winds down.
+// The pipeline advances in groups of K = 256 (16 MMAs): one packed-weight stage, and one group
+// stage made of a TMEM stage of dequantized A and an SMEM stage of activations, behind a single
+// barrier.  Each readiness check of the MMA warp idles the tensor pipe for about 200 cycles at
+// N <= 128 (measured on GB300), so the MMA warp checks once per group.  The accumulator is
+// double-buffered in TMEM so the epilogue of one tile overlaps the next tile's main loop.  Every
+// mbarrier wait is bounded; on timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the
+// workspace status word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,20 +43,18 @@ constexpr int kBN = kTcTileRows;              // tokens per tile at most (MMA N,
 constexpr int kBK = 64;                       // K per 128-byte swizzled operand row
 constexpr int kGK = 256;                      // K per pipeline group
 constexpr int kAStages = 4;                   // packed-weight ring (SMEM), one group per stage
-constexpr int kTStages = 2;                   // dequantized-A ring (TMEM), one group per stage
-constexpr int kBStageK = 128;                 // K per activation stage (two 64-wide sub-tiles)
-constexpr int kBStages = 4;                   // activation ring (SMEM)
+constexpr int kGStages = 2;                   // group ring: dequantized A (TMEM) + activations (SMEM)
 constexpr int kAPackedBytes = kBM * kGK / 2;  // 16 KB: 128 rows x 128 B, 128B swizzle
 constexpr int kAScaleBytes = kBM * kGK / 16;  // 2 KB: 128 rows x 16 B
 constexpr int kAStageBytes = kAPackedBytes + kAScaleBytes;
 constexpr int kBSubBytes = kBN * kBK * 2;     // 16 KB: 128 rows x 128 B, 128B swizzle
-constexpr int kBStageBytes = (kBStageK / kBK) * kBSubBytes;
+constexpr int kBStageBytes = (kGK / kBK) * kBSubBytes;   // 64 KB: four 64-wide sub-tiles
 constexpr int kTmemCols = 512;
 constexpr int kDCol = 0;                      // accumulators: 2 x kBN columns
-constexpr int kACol = 2 * kBN;                // A stages: kTStages x kGK / 2 columns
-static_assert(kACol + kTStages * (kGK / 2) <= kTmemCols, "TMEM budget");
+constexpr int kACol = 2 * kBN;                // A stages: kGStages x kGK / 2 columns
+static_assert(kACol + kGStages * (kGK / 2) <= kTmemCols, "TMEM budget");
 static_assert(kBN == 128, "the epilogue holds four 32-column groups of row factors");
-static_assert(kGK == 2 * kBStageK && kGK / kBK == 4, "a group is four 64-wide chunks, two activation stages");
+static_assert(kGK / kBK == 4, "a group is four 64-wide chunks");
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpTmaB = 10, kWarpEpi = 11;
 constexpr int kDeqWarps = 8;
@@ -89,10 +88,9 @@ struct TcArgs {
 struct Smem {
   uint64_t a_full[kAStages];     // packed tile + scales landed (TMA transaction)
   uint64_t a_free[kAStages];     // every dequant warp is done reading the stage
-  uint64_t t_full[kTStages];     // dequantized A written to TMEM (one arrival per dequant warp)
-  uint64_t t_free[kTStages];     // the MMAs reading that TMEM stage completed
-  uint64_t b_full[kBStages];     // activation stage landed (TMA transaction)
-  uint64_t b_free[kBStages];     // the MMAs reading that activation stage completed
+  uint64_t g_full[kGStages];     // a group's A is in TMEM (one arrival per dequant warp) and its
+                                 // activations have landed (the producer's arrival + transaction)
+  uint64_t g_free[kGStages];     // the MMAs reading that group's TMEM and SMEM stages completed
   uint64_t acc_full[2];
   uint64_t acc_empty[2];         // one arrival per epilogue warp
   uint64_t drain;
@@ -271,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = base;                                   // kBStages x 32 KB (1024-aligned)
-  uint8_t* sA = base + kBStages * kBStageBytes;         // kAStages x 18 KB (1024-aligned)
+  uint8_t* sB = base;                                   // kGStages x 64 KB (1024-aligned)
+  uint8_t* sA = base + kGStages * kBStageBytes;         // kAStages x 18 KB (1024-aligned)
   Smem* sm = reinterpret_cast<Smem*>(sA + kAStages * kAStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -285,13 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->a_full[s], 1);
       mbar_init(&sm->a_free[s], kDeqWarps);
     }
-    for (int s = 0; s < kTStages; ++s) {
-      mbar_init(&sm->t_full[s], kDeqWarps);
-      mbar_init(&sm->t_free[s], 1);
-    }
-    for (int s = 0; s < kBStages; ++s) {
-      mbar_init(&sm->b_full[s], 1);
-      mbar_init(&sm->b_free[s], 1);
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(&sm->g_full[s], kDeqWarps + 1);
+      mbar_init(&sm->g_free[s], 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm->acc_full[d], 1);
@@ -349,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpTmaB) {
     if (lane == 0) {
       // activation rows [td.y, td.y + n16) of the expert-ordered f16 operand (n16 = the tile's
-      // rows rounded up to 16), both 64-wide sub-tiles of a stage in one box; rows past the
+      // rows rounded up to 16), the four 64-wide sub-tiles of a group in one box; rows past the
       // tile's own belong to the next tiles (or lie beyond the tensor and read as zero) and only
       // feed accumulator columns the epilogue skips
       uint32_t ib = 0;
@@ -360,25 +354,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         td_next = load_tile(a, item + gridDim.x, n_items, MB);
         const int n16 = (td.z + 15) >> 4;                 // 16-row blocks of the tile
         const CUtensorMap* mb_map = &maps.b[n16 - 1];
-        for (int kb = 0; kb < a.K / kBStageK; ++kb, ++ib) {
-          const int sb = ib % kBStages;
-          if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
-          mbar_expect_tx(&sm->b_full[sb], (kBStageK / kBK) * n16 * 16 * kBK * 2);
-          tma_load_3d(sB + sb * kBStageBytes, mb_map, 0, td.y, kb * (kBStageK / kBK), &sm->b_full[sb]);
+        for (int g = 0; g < KG; ++g, ++ib) {
+          const int sb = ib % kGStages;
+          if (!(ok = mbar_wait(&sm->g_free[sb], ((ib / kGStages) & 1) ^ 1, sm, a.status))) break;
+          mbar_expect_tx(&sm->g_full[sb], (kGK / kBK) * n16 * 16 * kBK * 2);
+          tma_load_3d(sB + sb * kBStageBytes, mb_map, 0, td.y, g * (kGK / kBK), &sm->g_full[sb]);
         }
       }
-      if (!ok) {
-        for (int j = 0; j < kBStages && ib > 0; ++j, --ib) {
+      if (!ok) {  // let the copies in flight land: the last stages' transactions (bounded)
+        for (int j = 0; j < kGStages && ib > 0; ++j, --ib) {
           const uint32_t q = ib - 1;
-          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->b_full[q % kBStages], (q / kBStages) & 1); ++i) {
+          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->g_full[q % kGStages], (q / kGStages) & 1); ++i) {
           }
         }
       }
     }
   } else if (warp == kWarpMma) {
-    // The whole warp waits (converged); one elected lane issues the 16 MMAs of a group and the
-    // commits that release its TMEM stage and its two activation stages.
-    uint32_t ig = 0, ib = 0, ic = 0;
+    // The whole warp waits (converged) once per group; one elected lane issues the group's 16
+    // MMAs and the commit that releases its TMEM and activation stages.
+    uint32_t ig = 0, ic = 0;
     bool ok = true;
     int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
@@ -390,20 +384,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(&sm->acc_empty[d], ((ic >> 1) & 1) ^ 1, sm, a.status))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + kDCol + d * kBN;
-      for (int g = 0; g < KG; ++g, ++ig, ib += 2) {
-        const int ts = ig % kTStages;
-        const int sb0 = ib % kBStages, sb1 = (ib + 1) % kBStages;
-        ok = warp_wait(&sm->t_full[ts], (ig / kTStages) & 1, sm, a.status) &&
-             warp_wait(&sm->b_full[sb0], (ib / kBStages) & 1, sm, a.status) &&
-             warp_wait(&sm->b_full[sb1], ((ib + 1) / kBStages) & 1, sm, a.status);
-        if (!ok) break;
+      for (int g = 0; g < KG; ++g, ++ig) {
+        const int gs = ig % kGStages;
+        if (!(ok = warp_wait(&sm->g_full[gs], (ig / kGStages) & 1, sm, a.status))) break;
         tc_fence_after();
         if (elect_one()) {
-          const uint32_t a_tmem = tmem + kACol + ts * (kGK / 2);
+          const uint32_t a_tmem = tmem + kACol + gs * (kGK / 2);
 #pragma unroll
           for (int c = 0; c < kGK / kBK; ++c) {       // 64-wide chunk c of the group
-            // sub-tile c & 1 of the stage starts n rows (n * 128 B, a multiple of 2 KB) in
-            const uint32_t b_addr = smem_u32(sB + ((c >> 1) ? sb1 : sb0) * kBStageBytes + (c & 1) * n * (kBK * 2));
+            // sub-tile c of the stage starts c * n rows (n * 128 B, a multiple of 2 KB) in
+            const uint32_t b_addr = smem_u32(sB + gs * kBStageBytes + c * n * (kBK * 2));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t at = a_tmem + c * (kBK / 2) + kk * 8;
@@ -414,9 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_mma_acc(d_tmem, at, bd, idesc);
             }
           }
-          tc_commit(&sm->t_free[ts]);
-          tc_commit(&sm->b_free[sb0]);
-          tc_commit(&sm->b_free[sb1]);
+          tc_commit(&sm->g_free[gs]);
         }
         __syncwarp();
       }
@@ -447,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       for (int g = 0; g < KG; ++g, ++ia) {
-        const int st = ia % kAStages, ts = ia % kTStages;
+        const int st = ia % kAStages, ts = ia % kGStages;
         if (!(ok = warp_wait(&sm->a_full[st], (ia / kAStages) & 1, sm, a.status))) break;
         const uint8_t* stage = sA + st * kAStageBytes;
         const uint8_t* rowp = stage + srow * (kGK / 2);
@@ -464,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->a_free[st]);
-        if (!(ok = warp_wait(&sm->t_free[ts], ((ia / kTStages) & 1) ^ 1, sm, a.status))) break;
+        if (!(ok = warp_wait(&sm->g_free[ts], ((ia / kGStages) & 1) ^ 1, sm, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -485,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->t_full[ts]);
+        if (lane == 0) mbar_arrive(&sm->g_full[ts]);
       }
     }
   } else if (warp >= kWarpEpi && warp < kWarpEpi + kEpiWarps) {
@@ -617,7 +605,7 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemBytes = 1024 + kBStages * kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
+constexpr size_t kSmemBytes = 1024 + kGStages * kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 int sm_count() {
@@ -662,7 +650,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   // activations viewed as {64 columns, rows, K / 64 chunks}: chunk z of row y at y * 2K + 128 z bytes
   for (int i = 0; ok && i < kBN / 16; ++i)
     ok = make_map_3d(&maps.b[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, kBK, act_rows, g.K / kBK,
-                     static_cast<uint64_t>(g.K) * 2, kBK * 2, kBK, 16 * (i + 1), kBStageK / kBK,
+                     static_cast<uint64_t>(g.K) * 2, kBK * 2, kBK, 16 * (i + 1), kGK / kBK,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   TcArgs a;
