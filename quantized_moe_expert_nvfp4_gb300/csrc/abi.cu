@@ -413,7 +413,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     if (e == cudaSuccess) e = mark(4);
     return cuda_status(e);
   }
-  // prefill arm
+  // grouped-GEMM arms: routing, permutation and work list
   e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, cs);
   if (e == cudaSuccess)
     e = launch_permute_large(w.ids, s.T, s.E, s.k, w.counts, w.offsets, w.sorted_slot, w.slot_pos,
