@@ -195,6 +195,7 @@ WsLayout ws_layout(const moe_shape_t& s) {
   const int64_t R = S + s.T;
   L.status = take(256);
   L.meta = take(256);
+  L.fdsync = take(4 * kFdSyncWords);
   L.ids = take(4 * S);
   L.w = take(4 * S);
   L.counts = take(4 * static_cast<size_t>(s.E));
@@ -369,6 +370,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     f.sorted_slot = w.sorted_slot;
     f.slot_pos = w.slot_pos;
     f.h = w.h;
+    f.sync = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + w.L.fdsync);
     f.y = w.y;
     f.out = out;
     f.out_is_fp32 = out_is_fp32;

@@ -1,9 +1,9 @@
 // bf16 activation rows -> f16 rows with a per-row power-of-two scale, for the f16 tensor-core
 // GEMMs of the prefill arm.
 //
-// Row r is written as f16(x[r] * 2^-e[r]) with e[r] = floor(log2(max |x[r]|)) - 14 (and the factor
-// 2^e[r] as a float for the GEMM epilogue), so the row's
-// largest element lands in [2^14, 2^15), well inside f16's range.  A bf16 value has 8 significant
+// Row r is written as f16(x[r] * 2^-e[r]) with e[r] = floor(log2(max |x[r]|)) - 14, at least
+// -126 (and the factor 2^e[r] as a float for the GEMM epilogue), so the row's largest element
+// lands in [2^14, 2^15), well inside f16's range.  A bf16 value has 8 significant
 // bits and f16 11, so every element of at least 2^-31 of the row maximum converts exactly; only
 // smaller ones (below f16's subnormal grid) are rounded.  The GEMM epilogue multiplies the fp32
 // accumulator by 2^e[r] again, so the products are the bf16 activations' own.
@@ -49,8 +49,10 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const int e = (m > 0.0f && m <= 3.4e38f) ? ilogbf(m) - 14 : 0;
-  if (lane == 0) factor[r] = ldexpf(1.0f, e);   // the epilogue's 2^e
+  // e >= -126 keeps 2^-e a normal float (a row whose maximum is below 2^-112 is scaled less)
+  const int e = (m > 0.0f && m <= 3.4e38f) ? max(ilogbf(m) - 14, -126) : 0;
+  const float inv = __int_as_float((127 - e) << 23);           // 2^-e, exactly
+  if (lane == 0) factor[r] = __int_as_float((127 + e) << 23);  // the epilogue's 2^e
   uint4* d = reinterpret_cast<uint4*>(dst + r * K);
   for (int c = lane; c < K / 8; c += 32) {
     const uint4 v = __ldg(s + c);
@@ -58,8 +60,8 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float lo = ldexpf(__uint_as_float(w[i] << 16), -e);
-      const float hi = ldexpf(__uint_as_float(w[i] & 0xffff0000u), -e);
+      const float lo = __uint_as_float(w[i] << 16) * inv;
+      const float hi = __uint_as_float(w[i] & 0xffff0000u) * inv;
       const __half2 h = __floats2half2_rn(lo, hi);
       o[i] = *reinterpret_cast<const uint32_t*>(&h);
     }

@@ -5,13 +5,15 @@
 // done when within 1.3x of it), the routed top-k and the shared expert in one launch per
 // projection, gate+up fused and silu+down fused, and no host round trip.  Here one launch does
 // all of it:
-//   phase A  every CTA routes the T tokens itself (same result everywhere, no launch boundary
-//            between routing and the weight stream) and builds the permutation in SMEM;
+//   phase A  every CTA routes the T tokens itself (one warp per token, the same selection as the
+//            routing kernel; no launch boundary between routing and the weight stream) and
+//            builds the permutation in SMEM with block-wide scans;
 //   phase B  gate_up units (8 gate + 8 up rows of one active expert): h = SiLU(g) * u in bf16;
 //   grid barrier (h complete);
-//   phase C  down units (64 output rows of one active expert): y in fp32;
-//   grid barrier (y complete);
-//   phase D  fixed-order fp32 combine  out[t] = sum_j w[t,j] y[slot(t,j)] + y[shared t].
+//   phase C  down units (64 output rows of one active expert): y in fp32; the unit that
+//            completes a 64-column block (the last of the active experts' units for it, found by
+//            an arrival counter) runs the fixed-order fp32 combine of that block,
+//            out[t] = sum_j w[t,j] y[slot(t,j)] + y[shared t].
 // A producer warp streams each CTA's units (phase B then C, without waiting for the barrier)
 // into a ring of SMEM slots with TMA bulk copies; 8 compute warps dequantize (e2m1 x e4m3,
 // exact) and accumulate in fp32.  Units are dealt round-robin to the CTAs, one CTA per SM.
@@ -57,7 +59,8 @@ struct FdArgs {
   float* y;             // [S + T, H]
   void* out;
   int out_is_fp32;
-  unsigned* grid_bar;   // {count, generation}
+  unsigned long long* grid_ctr;   // grid-barrier arrivals, monotonic
+  unsigned* ccnt;                 // arrivals per 64-column output block, zeroed each launch
   int32_t* status;
   int x_bytes, smem_off, ring_off, slot_bytes, n_slots;
 };
@@ -65,7 +68,6 @@ struct FdArgs {
 struct FdSmem {
   uint64_t full[kFdMaxSlots];
   uint64_t empty[kFdMaxSlots];
-  unsigned long long win[kFdMaxT][kMaxK];   // routing winners: (logit key << 32) | ~index
   int32_t ids[kFdMaxS];
   float w[kFdMaxS];
   int32_t sorted[kFdMaxS];
@@ -74,6 +76,9 @@ struct FdSmem {
   int32_t act_row[kFdMaxS + 1];
   int32_t act_cnt[kFdMaxS + 1];
   int32_t cnt[kMaxE];
+  int wsum[kFdComputeWarps];   // block scan of the expert counts: per-warp totals, then bases
+  int wnz[kFdComputeWarps];
+  int last[kFdGroups];         // this group's down unit completed its output block
   int n_act;
   int abort_flag;
 };
@@ -123,22 +128,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void compute_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kFdComputeWarps * 32) : "memory");
 }
+__device__ __forceinline__ void group_sync(int wg) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + wg), "n"(kFdGroupWarps * 32) : "memory");
+}
 
-// Grid-wide barrier of a cooperative launch (one thread per CTA): arrive on the counter, the
-// last CTA resets it and bumps the generation; others wait for the generation to move.
-__device__ bool grid_barrier(unsigned* bar, FdSmem* sm, int32_t* status) {
-  volatile unsigned* vgen = bar + 1;
-  const unsigned gen = *vgen;
+// Grid-wide barrier of a cooperative launch (one thread per CTA): arrivals on a monotonic 64-bit
+// counter; the barrier instance an arrival belongs to is old / gridDim, so each CTA waits for the
+// counter to reach the end of its instance.  One atomic per CTA, no reset.
+__device__ bool grid_barrier(unsigned long long* ctr, FdSmem* sm, int32_t* status) {
   __threadfence();
-  if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-    atomicExch(bar, 0u);
-    __threadfence();
-    atomicAdd(bar + 1, 1u);
-    return true;
-  }
-  uint64_t t0 = now_ns();
+  const unsigned long long n = gridDim.x;
+  const unsigned long long target = (atomicAdd(ctr, 1ull) / n + 1) * n;
+  volatile unsigned long long* v = ctr;
+  const uint64_t t0 = now_ns();
   for (uint32_t i = 0;; ++i) {
-    if (*vgen != gen) break;
+    if (*v >= target) break;
     if ((i & 1023u) == 1023u && now_ns() - t0 > kFdTimeoutNs) {
       report_device_error(status, kDevTimeout);
       sm->abort_flag = 1;
@@ -208,28 +212,6 @@ __device__ __forceinline__ float warp_reduce_multi(float (&v)[N], int lane) {
   return v[0];
 }
 
-__device__ __forceinline__ unsigned long long expert_key(const float* row, int e, int E) {
-  if (e >= E) return 0ull;
-  return (static_cast<unsigned long long>(logit_key(__ldg(row + e))) << 32) |
-         static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e));
-}
-
-// Descending bitonic sort of one 64-bit key per lane across the warp.
-__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long key, int lane) {
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
-      const bool desc = ((lane & size) == 0);          // direction of this bitonic subsequence
-      const bool lower = ((lane & stride) == 0);       // this lane holds the first element
-      const bool take_max = (desc == lower);
-      key = take_max ? (other > key ? other : key) : (other < key ? other : key);
-    }
-  }
-  return key;
-}
-
 template <int EPL>
 __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   extern __shared__ __align__(1024) uint8_t fd_raw[];
@@ -237,9 +219,6 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
   uint16_t* xs = reinterpret_cast<uint16_t*>(base);
   FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.smem_off);
   uint8_t* ring = base + a.ring_off;
-  // routing candidates live in ring slots 1.. (idle until routing is done; slot 0 may already
-  // be receiving the shared expert's first unit)
-  unsigned long long* cand = reinterpret_cast<unsigned long long*>(ring + a.slot_bytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = T * k;
   const int NS = a.n_slots;
@@ -295,133 +274,110 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
+  if (blockIdx.x == 0)   // the block counters of phase C, which only runs after the grid barrier
+    for (int i = threadIdx.x; i < kFdMaxBlocks; i += blockDim.x) a.ccnt[i] = 0u;
   {
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
     for (int i = threadIdx.x; i < T * H / 8; i += blockDim.x) dst[i] = __ldg(src + i);
   }
-  // routing step 1: the top-k of every 32-expert slice of every token, by a warp bitonic sort
-  const int n_slices = (E + 31) / 32;
-  const int kk = min(k, 32);
+  // routing: warp t < T ranks token t; lane j < k keeps the rank-j winner and its weight
+  int my_id = 0;
+  float my_w = 0.0f;
+  if (warp < T) warp_topk<EPL>(a.logits + static_cast<int64_t>(warp) * E, E, k, lane, my_id, my_w);
+  __syncthreads();
+  if (warp < T && lane < k) {
+    sm->ids[warp * k + lane] = my_id;
+    sm->w[warp * k + lane] = my_w;
+    atomicAdd(&sm->cnt[my_id], 1);
+    if (blockIdx.x == 0) {
+      a.ids[warp * k + lane] = my_id;
+      a.topk_w[warp * k + lane] = my_w;
+    }
+  }
+  __syncthreads();
+  // exclusive scan of the counts over the block: compute thread u takes experts 2u, 2u + 1
+  // (E <= 1024); the active list is the shared expert first, then the routed experts ascending
+  const int sh = a.has_shared;
+  const int u2 = 2 * threadIdx.x;
+  int c0 = 0, c1 = 0;
   if (warp < kFdComputeWarps) {
-    for (int task = warp; task < T * n_slices; task += kFdComputeWarps) {
-      const int t = task / n_slices, sl = task % n_slices;
-      const unsigned long long key = warp_sort_desc(expert_key(a.logits + static_cast<int64_t>(t) * E, sl * 32 + lane, E), lane);
-      if (lane < kk) cand[t * n_slices * kk + sl * kk + lane] = key;
+    c0 = (u2 < E) ? sm->cnt[u2] : 0;
+    c1 = (u2 + 1 < E) ? sm->cnt[u2 + 1] : 0;
+  }
+  int vs = c0 + c1, vn = (c0 > 0) + (c1 > 0);   // inclusive warp scans of rows and of active experts
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int ys = __shfl_up_sync(0xffffffffu, vs, off), yn = __shfl_up_sync(0xffffffffu, vn, off);
+    if (lane >= off) {
+      vs += ys;
+      vn += yn;
     }
   }
-  __syncthreads();
-  // routing step 2: rank of every candidate among its token's candidates; rank < k wins
-  {
-    const int nc = n_slices * kk;
-    for (int task = threadIdx.x; task < T * nc; task += blockDim.x) {
-      const int t = task / nc, c = task % nc;
-      const unsigned long long* ct = cand + t * nc;
-      const unsigned long long key = ct[c];
-      int rank = 0;
-      for (int j = 0; j < nc; ++j) rank += ct[j] > key;
-      if (rank < k && key != 0ull) sm->win[t][rank] = key;
-    }
-  }
-  __syncthreads();
-  if (warp < T) {  // weights: renormalised softmax over the k winners, summed in rank order
-    float my_val = -INFINITY;
-    int my_id = 0;
-    if (lane < k) {
-      const unsigned long long key = sm->win[warp][lane];
-      my_id = static_cast<int>(0xffffffffu - static_cast<uint32_t>(key & 0xffffffffull));
-      my_val = key_value(static_cast<uint32_t>(key >> 32));
-    }
-    const float m = __shfl_sync(0xffffffffu, my_val, 0);
-    const bool live = lane < k;
-    float ev;
-    if (m == -INFINITY) {
-      ev = 0.0f;
-    } else if (m == INFINITY) {
-      ev = (live && my_val == INFINITY) ? 1.0f : 0.0f;
-    } else {
-      ev = live ? expf(my_val - m) : 0.0f;
-    }
-    float sum = 0.0f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ev, j);
-    const float my_w = (sum > 0.0f) ? ev / sum : 0.0f;
-    if (lane < k) {
-      sm->ids[warp * k + lane] = my_id;
-      sm->w[warp * k + lane] = my_w;
-      atomicAdd(&sm->cnt[my_id], 1);
-      if (blockIdx.x == 0) {
-        a.ids[warp * k + lane] = my_id;
-        a.topk_w[warp * k + lane] = my_w;
-      }
-    }
+  if (warp < kFdComputeWarps && lane == 31) {
+    sm->wsum[warp] = vs;
+    sm->wnz[warp] = vn;
   }
   __syncthreads();
   if (warp == 0) {
-    // exclusive scan of the expert counts (each lane a contiguous run of experts), the active
-    // list (shared expert first, then routed experts ascending), then the stable scatter
-    const int sh = a.has_shared;
-    const int per = (E + 31) / 32;
-    const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-    int sum = 0, nz = 0;
-    for (int e = e0; e < e1; ++e) {
-      sum += sm->cnt[e];
-      nz += sm->cnt[e] > 0;
-    }
-    int is = sum, in = nz;
+    int ts = lane < kFdComputeWarps ? sm->wsum[lane] : 0, tn = lane < kFdComputeWarps ? sm->wnz[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int ys = __shfl_up_sync(0xffffffffu, is, off);
-      const int yn = __shfl_up_sync(0xffffffffu, in, off);
+      const int ys = __shfl_up_sync(0xffffffffu, ts, off), yn = __shfl_up_sync(0xffffffffu, tn, off);
       if (lane >= off) {
-        is += ys;
-        in += yn;
+        ts += ys;
+        tn += yn;
       }
     }
-    int run = is - sum, pos = in - nz + sh;
-    for (int e = e0; e < e1; ++e) {
-      const int c = sm->cnt[e];
-      if (blockIdx.x == 0) {
-        a.counts[e] = c;
-        a.offsets[e] = run;
-      }
-      if (c > 0) {
-        sm->act[pos] = e;
-        sm->act_row[pos] = run;
-        sm->act_cnt[pos] = c;
-        ++pos;
-      }
-      sm->cnt[e] = run;  // becomes the scatter cursor
-      run += c;
+    __syncwarp();
+    if (lane < kFdComputeWarps) {   // exclusive bases of each warp
+      sm->wsum[lane] = ts - sm->wsum[lane];
+      sm->wnz[lane] = tn - sm->wnz[lane];
     }
-    const int n_routed = __shfl_sync(0xffffffffu, in, 31);
-    if (lane == 0) {
+    if (lane == kFdComputeWarps - 1) {
       if (sh) {
         sm->act[0] = E;
         sm->act_row[0] = S;
         sm->act_cnt[0] = T;
       }
-      sm->n_act = n_routed + sh;
+      sm->n_act = tn + sh;
       if (blockIdx.x == 0) a.offsets[E] = S;
     }
-    __syncwarp();
-    const unsigned lt = (1u << lane) - 1u;
-    for (int b = 0; b < S; b += 32) {
-      const int s = b + lane;
-      const int e = (s < S) ? sm->ids[s] : -1;
-      const unsigned grp = __match_any_sync(0xffffffffu, e);
-      const int rank = __popc(grp & lt);
-      if (e >= 0) {
-        const int p = sm->cnt[e] + rank;
-        sm->sorted[p] = s;
-        sm->slot_pos[s] = p;
+  }
+  __syncthreads();
+  if (warp < kFdComputeWarps) {
+    int run = sm->wsum[warp] + vs - (c0 + c1), pos = sm->wnz[warp] + vn - ((c0 > 0) + (c1 > 0)) + sh;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int e = u2 + q, c = q ? c1 : c0;
+      if (e < E) {
         if (blockIdx.x == 0) {
-          a.sorted_slot[p] = s;
-          a.slot_pos[s] = p;
+          a.counts[e] = c;
+          a.offsets[e] = run;
         }
+        if (c > 0) {
+          sm->act[pos] = e;
+          sm->act_row[pos] = run;
+          sm->act_cnt[pos] = c;
+          ++pos;
+        }
+        sm->cnt[e] = run;   // the expert's first sorted position
+        run += c;
       }
-      __syncwarp();
-      if (e >= 0 && rank == 0) sm->cnt[e] += __popc(grp);
-      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // stable scatter: slot s goes after the earlier slots of its expert
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const int e = sm->ids[s];
+    int rank = 0;
+    for (int s2 = 0; s2 < s; ++s2) rank += sm->ids[s2] == e;
+    const int p = sm->cnt[e] + rank;
+    sm->sorted[p] = s;
+    sm->slot_pos[s] = p;
+    if (blockIdx.x == 0) {
+      a.sorted_slot[p] = s;
+      a.slot_pos[s] = p;
     }
   }
   __syncthreads();
@@ -496,7 +452,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
   }
   compute_sync();
-  if (threadIdx.x == 0 && ok && !sm->abort_flag) grid_barrier(a.grid_bar, sm, a.status);
+  if (threadIdx.x == 0 && ok && !sm->abort_flag) grid_barrier(a.grid_ctr, sm, a.status);
   compute_sync();
   ok = ok && !*reinterpret_cast<volatile int*>(&sm->abort_flag);
 
@@ -533,27 +489,32 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(FdArgs a) {
         const float r = warp_reduce_multi<8>(acc, lane);   // lane l: row (l >> 2) & 7
         if ((lane & 3) == 0) a.y[static_cast<int64_t>(p) * H + n0 + (lane >> 2)] = r * s2;
       }
+      __threadfence();   // this warp's y visible device-wide before the unit's arrival is counted
     }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
-  }
-  compute_sync();
-  if (threadIdx.x == 0 && ok && !sm->abort_flag) grid_barrier(a.grid_bar, sm, a.status);
-  compute_sync();
-  if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return;
-
-  // phase D: out[t, n] = sum_j w[t, j] * y[slot_pos[t*k + j], n] + y[S + t, n], in that order
-  const int nthr = kFdComputeWarps * 32;
-  for (int idx = blockIdx.x * nthr + threadIdx.x; idx < T * H; idx += gridDim.x * nthr) {
-    const int t = idx / H, n = idx - t * H;
-    float s = 0.0f;
-    for (int j = 0; j < k; ++j)
-      s = fmaf(sm->w[t * k + j], __ldcg(a.y + static_cast<int64_t>(sm->slot_pos[t * k + j]) * H + n), s);
-    if (a.has_shared) s += __ldcg(a.y + static_cast<int64_t>(S + t) * H + n);
-    if (a.out_is_fp32)
-      static_cast<float*>(a.out)[idx] = s;
-    else
-      static_cast<uint16_t*>(a.out)[idx] = f32_to_bf16_bits(s);
+    // the unit's arrival on its 64-column block; the last arrival of a block runs its combine
+    group_sync(wg);
+    const int blk = (u - nB) % dn_per_group;
+    if (gw == 0 && lane == 0)
+      sm->last[wg] = ok && (atomicAdd(a.ccnt + blk, 1u) == static_cast<unsigned>(n_act) - 1u);
+    group_sync(wg);
+    if (sm->last[wg]) {
+      // every active expert's y of columns [64 blk, 64 blk + 64) is final: the fixed-order combine
+      // out[t, n] = sum_j w[t, j] * y[slot_pos[t*k + j], n] + y[S + t, n]
+      __threadfence();
+      for (int idx = gw * 32 + lane; idx < T * kFdDnRows; idx += kFdGroupWarps * 32) {
+        const int t = idx / kFdDnRows, n = blk * kFdDnRows + idx % kFdDnRows;
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j)
+          acc = fmaf(sm->w[t * k + j], __ldcg(a.y + static_cast<int64_t>(sm->slot_pos[t * k + j]) * H + n), acc);
+        if (a.has_shared) acc += __ldcg(a.y + static_cast<int64_t>(S + t) * H + n);
+        if (a.out_is_fp32)
+          static_cast<float*>(a.out)[t * H + n] = acc;
+        else
+          static_cast<uint16_t*>(a.out)[t * H + n] = f32_to_bf16_bits(acc);
+      }
+    }
   }
 }
 
@@ -573,8 +534,7 @@ bool fd_plan(const moe_shape_t& s, FdPlan* p) {
   const int avail = kFdSmemLimit - 1024 - p->ring_off;
   p->n_slots = std::min(kFdMaxSlots, avail / p->slot_bytes);
   p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * p->slot_bytes;
-  const int cand_bytes = s.T * ((s.E + 31) / 32) * std::min(s.k, 32) * 8;
-  return p->n_slots >= 3 && (p->n_slots - 1) * p->slot_bytes >= cand_bytes;
+  return p->n_slots >= 3;
 }
 
 template <int EPL>
@@ -642,7 +602,8 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   a.y = d.y;
   a.out = d.out;
   a.out_is_fp32 = d.out_is_fp32;
-  a.grid_bar = d.grid_bar;
+  a.grid_ctr = reinterpret_cast<unsigned long long*>(d.grid_bar);
+  a.ccnt = d.sync;
   a.status = d.status;
   a.x_bytes = plan.x_bytes;
   a.smem_off = plan.smem_off;

@@ -19,12 +19,16 @@ constexpr int kSimtTileRows = 64;      // rows per work item of the SIMT grouped
 constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutation
 constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 grouped GEMM
 constexpr int kFdMaxT = 8;             // the fused single-launch decode kernel handles T <= 8
+constexpr int kFdMaxBlocks = 64;       // 64-column output blocks of the one-launch decode kernel
+constexpr int kFdSyncWords = kFdMaxBlocks;   // its arrival counter per output block
 
 // ------------------------------------------------------------------ workspace layout
 // All offsets are in bytes from the workspace base and 256-byte aligned.
 struct WsLayout {
   size_t status;       // int32 device status word (+ padding)
-  size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] grid barrier
+  size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] 64-bit grid-barrier count
+  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: block arrival counters
+                       // (fixed offset; the kernel zeroes them at the start of every launch)
   size_t ids;          // int32 [S]
   size_t w;            // fp32  [S]
   size_t counts;       // int32 [E]
@@ -176,6 +180,7 @@ struct DecodeFusedArgs {
   int32_t* sorted_slot;
   int32_t* slot_pos;
   uint16_t* h;
+  unsigned* sync;     // [kFdSyncWords] block arrival counters (the kernel zeroes them itself)
   float* y;
   void* out;
   int out_is_fp32;

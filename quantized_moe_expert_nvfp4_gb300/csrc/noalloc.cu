@@ -16,9 +16,10 @@
 //    streams, or two host threads) race on it and produce garbage; serialize them.
 //  - The first call on a device looks up the array's device address (cudaGetSymbolAddress).  Make
 //    that first call outside any CUDA stream capture.
-//  - Each call clears the status and grid-barrier words it needs at the start (an asynchronous
-//    memset on the caller's stream, not an allocation), so a device-side timeout of one call does
-//    not poison the next; such a timeout is not reported back by this entry point.
+//  - Each call clears the status word, the grid-barrier counter and the decode kernel's other
+//    synchronisation words at the start (an asynchronous memset on the caller's stream, not an allocation), so a
+//    device-side timeout of one call does not poison the next; such a timeout is not reported
+//    back by this entry point.
 #include <mutex>
 
 #include "internal.cuh"
@@ -35,7 +36,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 size_t up256(size_t x) { return (x + 255) & ~size_t{255}; }
 
 struct Carve {
-  size_t meta, ids, w, counts, offsets, sorted, slot_pos, h, y, total;
+  size_t meta, fdsync, ids, w, counts, offsets, sorted, slot_pos, h, y, total;
 };
 
 Carve carve_for(const moe_shape_t& s) {
@@ -48,6 +49,7 @@ Carve carve_for(const moe_shape_t& s) {
     return o;
   };
   c.meta = take(256);        // [0] status word, [2..3] grid barrier {count, generation}
+  c.fdsync = take(4 * static_cast<size_t>(kFdSyncWords));   // the decode kernel's sync words
   c.ids = take(4 * S);
   c.w = take(4 * S);
   c.counts = take(4 * static_cast<size_t>(s.E));
@@ -119,8 +121,8 @@ extern "C" moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, con
   char* base = static_cast<char*>(scratch_address(&e));
   if (!base) return MOE_ERR_CUDA;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  // the status word and the grid-barrier counters must start at zero
-  e = cudaMemsetAsync(base + c.meta, 0, 256, cs);
+  // the status word, the grid-barrier counter and the sync words must start at zero
+  e = cudaMemsetAsync(base + c.meta, 0, c.ids - c.meta, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   DecodeFusedArgs f;
@@ -136,6 +138,7 @@ extern "C" moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, con
   f.sorted_slot = reinterpret_cast<int32_t*>(base + c.sorted);
   f.slot_pos = reinterpret_cast<int32_t*>(base + c.slot_pos);
   f.h = reinterpret_cast<uint16_t*>(base + c.h);
+  f.sync = reinterpret_cast<unsigned*>(base + c.fdsync);
   f.y = reinterpret_cast<float*>(base + c.y);
   f.out = out;
   f.out_is_fp32 = out_is_fp32;

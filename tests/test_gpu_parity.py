@@ -26,12 +26,11 @@ SMALL = [
     (300, 256, 16, 16, 128, 0, "none", 106),
     (3000, 256, 64, 8, 128, 1, "normal", 107),
     (16, 128, 1024, 16, 128, 1, "none", 108),
-    # one-launch decode arm (T <= 8, H % 512 == 0): E = 1024 with k = 16 and no shared expert,
-    # a skewed batch where experts are shared by several tokens, I = 1024
+    # one-launch decode arm (T <= 8, H % 512 == 0, H <= 4096, I <= 1024): E = 1024 with k = 16
+    # and no shared expert, a skewed batch where experts are shared by several tokens
     (3, 512, 16, 4, 128, 1, "none", 112),
     (8, 1024, 64, 8, 256, 1, "zipf", 113),
     (5, 512, 1024, 16, 128, 0, "none", 114),
-    (2, 512, 32, 2, 1024, 1, "normal", 115),
     # tcgen05 arm (T > 8, H and I multiples of 256): ragged token tiles, several tiles per
     # expert, no shared expert, the N tail of a single 16-column step, single-token experts
     (9, 256, 16, 2, 256, 1, "none", 116),
@@ -102,7 +101,8 @@ def test_small_layers_all_stages(cuda_lib, case):
 def test_forward_arm_selection(cuda_lib):
     moe = cuda_lib
     arm = lambda **kw: moe.forward_arm(moe.Shape(**{**dict(T=1, H=2048, I=512, E=512, k=10), **kw}))
-    assert arm(T=1) == 0 and arm(T=8) == 0
+    assert arm(T=1) == 0 and arm(T=8) == 0 and arm(T=4, H=4096, I=1024) == 0 and arm(T=4, H=1024, I=256) == 0
+    assert arm(T=4, H=8192) == 1 and arm(T=4, I=2048) == 1
     assert arm(T=4, H=256) == 1 and arm(T=9, I=128) == 1 and arm(T=64, I=128) == 1
     assert arm(T=9) == 2 and arm(T=64) == 2 and arm(T=65) == 2 and arm(T=4096) == 2
     assert arm(T=65, I=128) == 3
@@ -220,6 +220,25 @@ def _check_full(moe, L, tokens):
     check_layer_close(to_np(out[torch.tensor(tokens, device="cuda")]), ref, "forward sampled rows")
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
+
+
+# one-launch decode arm at larger shapes than the small cases: E = 1024 with k = 16 and no
+# shared expert, a skewed batch where experts are shared by several tokens, I = 1024, H = 4096.
+# Weights drawn on the GPU; the oracle quantizes the groups the batch uses.
+ONE_LAUNCH = [
+    (2, 2048, 1024, 16, 512, 0, "none", 118),
+    (8, 2048, 64, 8, 512, 1, "zipf", 120),
+    (2, 2048, 32, 2, 1024, 1, "normal", 115),
+    (4, 4096, 64, 4, 512, 1, "zipf", 119),
+]
+
+
+@pytest.mark.parametrize("case", ONE_LAUNCH, ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_I{c[4]}_sh{c[5]}")
+def test_one_launch_decode_shapes(cuda_lib, case):
+    T, H, E, k, I, sh, bias, seed = case
+    L = Layer(synth.Shape(T=T, H=H, E=E, k=k, I=I, has_shared=sh), seed, logit_bias=bias, gen_device="cuda")
+    assert cuda_lib.forward_arm(moe_shape(cuda_lib, L.shape)) == 0
+    _check_full(cuda_lib, L, list(range(T)))
 
 
 @pytest.mark.parametrize("T,seed", list(zip(synth.WORKLOADS["decode"].Ts, synth.WORKLOADS["decode"].seeds)))

@@ -17,7 +17,7 @@ from moe_cases import Layer, check_layer_close, moe_shape, to_np
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    (3, 512, 16, 4, 128, 1, "none", 201),
+    (3, 2048, 16, 4, 512, 1, "none", 201),
     (8, 2048, 512, 10, 512, 1, "none", 202),
 ]
 
