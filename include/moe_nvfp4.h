@@ -15,7 +15,9 @@
  *    allocates or frees.  Scratch comes from the caller's workspace `ws` (size from
  *    moe_workspace_size), which the call may overwrite; 256-byte alignment is required for
  *    `ws` and 16-byte alignment for every other device pointer.  The first 4 bytes of `ws` hold
- *    the device status word: zero-fill a new workspace once before its first use.
+ *    the device status word: zero-fill a new workspace once before its first use, and again
+ *    after a call reported MOE_ERR_DEVICE_TIMEOUT (the one-launch decode kernel keeps a grid
+ *    barrier counter in the workspace, which a timed-out launch may leave mid-instance).
  *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls only
  *    enqueue work; none synchronizes the host, none copies device data to the host (the
  *    route and permutation results stay on the device, so no host round trip breaks stream
