@@ -286,9 +286,12 @@ def run_ours(args):
     arms = [moe.forward_arm(L["ms"]) for L in layers]
     decode_arm = all(a in (0, 1) for a in arms)
     # kernels per forward: arm 0 one; arm 1 route+permute, gate_up, down+combine; arm 2 route,
-    # permute (3), work list, activation gather, gate_up, h conversion, down, combine; arm 3 the
-    # same without the two f16 conversions
-    launches = sum({0: 1, 1: 3, 2: 10, 3: 8}[a] for a in arms)
+    # permute (3), work list (one kernel for the permutation and work list up to 64 tokens),
+    # activation gather, gate_up, h conversion, down, combine; arm 3 the same without the two
+    # f16 conversions
+    def n_launch(arm, T):
+        return {0: 1, 1: 3, 2: 7 if T <= 64 else 10, 3: 5 if T <= 64 else 8}[arm]
+    launches = sum(n_launch(a, L["T"]) for a, L in zip(arms, layers))
     stream = torch.cuda.Stream(device)
 
     # graphs[b][p]: one step on input batch p, recording event set b

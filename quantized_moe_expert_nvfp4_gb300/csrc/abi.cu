@@ -415,12 +415,15 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     if (e == cudaSuccess) e = mark(4);
     return cuda_status(e);
   }
-  // grouped-GEMM arms: routing, permutation and work list
+  // grouped-GEMM arms: routing, then permutation and work list (one CTA for a small batch)
   e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, cs);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && s.T <= kDecodeMaxT)
+    e = launch_route_permute_small(nullptr, w.ids, s.T, s.E, s.k, s.has_shared, nullptr, nullptr, w.counts,
+                                   w.offsets, w.sorted_slot, w.slot_pos, w.tiles, w.meta, tile_rows_for(s), cs);
+  if (e == cudaSuccess && s.T > kDecodeMaxT)
     e = launch_permute_large(w.ids, s.T, s.E, s.k, w.counts, w.offsets, w.sorted_slot, w.slot_pos,
                              w.hist, w.L.n_chunks, cs);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess && s.T > kDecodeMaxT)
     e = launch_build_tiles(w.offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s), w.tiles,
                            w.meta, w.status, cs);
   if (e == cudaSuccess) e = mark(1);
