@@ -65,10 +65,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Four e2m1 codes packed in the low 16 bits ... eight codes in a 32-bit word (element i in
-// bits 4i..4i+3) -> eight exact fp32 values, via the hardware e2m1x2 -> f16x2 conversion.
-__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&v)[8]) {
-  uint32_t h[4];
+// Eight e2m1 codes in a 32-bit word (element i in bits 4i..4i+3) -> four f16x2 words holding
+// elements (0, 1), (2, 3), (4, 5), (6, 7), the lower element in the low half; exact, since every
+// e2m1 value is an f16 value.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
   asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
       "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
       "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
@@ -77,6 +77,12 @@ __device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&v)[8]) {
       "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
       : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
       : "r"(w));
+}
+
+// The same eight codes -> eight exact fp32 values.
+__device__ __forceinline__ void e2m1x8_to_f32(uint32_t w, float (&v)[8]) {
+  uint32_t h[4];
+  e2m1x8_to_f16x2(w, h);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
