@@ -38,13 +38,14 @@
 namespace moe {
 namespace {
 
-constexpr int kFdComputeWarps = 16;
-constexpr int kFdThreads = (kFdComputeWarps + 1) * 32;
+constexpr int kFdWarps = 16;                   // 4 per SM sub-partition: up to 128 registers a thread
+constexpr int kFdThreads = kFdWarps * 32;
+constexpr int kFdComputeWarps = kFdWarps - 1;
 constexpr int kFdProducer = kFdComputeWarps;   // warp index of the producer
 constexpr int kFdXWarp0 = 8;                   // warps 8 .. 8 + T - 1 stage the activations
 constexpr int kFdGuPairs = 8;                  // gate_up unit: 8 gate rows + the 8 up rows (one m16 tile)
 constexpr int kFdDnRows = 64;                  // down unit: 64 output rows (four m16 tiles)
-constexpr int kFdMaxSlots = 8;                 // ring slots; slot s is consumed by warps s and s + NS
+constexpr int kFdMaxSlots = kFdComputeWarps / 2;   // ring slots; slot s is consumed by warps s and s + NS
 constexpr int kFdMaxS = kFdMaxT * kMaxK;
 constexpr int kFdSmemLimit = 227 * 1024;
 constexpr uint64_t kFdTimeoutNs = 1000000000ull;
@@ -97,8 +98,8 @@ struct FdSmem {
   int32_t act_row[kFdMaxS + 1];
   int32_t act_cnt[kFdMaxS + 1];
   int32_t cnt[kMaxE];
-  int wsum[kFdComputeWarps];   // block scan of the expert counts: per-warp totals, then bases
-  int wnz[kFdComputeWarps];
+  int wsum[kFdWarps];          // block scan of the expert counts: per-warp totals, then bases
+  int wnz[kFdWarps];
   float xfac[kFdMaxT];         // 2^e of each staged f16 activation row
   alignas(16) float red[kFdMaxSlots][32 * 4];   // gate_up: the second warp's partial sums, per slot
   float hfac[kFdMaxSlots][kFdMaxT];              // down: 2^e of each staged h row, per slot
@@ -363,15 +364,12 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     }
   }
   __syncthreads();
-  // exclusive scan of the counts over the block: compute thread u takes experts 2u, 2u + 1
-  // (E <= 1024); the active list is the shared expert first, then the routed experts ascending
+  // exclusive scan of the counts over the block: thread u takes experts 2u, 2u + 1 (E <= 1024);
+  // the active list is the shared expert first, then the routed experts ascending
   const int sh = a.has_shared;
   const int u2 = 2 * threadIdx.x;
-  int c0 = 0, c1 = 0;
-  if (warp < kFdComputeWarps) {
-    c0 = (u2 < E) ? sm->cnt[u2] : 0;
-    c1 = (u2 + 1 < E) ? sm->cnt[u2 + 1] : 0;
-  }
+  const int c0 = (u2 < E) ? sm->cnt[u2] : 0;
+  const int c1 = (u2 + 1 < E) ? sm->cnt[u2 + 1] : 0;
   int vs = c0 + c1, vn = (c0 > 0) + (c1 > 0);   // inclusive warp scans of rows and of active experts
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -381,13 +379,13 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       vn += yn;
     }
   }
-  if (warp < kFdComputeWarps && lane == 31) {
+  if (lane == 31) {
     sm->wsum[warp] = vs;
     sm->wnz[warp] = vn;
   }
   __syncthreads();
   if (warp == 0) {
-    int ts = lane < kFdComputeWarps ? sm->wsum[lane] : 0, tn = lane < kFdComputeWarps ? sm->wnz[lane] : 0;
+    int ts = lane < kFdWarps ? sm->wsum[lane] : 0, tn = lane < kFdWarps ? sm->wnz[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int ys = __shfl_up_sync(0xffffffffu, ts, off), yn = __shfl_up_sync(0xffffffffu, tn, off);
@@ -397,11 +395,11 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       }
     }
     __syncwarp();
-    if (lane < kFdComputeWarps) {   // exclusive bases of each warp
+    if (lane < kFdWarps) {   // exclusive bases of each warp
       sm->wsum[lane] = ts - sm->wsum[lane];
       sm->wnz[lane] = tn - sm->wnz[lane];
     }
-    if (lane == kFdComputeWarps - 1) {
+    if (lane == kFdWarps - 1) {
       if (sh) {
         sm->act[0] = E;
         sm->act_row[0] = S;
@@ -412,7 +410,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     }
   }
   __syncthreads();
-  if (warp < kFdComputeWarps) {
+  {
     int run = sm->wsum[warp] + vs - (c0 + c1), pos = sm->wnz[warp] + vn - ((c0 > 0) + (c1 > 0)) + sh;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -771,7 +769,7 @@ bool fd_plan(const moe_shape_t& s, FdPlan* p) {
   const int slot = w_b + sc_b + s.T * s.I * 2;   // weights, scales, a down unit's h rows
   p->slot_bytes = ((slot + 1023) / 1024) * 1024;     // 1024-aligned for the swizzle
   const int avail = kFdSmemLimit - 1024 - p->ring_off;
-  p->n_slots = std::min(kFdMaxSlots, avail / p->slot_bytes);   // 2 n_slots <= the 16 compute warps
+  p->n_slots = std::min(kFdMaxSlots, avail / p->slot_bytes);   // 2 n_slots <= the compute warps
   p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * p->slot_bytes;
   return p->n_slots >= 3;
 }
