@@ -630,14 +630,12 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     const int slot = my_slot;
     const int blk = (u - nB) % dn_per_group;
     if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (i / NS) & 1, sm, a.status));
+    const int gi = (u - nB) / dn_per_group;
+    const int g = sm->act[gi];
+    const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
+    uint8_t* sl = ring + slot * a.slot_bytes;
+    uint16_t* hs = reinterpret_cast<uint16_t*>(sl + h_off);   // h rows [nt][I]
     if (ok) {
-      const int gi = (u - nB) / dn_per_group;
-      const int g = sm->act[gi];
-      const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
-      const float s2 = __ldg(a.dn_scale2 + g);
-      const uint8_t* sl = ring + slot * a.slot_bytes;
-      const uint8_t* sc = sl + w_b;                                       // scales [64][I/16]
-      uint16_t* hs = reinterpret_cast<uint16_t*>(ring + slot * a.slot_bytes + h_off);   // h rows [nt][I]
       // each h row, in place, as f16(h * 2^-e) with e from the row's maximum (half h takes the
       // rows te with te % 2 == h); 2^e goes to hfac for the epilogue
       for (int te = half; te < nt; te += 2) {
@@ -664,7 +662,13 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
                                            f32x2_to_f16x2(bf16_lo(v[q].w) * inv, bf16_hi(v[q].w) * inv));
         if (lane == 0) sm->hfac[slot][te] = pow2i(e);
       }
-      asm volatile("bar.sync %0, 64;" ::"r"(2 + slot) : "memory");   // both halves' rows converted
+    }
+    // both halves' rows converted (executed by both warps whatever their status, so that neither
+    // waits for a partner that skipped it)
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + slot) : "memory");
+    if (ok) {
+      const float s2 = __ldg(a.dn_scale2 + g);
+      const uint8_t* sc = sl + w_b;   // scales [64][I/16]
       const float fac0 = (2 * tig < nt) ? sm->hfac[slot][2 * tig] : 0.0f;
       const float fac1 = (2 * tig + 1 < nt) ? sm->hfac[slot][2 * tig + 1] : 0.0f;
       const uint8_t* hb = reinterpret_cast<const uint8_t*>(hs + ((grp < nt) ? grp : 0) * I) + 16 * tig;
