@@ -52,6 +52,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--warmup-seconds", type=float, default=2.0,
                    help="keep warming up (whole steps) at least this long, for steady clocks")
+    p.add_argument("--one-forward", type=int, default=None, metavar="LAYER",
+                   help="profiling aid: build layer LAYER of the workload, run four forwards, exit "
+                        "(no timing, no JSON line)")
     return p.parse_args()
 
 
@@ -281,6 +284,16 @@ def run_ours(args):
     warmup = max(3, args.warmup if args.warmup is not None else d_warm)
     pool = args.pool or d_pool
     moe.load()
+    if args.one_forward is not None:   # for ncu: -s 3 -c 1 on the arm's kernel selects the fourth forward
+        T, seed = workload_entries(name)[args.one_forward]
+        L = build_layer(moe, w, T, seed, 1, device)
+        for _ in range(4):
+            moe.forward(L["xs"][0], L["lgs"][0], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+        torch.cuda.synchronize()
+        if moe.device_status(L["ws"]) != 0:
+            raise RuntimeError(f"device status {moe.device_status(L['ws'])}")
+        print(f"one forward: {name} layer {args.one_forward} (T={T}), arm {moe.forward_arm(L['ms'])}")
+        return 0
     layers = [build_layer(moe, w, T, seed, pool, device) for T, seed in workload_entries(name)]
     tokens_per_step = sum(L["T"] for L in layers)
     arms = [moe.forward_arm(L["ms"]) for L in layers]
