@@ -429,12 +429,12 @@ def run_ours(args):
     if all(a == 0 for a in arms):
         stage_names[0] = "whole layer (one launch)"
         t_ms, alg = tot_stage[0], fwd_bytes
-        kname, kfile = "decode_fused_kernel (route+gate_up+down+combine)", ["decode_fused.cu"]
+        kname, kfile = "decode_fused_kernel (route+gate_up+down+combine)", ["decode_fused.cu", "topk.cuh", "internal.cuh"]
     elif hbm_bound:
         dom = 1 if tot_stage[1] >= tot_stage[2] else 2
         t_ms, alg = tot_stage[dom], (gate_up_bytes if dom == 1 else down_bytes)
         if all(a == 2 for a in arms):
-            kname, kfile = f"grouped_gemm_tc_kernel<{'gate_up' if dom == 1 else 'down'}>", ["gemm_tc.cu"]
+            kname, kfile = f"grouped_gemm_tc_kernel<{'gate_up' if dom == 1 else 'down'}>", ["gemm_tc.cu", "internal.cuh"]
         else:
             kname = "grouped_simt_kernel<gate_up>" if dom == 1 else "down_combine_gemv_kernel"
             kfile = ["grouped_simt.cu"]
@@ -453,7 +453,7 @@ def run_ours(args):
                     "frac": achieved / peak, "peak_source": pk["source"], "kernel": kname,
                     "algorithmic_flops_per_launch": gate_up_flops / n_launch,
                     "avg_launch_us": 1e3 * gu_ms / n_launch,
-                    "traffic": stored_traffic(name, kname, [src + "gemm_tc.cu"])}
+                    "traffic": stored_traffic(name, kname, [src + "gemm_tc.cu", src + "internal.cuh"])}
 
     # end to end through host buffers: H2D of x and logits from pinned memory, the C-ABI call,
     # D2H of the output, every step.

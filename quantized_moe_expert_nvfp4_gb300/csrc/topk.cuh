@@ -50,15 +50,11 @@ __device__ __forceinline__ void warp_topk(const float* __restrict__ row, int E, 
         be = lane + 32 * i;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint32_t ok = __shfl_xor_sync(kFullMask, bk, off);
-      const int oe = __shfl_xor_sync(kFullMask, be, off);
-      if (ok > bk || (ok == bk && oe < be)) {
-        bk = ok;
-        be = oe;
-      }
-    }
+    // the warp's winner: the largest key, and among lanes holding it the smallest index (two
+    // warp-wide reductions)
+    const uint32_t wk = __reduce_max_sync(kFullMask, bk);
+    be = static_cast<int>(__reduce_min_sync(kFullMask, bk == wk ? static_cast<uint32_t>(be) : 0xffffffffu));
+    bk = wk;
     if ((be & 31) == lane) taken |= 1u << (be >> 5);
     if (lane == j) {
       my_id = be;
