@@ -11,24 +11,26 @@
 //            power of two per row (the tensor-core arm's convention: exact for every element of
 //            at least 2^-31 of the row maximum);
 //   phase B  gate_up units (8 gate rows + the 8 matching up rows of one active expert):
-//            h = SiLU(g) * u in bf16;
-//   grid barrier (h complete);
-//   phase C  down units (64 output rows of one active expert): y in fp32; the unit that
-//            completes a 64-column block (the last of the active experts' units for it, found by
-//            an arrival counter) runs the fixed-order fp32 combine of that block,
+//            h = SiLU(g) * u in bf16; each unit counts itself on its expert's readiness counter;
+//   phase C  down units (64 output rows of one active expert), each once its expert's h is
+//            complete (no grid-wide barrier): y in fp32; the unit that completes a 64-column
+//            block (the last of the active experts' units for it, found by an arrival counter)
+//            runs the fixed-order fp32 combine of that block,
 //            out[t] = sum_j w[t,j] y[slot(t,j)] + y[shared t].
-// A producer warp streams each CTA's units (phase B then C, without waiting for the barrier)
-// into a ring of SMEM slots: one TMA tensor copy of the unit's packed weights in the 128-byte
-// swizzled layout (few, large copies keep the SM's copy engine streaming at full rate) and, for
-// a down unit, its h rows, copied once the grid barrier has passed; the unit's scales by one more
-// copy (few, large copies keep the SM's copy engine streaming at full rate).  One compute warp takes one whole unit on the tensor cores (mma.sync
-// m16n8k16, f16 operands, fp32 accumulation): the weights are dequantized exactly into f16
-// (e2m1 x e4m3 has at most 6 significant bits and lies in [2^-10, 2688]), the MMA columns are
-// the expert's tokens (up to 8), and the activations are f16 rows scaled by a power of two (x
-// in phase A; each h row by the warp from its maximum).  Units are dealt round-robin to the
-// CTAs, one CTA per SM, and in turn to the CTA's warps (warp w takes the units of ring slot w).  Every wait is bounded: an mbarrier or
-// grid-barrier wait that runs past 1 s records MOE_ERR_DEVICE_TIMEOUT in the status word and
-// the kernel winds down.
+// A producer warp streams each CTA's units (phase B then C) into a ring of SMEM slots: one TMA
+// tensor copy of the unit's packed weights in the 128-byte swizzled layout, one copy of its
+// scales (few, large copies keep the SM's copy engine streaming at full rate) and, for a down
+// unit, its h rows, copied once the expert's readiness counter shows all its gate_up units done.
+// The counters (and the combine's arrival counters) come in two sets used by alternate
+// launches: a launch's set is the parity of the launch count, which every CTA takes with one
+// atomic at entry, and each launch zeroes the other set for the next one.
+// The products run on the tensor cores (mma.sync m16n8k16, f16 operands, fp32 accumulation):
+// the weights are dequantized exactly into f16 (e2m1 x e4m3 has at most 6 significant bits and
+// lies in [2^-10, 2688]), the MMA columns are the expert's tokens (up to 8), and the activations
+// are f16 rows scaled by a power of two (x in phase A; each h row in its slot, from its maximum).
+// Units are dealt round-robin to the CTAs, one CTA per SM; ring slot s belongs to the warp pair
+// (s, s + NS).  Every wait is bounded: an mbarrier or counter wait that runs past 1 s records
+// MOE_ERR_DEVICE_TIMEOUT in the status word and the kernel winds down.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -81,8 +83,8 @@ struct FdArgs {
   float* y;             // [S + T, H]
   void* out;
   int out_is_fp32;
-  unsigned long long* grid_ctr;   // grid-barrier arrivals, monotonic
-  unsigned* ccnt;                 // arrivals per 64-column output block, zeroed each launch
+  unsigned long long* grid_ctr;   // launch count: one arrival per CTA and launch, monotonic
+  unsigned* ccnt;                 // [2][kFdMaxBlocks] block arrivals, then [2][kFdMaxActive] readiness
   int32_t* status;
   int x_pitch, smem_off, ring_off, slot_bytes, n_slots;
 };
@@ -105,7 +107,7 @@ struct FdSmem {
   float hfac[kFdMaxSlots][kFdMaxT];              // down: 2^e of each staged h row, per slot
   int n_act;
   int abort_flag;
-  int bar_passed;              // set once the grid barrier has passed (h is complete)
+  int ep;                      // this launch's counter set (parity of the launch count)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -221,30 +223,6 @@ __device__ __forceinline__ float absmax_bf16x8(float m, const uint4& v) {
   return m;
 }
 
-__device__ __forceinline__ void compute_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kFdComputeWarps * 32) : "memory");
-}
-
-// Grid-wide barrier of a cooperative launch (one thread per CTA): arrivals on a monotonic 64-bit
-// counter; the barrier instance an arrival belongs to is old / gridDim, so each CTA waits for the
-// counter to reach the end of its instance.  One atomic per CTA, no reset.
-__device__ bool grid_barrier(unsigned long long* ctr, FdSmem* sm, int32_t* status) {
-  __threadfence();
-  const unsigned long long n = gridDim.x;
-  const unsigned long long target = (atomicAdd(ctr, 1ull) / n + 1) * n;
-  volatile unsigned long long* v = ctr;
-  const uint64_t t0 = now_ns();
-  for (uint32_t i = 0;; ++i) {
-    if (*v >= target) break;
-    if ((i & 1023u) == 1023u && now_ns() - t0 > kFdTimeoutNs) {
-      report_device_error(status, kDevTimeout);
-      sm->abort_flag = 1;
-      return false;
-    }
-  }
-  __threadfence();
-  return true;
-}
 
 template <int EPL>
 __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __grid_constant__ FdMaps maps, FdArgs a) {
@@ -308,7 +286,6 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_addr(&sm->empty[s])));   // the slot's 2 warps
     }
     sm->abort_flag = 0;
-    sm->bar_passed = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     if (a.has_shared && blockIdx.x < gu_per_group) {   // first unit: shared expert, gate_up
       issue(blockIdx.x, 1 << 30, 0);
@@ -316,8 +293,10 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
-  if (blockIdx.x == 0)   // the block counters of phase C, which only runs after the grid barrier
-    for (int i = threadIdx.x; i < kFdMaxBlocks; i += blockDim.x) a.ccnt[i] = 0u;
+  if (threadIdx.x == 32) {   // this launch's counter set: the launch count's parity
+    const unsigned long long n = atomicAdd(a.grid_ctr, 1ull);
+    sm->ep = static_cast<int>((n / gridDim.x) & 1ull);
+  }
   // activations: warp 8 + t stages token t as f16(x * 2^-e), e = floor(log2 max|x|) - 14 (at
   // least -126), the row maximum in [2^14, 2^15); the factor 2^e is applied to the dot products
   if (warp >= kFdXWarp0 && warp < kFdXWarp0 + T) {
@@ -354,6 +333,14 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   float my_w = 0.0f;
   if (warp < T) warp_topk<EPL>(a.logits + static_cast<int64_t>(warp) * E, E, k, lane, my_id, my_w);
   __syncthreads();
+  const int ep = sm->ep;
+  unsigned* const ccnt = a.ccnt + ep * kFdMaxBlocks;                       // this launch's arrivals
+  unsigned* const ready = a.ccnt + 2 * kFdMaxBlocks + ep * kFdMaxActive;   // and readiness counters
+  if (blockIdx.x == 0) {   // the next launch's set (no CTA of this launch touches it)
+    for (int i = threadIdx.x; i < kFdMaxBlocks; i += blockDim.x) a.ccnt[(ep ^ 1) * kFdMaxBlocks + i] = 0u;
+    for (int i = threadIdx.x; i < kFdMaxActive; i += blockDim.x)
+      a.ccnt[2 * kFdMaxBlocks + (ep ^ 1) * kFdMaxActive + i] = 0u;
+  }
   if (warp < T && lane < k) {
     sm->ids[warp * k + lane] = my_id;
     sm->w[warp * k + lane] = my_w;
@@ -456,26 +443,31 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     if (lane == 0) {
       uint32_t it = early ? 1 : 0;
       bool ok = true;
-      // down units issued before the grid barrier passed wait here for their h copy (at most the
-      // ring's slots: no down unit is consumed before the barrier)
+      // down units whose expert's h is not complete yet wait here for their h copy, in order (at
+      // most the ring's slots)
       int pend_u[kFdMaxSlots];
       uint32_t pend_it[kFdMaxSlots];
-      int np = 0;
-      bool passed = false;
-      auto flush = [&]() {
-        __threadfence();
-        asm volatile("fence.proxy.async.global;" ::: "memory");   // h was written by generic stores
-        for (int q = 0; q < np; ++q) issue_h(pend_u[q], nB, pend_it[q]);
-        np = 0;
-        passed = true;
+      int ph = 0, pt = 0;   // head and tail counts
+      auto expert_ready = [&](int u) {
+        const int gi = (u - nB) / dn_per_group;
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ready + gi) : "memory");
+        return v >= static_cast<unsigned>(gu_per_group);
       };
-      auto barrier_seen = [&]() { return *reinterpret_cast<volatile int*>(&sm->bar_passed) != 0; };
+      // issue the waiting h copies whose expert is ready (all of them when force is set)
+      auto drain = [&](bool force) {
+        while (ph < pt && (force || expert_ready(pend_u[ph % kFdMaxSlots]))) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");   // h was written by generic stores
+          issue_h(pend_u[ph % kFdMaxSlots], nB, pend_it[ph % kFdMaxSlots]);
+          ++ph;
+        }
+      };
       for (int u = blockIdx.x + static_cast<int>(it) * gridDim.x; u < nB + nC; u += gridDim.x, ++it) {
         const int slot = it % NS;
         const uint32_t parity = ((it / NS) & 1) ^ 1;
         uint64_t t0 = 0;
         for (uint32_t i = 0;; ++i) {   // bounded wait for the slot; start h copies meanwhile
-          if (!passed && barrier_seen()) flush();
+          if ((i & 7u) == 0u) drain(false);
           if (fd_try(&sm->empty[slot], parity)) break;
           if ((i & 255u) == 255u) {
             if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) {
@@ -496,19 +488,16 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
         if (!ok) break;
         issue(u, nB, it);
         if (u >= nB) {
-          if (!passed && barrier_seen()) flush();
-          if (passed) {
-            issue_h(u, nB, it);
-          } else {
-            pend_u[np] = u;
-            pend_it[np] = it;
-            ++np;
-          }
+          pend_u[pt % kFdMaxSlots] = u;
+          pend_it[pt % kFdMaxSlots] = it;
+          ++pt;
+          drain(false);
         }
       }
-      if (np > 0) {   // the last down units still wait for the barrier (bounded)
+      {   // the last down units wait for their experts (bounded)
         const uint64_t t0 = now_ns();
-        for (uint32_t i = 0; ok && !barrier_seen(); ++i) {
+        for (uint32_t i = 0; ok && ph < pt; ++i) {
+          drain(false);
           if ((i & 255u) == 255u) {
             if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) ok = false;
             else if (now_ns() - t0 > kFdTimeoutNs) {
@@ -518,7 +507,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
             }
           }
         }
-        flush();   // also on abort: every issued slot then completes, and the drain below is short
+        drain(true);   // on abort too: every issued slot then completes, and the drain below is short
       }
       if (!ok) {  // let copies already issued land before the CTA exits (bounded)
         for (uint32_t j = 0; j < static_cast<uint32_t>(NS) && j < it; ++j) {
@@ -612,14 +601,12 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+    __syncwarp();   // the warp's h stores are ordered before lane 0's release below
+    if (lane == 0) {
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+      if (half == 0 && ok) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ready + gi) : "memory");
+    }
   }
-  compute_sync();
-  if (threadIdx.x == 0 && ok && !sm->abort_flag && grid_barrier(a.grid_ctr, sm, a.status))
-    *reinterpret_cast<volatile int*>(&sm->bar_passed) = 1;   // the producer may now copy h
-  compute_sync();
-  ok = ok && !*reinterpret_cast<volatile int*>(&sm->abort_flag);
 
   // phase C: down units.  The unit's 64 rows are four MMA tiles (rows 16 r + grp, + 8); half h
   // takes tiles 2 h and 2 h + 1.  Column n is h row row0 + n, staged as f16 scaled by 2^-e_n with
@@ -723,7 +710,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     unsigned last = 0;
     if (lane == 0 && ok) {
       unsigned old;
-      asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.ccnt + blk) : "memory");
+      asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(ccnt + blk) : "memory");
       last = old == 2u * static_cast<unsigned>(n_act) - 1u;
     }
     last = __shfl_sync(0xffffffffu, last, 0);

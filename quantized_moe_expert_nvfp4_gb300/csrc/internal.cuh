@@ -20,15 +20,18 @@ constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutati
 constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 grouped GEMM
 constexpr int kFdMaxT = 8;             // the fused single-launch decode kernel handles T <= 8
 constexpr int kFdMaxBlocks = 64;       // 64-column output blocks of the one-launch decode kernel
-constexpr int kFdSyncWords = kFdMaxBlocks;   // its arrival counter per output block
+constexpr int kFdMaxActive = kFdMaxT * kMaxK + 1;   // active groups of one decode launch
+// its sync words, two sets alternating between launches: an arrival counter per output block,
+// then a readiness counter per active group (gate_up units done)
+constexpr int kFdSyncWords = 2 * (kFdMaxBlocks + kFdMaxActive);
 
 // ------------------------------------------------------------------ workspace layout
 // All offsets are in bytes from the workspace base and 256-byte aligned.
 struct WsLayout {
   size_t status;       // int32 device status word (+ padding)
-  size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] 64-bit grid-barrier count
-  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: block arrival counters
-                       // (fixed offset; the kernel zeroes them at the start of every launch)
+  size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] 64-bit launch count
+  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: block arrival and group
+                       // readiness counters, two sets (each launch zeroes the next launch's set)
   size_t ids;          // int32 [S]
   size_t w;            // fp32  [S]
   size_t counts;       // int32 [E]
@@ -186,7 +189,7 @@ struct DecodeFusedArgs {
   int32_t* sorted_slot;
   int32_t* slot_pos;
   uint16_t* h;
-  unsigned* sync;     // [kFdSyncWords] block arrival counters (the kernel zeroes them itself)
+  unsigned* sync;     // [kFdSyncWords] arrival and readiness counters (the kernel zeroes them itself)
   float* y;
   void* out;
   int out_is_fp32;
