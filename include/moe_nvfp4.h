@@ -157,11 +157,11 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                                   void* stream, void* const* stage_events);
 
 /* The one-launch decode forward (moe_forward_arm == 0 shapes: T <= 8, H % 512 == 0, H <= 4096,
- * I <= 1024) for callers that cannot allocate device memory -- code running where cudaMalloc is
+ * I % 256 == 0, I <= 1024) for callers that cannot allocate device memory -- code running where cudaMalloc is
  * not allowed or not available, such as inside a framework's memory-planning phase, a host
  * callback, or a plugin whose host application owns every device allocation and only passes in
  * tensor pointers.  No workspace argument: the scratch (routing results, permutation, h, y, the
- * status word and grid-barrier counters) lives in one 4 MiB array in device global memory that
+ * status word and the decode kernel's counters) lives in one 4 MiB array in device global memory that
  * the library declares at file scope; every GPU that loads the library holds it until the
  * library is unloaded.  The pages have no counterpart to this call; it is a deployment aid.
  *   - Inputs, weights and out are as for moe_forward; nothing is allocated or freed.

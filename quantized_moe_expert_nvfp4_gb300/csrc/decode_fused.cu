@@ -269,8 +269,8 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       bulk_g2s(dst + w_b, a.dn_scales + static_cast<int64_t>(r0) * (I / 16), dn_sb, bar);
     }
   };
-  // The h rows of down unit u (issued as ring position it) into the end of its slot; only after
-  // the grid barrier, since other CTAs write them in phase B.
+  // The h rows of down unit u (issued as ring position it) into the end of its slot; only once
+  // the expert's readiness counter shows every gate_up unit of it done (other CTAs write them).
   auto issue_h = [&](int u, int nB, uint32_t it) {
     const int gi = (u - nB) / dn_per_group;
     const int slot = it % NS;

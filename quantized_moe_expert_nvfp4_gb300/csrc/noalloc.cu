@@ -6,7 +6,7 @@
 // forbids new allocations, inside a host callback, or a plugin whose host application owns
 // every device allocation and only passes in tensor pointers).  For them this entry point keeps
 // its scratch (routing results, the permutation, the bf16 intermediate h, the fp32 expert
-// outputs y, the device status word and the grid-barrier counters) in one fixed-size array in
+// outputs y, the device status word and the decode kernel's counters) in one fixed-size array in
 // device global memory, declared below at file scope.  It calls no allocator at all.
 //
 // Costs and rules, in plain terms:
@@ -16,7 +16,7 @@
 //    streams, or two host threads) race on it and produce garbage; serialize them.
 //  - The first call on a device looks up the array's device address (cudaGetSymbolAddress).  Make
 //    that first call outside any CUDA stream capture.
-//  - Each call clears the status word, the grid-barrier counter and the decode kernel's other
+//  - Each call clears the status word, the launch counter and the decode kernel's other
 //    synchronisation words at the start (an asynchronous memset on the caller's stream, not an allocation), so a
 //    device-side timeout of one call does not poison the next; such a timeout is not reported
 //    back by this entry point.
@@ -48,7 +48,7 @@ Carve carve_for(const moe_shape_t& s) {
     off = up256(off + bytes);
     return o;
   };
-  c.meta = take(256);        // [0] status word, [2..3] grid barrier {count, generation}
+  c.meta = take(256);        // [0] status word, [2..3] the decode kernel's 64-bit launch count
   c.fdsync = take(4 * static_cast<size_t>(kFdSyncWords));   // the decode kernel's sync words
   c.ids = take(4 * S);
   c.w = take(4 * S);
@@ -121,7 +121,7 @@ extern "C" moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, con
   char* base = static_cast<char*>(scratch_address(&e));
   if (!base) return MOE_ERR_CUDA;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  // the status word, the grid-barrier counter and the sync words must start at zero
+  // the status word, the launch counter and the sync words must start at zero
   e = cudaMemsetAsync(base + c.meta, 0, c.ids - c.meta, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
