@@ -48,6 +48,7 @@ constexpr int kFdXWarp0 = 8;                   // warps 8 .. 8 + T - 1 stage the
 constexpr int kFdGuPairs = 8;                  // gate_up unit: 8 gate rows + the 8 up rows (one m16 tile)
 constexpr int kFdDnRows = 64;                  // down unit: 64 output rows (four m16 tiles)
 constexpr int kFdMaxSlots = kFdComputeWarps / 2;   // ring slots; slot s is consumed by warps s and s + NS
+static_assert(2 + 2 * kFdMaxSlots <= 16, "two named barriers per slot after barriers 0 and 1");
 constexpr int kFdMaxS = kFdMaxT * kMaxK;
 constexpr int kFdSmemLimit = 227 * 1024;
 constexpr uint64_t kFdTimeoutNs = 1000000000ull;
@@ -601,10 +602,16 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
         }
       }
     }
-    __syncwarp();   // the warp's h stores are ordered before lane 0's release below
-    if (lane == 0) {
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
-      if (half == 0 && ok) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ready + gi) : "memory");
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+    // the unit counts on its expert's readiness: half 0 signals its h stores with a non-blocking
+    // arrive and goes on; half 1 (otherwise idle until its next unit's data) waits for that and
+    // publishes them with its release, which the barrier makes cover half 0's stores
+    if (half == 0) {
+      asm volatile("bar.arrive %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
+    } else {
+      asm volatile("bar.sync %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
+      if (lane == 0 && ok) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ready + gi) : "memory");
     }
   }
 
@@ -706,12 +713,18 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
-    // each half's arrival on its 64-column block (2 n_act in all); the last arrival runs the combine
+    // the unit's arrival on its 64-column block (n_act in all), by half 1 once half 0's y stores
+    // are ordered before it (half 0 goes on); the last arrival runs the combine
     unsigned last = 0;
-    if (lane == 0 && ok) {
-      unsigned old;
-      asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(ccnt + blk) : "memory");
-      last = old == 2u * static_cast<unsigned>(n_act) - 1u;
+    if (half == 0) {
+      asm volatile("bar.arrive %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
+    } else {
+      asm volatile("bar.sync %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
+      if (lane == 0 && ok) {
+        unsigned old;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(ccnt + blk) : "memory");
+        last = old == static_cast<unsigned>(n_act) - 1u;
+      }
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
