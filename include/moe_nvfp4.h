@@ -157,8 +157,8 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                                   void* stream, void* const* stage_events);
 
 /* The one-launch decode forward (moe_forward_arm == 0 shapes: T <= 8, H % 512 == 0, H <= 4096,
- * I % 256 == 0, I <= 1024) for callers that cannot allocate device memory -- code running where cudaMalloc is
- * not allowed or not available, such as inside a framework's memory-planning phase, a host
+ * I % 256 == 0, I <= 1024) for callers that cannot allocate device memory -- code running where
+ * cudaMalloc is not allowed or not available, such as inside a framework's memory-planning phase, a host
  * callback, or a plugin whose host application owns every device allocation and only passes in
  * tensor pointers.  No workspace argument: the scratch (routing results, permutation, h, y, the
  * status word and the decode kernel's counters) lives in one 4 MiB array in device global memory that
@@ -171,7 +171,8 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
  *     threads) race and corrupt each other; serialize them.
  *   - The first call on a device looks up the array's device address; make it outside any CUDA
  *     stream capture.
- *   - Each call first clears the status and barrier words on `stream` (an asynchronous memset).
+ *   - Each call first clears the status word, the launch count and the decode kernel's counters
+ *     on `stream` (an asynchronous memset).
  *     Device-side timeouts are not reported back by this call. */
 moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, const float* logits,
                                                const moe_nvfp4_weights_t* gate_up,
@@ -191,9 +192,19 @@ moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K,
  * first device-side error recorded since the last read.  Synchronizes `stream`. */
 moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream);
 
+/* Test hook for the device-side timeout path (the pages have no counterpart): one warp waits,
+ * with the one-launch decode kernel's bounded wait, on a shared-memory barrier that nothing
+ * arrives at, for limit_ns nanoseconds of the global timer (1 .. 1e9).  The wait runs out and
+ * records MOE_ERR_DEVICE_TIMEOUT in the workspace status word, as a stalled wait inside a
+ * forward would; nothing faults or hangs.  ws: a workspace (256-byte aligned; only its status
+ * word is written).  Returns MOE_OK once the probe is launched on `stream`; read the result
+ * with moe_get_device_status. */
+moe_status_t moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream);
+
 /* Which kernels moe_forward runs for a shape (-1 for an unsupported shape):
- *   0  T <= 8 (H % 512 == 0, H <= 4096, I <= 1024): one cooperative launch that routes,
- *      streams the active experts' weights with TMA bulk copies and combines (grouped GEMV);
+ *   0  T <= 8 (H % 512 == 0, H <= 4096, I % 256 == 0, I <= 1024, and room in shared memory for
+ *      a ring of three slots): one cooperative launch that routes, streams the active experts'
+ *      weights with TMA copies, multiplies on the tensor cores and combines;
  *   1  T <= 8 otherwise, and 8 < T <= 64 when H or I is not a multiple of 256: three launches
  *      (route+permute, gate_up GEMV, down GEMV + combine);
  *   2  T > 8, H and I multiples of 256: tcgen05 grouped GEMMs (batched decode and prefill);

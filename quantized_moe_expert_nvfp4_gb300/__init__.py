@@ -248,7 +248,17 @@ def device_status(ws: torch.Tensor, stream=None) -> int:
     return v.value
 
 
-ARM_NAMES = {0: "decode, one cooperative launch (grouped GEMV)",
+def debug_timeout_probe(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
+    """Run the decode kernel's bounded wait on a barrier nothing arrives at (test hook): it runs
+    out after limit_ns and records MOE_ERR_DEVICE_TIMEOUT in the workspace status word."""
+    lib = load()
+    lib.moe_debug_timeout_probe.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+    lib.moe_debug_timeout_probe.restype = ctypes.c_int32
+    _check("moe_debug_timeout_probe", lib.moe_debug_timeout_probe(
+        _ptr(ws, torch.uint8, "ws"), int(limit_ns), _stream(stream)))
+
+
+ARM_NAMES = {0: "decode, one cooperative launch (tensor-core grouped GEMV)",
              1: "decode, three launches (grouped GEMV)",
              2: "batched decode / prefill, tcgen05 grouped GEMM", 3: "prefill, CUDA-core grouped GEMM"}
 

@@ -463,6 +463,14 @@ moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream) {
   return MOE_OK;
 }
 
+moe_status_t moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID_ARG;
+  if (limit_ns < 1 || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_arch();
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_fd_timeout_probe(static_cast<int32_t*>(ws), limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
 int moe_forward_arm(const moe_shape_t* shape) {
   if (check_shape(shape) != MOE_OK) return -1;
   return forward_arm(*shape);

@@ -129,7 +129,8 @@ __device__ __forceinline__ bool fd_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ bool fd_wait(uint64_t* b, uint32_t parity, FdSmem* sm, int32_t* status) {
+__device__ bool fd_wait(uint64_t* b, uint32_t parity, FdSmem* sm, int32_t* status,
+                        uint64_t limit_ns = kFdTimeoutNs) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (fd_try(b, parity)) return true;
@@ -138,13 +139,27 @@ __device__ bool fd_wait(uint64_t* b, uint32_t parity, FdSmem* sm, int32_t* statu
       const uint64_t t = now_ns();
       if (t0 == 0) {
         t0 = t;
-      } else if (t - t0 > kFdTimeoutNs) {
+      } else if (t - t0 > limit_ns) {
         report_device_error(status, kDevTimeout);
         *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
         return false;
       }
     }
   }
+}
+
+// One warp waits, with the kernel's bounded wait, on an mbarrier that nothing arrives at: the
+// wait runs out after limit_ns and records the timeout in the status word (the test of the
+// timeout path; nothing faults or hangs).
+__global__ void __launch_bounds__(32) fd_timeout_probe_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ FdSmem sm;
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[0])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  fd_wait(&sm.full[0], 0, &sm, status, limit_ns);
 }
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -808,6 +823,11 @@ cudaError_t launch_fd(const FdMaps& maps, const FdArgs& args, const FdPlan& plan
 }
 
 }  // namespace
+
+cudaError_t launch_fd_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t st) {
+  fd_timeout_probe_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
 
 bool decode_fused_supported(const moe_shape_t& s) {
   FdPlan p;

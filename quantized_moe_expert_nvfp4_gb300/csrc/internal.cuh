@@ -197,6 +197,8 @@ struct DecodeFusedArgs {
   int32_t* status;
 };
 bool decode_fused_supported(const moe_shape_t& s);
+// One warp running the decode kernel's bounded wait on a barrier nothing arrives at (test hook).
+cudaError_t launch_fd_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st);
 
 cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,

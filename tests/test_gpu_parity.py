@@ -26,11 +26,11 @@ SMALL = [
     (300, 256, 16, 16, 128, 0, "none", 106),
     (3000, 256, 64, 8, 128, 1, "normal", 107),
     (16, 128, 1024, 16, 128, 1, "none", 108),
-    # one-launch decode arm (T <= 8, H % 512 == 0, H <= 4096, I <= 1024): E = 1024 with k = 16
-    # and no shared expert, a skewed batch where experts are shared by several tokens
-    (3, 512, 16, 4, 128, 1, "none", 112),
+    # one-launch decode arm (T <= 8, H % 512 == 0, H <= 4096, I % 256 == 0, I <= 1024): E = 1024
+    # with k = 16 and no shared expert, a skewed batch where experts are shared by several tokens
+    (3, 512, 16, 4, 256, 1, "none", 112),
     (8, 1024, 64, 8, 256, 1, "zipf", 113),
-    (5, 512, 1024, 16, 128, 0, "none", 114),
+    (5, 512, 1024, 16, 256, 0, "none", 114),
     # tcgen05 arm (T > 8, H and I multiples of 256): ragged token tiles, several tiles per
     # expert, no shared expert, the N tail of a single 16-column step, single-token experts
     (9, 256, 16, 2, 256, 1, "none", 116),
@@ -102,6 +102,7 @@ def test_forward_arm_selection(cuda_lib):
     moe = cuda_lib
     arm = lambda **kw: moe.forward_arm(moe.Shape(**{**dict(T=1, H=2048, I=512, E=512, k=10), **kw}))
     assert arm(T=1) == 0 and arm(T=8) == 0 and arm(T=4, H=4096, I=1024) == 0 and arm(T=4, H=1024, I=256) == 0
+    assert arm(T=4, I=128) == 1 and arm(T=4, I=640) == 1   # the one-launch kernel wants I % 256 == 0
     assert arm(T=4, H=8192) == 1 and arm(T=4, I=2048) == 1
     assert arm(T=4, H=256) == 1 and arm(T=9, I=128) == 1 and arm(T=64, I=128) == 1
     assert arm(T=9) == 2 and arm(T=64) == 2 and arm(T=65) == 2 and arm(T=4096) == 2
@@ -120,6 +121,51 @@ def test_forward_deterministic_and_matches_stages(cuda_lib):
         a = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
         b = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
         assert torch.equal(a, b)
+
+
+def test_one_launch_consecutive_calls(cuda_lib):
+    """Consecutive one-launch forwards on one workspace alternate the kernel's counter sets (the
+    parity of its launch count): five calls with different token/logit pairings, so the routing
+    differs from call to call, each against the oracle."""
+    moe = cuda_lib
+    L = _small_layer((8, 1024, 64, 8, 256, 1, "zipf", 113))
+    s = L.shape
+    ms = moe_shape(moe, s)
+    assert moe.forward_arm(ms) == 0
+    gu, dn = L.gpu_weights(moe)
+    ogu, odn = L.oracle_weights()
+    ws = moe.workspace(ms)
+    for r in range(5):
+        x = torch.roll(L.x, shifts=r, dims=0)
+        lg = torch.roll(L.logits, shifts=3 * r, dims=0)
+        out = torch.full((s.T, s.H), float("nan"), device="cuda", dtype=torch.bfloat16)
+        moe.forward(x.cuda(), lg.cuda(), gu, dn, ms, ws, out=out)
+        torch.cuda.synchronize()
+        assert moe.device_status(ws) == 0
+        ref = oracle.moe_forward(x, lg, ogu, odn, s.k, s.has_shared)
+        check_layer_close(to_np(out), ref, f"call {r}")
+
+
+def test_device_timeout_is_reported_without_fault(cuda_lib):
+    """The decode kernel's bounded wait, run on a barrier nothing arrives at with a 2 ms limit,
+    records MOE_ERR_DEVICE_TIMEOUT in the status word; the read clears it and the context stays
+    usable (a forward afterwards is correct)."""
+    moe = cuda_lib
+    L = _small_layer((3, 512, 16, 4, 256, 1, "none", 112))
+    s = L.shape
+    ms = moe_shape(moe, s)
+    ws = moe.workspace(ms)
+    assert moe.device_status(ws) == 0
+    moe.debug_timeout_probe(ws, 2_000_000)
+    assert moe.device_status(ws) == -6   # MOE_ERR_DEVICE_TIMEOUT
+    assert moe.device_status(ws) == 0
+    gu, dn = L.gpu_weights(moe)
+    ogu, odn = L.oracle_weights()
+    out = torch.full((s.T, s.H), float("nan"), device="cuda", dtype=torch.bfloat16)
+    moe.forward(L.x.cuda(), L.logits.cuda(), gu, dn, ms, ws, out=out)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+    check_layer_close(to_np(out), oracle.moe_forward(L.x, L.logits, ogu, odn, s.k, s.has_shared), "after the probe")
 
 
 def test_forward_profiled_matches_forward(cuda_lib):
