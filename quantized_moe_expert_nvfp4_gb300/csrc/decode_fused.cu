@@ -87,7 +87,7 @@ struct FdArgs {
   unsigned long long* grid_ctr;   // launch count: one arrival per CTA and launch, monotonic
   unsigned* ccnt;                 // [2][kFdMaxBlocks] block arrivals, then [2][kFdMaxActive] readiness
   int32_t* status;
-  int x_pitch, smem_off, ring_off, slot_bytes, n_slots;
+  int x_pitch, smem_off, sh_off, ring_off, ring_bytes;
 };
 
 struct FdSmem {
@@ -103,6 +103,9 @@ struct FdSmem {
   int32_t cnt[kMaxE];
   int wsum[kFdWarps];          // block scan of the expert counts: per-warp totals, then bases
   int wnz[kFdWarps];
+  int wmax[kFdWarps];          // and per-warp maxima of the routed counts
+  int ns;                      // this launch's ring: slots and slot size (from the routing)
+  int slot_b;
   float xfac[kFdMaxT];         // 2^e of each staged f16 activation row
   alignas(16) float red[kFdMaxSlots][32 * 4];   // gate_up: the second warp's partial sums, per slot
   float hfac[kFdMaxSlots][kFdMaxT];              // down: 2^e of each staged h row, per slot
@@ -247,14 +250,20 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   uint8_t* xs = base;   // f16 activation rows, x_pitch bytes apart
   FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.smem_off);
   uint8_t* ring = base + a.ring_off;
+  uint8_t* sh_h = base + a.sh_off;   // the shared expert's h rows [T][I] for its down unit in this CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = T * k;
-  const int NS = a.n_slots;
+  // The ring's layout is set after routing: a slot holds a down unit's h rows for at most the
+  // largest routed count (the shared expert's T rows have their own buffer), so routings that
+  // spread the tokens get more slots.  Slot 0 starts at the ring in every layout, so the unit
+  // issued before routing stays valid.
+  int NS = kFdMaxSlots;
+  uint32_t slot_bytes = 0;
   const int gu_per_group = I / kFdGuPairs;
   const int dn_per_group = H / kFdDnRows;
   // slot: the unit's packed weights (gate_up: 16 rows x H/2 bytes; down: 64 rows x I/2 bytes; in
   // swizzled 128-byte lines), then its scales (gate_up: [gate 8 | up 8][H/16]; down: [64][I/16]),
-  // then the down unit's h rows [nt][I]
+  // then a routed expert's down unit's h rows [nt][I]
   const uint32_t gu_wb = 2 * kFdGuPairs * (H / 2), gu_sb = kFdGuPairs * (H / 16);
   const uint32_t dn_wb = kFdDnRows * (I / 2), dn_sb = kFdDnRows * (I / 16);
   const uint32_t w_b = max(gu_wb, dn_wb), sc_b = max(2 * gu_sb, dn_sb), h_off = w_b + sc_b;
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   // known before routing when blockIdx.x < gu_per_group.
   auto issue = [&](int u, int nB, uint32_t it) {
     const int slot = it % NS;
-    uint8_t* dst = ring + slot * a.slot_bytes;
+    uint8_t* dst = ring + slot * slot_bytes;
     uint64_t* bar = &sm->full[slot];
     if (u < nB) {
       const int g = (u < gu_per_group && a.has_shared) ? E : sm->act[u / gu_per_group];
@@ -285,19 +294,21 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       bulk_g2s(dst + w_b, a.dn_scales + static_cast<int64_t>(r0) * (I / 16), dn_sb, bar);
     }
   };
-  // The h rows of down unit u (issued as ring position it) into the end of its slot; only once
-  // the expert's readiness counter shows every gate_up unit of it done (other CTAs write them).
+  // The h rows of down unit u (issued as ring position it) into the end of its slot (the shared
+  // expert's into its own buffer: a CTA holds at most one of its H/64 <= 64 down units); only
+  // once the expert's readiness counter shows every gate_up unit of it done (other CTAs write them).
   auto issue_h = [&](int u, int nB, uint32_t it) {
     const int gi = (u - nB) / dn_per_group;
     const int slot = it % NS;
-    bulk_g2s(ring + slot * a.slot_bytes + h_off, a.h + static_cast<int64_t>(sm->act_row[gi]) * I,
+    uint8_t* dst = (sm->act[gi] == E) ? sh_h : ring + slot * slot_bytes + h_off;
+    bulk_g2s(dst, a.h + static_cast<int64_t>(sm->act_row[gi]) * I,
              static_cast<uint32_t>(sm->act_cnt[gi]) * I * 2, &sm->full[slot]);
   };
 
   // ------------------------------------------------------------ phase A: route + permute
   bool early = false;
   if (warp == kFdProducer && lane == 0) {
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < kFdMaxSlots; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm->full[s])));
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_addr(&sm->empty[s])));   // the slot's 2 warps
     }
@@ -382,9 +393,11 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       vn += yn;
     }
   }
+  const int vmax = __reduce_max_sync(0xffffffffu, max(c0, c1));
   if (lane == 31) {
     sm->wsum[warp] = vs;
     sm->wnz[warp] = vn;
+    sm->wmax[warp] = vmax;
   }
   __syncthreads();
   if (warp == 0) {
@@ -410,6 +423,13 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       }
       sm->n_act = tn + sh;
       if (blockIdx.x == 0) a.offsets[E] = S;
+    }
+    if (lane == 0) {   // the ring: h room for the largest routed count
+      int mr = 0;
+      for (int w2 = 0; w2 < kFdWarps; ++w2) mr = max(mr, sm->wmax[w2]);
+      const uint32_t sb = ((w_b + sc_b + static_cast<uint32_t>(mr) * I * 2 + 1023u) / 1024u) * 1024u;
+      sm->slot_b = static_cast<int>(sb);
+      sm->ns = min(kFdMaxSlots, static_cast<int>(static_cast<uint32_t>(a.ring_bytes) / sb));
     }
   }
   __syncthreads();
@@ -451,6 +471,8 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   __syncthreads();
 
   const int n_act = sm->n_act;
+  NS = sm->ns;
+  slot_bytes = static_cast<uint32_t>(sm->slot_b);
   const int nB = n_act * gu_per_group;
   const int nC = n_act * dn_per_group;
 
@@ -564,7 +586,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     const float s2 = (half == 0) ? __ldg(a.gu_scale2 + g) : 0.0f;   // used by the epilogue
     float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // rows grp / grp + 8, columns 2 tig, 2 tig + 1
     if (ok) {
-      const uint8_t* sl = ring + slot * a.slot_bytes;
+      const uint8_t* sl = ring + slot * slot_bytes;
       const uint8_t* scg = sl + w_b + grp * (H / 16);      // scales of gate row grp
       const uint8_t* scu = scg + gu_sb;                    // and of its up row
       const int cb = (grp < nt) ? grp : 0;                 // B column grp (row 0 past nt: ignored)
@@ -642,8 +664,8 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     const int gi = (u - nB) / dn_per_group;
     const int g = sm->act[gi];
     const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
-    uint8_t* sl = ring + slot * a.slot_bytes;
-    uint16_t* hs = reinterpret_cast<uint16_t*>(sl + h_off);   // h rows [nt][I]
+    uint8_t* sl = ring + slot * slot_bytes;
+    uint16_t* hs = reinterpret_cast<uint16_t*>(g == E ? sh_h : sl + h_off);   // h rows [nt][I]
     if (ok) {
       // each h row, in place, as f16(h * 2^-e) with e from the row's maximum (half h takes the
       // rows te with te % 2 == h); 2^e goes to hfac for the epilogue
@@ -773,7 +795,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
 }
 
 struct FdPlan {
-  int x_pitch, x_bytes, smem_off, ring_off, slot_bytes, n_slots;
+  int x_pitch, x_bytes, smem_off, sh_off, ring_off, ring_bytes, n_slots_worst;
   size_t smem_total;
 };
 
@@ -782,15 +804,17 @@ bool fd_plan(const moe_shape_t& s, FdPlan* p) {
   p->x_pitch = 2 * s.H + 64;   // the 64 extra bytes put the 8 rows of an MMA's B loads in distinct banks
   p->x_bytes = ((s.T * p->x_pitch + 127) / 128) * 128;
   p->smem_off = p->x_bytes;
-  p->ring_off = ((p->smem_off + static_cast<int>(sizeof(FdSmem)) + 1023) / 1024) * 1024;
+  p->sh_off = ((p->smem_off + static_cast<int>(sizeof(FdSmem)) + 127) / 128) * 128;
+  const int sh_bytes = s.has_shared ? s.T * s.I * 2 : 0;   // the shared expert's h rows
+  p->ring_off = ((p->sh_off + sh_bytes + 1023) / 1024) * 1024;
+  p->ring_bytes = kFdSmemLimit - 1024 - p->ring_off;
   const int w_b = std::max(2 * kFdGuPairs * (s.H / 2), kFdDnRows * (s.I / 2));
   const int sc_b = std::max(2 * kFdGuPairs * (s.H / 16), kFdDnRows * (s.I / 16));
-  const int slot = w_b + sc_b + s.T * s.I * 2;   // weights, scales, a down unit's h rows
-  p->slot_bytes = ((slot + 1023) / 1024) * 1024;     // 1024-aligned for the swizzle
-  const int avail = kFdSmemLimit - 1024 - p->ring_off;
-  p->n_slots = std::min(kFdMaxSlots, avail / p->slot_bytes);   // 2 n_slots <= the compute warps
-  p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * p->slot_bytes;
-  return p->n_slots >= 3;
+  // the kernel sizes its slots after routing; at worst a routed expert holds all T rows
+  const int worst = ((w_b + sc_b + s.T * s.I * 2 + 1023) / 1024) * 1024;
+  p->n_slots_worst = std::min(kFdMaxSlots, p->ring_bytes / worst);
+  p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->ring_bytes);
+  return p->n_slots_worst >= 3;
 }
 
 template <int EPL>
@@ -809,6 +833,7 @@ cudaError_t launch_fd(const FdMaps& maps, const FdArgs& args, const FdPlan& plan
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFdThreads, plan.smem_total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  if (n_sm < args.H / kFdDnRows) return cudaErrorInvalidValue;   // one shared-expert down unit per CTA at most
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_sm);
   cfg.blockDim = dim3(kFdThreads);
@@ -869,8 +894,8 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   a.x_pitch = plan.x_pitch;
   a.smem_off = plan.smem_off;
   a.ring_off = plan.ring_off;
-  a.slot_bytes = plan.slot_bytes;
-  a.n_slots = plan.n_slots;
+  a.sh_off = plan.sh_off;
+  a.ring_bytes = plan.ring_bytes;
   FdMaps maps;
   const uint64_t gu_dims[4] = {128, static_cast<uint64_t>(d.gate_up.G) * 2 * s.I, 2, static_cast<uint64_t>(s.H) / 256};
   const uint64_t gu_strides[3] = {static_cast<uint64_t>(s.H) / 2, static_cast<uint64_t>(s.I) * (s.H / 2), 128};
