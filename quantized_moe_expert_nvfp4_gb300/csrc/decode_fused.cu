@@ -320,10 +320,10 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
-  if (threadIdx.x == 32) {   // this launch's counter set: the launch count's parity
-    const unsigned long long n = atomicAdd(a.grid_ctr, 1ull);
-    sm->ep = static_cast<int>((n / gridDim.x) & 1ull);
-  }
+  // this launch's counter set: the launch count's parity (the atomic's result is used after
+  // routing, so its round trip overlaps the logits loads)
+  unsigned long long launch_n = 0;
+  if (threadIdx.x == 32) launch_n = atomicAdd(a.grid_ctr, 1ull);
   // activations: warp 8 + t stages token t as f16(x * 2^-e), e = floor(log2 max|x|) - 14 (at
   // least -126), the row maximum in [2^14, 2^15); the factor 2^e is applied to the dot products
   if (warp >= kFdXWarp0 && warp < kFdXWarp0 + T) {
@@ -359,6 +359,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   int my_id = 0;
   float my_w = 0.0f;
   if (warp < T) warp_topk<EPL>(a.logits + static_cast<int64_t>(warp) * E, E, k, lane, my_id, my_w);
+  if (threadIdx.x == 32) sm->ep = static_cast<int>((launch_n / gridDim.x) & 1ull);
   __syncthreads();
   const int ep = sm->ep;
   unsigned* const ccnt = a.ccnt + ep * kFdMaxBlocks;                       // this launch's arrivals
