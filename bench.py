@@ -92,6 +92,22 @@ def peaks():
         return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
+def slowest_rank_ms(elapsed_ms, dist=None, device="cpu"):
+    """The job's time: the largest of the ranks' times (a MAX all-reduce over the process group),
+    or the value itself on one rank."""
+    if dist is None:
+        return float(elapsed_ms)
+    tt = torch.tensor([float(elapsed_ms)], device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def replica_throughput(world, steps, tokens_per_step, max_ms):
+    """Whole-job tokens/s of `world` independent replicas: every rank's tokens over the slowest
+    rank's time."""
+    return world * steps * tokens_per_step / (max_ms / 1e3)
+
+
 def stored_traffic(workload, kernel, src_files):
     """DRAM bytes per launch from the committed ncu summary, or None when absent or when the
     kernel's source changed since the capture."""
@@ -409,13 +425,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-    elapsed_ms = t0.elapsed_time(t1)
-    max_ms = elapsed_ms
-    if dist:
-        tt = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        max_ms = float(tt.item())
-    value = world * steps * tokens_per_step / (max_ms / 1e3)
+    max_ms = slowest_rank_ms(t0.elapsed_time(t1), dist, device)
+    value = replica_throughput(world, steps, tokens_per_step, max_ms)
 
     # dominant kernel: the whole-layer kernel on the one-launch decode arm, otherwise the stage
     # with the largest summed time
@@ -463,6 +474,8 @@ def run_ours(args):
     ho = [torch.empty(L["T"], H, dtype=torch.bfloat16).pin_memory() for L in layers]
     dx = [torch.empty_like(L["xs"][0]) for L in layers]
     dl = [torch.empty_like(L["lgs"][0]) for L in layers]
+    if dist:
+        dist.barrier()
     with torch.cuda.stream(stream):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -477,10 +490,10 @@ def run_ours(args):
                 ho[li].copy_(L["out"], non_blocking=True)
         e1.record(stream)
     e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = slowest_rank_ms(e0.elapsed_time(e1), dist, device)
     h2d = sum(L["T"] * H * 2 + L["T"] * E * 4 for L in layers)
     d2h = sum(L["T"] * H * 2 for L in layers)
-    e2e = {"value": world * e2e_steps * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT,
+    e2e = {"value": replica_throughput(world, e2e_steps, tokens_per_step, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     status = [moe.device_status(L["ws"]) for L in layers]
