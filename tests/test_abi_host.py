@@ -74,3 +74,19 @@ def test_host_validation_errors(lib):
     assert L.moe_quantize_nvfp4(mis, 1, 16, 32, fake, fake, fake, None) == -1
     for code in range(-6, 1):
         assert L.moe_status_string(code)
+
+
+def test_arm_selection_on_the_host(lib):
+    """moe_forward_arm is host logic (no CUDA call): the arm boundaries of the header."""
+    moe, L = lib
+    arm = lambda **kw: moe.forward_arm(moe.Shape(**{**dict(T=1, H=2048, I=512, E=512, k=10), **kw}))
+    # one-launch decode kernel: T <= 8, H % 512 == 0, H <= 4096, I % 256 == 0, I <= 1024
+    assert [arm(T=t) for t in (1, 2, 4, 8)] == [0, 0, 0, 0]
+    assert arm(T=4, H=4096, I=1024) == 0 and arm(T=4, H=1024, I=256) == 0 and arm(T=3, H=512, E=16, k=4, I=256) == 0
+    # three-launch decode arm for the other small-T shapes
+    assert arm(T=4, H=8192) == 1 and arm(T=4, I=2048) == 1 and arm(T=4, I=128) == 1 and arm(T=4, I=640) == 1
+    assert arm(T=4, H=256) == 1 and arm(T=9, I=128) == 1 and arm(T=64, I=128) == 1
+    # tcgen05 grouped GEMMs above 8 tokens (H, I multiples of 256); CUDA-core GEMMs otherwise
+    assert arm(T=9) == 2 and arm(T=64) == 2 and arm(T=65) == 2 and arm(T=4096) == 2
+    assert arm(T=65, I=128) == 3
+    assert arm(H=100) == -1
