@@ -1,13 +1,18 @@
 #!/usr/bin/env python
 """Benchmark of the NVFP4 routed-MoE layer (moe_forward) on GB300.
 
-Metric: MoE-layer tokens/s (token-layers per second for stacked workloads), with the
-dominant kernel's roofline fraction (HBM GB/s for the decode and batched-decode workloads, bf16
-tensor TFLOP/s for the prefill workloads) against the measured peaks, the CPU oracle timed
-beside it, and an end-to-end number through host buffers.
+Metric: MoE-layer tokens/s (token-layers per second for stacked workloads), with the dominant
+kernel's roofline fraction (HBM GB/s for the decode and batched-decode workloads, 16-bit tensor
+TFLOP/s for the prefill workloads) against the measured peaks, the CPU oracle timed beside it,
+and an end-to-end number through host buffers.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|batched|prefill|long|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|batched|prefill|long|tiny]
     python bench.py --impl reference ...      # the CPU oracle as the reference arm
+
+The default (--workload all) measures the four benchmark workloads in one run and prints ONE
+JSON line: the long cold prefill (4 layers x T = 32768, Zipf routing) is the headline (its
+value, roofline, e2e and CPU baseline are the line's own keys), and `workloads` holds the same
+fields for the decode/verify sweep, the batched decode and the prefill chunk.
 
 One step = one pass of the whole layer over one batch of every layer of the workload (decode:
 four layers with T = 1, 2, 4, 8; long: four layers of T = 32768).  Inputs are synthetic
@@ -38,7 +43,10 @@ import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s"
 UNIT = "tokens/s"
-GU_BYTES_PER_EXPERT = None  # filled from the shape
+HEADLINE = "long"                       # the workload of the line's own keys under --workload all
+SUBWORKLOADS = ("decode", "batched", "prefill")
+DTYPE = ("nvfp4 weights (e2m1 x e4m3 per 16 x fp32 scale2) x bf16 activations; "
+         "f16 x f16 tensor-core products (exact for both operands), fp32 accumulate")
 
 
 def parse_args():
@@ -47,10 +55,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=None)
     p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="decode", choices=list(synth.WORKLOADS))
+    p.add_argument("--workload", default="all", choices=["all"] + list(synth.WORKLOADS))
     p.add_argument("--pool", type=int, default=None, help="distinct input batches cycled through")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--warmup-seconds", type=float, default=2.0,
+    p.add_argument("--warmup-seconds", type=float, default=1.0,
                    help="keep warming up (whole steps) at least this long, for steady clocks")
     p.add_argument("--one-forward", type=int, default=None, metavar="LAYER",
                    help="profiling aid: build layer LAYER of the workload, run four forwards, exit "
@@ -73,6 +81,7 @@ def workload_entries(name):
 
 
 def describe(name):
+    """The workload, as both arms state it in `config`."""
     w = synth.WORKLOADS[name]
     return {"workload": w.description, "T": list(w.Ts), "H": w.H, "E": w.E, "k": w.k, "I": w.I,
             "shared_expert": True, "layers_per_step": len(workload_entries(name)),
@@ -135,6 +144,7 @@ class ClockSampler:
     def __init__(self, device):
         self.uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", "")).lower()
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -146,7 +156,6 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -176,9 +185,9 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- oracle legs
 
-def oracle_sample(name, gen_device, reps_budget_s=10.0, max_reps=8, n_steps=None):
-    """Time the CPU oracle on one token of every layer of the workload (its first input batch).
-    Quantizing the needed experts with the oracle's quantizer is setup, not timed."""
+def oracle_prepare(name, gen_device):
+    """The oracle's inputs for one token of every layer of the workload (its first input batch):
+    x, logits and the oracle-quantized weights of the groups that token uses (set-up, untimed)."""
     import concurrent.futures as cf
 
     import oracle
@@ -209,19 +218,23 @@ def oracle_sample(name, gen_device, reps_budget_s=10.0, max_reps=8, n_steps=None
         for x, lg, gu, dn in prepared:
             oracle.moe_forward(x, lg, gu, dn, w.k, tokens=[0])
         return len(prepared)
+    return run_once
 
-    if n_steps is not None:
-        return prepared, run_once
+
+def oracle_sample(name, gen_device, budget_s=8.0, max_reps=8):
+    """Time the CPU oracle on one token of every layer of the workload, repeated within a
+    bounded budget."""
+    run_once = oracle_prepare(name, gen_device)
     run_once()  # warm
     t0 = time.perf_counter()
     toks, reps = 0, 0
-    while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < reps_budget_s):
+    while reps < max_reps and (reps == 0 or time.perf_counter() - t0 < budget_s):
         toks += run_once()
         reps += 1
     dt = time.perf_counter() - t0
     return {"value": toks / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{toks} tokens: token 0 of each of the {len(prepared)} layer(s) of the workload, "
-                      f"{reps} repetition(s); fp64 C++ oracle with std::thread over experts"}
+            "sample": f"{toks} tokens: token 0 of each of the {toks // reps} layer(s) of the workload, "
+                      f"{reps} repetition(s); fp64 C++ oracle with std::thread over its work items"}
 
 
 def run_reference(args):
@@ -229,11 +242,11 @@ def run_reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return 0
-    name = args.workload
+    name = HEADLINE if args.workload == "all" else args.workload
     steps = args.steps if args.steps is not None else 20
     warmup = args.warmup if args.warmup is not None else 3
     gen = "cuda" if torch.cuda.is_available() else "cpu"
-    _, run_once = oracle_sample(name, gen, n_steps=steps)
+    run_once = oracle_prepare(name, gen)
     for _ in range(warmup):
         run_once()
     t0 = time.perf_counter()
@@ -247,7 +260,8 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": describe(name),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": "each step: token 0 of each layer of the workload through the fp64 oracle"},
+                             "sample": f"each step: token 0 of each of the {len(workload_entries(name))} "
+                                       "layer(s) of the workload through the fp64 oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -282,56 +296,29 @@ def build_layer(moe, w, T, seed, pool, device):
     return dict(T=T, ms=ms, gu=weights[0], dn=weights[1], xs=xs, lgs=lgs, ws=ws, out=out, uniq=uniq)
 
 
-def run_ours(args):
-    import quantized_moe_expert_nvfp4_gb300 as moe
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    name = args.workload
+def launches_per_forward(arm, T):
+    """Kernels one moe_forward launches: arm 0 one; arm 1 route+permute, gate_up, down+combine;
+    arm 2 route, the permutation (one kernel up to 64 tokens, else three plus the work list),
+    the activation gather, gate_up, the h conversion, down, combine; arm 3 the same without the
+    two f16 conversions."""
+    return {0: 1, 1: 3, 2: 7 if T <= 64 else 10, 3: 5 if T <= 64 else 8}[arm]
+
+
+def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds, cpu_baseline):
+    """Time `steps` steps of workload `name` and return its part of the JSON line."""
     w = synth.WORKLOADS[name]
-    d_steps, d_warm, d_pool = DEFAULTS[name]
-    steps = args.steps if args.steps is not None else d_steps
-    warmup = max(3, args.warmup if args.warmup is not None else d_warm)
-    pool = args.pool or d_pool
-    moe.load()
-    if args.one_forward is not None:   # for ncu: -s 3 -c 1 on the arm's kernel selects the fourth forward
-        T, seed = workload_entries(name)[args.one_forward]
-        L = build_layer(moe, w, T, seed, 1, device)
-        for _ in range(4):
-            moe.forward(L["xs"][0], L["lgs"][0], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
-        torch.cuda.synchronize()
-        if moe.device_status(L["ws"]) != 0:
-            raise RuntimeError(f"device status {moe.device_status(L['ws'])}")
-        print(f"one forward: {name} layer {args.one_forward} (T={T}), arm {moe.forward_arm(L['ms'])}")
-        return 0
     layers = [build_layer(moe, w, T, seed, pool, device) for T, seed in workload_entries(name)]
     tokens_per_step = sum(L["T"] for L in layers)
     arms = [moe.forward_arm(L["ms"]) for L in layers]
-    decode_arm = all(a in (0, 1) for a in arms)
-    # kernels per forward: arm 0 one; arm 1 route+permute, gate_up, down+combine; arm 2 route,
-    # permute (3), work list (one kernel for the permutation and work list up to 64 tokens),
-    # activation gather, gate_up, h conversion, down, combine; arm 3 the same without the two
-    # f16 conversions
-    def n_launch(arm, T):
-        return {0: 1, 1: 3, 2: 7 if T <= 64 else 10, 3: 5 if T <= 64 else 8}[arm]
-    launches = sum(n_launch(a, L["T"]) for a, L in zip(arms, layers))
+    launches = sum(launches_per_forward(a, L["T"]) for a, L in zip(arms, layers))
     stream = torch.cuda.Stream(device)
 
-    # graphs[b][p]: one step on input batch p, recording event set b
-    def new_events():
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in layers]
-    events = [[new_events() for _ in range(pool)] for _ in range(2)]
+    # events[p][layer]: the 5 stage events of one profiled step on input batch p
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in layers] for _ in range(pool)]
     with torch.cuda.stream(stream):   # torch creates an event's handle on its first record
-        for ev in (e for b in events for p in b for L_ in p for e in L_):
+        for ev in (e for p in events for L_ in p for e in L_):
             ev.record(stream)
     stream.synchronize()
-    graphs = [[None] * pool for _ in range(2)]
     with torch.cuda.stream(stream):
         for p in range(pool):  # one eager pass per batch before capture
             for L in layers:
@@ -339,72 +326,56 @@ def run_ours(args):
     stream.synchronize()
     bad = [moe.device_status(L["ws"]) for L in layers]
     if any(bad):
-        raise RuntimeError(f"device status after the first pass: {bad}")
-    for b in range(2):
-        for p in range(pool):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for li, L in enumerate(layers):
-                    moe.forward_profiled(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"],
-                                         L["out"], events[b][p][li])
-            graphs[b][p] = g
-    # the timed steps themselves run graphs of plain moe_forward: event nodes between the
-    # stages cost about 2 us each, so the per-stage times come from a second pass of the same
-    # steps with the profiled graphs
-    pgraphs = [None] * pool
+        raise RuntimeError(f"{name}: device status after the first pass: {bad}")
+    # plain graphs (the timed steps) and profiled graphs (event nodes at the stage boundaries,
+    # about 2 us each, so they stay out of the timed value; they give the per-stage times)
+    graphs, pgraphs = [], []
     for p in range(pool):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for L in layers:
                 moe.forward(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
-        pgraphs[p] = g
+        graphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for li, L in enumerate(layers):
+                moe.forward_profiled(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"], L["out"],
+                                     events[p][li])
+        pgraphs.append(g)
 
-    stage_ms = [[0.0] * 4 for _ in layers]
-    gate_up_bytes = 0.0
-    down_bytes = 0.0
-    gate_up_flops = 0.0
-    fwd_bytes = 0.0
-    H, I, E = w.H, w.I, w.E
+    H, I, E, k = w.H, w.I, w.E, w.k
     gu_expert = 2 * I * H // 2 + 2 * I * H // 16 + 4
     dn_expert = H * I // 2 + H * I // 16 + 4
+    acc = dict(stage=[[0.0] * 4 for _ in layers], gu_bytes=0.0, dn_bytes=0.0, gu_flops=0.0, fwd_bytes=0.0,
+               fwd_flops=0.0)
 
-    def collect(b, batch_steps):
-        nonlocal gate_up_bytes, down_bytes, gate_up_flops, fwd_bytes
-        for p in batch_steps:
-            evs = events[b][p]
-            evs[-1][4].synchronize()
-            for li, L in enumerate(layers):
-                e = evs[li]
-                for s in range(4):
-                    stage_ms[li][s] += e[s].elapsed_time(e[s + 1])
-                T, U = L["T"], L["uniq"][p] + 1
-                S = T * w.k
-                gate_up_bytes += U * gu_expert + T * H * 2 + (S + T) * I * 2
-                down_bytes += U * dn_expert + (S + T) * I * 2 + T * H * 2 + S * 8
-                gate_up_flops += 2.0 * (2 * I) * H * (S + T)
-                fwd_bytes += U * (gu_expert + dn_expert) + T * H * 2 + T * E * 4 + T * H * 2
+    def collect(p):
+        evs = events[p]
+        evs[-1][4].synchronize()
+        for li, L in enumerate(layers):
+            e = evs[li]
+            for s in range(4):
+                acc["stage"][li][s] += e[s].elapsed_time(e[s + 1])
 
-    def run_steps(n, timed):
-        pending = None
-        for i in range(n):
-            b, p = (i // pool) % 2, i % pool
-            graphs[b][p].replay()
-            if timed and (p == pool - 1 or i == n - 1):
-                batch = (b, list(range(0, p + 1)))
-                if pending is not None:
-                    collect(*pending)
-                pending = batch
-        return pending
+    def work(p):
+        for L in layers:
+            T, U = L["T"], L["uniq"][p] + 1
+            S = T * k
+            acc["gu_bytes"] += U * gu_expert + T * H * 2 + (S + T) * I * 2
+            acc["dn_bytes"] += U * dn_expert + (S + T) * I * 2 + T * H * 2 + S * 8
+            acc["gu_flops"] += 2.0 * (2 * I) * H * (S + T)
+            acc["fwd_flops"] += 2.0 * 3 * I * H * (S + T)
+            acc["fwd_bytes"] += U * (gu_expert + dn_expert) + T * H * 2 + T * E * 4 + T * H * 2
 
     with ClockSampler(device) as clk:
         with torch.cuda.stream(stream):
             t_w = time.perf_counter()
             i = 0
-            while i < warmup or time.perf_counter() - t_w < args.warmup_seconds:
-                run_steps(pool, timed=False)
+            while i < warmup or time.perf_counter() - t_w < warmup_seconds:
                 for p in range(pool):
+                    graphs[p].replay()
                     pgraphs[p].replay()
-                i += 2 * pool
+                i += pool
             stream.synchronize()
             if dist:
                 dist.barrier()
@@ -413,58 +384,72 @@ def run_ours(args):
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
             for i in range(steps):
-                pgraphs[i % pool].replay()
+                graphs[i % pool].replay()
             t1.record(stream)
             t1.synchronize()
             if dist:
                 dist.barrier()
-            pending = run_steps(steps, timed=True)   # stage times: the same steps, profiled
+            # stage times: the same steps again, profiled
+            for i in range(steps):
+                p = i % pool
+                pgraphs[p].replay()
+                work(p)
+                collect(p)
         stream.synchronize()
-        if pending is not None:
-            collect(*pending)
-        torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
     max_ms = slowest_rank_ms(t0.elapsed_time(t1), dist, device)
+    ms_per_step = max_ms / steps
     value = replica_throughput(world, steps, tokens_per_step, max_ms)
-
-    # dominant kernel: the whole-layer kernel on the one-launch decode arm, otherwise the stage
-    # with the largest summed time
-    tot_stage = [sum(stage_ms[li][s] for li in range(len(layers))) for s in range(4)]
-    stage_names = ["route+permute", "gate_up", "down" if not decode_arm else "down+combine", "combine"]
     n_launch = steps * len(layers)
+    tot_stage = [sum(acc["stage"][li][s] for li in range(len(layers))) for s in range(4)]
     pk = peaks()
     src = "quantized_moe_expert_nvfp4_gb300/csrc/"
-    # decode and batched decode stream weights (HBM roofline); prefill is a contraction (tensor)
+    # HBM-bound workloads stream the selected experts' weights; the prefill workloads are
+    # contractions (tensor-bound).  The dominant kernel: the whole-layer kernel of the one-launch
+    # decode arm (timed by the plain graphs: per launch = the step's time / layers), else the
+    # stage with the largest time (event-timed in the profiled pass).
     hbm_bound = name in ("decode", "batched", "tiny")
+    long_step = ms_per_step * steps > 50.0
     if all(a == 0 for a in arms):
-        stage_names[0] = "whole layer (one launch)"
-        t_ms, alg = tot_stage[0], fwd_bytes
-        kname, kfile = "decode_fused_kernel (route+gate_up+down+combine)", ["decode_fused.cu", "topk.cuh", "internal.cuh"]
+        t_launch_ms = ms_per_step / len(layers)
+        alg = acc["fwd_bytes"] / n_launch
+        kname, kfile = "decode_fused_kernel", ["decode_fused.cu", "topk.cuh", "internal.cuh"]
+        roofline = {"bound": "hbm", "achieved": alg / (t_launch_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+                    "kernel": kname + " (the whole layer: route, gate_up, down, combine)",
+                    "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * t_launch_ms,
+                    "timing": "plain CUDA graphs, the step's time divided by its launches"}
     elif hbm_bound:
         dom = 1 if tot_stage[1] >= tot_stage[2] else 2
-        t_ms, alg = tot_stage[dom], (gate_up_bytes if dom == 1 else down_bytes)
-        if all(a == 2 for a in arms):
-            kname, kfile = f"grouped_gemm_tc_kernel<{'gate_up' if dom == 1 else 'down'}>", ["gemm_tc.cu", "internal.cuh"]
-        else:
-            kname = "grouped_simt_kernel<gate_up>" if dom == 1 else "down_combine_gemv_kernel"
-            kfile = ["grouped_simt.cu"]
-    if hbm_bound:
-        achieved = alg / (t_ms / 1e3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
-                    "frac": achieved / pk["hbm"], "peak_source": pk["source"], "kernel": kname,
-                    "algorithmic_bytes_per_launch": alg / n_launch, "avg_launch_us": 1e3 * t_ms / n_launch,
-                    "traffic": stored_traffic(name, kname.split(" ")[0], [src + f for f in kfile])}
+        t_launch_ms = tot_stage[dom] / n_launch
+        alg = (acc["gu_bytes"] if dom == 1 else acc["dn_bytes"]) / n_launch
+        kname = f"grouped_gemm_tc_kernel<{'gate_up' if dom == 1 else 'down'}>" if all(a == 2 for a in arms) \
+            else ("grouped_simt_kernel<gate_up>" if dom == 1 else "down_combine_gemv_kernel")
+        kfile = ["gemm_tc.cu", "internal.cuh"] if all(a == 2 for a in arms) else ["grouped_simt.cu"]
+        roofline = {"bound": "hbm", "achieved": alg / (t_launch_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+                    "kernel": kname, "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * t_launch_ms,
+                    "timing": "CUDA events around the kernel on its stream (profiled replay of the timed steps)"}
     else:
-        gu_ms = tot_stage[1]
-        achieved = gate_up_flops / (gu_ms / 1e3) / 1e12
-        peak = pk["bf16_sustained"] if name == "long" else pk["bf16"]
+        t_launch_ms = tot_stage[1] / n_launch
+        alg = acc["gu_flops"] / n_launch
         kname = "grouped_gemm_tc_kernel<gate_up>" if all(a == 2 for a in arms) else "grouped_simt_kernel<gate_up>"
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "peak_source": pk["source"], "kernel": kname,
-                    "algorithmic_flops_per_launch": gate_up_flops / n_launch,
-                    "avg_launch_us": 1e3 * gu_ms / n_launch,
-                    "traffic": stored_traffic(name, kname, [src + "gemm_tc.cu", src + "internal.cuh"])}
+        kfile = ["gemm_tc.cu", "internal.cuh"]
+        peak = pk["bf16_sustained"] if long_step else pk["bf16"]
+        roofline = {"bound": "tensor", "achieved": alg / (t_launch_ms / 1e3) / 1e12, "peak": peak,
+                    "unit": "TFLOP/s", "kernel": kname, "algorithmic_flops_per_launch": alg,
+                    "avg_launch_us": 1e3 * t_launch_ms,
+                    "timing": "CUDA events around the kernel on its stream (profiled replay of the timed steps)"}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline["peak_source"] = pk["source"] + (" (sustained)" if roofline["bound"] == "tensor" and long_step else
+                                              " (burst)" if roofline["bound"] == "tensor" else "")
+    roofline["traffic"] = stored_traffic(name, kname, [src + f for f in kfile])
+    # the whole layer against the same roofline, from the plain timing
+    if roofline["bound"] == "hbm":
+        layer_ach = acc["fwd_bytes"] / steps / (ms_per_step / 1e3) / 1e9
+        layer = {"achieved": layer_ach, "unit": "GB/s", "frac": layer_ach / pk["hbm"],
+                 "algorithmic_bytes_per_step": acc["fwd_bytes"] / steps}
+    else:
+        layer_ach = acc["fwd_flops"] / steps / (ms_per_step / 1e3) / 1e12
+        layer = {"achieved": layer_ach, "unit": "TFLOP/s", "frac": layer_ach / roofline["peak"],
+                 "algorithmic_flops_per_step": acc["fwd_flops"] / steps}
 
     # end to end through host buffers: H2D of x and logits from pinned memory, the C-ABI call,
     # D2H of the output, every step.
@@ -498,27 +483,79 @@ def run_ours(args):
 
     status = [moe.device_status(L["ws"]) for L in layers]
     if any(status):
-        raise RuntimeError(f"device status {status}")
+        raise RuntimeError(f"{name}: device status {status}")
+    stage_names = (["whole layer (one launch)", "-", "-", "-"] if all(a == 0 for a in arms)
+                   else ["route+permute", "gate_up", "down", "combine"])
+    res = {"value": value, "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
+           "config": describe(name), "roofline": roofline, "layer_roofline": layer, "e2e": e2e,
+           "gpu_launches": steps * launches, "clocks": clk.summary(),
+           "arm": sorted({moe.ARM_NAMES[a] for a in arms}),
+           "method": {"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh input "
+                            f"batch each step ({pool} batches cycled), experts differ per step",
+                      "cuda_graphs": True, "timed": "CUDA events on the launching stream around the plain graphs"},
+           "stages_us_per_forward": {f"layer {li} (T={L['T']})": {stage_names[s]: round(1e3 * acc["stage"][li][s] / steps, 2)
+                                                                   for s in range(4) if stage_names[s] != "-"}
+                                     for li, L in enumerate(layers)},
+           "distinct_experts_mean": [float(np.mean(L["uniq"])) for L in layers]}
+    if cpu_baseline:
+        res["cpu_baseline"] = oracle_sample(name, device)
+    del layers, graphs, pgraphs, hx, hl, ho, dx, dl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
 
+
+def run_ours(args):
+    import quantized_moe_expert_nvfp4_gb300 as moe
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    moe.load()
+    head = HEADLINE if args.workload == "all" else args.workload
+    if args.one_forward is not None:   # for ncu: -s 3 -c 1 on the arm's kernel selects the fourth forward
+        w = synth.WORKLOADS[head]
+        T, seed = workload_entries(head)[args.one_forward]
+        L = build_layer(moe, w, T, seed, 1, device)
+        for _ in range(4):
+            moe.forward(L["xs"][0], L["lgs"][0], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+        torch.cuda.synchronize()
+        if moe.device_status(L["ws"]) != 0:
+            raise RuntimeError(f"device status {moe.device_status(L['ws'])}")
+        print(f"one forward: {head} layer {args.one_forward} (T={T}), arm {moe.forward_arm(L['ms'])}")
+        return 0
+    cpu = world == 1 and not args.no_cpu_baseline and rank == 0
+
+    def run(name, steps_arg):
+        d_steps, d_warm, d_pool = DEFAULTS[name]
+        steps = steps_arg if steps_arg is not None else d_steps
+        warmup = max(3, args.warmup if args.warmup is not None else d_warm)
+        return measure(moe, name, steps, warmup, args.pool or d_pool, device, dist, world,
+                       args.warmup_seconds, cpu)
+
+    subs = {}
+    if args.workload == "all":
+        for name in SUBWORKLOADS:   # each with its own default step count (reported in its entry)
+            subs[name] = run(name, None)
+    main = run(head, args.steps)
     if rank == 0:
-        cfg = describe(name)
-        cfg.update({"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh "
-                          f"input batch each step ({pool} batches cycled), experts differ per step",
-                    "cuda_graphs": True, "parallelism": f"replicas x{world}",
-                    "arm": sorted({moe.ARM_NAMES[a] for a in arms})})
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
-                "warmup": warmup, "ms_per_step": max_ms / steps, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "nvfp4 x bf16 -> f32 accumulate", "data": "synthetic",
-                "config": cfg, "roofline": roofline, "e2e": e2e,
-                "gpu_launches": steps * launches,
-                "clocks": clk.summary(),
-                "stages_ms_per_step": {stage_names[s]: tot_stage[s] / steps for s in range(4)},
-                "stages_us_per_forward": {f"T={L['T']}": [round(1e3 * stage_ms[li][s] / steps, 2) for s in range(4)]
-                                          for li, L in enumerate(layers)},
-                "forward_hbm_gbs": fwd_bytes / (sum(tot_stage) / 1e3) / 1e9,
-                "distinct_experts_mean": [float(np.mean(L["uniq"])) for L in layers]}
-        if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = oracle_sample(name, device)
+        line = {"metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world, "steps": main["steps"],
+                "warmup": main["warmup"], "ms_per_step": main["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
+                "config": main["config"], "roofline": main["roofline"], "e2e": main["e2e"],
+                "gpu_launches": main["gpu_launches"], "clocks": main["clocks"],
+                "parallelism": f"replicas x{world}"}
+        for key in ("cpu_baseline", "layer_roofline", "arm", "method", "stages_us_per_forward",
+                    "distinct_experts_mean"):
+            if key in main:
+                line[key] = main[key]
+        if subs:
+            line["workloads"] = subs
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -5,9 +5,10 @@ this package.  The CUDA library never imports, links or calls it, and this packa
 nothing from the library: the two meet only in the seeded inputs drawn by `synth`.
 
 The oracle is plain C++ (`moe_oracle.cpp`) compiled with g++ into `_build/liboracle.so` and
-called through ctypes.  Every function computes the plain definition of its step in fp64 (the
-quantizer takes its rounding decisions in fp32, the precision of the GPU quantizer).  What each
-function follows is cited in `moe_oracle.h` / `moe_oracle.cpp`.
+called through ctypes.  Every function computes the plain definition of its step in fp64; the
+quantizer's steps are fp32 operations, because its input weights are fp32 and the recipe states
+each step on those fp32 values.  What each function follows is cited in `moe_oracle.h` /
+`moe_oracle.cpp`.
 """
 from __future__ import annotations
 

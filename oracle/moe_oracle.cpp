@@ -56,9 +56,13 @@ int round_to_table(double v, const double* table, int n) {
 struct Tables {
   double e2m1_pos[8];
   double e4m3_pos[127];  // codes 0x00..0x7E
+  double e2m1_all[16];   // every code's value, for the dequantizer
+  double e4m3_all[256];
   Tables() {
     for (int c = 0; c < 8; ++c) e2m1_pos[c] = e2m1_value(c);
     for (int c = 0; c < 127; ++c) e4m3_pos[c] = e4m3_value(c);
+    for (int c = 0; c < 16; ++c) e2m1_all[c] = e2m1_value(c);
+    for (int c = 0; c < 256; ++c) e4m3_all[c] = e4m3_value(c);
   }
 };
 const Tables& tables() {
@@ -112,15 +116,17 @@ void parallel_for(int64_t n, unsigned nt, F&& f) {
 }
 
 // Exact dequantization of one [N, K] matrix of one group into fp64:
-// w[n, k] = e2m1(q[n, k]) * e4m3(s[n, k/16]) * scale2.
+// w[n, k] = e2m1(q[n, k]) * e4m3(s[n, k/16]) * scale2.  The code values are read from tables
+// filled by e2m1_value / e4m3_value above (the same values, looked up instead of recomputed).
 void dequant_matrix(const uint8_t* packed, const uint8_t* scales, float scale2, int64_t N,
                     int64_t K, double* out) {
+  const Tables& tb = tables();
   for (int64_t n = 0; n < N; ++n) {
     for (int64_t kk = 0; kk < K; ++kk) {
       const uint8_t byte = packed[n * (K / 2) + kk / 2];
       const unsigned code = (kk % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
-      const double s = e4m3_value(scales[n * (K / 16) + kk / 16]);
-      out[n * K + kk] = e2m1_value(code) * s * static_cast<double>(scale2);
+      const double s = tb.e4m3_all[scales[n * (K / 16) + kk / 16]];
+      out[n * K + kk] = tb.e2m1_all[code] * s * static_cast<double>(scale2);
     }
   }
 }
@@ -279,15 +285,25 @@ int orc_moe_forward(const uint16_t* x, const float* logits, const uint8_t* gu_pa
   std::vector<double> hbuf(h ? static_cast<size_t>(n) * J * I : 0, 0.0);
   const int64_t gu_N = 2LL * I, gu_K = H, dn_N = H, dn_K = I;
 
-  parallel_for(G, thread_count(n_threads), [&](int64_t g) {
-    if (work[g].empty()) return;
+  // Tasks: consecutive runs of at most kChunk work items of one group, so that a group with
+  // many tokens (the shared expert, a popular expert) is spread over the threads.  Every item
+  // is still computed on its own, exactly as below; only the split of the loop changes.
+  constexpr size_t kChunk = 64;
+  std::vector<std::pair<int, size_t>> tasks;   // (group, first item)
+  for (int g = 0; g < G; ++g)
+    for (size_t b = 0; b < work[g].size(); b += kChunk) tasks.push_back({g, b});
+
+  parallel_for(static_cast<int64_t>(tasks.size()), thread_count(n_threads), [&](int64_t ti) {
+    const int64_t g = tasks[ti].first;
+    const size_t b0 = tasks[ti].second, b1 = std::min(work[g].size(), b0 + kChunk);
     std::vector<double> wgu(static_cast<size_t>(gu_N * gu_K)), wdn(static_cast<size_t>(dn_N * dn_K));
     dequant_matrix(gu_packed + g * gu_N * (gu_K / 2), gu_scales + g * gu_N * (gu_K / 16),
                    gu_scale2[g], gu_N, gu_K, wgu.data());
     dequant_matrix(dn_packed + g * dn_N * (dn_K / 2), dn_scales + g * dn_N * (dn_K / 16),
                    dn_scale2[g], dn_N, dn_K, wdn.data());
     std::vector<double> xv(H), a(I);
-    for (const auto& item : work[g]) {
+    for (size_t wi = b0; wi < b1; ++wi) {
+      const auto& item = work[g][wi];
       const int64_t i = item.first;
       const int j = item.second;
       const uint16_t* xr = x + static_cast<int64_t>(tok[i]) * H;

@@ -14,8 +14,10 @@
  * "handover briefs" page (device-side indexer selection: lower index wins, NaN never wins).
  *
  * Every function computes the plain definition: no blocking, no fusion, fp64 arithmetic for
- * the layer.  The quantizer takes its rounding decisions in fp32, the precision in which the
- * GPU quantizer takes them, so that both produce the same codes.
+ * the layer.  The quantizer is the exception: its inputs are fp32 weights and the recipe it
+ * follows (scale2 = amax / (448*6), block scale = block amax / 6 / scale2, code = w / (block
+ * scale * scale2)) is stated on those fp32 values, so each of its steps is one fp32 operation
+ * on fp32 data, taken in the order the recipe writes them.
  *
  * Status: 0 = ok, -1 = invalid argument.
  */

@@ -55,6 +55,20 @@ moe_status_t check_arch() {
   return ok ? MOE_OK : MOE_ERR_ARCH;
 }
 
+// The current device must be compute capability 10.3 and `stream` must belong to it (a stream
+// created on another device would run the launches there, against pointers of this one).  The
+// legacy and per-thread default stream handles always name the current device.
+moe_status_t check_device(void* stream) {
+  moe_status_t st = check_arch();
+  if (st != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cs == nullptr || cs == cudaStreamLegacy || cs == cudaStreamPerThread) return MOE_OK;
+  int dev = 0, sdev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamGetDevice(cs, &sdev) != cudaSuccess) return MOE_ERR_INVALID_ARG;
+  return sdev == dev ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 struct Ws {
@@ -234,7 +248,7 @@ moe_status_t moe_route_topk(const float* logits, const moe_shape_t* shape, int32
   if (st != MOE_OK) return st;
   if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
   if (shape->T == 0) return MOE_OK;
-  if ((st = check_arch()) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
   return cuda_status(launch_route_topk(logits, shape->T, shape->E, shape->k, topk_ids, topk_w,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -248,7 +262,7 @@ moe_status_t moe_permute(const int32_t* topk_ids, const moe_shape_t* shape, int3
       !aligned16(sorted_slot) || !aligned16(slot_pos))
     return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
-  if ((st = check_arch()) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const moe_shape_t& s = *shape;
   if (s.T == 0) {  // offsets of an empty batch are all zero
@@ -276,7 +290,7 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
   if ((st = check_weights(gate_up, *shape, true)) != MOE_OK) return st;
   if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
   if (shape->T == 0) return MOE_OK;
-  if ((st = check_arch()) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const moe_shape_t& s = *shape;
   Ws w = carve(ws, s);
@@ -295,7 +309,7 @@ moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
   if ((st = check_weights(down, *shape, false)) != MOE_OK) return st;
   if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
   if (shape->T == 0) return MOE_OK;
-  if ((st = check_arch()) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const moe_shape_t& s = *shape;
   Ws w = carve(ws, s);
@@ -313,7 +327,7 @@ moe_status_t moe_combine(const float* y, const int32_t* slot_pos, const float* t
     return MOE_ERR_INVALID_ARG;
   if (out_is_fp32 != 0 && out_is_fp32 != 1) return MOE_ERR_INVALID_ARG;
   if (shape->T == 0) return MOE_OK;
-  if ((st = check_arch()) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
   return cuda_status(launch_combine(y, slot_pos, topk_w, shape->T, shape->H, shape->k,
                                     shape->has_shared, out, out_is_fp32, nullptr,
                                     static_cast<cudaStream_t>(stream)));
@@ -340,7 +354,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
   if ((st = check_weights(down, *shape, false)) != MOE_OK) return st;
   if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
   if (shape->T == 0) return MOE_OK;
-  if ((st = check_arch()) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const moe_shape_t& s = *shape;
   Ws w = carve(ws, s);
@@ -445,7 +459,7 @@ moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K,
     return MOE_ERR_INVALID_ARG;
   if (G < 1 || G > 65535 || N < 1 || K < 16 || K % 16 || N * K > (int64_t{1} << 40))
     return MOE_ERR_UNSUPPORTED_SHAPE;
-  moe_status_t st = check_arch();
+  moe_status_t st = check_device(stream);
   if (st != MOE_OK) return st;
   return cuda_status(launch_quantize(w, G, N, K, packed, scales, scale2,
                                      static_cast<cudaStream_t>(stream)));
@@ -466,7 +480,7 @@ moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream) {
 moe_status_t moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID_ARG;
   if (limit_ns < 1 || limit_ns > 1000000000ull) return MOE_ERR_INVALID_ARG;
-  moe_status_t st = check_arch();
+  moe_status_t st = check_device(stream);
   if (st != MOE_OK) return st;
   return cuda_status(launch_fd_timeout_probe(static_cast<int32_t*>(ws), limit_ns, static_cast<cudaStream_t>(stream)));
 }

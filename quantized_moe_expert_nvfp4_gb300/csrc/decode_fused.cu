@@ -820,18 +820,12 @@ bool fd_plan(const moe_shape_t& s, FdPlan* p) {
 
 template <int EPL>
 cudaError_t launch_fd(const FdMaps& maps, const FdArgs& args, const FdPlan& plan, cudaStream_t st) {
-  static int configured_smem = 0;
   const auto kern = decode_fused_kernel<EPL>;
-  if (configured_smem < static_cast<int>(plan.smem_total)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(plan.smem_total));
-    if (e != cudaSuccess) return e;
-    configured_smem = static_cast<int>(plan.smem_total);
-  }
-  int dev = 0, n_sm = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFdThreads, plan.smem_total);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), static_cast<int>(plan.smem_total));
+  if (e != cudaSuccess) return e;
+  int n_sm = 0, per_sm = 0;
+  if ((e = current_sm_count(&n_sm)) != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFdThreads, plan.smem_total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   if (n_sm < args.H / kFdDnRows) return cudaErrorInvalidValue;   // one shared-expert down unit per CTA at most

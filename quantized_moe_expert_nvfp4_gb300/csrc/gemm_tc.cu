@@ -580,26 +580,13 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
 constexpr size_t kSmemBytes = 1024 + kGStages * kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
-  return n;
-}
-
 template <bool kGateUp>
 cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<kGateUp>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp>),
+                                      static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  int n_sm = 0;
+  if ((e = current_sm_count(&n_sm)) != cudaSuccess) return e;
   const int G = g.E + 1;
   const uint64_t rows = static_cast<uint64_t>(G) * g.N;
   const uint64_t act_rows = static_cast<uint64_t>(g.S) + g.T;
@@ -636,7 +623,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.act_factor = g.act_factor;
   a.status = g.status;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
-  const int grid = static_cast<int>(std::min<int64_t>(items_max, sm_count()));
+  const int grid = static_cast<int>(std::min<int64_t>(items_max, n_sm));
   grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(maps, a);
   return cudaGetLastError();
 }

@@ -258,9 +258,8 @@ cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st) {
 cudaError_t launch_down_combine_gemv(const DownCombineArgs& a, cudaStream_t st) {
   const size_t smem = static_cast<size_t>(a.S + a.T) * kDcRows * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(down_combine_gemv_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(down_combine_gemv_kernel),
+                                        static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
   down_combine_gemv_kernel<<<a.H / kDcRows, 256, smem, st>>>(a);

@@ -105,6 +105,13 @@ __device__ __forceinline__ void report_device_error(int32_t* status, int32_t cod
   atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------------------------------ per-device host state
+// SM count of the current device (cached per device).
+cudaError_t current_sm_count(int* n);
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at least `bytes`, once
+// per (device, kernel) and size; thread-safe.
+cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
+
 // ------------------------------------------------------------------ launchers
 // Each returns cudaGetLastError() of its launches.
 cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,

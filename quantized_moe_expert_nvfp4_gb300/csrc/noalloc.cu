@@ -14,12 +14,16 @@
 //    for as long as the library stays loaded.  Shapes whose scratch would not fit are rejected.
 //  - All calls on a device share the one array.  Calls whose work overlaps on the GPU (two
 //    streams, or two host threads) race on it and produce garbage; serialize them.
-//  - The first call on a device looks up the array's device address (cudaGetSymbolAddress).  Make
-//    that first call outside any CUDA stream capture.
+//  - The first call on a device looks up the array's device address (cudaGetSymbolAddress), and
+//    looks it up again when the device's context has changed (after a device reset).  Make that
+//    first call outside any CUDA stream capture.
 //  - Each call clears the status word, the launch counter and the decode kernel's other
 //    synchronisation words at the start (an asynchronous memset on the caller's stream, not an allocation), so a
 //    device-side timeout of one call does not poison the next; such a timeout is not reported
 //    back by this entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.cuh"
@@ -64,22 +68,56 @@ Carve carve_for(const moe_shape_t& s) {
 
 bool ok16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Device address of the scratch array, looked up once per device with that device current.
+// The current context's unique id, or 0 when no context is current on this thread yet
+// (cuCtxGetCurrent + cuCtxGetId, reached through the runtime's driver entry-point query, so the
+// library needs no link against the driver library).
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  *id = 0;
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (!ctx) return cudaSuccess;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch array in the current context.  It is looked up once per device
+// with that device current (cudaGetSymbolAddress) and kept together with the id of the context it
+// was taken in: after a device reset the runtime creates a new context (a new id), in which the
+// module, and so the array, may sit at another address, and the lookup is then made again.
 void* scratch_address(cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess || dev < 0 || dev >= 64) {
     if (*err == cudaSuccess) *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  unsigned long long ctx = 0;
+  if ((*err = current_context_id(&ctx)) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx == 0 || ctx_of[dev] != ctx) {
     void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);   // binds the device's context if none was
     if (*err != cudaSuccess) return nullptr;
+    if ((*err = current_context_id(&ctx)) != cudaSuccess) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   return addr[dev];
 }
@@ -117,6 +155,13 @@ extern "C" moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, con
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_ARCH;
+  {   // the stream must belong to the current device (the default stream handles always do)
+    const cudaStream_t cs0 = static_cast<cudaStream_t>(stream);
+    int sdev = -1;
+    if (cs0 != nullptr && cs0 != cudaStreamLegacy && cs0 != cudaStreamPerThread &&
+        (cudaStreamGetDevice(cs0, &sdev) != cudaSuccess || sdev != dev))
+      return MOE_ERR_INVALID_ARG;
+  }
   cudaError_t e = cudaSuccess;
   char* base = static_cast<char*>(scratch_address(&e));
   if (!base) return MOE_ERR_CUDA;

@@ -294,21 +294,62 @@ def test_decode_sweep_full_size(cuda_lib, T, seed):
 
 
 def test_batched_decode_full_size(cuda_lib):
+    """Every row of the skewed T = 64 batch."""
     w = synth.WORKLOADS["batched"]
     L = _full_case(w, 64, w.seeds[0])
-    _check_full(cuda_lib, L, [0, 5, 17, 31, 40, 63])
+    _check_full(cuda_lib, L, list(range(64)))
 
 
 def test_prefill_chunk_full_size(cuda_lib):
+    """Every row of the T = 4096 prefill chunk, outlier rows included."""
     w = synth.WORKLOADS["prefill"]
     L = _full_case(w, 4096, w.seeds[0])
     outliers = torch.nonzero(L.x.float().abs().amax(1) > 8).flatten().tolist()
     assert len(outliers) >= 30
-    _check_full(cuda_lib, L, [0, 1, 2047, 4095] + outliers[:3])
+    _check_full(cuda_lib, L, list(range(4096)))
 
 
-@pytest.mark.parametrize("layer", [0, 3])
+TC_TILE = 128   # token rows per work item of the tensor-core arm
+
+
+def _edge_tokens(L, n_total, rng_seed):
+    """Tokens of the rows where a tiling error would show first, then random ones up to n_total:
+    every row of the most popular expert's first and last 128-row tile, every row of the last
+    routed expert's last tile and of the shared expert's last tile (the last work item), and the
+    first and last token."""
+    s = L.shape
+    ids, _ = oracle.route(L.logits.cpu(), s.k)
+    counts, offsets, sorted_slot, _ = oracle.permute(ids, s.E)
+    toks = {0, s.T - 1}
+    hot = int(np.argmax(counts))
+    c, o = int(counts[hot]), int(offsets[hot])
+    last_tile = (c - 1) // TC_TILE * TC_TILE
+    rows = list(range(o, o + min(TC_TILE, c))) + list(range(o + last_tile, o + c))
+    e_last = int(np.nonzero(counts)[0][-1])
+    c2, o2 = int(counts[e_last]), int(offsets[e_last])
+    rows += list(range(o2 + (c2 - 1) // TC_TILE * TC_TILE, o2 + c2))
+    toks.update(int(sorted_slot[r]) // s.k for r in rows)
+    toks.update(range(s.T - ((s.T - 1) % TC_TILE + 1), s.T))   # the shared expert's last tile
+    rng = np.random.default_rng(rng_seed)
+    rest = np.setdiff1d(np.arange(s.T), np.fromiter(toks, int))
+    extra = max(0, n_total - len(toks))
+    toks.update(rng.choice(rest, size=min(extra, rest.size), replace=False).tolist())
+    return sorted(toks), counts[hot]
+
+
+@pytest.mark.parametrize("layer", [0, 1, 2, 3])
 def test_long_prefill_full_size(cuda_lib, layer):
+    """Each of the four T = 32768 Zipf layers: at least 512 rows, including every row of the
+    hottest expert's first and last tile and of the last work items."""
     w = synth.WORKLOADS["long"]
     L = _full_case(w, 32768, w.seeds[0], layer=layer)
-    _check_full(cuda_lib, L, [0, 12345, 32767])
+    tokens, hot_count = _edge_tokens(L, 512, 1000 + layer)
+    assert len(tokens) >= 512 and hot_count > 10 * TC_TILE
+    _check_full(cuda_lib, L, tokens)
+
+
+def test_zipf_prefill_8192_every_row(cuda_lib):
+    """One Zipf-routed layer of the long-prefill shape at T = 8192, every row checked."""
+    w = synth.WORKLOADS["long"]
+    L = Layer(w.shape(8192), 7_900, layer=0, logit_bias="zipf", gen_device="cuda")
+    _check_full(cuda_lib, L, list(range(8192)))

@@ -2,8 +2,8 @@
 
 It serves callers that cannot allocate device memory, so it keeps its scratch in a fixed array
 inside the library instead of a caller workspace.  This test calls it through the C ABI and
-checks it against moe_forward (the workspace-based entry point) on two calls in a row, with the
-layer tolerance the other parity tests use.  It sits in a file of its own, collected last.
+checks it against the CPU oracle and against moe_forward (the workspace-based entry point) on two
+calls in a row, with the layer tolerance the other parity tests use.  It sits in a file of its own, collected last.
 """
 import ctypes
 
@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from moe_cases import Layer, check_layer_close, moe_shape, to_np
 
@@ -35,8 +36,16 @@ def _call(moe, x, logits, gu, dn, ms, out, fp32):
     return st
 
 
+def _oracle_ref(L):
+    s = L.shape
+    ogu, odn = L.oracle_weights(L.used_groups(list(range(s.T))))
+    return oracle.moe_forward(L.x.cpu(), L.logits.cpu(), ogu, odn, s.k, s.has_shared)
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}")
-def test_static_scratch_matches_moe_forward(cuda_lib, case):
+def test_static_scratch_matches_oracle_and_moe_forward(cuda_lib, case):
+    """Two calls in a row of each output type, each checked against the CPU oracle and against
+    moe_forward (the workspace entry point), with the layer tolerance."""
     moe = cuda_lib
     T, H, E, k, I, sh, bias, seed = case
     L = Layer(synth.Shape(T=T, H=H, E=E, k=k, I=I, has_shared=sh), seed, logit_bias=bias,
@@ -46,6 +55,7 @@ def test_static_scratch_matches_moe_forward(cuda_lib, case):
     gu, dn = L.gpu_weights(moe)
     x, logits = L.x.cuda(), L.logits.cuda()
     ws = moe.workspace(ms)
+    oref = _oracle_ref(L)
     for fp32 in (False, True):
         dt = torch.float32 if fp32 else torch.bfloat16
         ref = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=fp32)
@@ -53,7 +63,25 @@ def test_static_scratch_matches_moe_forward(cuda_lib, case):
             out = torch.full((T, H), float("nan"), dtype=dt, device="cuda")
             assert _call(moe, x, logits, gu, dn, ms, out, fp32) == 0
             torch.cuda.synchronize()
-            check_layer_close(to_np(out), to_np(ref).astype(np.float64), f"static scratch fp32={fp32}")
+            check_layer_close(to_np(out), oref, f"static scratch vs oracle, fp32={fp32}")
+            check_layer_close(to_np(out), to_np(ref).astype(np.float64), f"static scratch vs moe_forward, fp32={fp32}")
+
+
+def test_static_scratch_after_a_device_timeout(cuda_lib):
+    """A device-side bounded wait that ran out (the timeout probe, on a workspace) leaves the
+    context usable: the next static-scratch call is still correct."""
+    moe = cuda_lib
+    T, H, E, k, I, sh, bias, seed = CASES[0]
+    L = Layer(synth.Shape(T=T, H=H, E=E, k=k, I=I, has_shared=sh), seed, logit_bias=bias, gen_device="cuda")
+    ms = moe_shape(moe, L.shape)
+    ws = moe.workspace(ms)
+    moe.debug_timeout_probe(ws, 2_000_000)
+    assert moe.device_status(ws) == -6   # MOE_ERR_DEVICE_TIMEOUT
+    gu, dn = L.gpu_weights(moe)
+    out = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    assert _call(moe, L.x.cuda(), L.logits.cuda(), gu, dn, ms, out, False) == 0
+    torch.cuda.synchronize()
+    check_layer_close(to_np(out), _oracle_ref(L), "static scratch after a timeout")
 
 
 def test_static_scratch_rejects_other_shapes(cuda_lib):
