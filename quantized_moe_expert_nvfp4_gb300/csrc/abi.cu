@@ -57,12 +57,17 @@ moe_status_t check_arch() {
 
 // The current device must be compute capability 10.3 and `stream` must belong to it (a stream
 // created on another device would run the launches there, against pointers of this one).  The
-// legacy and per-thread default stream handles always name the current device.
+// legacy and per-thread default stream handles always name the current device.  A stream that
+// is being captured is not asked (the query is not allowed during capture and would invalidate
+// it); the graph's launches then run on whatever stream the graph is launched into.
 moe_status_t check_device(void* stream) {
   moe_status_t st = check_arch();
   if (st != MOE_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (cs == nullptr || cs == cudaStreamLegacy || cs == cudaStreamPerThread) return MOE_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return MOE_ERR_INVALID_ARG;
+  if (cap != cudaStreamCaptureStatusNone) return MOE_OK;
   int dev = 0, sdev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamGetDevice(cs, &sdev) != cudaSuccess) return MOE_ERR_INVALID_ARG;

@@ -155,12 +155,16 @@ extern "C" moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, con
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (major != 10 || minor != 3) return MOE_ERR_ARCH;
-  {   // the stream must belong to the current device (the default stream handles always do)
+  {   // the stream must belong to the current device (the default stream handles always do; a
+      // stream being captured is not asked: the query would invalidate the capture)
     const cudaStream_t cs0 = static_cast<cudaStream_t>(stream);
     int sdev = -1;
-    if (cs0 != nullptr && cs0 != cudaStreamLegacy && cs0 != cudaStreamPerThread &&
-        (cudaStreamGetDevice(cs0, &sdev) != cudaSuccess || sdev != dev))
-      return MOE_ERR_INVALID_ARG;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cs0 != nullptr && cs0 != cudaStreamLegacy && cs0 != cudaStreamPerThread) {
+      if (cudaStreamIsCapturing(cs0, &cap) != cudaSuccess) return MOE_ERR_INVALID_ARG;
+      if (cap == cudaStreamCaptureStatusNone && (cudaStreamGetDevice(cs0, &sdev) != cudaSuccess || sdev != dev))
+        return MOE_ERR_INVALID_ARG;
+    }
   }
   cudaError_t e = cudaSuccess;
   char* base = static_cast<char*>(scratch_address(&e));

@@ -21,19 +21,34 @@ ROW_RMS_TOL = 2e-2
 MEAN_REL_TOL = 3e-3
 
 
-def check_layer_close(got, ref, what="output"):
+BF16_HALF_ULP = 2.0 ** -9   # |bf16(v) - v| <= 2^-9 |v| for round-to-nearest-even (normal v)
+
+
+def check_layer_close(got, ref, what="output", rounded_bf16=False):
+    """The layer tolerance on the layer's result: max over a row of |err| <= 2e-2 * RMS(ref row)
+    and sum|err| / sum|ref| <= 3e-3.  With rounded_bf16=True `got` is a bf16 output, i.e. the
+    layer's fp32 result rounded to nearest even, and each element may further differ by that
+    rounding: half a bf16 ulp, at most 2^-9 of its magnitude."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.isfinite(got).all(), f"{what}: non-finite values"
     err = np.abs(got - ref)
     rms = np.sqrt((ref ** 2).mean(axis=-1))
-    ratio = err.max(axis=-1) / np.maximum(rms, 1e-300)
-    assert (err.max(axis=-1) <= ROW_RMS_TOL * rms).all(), f"{what}: worst max|err|/rms = {ratio.max():.3e}"
+    allow = BF16_HALF_ULP * np.maximum(np.abs(got), np.abs(ref)) if rounded_bf16 else 0.0
+    excess = np.maximum(err - allow, 0.0)
+    ratio = excess.max(axis=-1) / np.maximum(rms, 1e-300)
+    assert (excess.max(axis=-1) <= ROW_RMS_TOL * rms).all(), \
+        f"{what}: worst max|err|/rms = {ratio.max():.3e} (row {int(ratio.argmax())})"
     denom = np.abs(ref).sum()
     rel = err.sum() / denom if denom > 0 else err.sum()
     assert rel <= MEAN_REL_TOL, f"{what}: mean relative error {rel:.3e}"
     return float(ratio.max()), float(rel)
+
+
+def bf16_round_bits(x32: torch.Tensor) -> torch.Tensor:
+    """fp32 -> bf16 round to nearest even (torch's conversion), as raw bits."""
+    return x32.to(torch.bfloat16).view(torch.int16)
 
 
 def check_bf16_stage_close(got, ref, what="stage"):

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from moe_cases import Layer, check_bf16_stage_close, check_layer_close, moe_shape, to_np
+from moe_cases import Layer, bf16_round_bits, check_bf16_stage_close, check_layer_close, moe_shape, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -87,7 +87,7 @@ def test_small_layers_all_stages(cuda_lib, case):
         check_layer_close(to_np(y[S:]), y_ref[:, s.k], "y shared")
     for fp32 in (False, True):
         out = moe.combine(y, slot_pos, w, ms, out_fp32=fp32)
-        check_layer_close(to_np(out), out_ref, f"combine fp32={fp32}")
+        check_layer_close(to_np(out), out_ref, f"combine fp32={fp32}", rounded_bf16=not fp32)
     # the fused forward, both output types
     for fp32 in (False, True):
         out = torch.full((s.T, s.H), float("nan"), device="cuda",
@@ -95,7 +95,8 @@ def test_small_layers_all_stages(cuda_lib, case):
         moe.forward(x, logits, gu, dn, ms, ws, out=out, out_fp32=fp32)
         torch.cuda.synchronize()
         assert moe.device_status(ws) == 0
-        check_layer_close(to_np(out), out_ref, f"forward fp32={fp32} arm={moe.forward_arm(ms)}")
+        check_layer_close(to_np(out), out_ref, f"forward fp32={fp32} arm={moe.forward_arm(ms)}",
+                          rounded_bf16=not fp32)
 
 
 def test_forward_arm_selection(cuda_lib):
@@ -143,7 +144,7 @@ def test_one_launch_consecutive_calls(cuda_lib):
         torch.cuda.synchronize()
         assert moe.device_status(ws) == 0
         ref = oracle.moe_forward(x, lg, ogu, odn, s.k, s.has_shared)
-        check_layer_close(to_np(out), ref, f"call {r}")
+        check_layer_close(to_np(out), ref, f"call {r}", rounded_bf16=True)
 
 
 def test_device_timeout_is_reported_without_fault(cuda_lib):
@@ -165,7 +166,8 @@ def test_device_timeout_is_reported_without_fault(cuda_lib):
     moe.forward(L.x.cuda(), L.logits.cuda(), gu, dn, ms, ws, out=out)
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
-    check_layer_close(to_np(out), oracle.moe_forward(L.x, L.logits, ogu, odn, s.k, s.has_shared), "after the probe")
+    check_layer_close(to_np(out), oracle.moe_forward(L.x, L.logits, ogu, odn, s.k, s.has_shared), "after the probe",
+                      rounded_bf16=True)
 
 
 def test_forward_profiled_matches_forward(cuda_lib):
@@ -236,15 +238,22 @@ def _full_case(w: synth.Workload, T, seed, layer=0, n_sample=None, rng_seed=0):
 
 
 def _check_full(moe, L, tokens):
+    """Routing and permutation in full (bit-exact); the layer output of the listed tokens in both
+    output types: the fp32 result against the oracle with the layer tolerance, the bf16 output
+    bit for bit the round-to-nearest-even of that fp32 result (and so within the tolerance plus
+    the rounding's half ulp)."""
     s = L.shape
     ms = moe_shape(moe, s)
     gu, dn = L.gpu_weights(moe)
     x, logits = L.x, L.logits
     ws = moe.workspace(ms)
     out = torch.full((s.T, s.H), float("nan"), device="cuda", dtype=torch.bfloat16)
+    out32 = torch.full((s.T, s.H), float("nan"), device="cuda", dtype=torch.float32)
     moe.forward(x, logits, gu, dn, ms, ws, out=out)
+    moe.forward(x, logits, gu, dn, ms, ws, out=out32, out_fp32=True)
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
+    assert torch.equal(out.view(torch.int16), bf16_round_bits(out32)), "bf16 output != rounded fp32 output"
     ids, w = moe.route_topk(logits, ms)
     oids, ow = oracle.route(logits.cpu(), s.k)
     assert np.array_equal(ids.cpu().numpy(), oids)
@@ -263,7 +272,9 @@ def _check_full(moe, L, tokens):
         assert np.array_equal(q.scales[gi].cpu().numpy(), o[1][groups])
         assert np.array_equal(q.scale2[gi].cpu().numpy(), o[2][groups])
     ref = oracle.moe_forward(x.cpu(), logits.cpu(), ogu, odn, s.k, s.has_shared, tokens=tokens)
-    check_layer_close(to_np(out[torch.tensor(tokens, device="cuda")]), ref, "forward sampled rows")
+    sel = torch.tensor(tokens, device="cuda")
+    check_layer_close(to_np(out32[sel]), ref, "forward fp32, checked rows")
+    check_layer_close(to_np(out[sel]), ref, "forward bf16, checked rows", rounded_bf16=True)
     torch.cuda.synchronize()
     assert moe.device_status(ws) == 0
 
