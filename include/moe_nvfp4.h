@@ -158,19 +158,21 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
 
 /* The one-launch decode forward (moe_forward_arm == 0 shapes: T <= 8, H % 512 == 0, H <= 4096,
  * I % 256 == 0, I <= 1024) for callers that cannot allocate device memory -- code running where
- * cudaMalloc is not allowed or not available, such as inside a framework's memory-planning phase, a host
- * callback, or a plugin whose host application owns every device allocation and only passes in
- * tensor pointers.  No workspace argument: the scratch (routing results, permutation, h, y, the
- * status word and the decode kernel's counters) lives in one 4 MiB array in device global memory that
- * the library declares at file scope; every GPU that loads the library holds it until the
- * library is unloaded.  The pages have no counterpart to this call; it is a deployment aid.
+ * cudaMalloc is not allowed or not available, such as inside a framework's memory-planning phase,
+ * a host callback, or a plugin whose host application owns every device allocation and only
+ * passes in tensor pointers.  No workspace argument: the scratch (routing results, permutation,
+ * the partial expert outputs, the status word and the decode kernel's counters) lives in one
+ * 16 MiB array in device global memory that the library declares at file scope; every GPU that
+ * loads the library holds it until the library is unloaded.  The pages have no counterpart to
+ * this call; it is a deployment aid.
  *   - Inputs, weights and out are as for moe_forward; nothing is allocated or freed.
- *   - Shapes whose scratch exceeds 4 MiB, and shapes outside arm 0, return
- *     MOE_ERR_UNSUPPORTED_SHAPE.
+ *   - Shapes whose scratch exceeds 16 MiB (the partial outputs take (I/64) * T * (k+1) * H * 4
+ *     bytes), and shapes outside arm 0, return MOE_ERR_UNSUPPORTED_SHAPE.
  *   - All calls on a device share the array: calls that overlap on the GPU (other streams or
  *     threads) race and corrupt each other; serialize them.
- *   - The first call on a device looks up the array's device address; make it outside any CUDA
- *     stream capture.
+ *   - The first call on a device looks up the array's device address, and looks it up again
+ *     after the device's context changed (a device reset); make the first call outside any
+ *     CUDA stream capture.
  *   - Each call first clears the status word, the launch count and the decode kernel's counters
  *     on `stream` (an asynchronous memset).
  *     Device-side timeouts are not reported back by this call. */

@@ -232,6 +232,7 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.xe = take(4 * tc_rows);
   L.hf = take(2 * tc_rows * s.I);
   L.he = take(4 * tc_rows);
+  L.yp = take(s.T <= kFdMaxT ? fd_partial_bytes(s) : 0);
   L.total = off;
   return L;
 }
@@ -388,12 +389,11 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     f.offsets = w.offsets;
     f.sorted_slot = w.sorted_slot;
     f.slot_pos = w.slot_pos;
-    f.h = w.h;
+    f.yp = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + w.L.yp);
     f.sync = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + w.L.fdsync);
-    f.y = w.y;
     f.out = out;
     f.out_is_fp32 = out_is_fp32;
-    f.grid_bar = reinterpret_cast<unsigned*>(w.meta + 2);
+    f.grid_ctr = reinterpret_cast<unsigned long long*>(w.meta + 2);
     f.status = w.status;
     e = launch_decode_fused(f, cs);
     for (int i = 1; i <= 4 && e == cudaSuccess; ++i) e = mark(i);

@@ -4,33 +4,35 @@
 // the selected experts' bytes (bandwidth floor = bytes of the active experts / stream bandwidth,
 // done when within 1.3x of it), the routed top-k and the shared expert in one launch per
 // projection, gate+up fused and silu+down fused, and no host round trip.  Here one launch does
-// all of it:
-//   phase A  every CTA routes the T tokens itself (one warp per token, the same selection as the
-//            routing kernel; no launch boundary between routing and the weight stream), builds
-//            the permutation in SMEM with block-wide scans, and stages x as f16 rows scaled by a
-//            power of two per row (the tensor-core arm's convention: exact for every element of
-//            at least 2^-31 of the row maximum);
-//   phase B  gate_up units (8 gate rows + the 8 matching up rows of one active expert):
-//            h = SiLU(g) * u in bf16; each unit counts itself on its expert's readiness counter;
-//   phase C  down units (64 output rows of one active expert), each once its expert's h is
-//            complete (no grid-wide barrier): y in fp32; the unit that completes a 64-column
-//            block (the last of the active experts' units for it, found by an arrival counter)
-//            runs the fixed-order fp32 combine of that block,
-//            out[t] = sum_j w[t,j] y[slot(t,j)] + y[shared t].
-// A producer warp streams each CTA's units (phase B then C) into a ring of SMEM slots: one TMA
-// tensor copy of the unit's packed weights in the 128-byte swizzled layout, one copy of its
-// scales (few, large copies keep the SM's copy engine streaming at full rate) and, for a down
-// unit, its h rows, copied once the expert's readiness counter shows all its gate_up units done.
-// The counters (and the combine's arrival counters) come in two sets used by alternate
-// launches: a launch's set is the parity of the launch count, which every CTA takes with one
-// atomic at entry, and each launch zeroes the other set for the next one.
-// The products run on the tensor cores (mma.sync m16n8k16, f16 operands, fp32 accumulation):
-// the weights are dequantized exactly into f16 (e2m1 x e4m3 has at most 6 significant bits and
-// lies in [2^-10, 2688]), the MMA columns are the expert's tokens (up to 8), and the activations
-// are f16 rows scaled by a power of two (x in phase A; each h row in its slot, from its maximum).
-// Units are dealt round-robin to the CTAs, one CTA per SM; ring slot s belongs to the warp pair
-// (s, s + NS).  Every wait is bounded: an mbarrier or counter wait that runs past 1 s records
-// MOE_ERR_DEVICE_TIMEOUT in the status word and the kernel winds down.
+// all of it, split so that no CTA ever waits for another one's intermediate:
+//   phase A  every CTA routes the T tokens itself (one warp per token), builds the permutation
+//            in shared memory with block-wide scans, and stages x as f16 rows scaled by a power
+//            of two per row (exact for every element of at least 2^-31 of the row maximum);
+//   phase B  work units: one active expert (the shared expert first) and one 64-wide slice of
+//            its intermediate dimension.  A unit streams the slice's 64 gate rows, their 64 up
+//            rows and the down projection's 64 matching columns (every output row's 32 bytes
+//            of the slice), computes h = SiLU(g) * u for its 64 columns on chip (rounded to
+//            bf16), and multiplies it by its down columns: a partial expert output over the
+//            slice, written in fp32.  Down is thereby split along I (split-K) instead of
+//            waiting for other CTAs' h;
+//   phase C  once every unit of the launch is done (one counter), each CTA sums, for a block
+//            of output columns, the I/64 partials of every (token, expert) in slice order and
+//            combines the experts in the fixed order out[t] = sum_j w[t,j] y[t,j] + y_shared[t],
+//            in fp32.
+// A producer warp streams each CTA's units into a ring of shared-memory slots with large copies
+// (a GB300 SM keeps only a few bulk copies in flight, so its stream rate grows with the copy
+// size): a gate_up chunk is one 32 KB TMA tensor copy (128 rows x 512 K, 128-byte swizzle) and
+// one copy of its 4 KB of scales; a down chunk is one 32 KB tensor copy (1024 output rows x the
+// slice's 32 bytes, 32-byte swizzle), its 4-byte scale words fetched by the producer lanes with
+// cp.async.  All 16 compute warps consume every chunk (each takes its share of the rows or of
+// K), so the ring is consumed in order and its depth does not depend on the warp count.
+// Products run on the tensor cores (mma.sync m16n8k16, f16 operands, fp32 accumulation): the
+// weights are dequantized exactly into f16 (e2m1 x e4m3 has at most 6 significant bits and lies
+// in [2^-10, 2688]) and the MMA columns are the expert's tokens (up to 8).
+// The launch's counter set is the parity of the launch count (one atomic per CTA at entry); each
+// launch zeroes the other set for the next one.  Every wait is bounded: an mbarrier or counter
+// wait that runs past 1 s records MOE_ERR_DEVICE_TIMEOUT in the status word and the kernel winds
+// down.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -40,37 +42,44 @@
 namespace moe {
 namespace {
 
-constexpr int kFdWarps = 16;                   // 4 per SM sub-partition: up to 128 registers a thread
-constexpr int kFdThreads = kFdWarps * 32;
-constexpr int kFdComputeWarps = kFdWarps - 1;
-constexpr int kFdProducer = kFdComputeWarps;   // warp index of the producer
-constexpr int kFdXWarp0 = 8;                   // warps 8 .. 8 + T - 1 stage the activations
-constexpr int kFdGuPairs = 8;                  // gate_up unit: 8 gate rows + the 8 up rows (one m16 tile)
-constexpr int kFdDnRows = 64;                  // down unit: 64 output rows (four m16 tiles)
-constexpr int kFdMaxSlots = kFdComputeWarps / 2;   // ring slots; slot s is consumed by warps s and s + NS
-static_assert(2 + 2 * kFdMaxSlots <= 16, "two named barriers per slot after barriers 0 and 1");
+constexpr int kDkCompute = 16;                 // compute warps
+constexpr int kDkWarps = kDkCompute + 1;       // + the producer
+constexpr int kDkThreads = kDkWarps * 32;
+constexpr int kDkCThreads = kDkCompute * 32;
+constexpr int kDkProducer = kDkCompute;        // warp index of the producer
+constexpr int kDkXWarp0 = 8;                   // warps 8 .. 8 + T - 1 stage the activations
+constexpr int kIs = kFdSlice;                  // intermediate columns of one unit
+constexpr int kGuK = 512;                      // K of one gate_up chunk (two 128-byte lines per row)
+constexpr int kGuPacked = 2 * kIs * kGuK / 2;  // 32 KB: [line 2][gate|up][64 rows][128 B]
+constexpr int kGuScales = 2 * kIs * kGuK / 16; // 4 KB:  [gate|up][64 rows][32 B]
+constexpr int kDnScaleOff = 32 * 1024;         // down chunk: packed [rows][32 B], then [rows][4 B] scales
+constexpr int kSlotBytes = 36 * 1024;
+constexpr int kDkMaxSlots = 8;
 constexpr int kFdMaxS = kFdMaxT * kMaxK;
 constexpr int kFdSmemLimit = 227 * 1024;
 constexpr uint64_t kFdTimeoutNs = 1000000000ull;
+constexpr int kRedCols = 16;                   // output columns per reduction block
 
-// TMA descriptors of the packed weights, rows cut into 128-byte lines (swizzled 128B):
-//   gu  {128 B, row of [G * 2I], gate/up half (stride I rows), line of the row (H / 256)}
-//   dn  {128 B, row of [G * H], line of the row (I / 256)}
-// and of the gate_up scales, {H/16 B, row of [G * 2I], gate/up half} (8 gate rows and their 8
-// up rows in one copy).
+static_assert(kIs == 64, "a unit's h slice is 8 MMA tiles of 8 gate + 8 up rows, and 32 bytes of a down row");
+
+// TMA descriptors:
+//   gu   packed gate_up {128 B, row of [G * 2I - I], gate/up half (stride I rows), 128-byte line
+//        (stride 128 B)}: a box of 64 rows x 2 halves x 2 lines is one gate_up chunk
+//   gus  gate_up scales {H/16 B, row of [G * 2I - I], gate/up half}: a box of 32 B x 64 x 2
+//   dn   packed down {I/2 B, row in a block of 256, block of 256 rows of [G * H]}: a box of
+//        32 B x 256 x (rows / 256) is one down chunk
+// (the row dimension of the gate_up maps stops I rows early, so that the up half of every box
+// stays inside the tensor and the out-of-range fill would cover a bad coordinate)
 struct FdMaps {
   CUtensorMap gu;
-  CUtensorMap dn;
   CUtensorMap gus;
+  CUtensorMap dn;
 };
 
 struct FdArgs {
   const uint16_t* x;
   const float* logits;
-  const uint8_t* gu_packed;
-  const uint8_t* gu_scales;
   const float* gu_scale2;
-  const uint8_t* dn_packed;
   const uint8_t* dn_scales;
   const float* dn_scale2;
   int T, H, I, E, k, has_shared;
@@ -80,19 +89,18 @@ struct FdArgs {
   int32_t* offsets;
   int32_t* sorted_slot;
   int32_t* slot_pos;
-  uint16_t* h;          // [S + T, I]
-  float* y;             // [S + T, H]
+  float* yp;                      // [I/64][S + T][H] partial expert outputs
   void* out;
   int out_is_fp32;
   unsigned long long* grid_ctr;   // launch count: one arrival per CTA and launch, monotonic
-  unsigned* ccnt;                 // [2][kFdMaxBlocks] block arrivals, then [2][kFdMaxActive] readiness
+  unsigned* done;                 // [2] units-done counters (CTAs), one per launch parity
   int32_t* status;
-  int x_pitch, smem_off, sh_off, ring_off, ring_bytes;
+  int x_pitch, ctl_off, ring_off, n_slots, dn_rows;
 };
 
 struct FdSmem {
-  uint64_t full[kFdMaxSlots];
-  uint64_t empty[kFdMaxSlots];
+  uint64_t full[kDkMaxSlots];
+  uint64_t empty[kDkMaxSlots];
   int32_t ids[kFdMaxS];
   float w[kFdMaxS];
   int32_t sorted[kFdMaxS];
@@ -101,14 +109,11 @@ struct FdSmem {
   int32_t act_row[kFdMaxS + 1];
   int32_t act_cnt[kFdMaxS + 1];
   int32_t cnt[kMaxE];
-  int wsum[kFdWarps];          // block scan of the expert counts: per-warp totals, then bases
-  int wnz[kFdWarps];
-  int wmax[kFdWarps];          // and per-warp maxima of the routed counts
-  int ns;                      // this launch's ring: slots and slot size (from the routing)
-  int slot_b;
+  int wsum[kDkCompute];        // block scan of the expert counts: per-warp totals, then bases
+  int wnz[kDkCompute];
   float xfac[kFdMaxT];         // 2^e of each staged f16 activation row
-  alignas(16) float red[kFdMaxSlots][32 * 4];   // gate_up: the second warp's partial sums, per slot
-  float hfac[kFdMaxSlots][kFdMaxT];              // down: 2^e of each staged h row, per slot
+  alignas(16) float red[8][32 * 4];            // gate_up: the second K half's sums, per MMA tile
+  alignas(16) uint16_t htile[kFdMaxT][kIs + 8];   // the unit's h (bf16), one row per token
   int n_act;
   int abort_flag;
   int ep;                      // this launch's counter set (parity of the launch count)
@@ -132,19 +137,20 @@ __device__ __forceinline__ bool fd_try(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ bool fd_wait(uint64_t* b, uint32_t parity, FdSmem* sm, int32_t* status,
+// Bounded wait on an mbarrier phase; false when the CTA is aborting or this wait ran out.
+__device__ bool fd_wait(uint64_t* b, uint32_t parity, int* abort_flag, int32_t* status,
                         uint64_t limit_ns = kFdTimeoutNs) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (fd_try(b, parity)) return true;
     if ((i & 255u) == 255u) {
-      if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return false;
+      if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
       const uint64_t t = now_ns();
       if (t0 == 0) {
         t0 = t;
       } else if (t - t0 > limit_ns) {
         report_device_error(status, kDevTimeout);
-        *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
+        *reinterpret_cast<volatile int*>(abort_flag) = 1;
         return false;
       }
     }
@@ -155,22 +161,17 @@ __device__ bool fd_wait(uint64_t* b, uint32_t parity, FdSmem* sm, int32_t* statu
 // wait runs out after limit_ns and records the timeout in the status word (the test of the
 // timeout path; nothing faults or hangs).
 __global__ void __launch_bounds__(32) fd_timeout_probe_kernel(int32_t* status, uint64_t limit_ns) {
-  __shared__ FdSmem sm;
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
   if (threadIdx.x == 0) {
-    sm.abort_flag = 0;
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm.full[0])));
+    abort_flag = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar)));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
-  fd_wait(&sm.full[0], 0, &sm, status, limit_ns);
+  fd_wait(&bar, 0, &abort_flag, status, limit_ns);
 }
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -185,6 +186,9 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, in
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
       : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
 // One m16n8k16 tensor-core step, D += A * B with f16 operands and fp32 accumulators.  Fragment
@@ -219,9 +223,8 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
 // first MMA of the piece uses 8 tig .. + 3 as its K positions (2 tig, 2 tig + 1 | 2 tig + 8,
 // 2 tig + 9) and the second MMA 8 tig + 4 .. + 7.  The B operand (activation rows) is read in the
 // same order, so each dot product is the pieces' own; the lane's elements all lie in block
-// 2 q + tig / 2 of the piece and share one scale.  w: the lane's word of the row, s: the scale as
-// an f16x2 splat; r[0], r[1] feed the first MMA, r[2], r[3] the second (e2m1 x e4m3 is exact in
-// f16).
+// 2 q + tig / 2 of piece q and share one scale.  w: the lane's word of the row, s: the scale as an
+// f16x2 splat; r[0], r[1] feed the first MMA, r[2], r[3] the second (e2m1 x e4m3 is exact in f16).
 __device__ __forceinline__ void piece_frag(uint32_t w, uint32_t s, uint32_t (&r)[4]) {
   e2m1x8_to_f16x2(w, r);
 #pragma unroll
@@ -241,82 +244,71 @@ __device__ __forceinline__ float absmax_bf16x8(float m, const uint4& v) {
   for (int c = 0; c < 4; ++c) m = fmaxf(m, fmaxf(fabsf(bf16_lo(q[c])), fabsf(bf16_hi(q[c]))));
   return m;
 }
-
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 
 template <int EPL>
-__global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __grid_constant__ FdMaps maps, FdArgs a) {
+__global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __grid_constant__ FdMaps maps, FdArgs a) {
   extern __shared__ __align__(1024) uint8_t fd_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fd_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* xs = base;   // f16 activation rows, x_pitch bytes apart
-  FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.smem_off);
+  FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.ctl_off);
   uint8_t* ring = base + a.ring_off;
-  uint8_t* sh_h = base + a.sh_off;   // the shared expert's h rows [T][I] for its down unit in this CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = T * k;
-  // The ring's layout is set after routing: a slot holds a down unit's h rows for at most the
-  // largest routed count (the shared expert's T rows have their own buffer), so routings that
-  // spread the tokens get more slots.  Slot 0 starts at the ring in every layout, so the unit
-  // issued before routing stays valid.
-  int NS = kFdMaxSlots;
-  uint32_t slot_bytes = 0;
-  const int gu_per_group = I / kFdGuPairs;
-  const int dn_per_group = H / kFdDnRows;
-  // slot: the unit's packed weights (gate_up: 16 rows x H/2 bytes; down: 64 rows x I/2 bytes; in
-  // swizzled 128-byte lines), then its scales (gate_up: [gate 8 | up 8][H/16]; down: [64][I/16]),
-  // then a routed expert's down unit's h rows [nt][I]
-  const uint32_t gu_wb = 2 * kFdGuPairs * (H / 2), gu_sb = kFdGuPairs * (H / 16);
-  const uint32_t dn_wb = kFdDnRows * (I / 2), dn_sb = kFdDnRows * (I / 16);
-  const uint32_t w_b = max(gu_wb, dn_wb), sc_b = max(2 * gu_sb, dn_sb), h_off = w_b + sc_b;
+  const int NS = a.n_slots;
+  const int nslice = I / kIs;
+  const int n_gu = H / kGuK;                 // gate_up chunks of a unit
+  const int n_dn = H / a.dn_rows;            // down chunks of a unit
+  const int n_chunk = n_gu + n_dn;
 
-  // The producer issues one unit: u < nB is a gate_up unit of active group u / gu_per_group,
-  // otherwise a down unit.  The shared expert is active group 0, so this CTA's first unit is
-  // known before routing when blockIdx.x < gu_per_group.
-  auto issue = [&](int u, int nB, uint32_t it) {
+  // The producer warp issues chunk c of unit (group g, slice m) into ring position it (warp-wide:
+  // the down chunk's scale words are fetched by all 32 lanes).
+  auto issue = [&](int g, int m, int c, uint32_t it) {
     const int slot = it % NS;
-    uint8_t* dst = ring + slot * slot_bytes;
+    uint8_t* dst = ring + slot * kSlotBytes;
     uint64_t* bar = &sm->full[slot];
-    if (u < nB) {
-      const int g = (u < gu_per_group && a.has_shared) ? E : sm->act[u / gu_per_group];
-      const int rg = g * 2 * I + (u % gu_per_group) * kFdGuPairs;   // first gate row; its up row is + I
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                   "r"(gu_wb + 2 * gu_sb)
-                   : "memory");
-      tma_load_4d(dst, &maps.gu, 0, rg, 0, 0, bar);
-      tma_load_3d(dst + w_b, &maps.gus, 0, rg, 0, bar);
+    if (c < n_gu) {
+      if (lane == 0) {
+        const int r0 = g * 2 * I + m * kIs;   // first gate row of the slice; its up row is + I
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                     "r"(kGuPacked + kGuScales)
+                     : "memory");
+        tma_load_4d(dst, &maps.gu, 0, r0, 0, 2 * c, bar);
+        tma_load_3d(dst + kGuPacked, &maps.gus, 32 * c, r0, 0, bar);
+      }
     } else {
-      const int v = u - nB, gi = v / dn_per_group;
-      const int r0 = sm->act[gi] * H + (v % dn_per_group) * kFdDnRows;
-      const uint32_t h_bytes = static_cast<uint32_t>(sm->act_cnt[gi]) * I * 2;
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                   "r"(dn_wb + dn_sb + h_bytes)
-                   : "memory");
-      tma_load_3d(dst, &maps.dn, 0, r0, 0, bar);
-      bulk_g2s(dst + w_b, a.dn_scales + static_cast<int64_t>(r0) * (I / 16), dn_sb, bar);
+      const int d = c - n_gu;
+      const int64_t row0 = static_cast<int64_t>(g) * H + static_cast<int64_t>(d) * a.dn_rows;
+      const uint8_t* src = a.dn_scales + row0 * (I / 16) + 4 * m;
+      for (int r = lane; r < a.dn_rows; r += 32) cp_async4(dst + kDnScaleOff + 4 * r, src + static_cast<int64_t>(r) * (I / 16));
+      // each lane's arrive (pending count +1 now, -1 once its copies land) before lane 0's
+      asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                     "r"(a.dn_rows * (kIs / 2))
+                     : "memory");
+        tma_load_3d(dst, &maps.dn, (kIs / 2) * m, 0, static_cast<int>(row0 / 256), bar);
+      }
     }
-  };
-  // The h rows of down unit u (issued as ring position it) into the end of its slot (the shared
-  // expert's into its own buffer: a CTA holds at most one of its H/64 <= 64 down units); only
-  // once the expert's readiness counter shows every gate_up unit of it done (other CTAs write them).
-  auto issue_h = [&](int u, int nB, uint32_t it) {
-    const int gi = (u - nB) / dn_per_group;
-    const int slot = it % NS;
-    uint8_t* dst = (sm->act[gi] == E) ? sh_h : ring + slot * slot_bytes + h_off;
-    bulk_g2s(dst, a.h + static_cast<int64_t>(sm->act_row[gi]) * I,
-             static_cast<uint32_t>(sm->act_cnt[gi]) * I * 2, &sm->full[slot]);
   };
 
   // ------------------------------------------------------------ phase A: route + permute
-  bool early = false;
-  if (warp == kFdProducer && lane == 0) {
-    for (int s = 0; s < kFdMaxSlots; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm->full[s])));
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" ::"r"(smem_addr(&sm->empty[s])));   // the slot's 2 warps
+  uint32_t early = 0;   // chunks the producer issued before routing
+  if (warp == kDkProducer) {
+    if (lane == 0) {
+      for (int s = 0; s < kDkMaxSlots; ++s) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&sm->full[s])));
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(&sm->empty[s])), "r"(kDkCompute));
+      }
+      sm->abort_flag = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    sm->abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (a.has_shared && blockIdx.x < gu_per_group) {   // first unit: shared expert, gate_up
-      issue(blockIdx.x, 1 << 30, 0);
-      early = true;
+    __syncwarp();
+    // the shared expert is active group 0: this CTA's first unit is known before routing
+    if (a.has_shared && static_cast<int>(blockIdx.x) < nslice) {
+      early = static_cast<uint32_t>(min(n_chunk, NS));
+      for (uint32_t c = 0; c < early; ++c) issue(E, blockIdx.x, c, c);
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
@@ -326,9 +318,9 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   if (threadIdx.x == 32) launch_n = atomicAdd(a.grid_ctr, 1ull);
   // activations: warp 8 + t stages token t as f16(x * 2^-e), e = floor(log2 max|x|) - 14 (at
   // least -126), the row maximum in [2^14, 2^15); the factor 2^e is applied to the dot products
-  if (warp >= kFdXWarp0 && warp < kFdXWarp0 + T) {
+  if (warp >= kDkXWarp0 && warp < kDkXWarp0 + T) {
     constexpr int kMaxV = 4096 / 256;   // uint4 per lane for H <= 4096
-    const int t = warp - kFdXWarp0, nv = H / 256;
+    const int t = warp - kDkXWarp0, nv = H / 256;
     const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t) * H);
     uint4 v[kMaxV];
     float m = 0.0f;
@@ -362,13 +354,7 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   if (threadIdx.x == 32) sm->ep = static_cast<int>((launch_n / gridDim.x) & 1ull);
   __syncthreads();
   const int ep = sm->ep;
-  unsigned* const ccnt = a.ccnt + ep * kFdMaxBlocks;                       // this launch's arrivals
-  unsigned* const ready = a.ccnt + 2 * kFdMaxBlocks + ep * kFdMaxActive;   // and readiness counters
-  if (blockIdx.x == 0) {   // the next launch's set (no CTA of this launch touches it)
-    for (int i = threadIdx.x; i < kFdMaxBlocks; i += blockDim.x) a.ccnt[(ep ^ 1) * kFdMaxBlocks + i] = 0u;
-    for (int i = threadIdx.x; i < kFdMaxActive; i += blockDim.x)
-      a.ccnt[2 * kFdMaxBlocks + (ep ^ 1) * kFdMaxActive + i] = 0u;
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.done[ep ^ 1] = 0u;   // the next launch's counter
   if (warp < T && lane < k) {
     sm->ids[warp * k + lane] = my_id;
     sm->w[warp * k + lane] = my_w;
@@ -379,12 +365,12 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
     }
   }
   __syncthreads();
-  // exclusive scan of the counts over the block: thread u takes experts 2u, 2u + 1 (E <= 1024);
-  // the active list is the shared expert first, then the routed experts ascending
+  // exclusive scan of the counts over the compute warps: thread u takes experts 2u, 2u + 1
+  // (E <= 1024); the active list is the shared expert first, then the routed experts ascending
   const int sh = a.has_shared;
   const int u2 = 2 * threadIdx.x;
-  const int c0 = (u2 < E) ? sm->cnt[u2] : 0;
-  const int c1 = (u2 + 1 < E) ? sm->cnt[u2 + 1] : 0;
+  const int c0 = (warp < kDkCompute && u2 < E) ? sm->cnt[u2] : 0;
+  const int c1 = (warp < kDkCompute && u2 + 1 < E) ? sm->cnt[u2 + 1] : 0;
   int vs = c0 + c1, vn = (c0 > 0) + (c1 > 0);   // inclusive warp scans of rows and of active experts
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -394,15 +380,13 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       vn += yn;
     }
   }
-  const int vmax = __reduce_max_sync(0xffffffffu, max(c0, c1));
-  if (lane == 31) {
+  if (lane == 31 && warp < kDkCompute) {
     sm->wsum[warp] = vs;
     sm->wnz[warp] = vn;
-    sm->wmax[warp] = vmax;
   }
   __syncthreads();
   if (warp == 0) {
-    int ts = lane < kFdWarps ? sm->wsum[lane] : 0, tn = lane < kFdWarps ? sm->wnz[lane] : 0;
+    int ts = lane < kDkCompute ? sm->wsum[lane] : 0, tn = lane < kDkCompute ? sm->wnz[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int ys = __shfl_up_sync(0xffffffffu, ts, off), yn = __shfl_up_sync(0xffffffffu, tn, off);
@@ -412,11 +396,11 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       }
     }
     __syncwarp();
-    if (lane < kFdWarps) {   // exclusive bases of each warp
+    if (lane < kDkCompute) {   // exclusive bases of each warp
       sm->wsum[lane] = ts - sm->wsum[lane];
       sm->wnz[lane] = tn - sm->wnz[lane];
     }
-    if (lane == kFdWarps - 1) {
+    if (lane == kDkCompute - 1) {
       if (sh) {
         sm->act[0] = E;
         sm->act_row[0] = S;
@@ -425,16 +409,9 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
       sm->n_act = tn + sh;
       if (blockIdx.x == 0) a.offsets[E] = S;
     }
-    if (lane == 0) {   // the ring: h room for the largest routed count
-      int mr = 0;
-      for (int w2 = 0; w2 < kFdWarps; ++w2) mr = max(mr, sm->wmax[w2]);
-      const uint32_t sb = ((w_b + sc_b + static_cast<uint32_t>(mr) * I * 2 + 1023u) / 1024u) * 1024u;
-      sm->slot_b = static_cast<int>(sb);
-      sm->ns = min(kFdMaxSlots, static_cast<int>(static_cast<uint32_t>(a.ring_bytes) / sb));
-    }
   }
   __syncthreads();
-  {
+  if (warp < kDkCompute) {
     int run = sm->wsum[warp] + vs - (c0 + c1), pos = sm->wnz[warp] + vn - ((c0 > 0) + (c1 > 0)) + sh;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
@@ -471,88 +448,30 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   }
   __syncthreads();
 
-  const int n_act = sm->n_act;
-  NS = sm->ns;
-  slot_bytes = static_cast<uint32_t>(sm->slot_b);
-  const int nB = n_act * gu_per_group;
-  const int nC = n_act * dn_per_group;
+  const int n_units = sm->n_act * nslice;
+  unsigned* const done = a.done + ep;
 
-  if (warp == kFdProducer) {
+  if (warp == kDkProducer) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t it = early ? 1 : 0;
-      bool ok = true;
-      // down units whose expert's h is not complete yet wait here for their h copy, in order (at
-      // most the ring's slots)
-      int pend_u[kFdMaxSlots];
-      uint32_t pend_it[kFdMaxSlots];
-      int ph = 0, pt = 0;   // head and tail counts
-      auto expert_ready = [&](int u) {
-        const int gi = (u - nB) / dn_per_group;
-        unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ready + gi) : "memory");
-        return v >= static_cast<unsigned>(gu_per_group);
-      };
-      // issue the waiting h copies whose expert is ready (all of them when force is set)
-      auto drain = [&](bool force) {
-        while (ph < pt && (force || expert_ready(pend_u[ph % kFdMaxSlots]))) {
-          asm volatile("fence.proxy.async.global;" ::: "memory");   // h was written by generic stores
-          issue_h(pend_u[ph % kFdMaxSlots], nB, pend_it[ph % kFdMaxSlots]);
-          ++ph;
-        }
-      };
-      for (int u = blockIdx.x + static_cast<int>(it) * gridDim.x; u < nB + nC; u += gridDim.x, ++it) {
+    uint32_t it = early;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      const int g = sm->act[u / nslice], m = u % nslice;
+      for (int c = (u == static_cast<int>(blockIdx.x)) ? static_cast<int>(early) : 0; c < n_chunk; ++c, ++it) {
         const int slot = it % NS;
-        const uint32_t parity = ((it / NS) & 1) ^ 1;
-        uint64_t t0 = 0;
-        for (uint32_t i = 0;; ++i) {   // bounded wait for the slot; start h copies meanwhile
-          if ((i & 7u) == 0u) drain(false);
-          if (fd_try(&sm->empty[slot], parity)) break;
-          if ((i & 255u) == 255u) {
-            if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) {
-              ok = false;
-              break;
-            }
-            const uint64_t t = now_ns();
-            if (t0 == 0) {
-              t0 = t;
-            } else if (t - t0 > kFdTimeoutNs) {
-              report_device_error(a.status, kDevTimeout);
-              *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
-              ok = false;
-              break;
-            }
-          }
+        if (it >= static_cast<uint32_t>(NS)) {   // the slot's previous chunk must be consumed
+          bool got = true;
+          if (lane == 0) got = fd_wait(&sm->empty[slot], ((it / NS) - 1) & 1, &sm->abort_flag, a.status);
+          ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+          if (!ok) break;
         }
-        if (!ok) break;
-        issue(u, nB, it);
-        if (u >= nB) {
-          pend_u[pt % kFdMaxSlots] = u;
-          pend_it[pt % kFdMaxSlots] = it;
-          ++pt;
-          drain(false);
-        }
+        issue(g, m, c, it);
       }
-      {   // the last down units wait for their experts (bounded)
-        const uint64_t t0 = now_ns();
-        for (uint32_t i = 0; ok && ph < pt; ++i) {
-          drain(false);
-          if ((i & 255u) == 255u) {
-            if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) ok = false;
-            else if (now_ns() - t0 > kFdTimeoutNs) {
-              report_device_error(a.status, kDevTimeout);
-              *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
-              ok = false;
-            }
-          }
-        }
-        drain(true);   // on abort too: every issued slot then completes, and the drain below is short
-      }
-      if (!ok) {  // let copies already issued land before the CTA exits (bounded)
-        for (uint32_t j = 0; j < static_cast<uint32_t>(NS) && j < it; ++j) {
-          const uint32_t q = it - 1 - j;
-          for (uint32_t i = 0; i < (1u << 20) && !fd_try(&sm->full[q % NS], (q / NS) & 1); ++i) {
-          }
+    }
+    if (!ok && lane == 0) {   // let copies already issued land before the CTA winds down (bounded)
+      for (uint32_t j = 0; j < static_cast<uint32_t>(NS) && j < it; ++j) {
+        const uint32_t q = it - 1 - j;
+        for (uint32_t i = 0; i < (1u << 20) && !fd_try(&sm->full[q % NS], (q / NS) & 1); ++i) {
         }
       }
     }
@@ -560,52 +479,36 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
   }
 
   // ------------------------------------------------------------ compute warps
-  // This CTA's units are u = blockIdx.x + i * gridDim.x, i = 0, 1, ... over [0, nB + nC), in
-  // the producer's order, unit i in slot i % NS.  Slot s belongs to warps s and s + NS (half 0
-  // and 1), which take its units i = s, s + NS, ... in order, so a slot's successive phases are
-  // awaited one after the other (a parity wait cannot tell phase n from phase n + 2).  A gate_up
-  // unit is split by K between the two warps (half 1's partial sums meet half 0's in SMEM), a
-  // down unit by rows.  Lane = 4 grp + tig.
   bool ok = true;
   const int grp = lane >> 2, tig = lane & 3;
   const uint32_t ssel = (tig >> 1) ? 0x3232u : 0x1010u;   // this lane's block of a piece: 2 q + tig / 2
-  const int nB_cta = (blockIdx.x < nB) ? (nB - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const int n_cta = (blockIdx.x < nB + nC) ? (nB + nC - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const bool consumer = warp < 2 * NS;
-  const int my_slot = warp % NS, half = warp / NS;
-
-  // phase B: gate_up units.  MMA rows 0-7 are the gate rows j0 .. j0 + 7, rows 8-15 the matching
-  // up rows; column n is the expert's n-th row of tokens (n < nt).
-  for (int i = consumer ? my_slot : nB_cta; i < nB_cta; i += NS) {
-    const int u = blockIdx.x + i * gridDim.x;
-    const int slot = my_slot;
-    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (i / NS) & 1, sm, a.status));
-    const int gi = u / gu_per_group;
-    const int g = sm->act[gi];
-    const int j0 = (u % gu_per_group) * kFdGuPairs;
-    const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
-    const float s2 = (half == 0) ? __ldg(a.gu_scale2 + g) : 0.0f;   // used by the epilogue
-    float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // rows grp / grp + 8, columns 2 tig, 2 tig + 1
-    if (ok) {
-      const uint8_t* sl = ring + slot * slot_bytes;
-      const uint8_t* scg = sl + w_b + grp * (H / 16);      // scales of gate row grp
-      const uint8_t* scu = scg + gu_sb;                    // and of its up row
-      const int cb = (grp < nt) ? grp : 0;                 // B column grp (row 0 past nt: ignored)
-      const int tb = (g == E) ? cb : sm->sorted[row0 + cb] / k;
-      const uint8_t* xr = xs + tb * a.x_pitch + 16 * tig;  // x[32 p + 8 tig .. + 7] of piece p at + 64 p
-      float d[4][4];   // four independent accumulation chains
+  const int mt = warp & 7, kh = warp >> 3;                 // gate_up: MMA tile and 128-byte line
+  uint32_t it = 0;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const int gi = u / nslice, m = u % nslice;
+    const int g = sm->act[gi], row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
+    // B column grp is the expert's token grp (columns past its count repeat token 0, ignored)
+    const int cb = (grp < nt) ? grp : 0;
+    const int tb = (g == E) ? cb : sm->sorted[row0 + cb] / k;
+    const uint8_t* xr = xs + tb * a.x_pitch + 16 * tig;
+    // ---- gate_up: rows 8 mt + grp of the slice's gate half and of its up half; this warp takes
+    // line kh (K 256 kh .. 256 kh + 255) of every chunk
+    float d[4][4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.0f;
-      const int nch = H / 256, c0 = half * (nch / 2);
-      for (int c = c0; c < c0 + nch / 2; ++c) {   // line c of every row: pieces 8 c .. 8 c + 7
-        const uint4 sgv = *reinterpret_cast<const uint4*>(scg + 16 * c);
-        const uint4 suv = *reinterpret_cast<const uint4*>(scu + 16 * c);
-        const uint8_t* lg = sl + (16 * c + grp) * 128 + 4 * tig;   // gate row grp; the up rows 8 lines on
-        const uint8_t* xc = xr + 512 * c;
+    for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.0f;
+    for (int c = 0; c < n_gu; ++c, ++it) {
+      const int slot = it % NS;
+      if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, &sm->abort_flag, a.status));
+      if (ok) {
+        const uint8_t* sl = ring + slot * kSlotBytes;
+        const uint8_t* lg = sl + kh * (2 * kIs * 128) + (8 * mt + grp) * 128 + 4 * tig;   // gate row; up 64 rows on
+        const uint4 sgv = *reinterpret_cast<const uint4*>(sl + kGuPacked + (8 * mt + grp) * 32 + 16 * kh);
+        const uint4 suv = *reinterpret_cast<const uint4*>(sl + kGuPacked + (kIs + 8 * mt + grp) * 32 + 16 * kh);
+        const uint8_t* xc = xr + 2 * (kGuK * c + 256 * kh);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {   // piece q of the line (stored at q ^ grp): blocks 16 c + 2 q, + 1
+        for (int q = 0; q < 8; ++q) {   // piece q of the line (stored at q ^ grp): blocks 2 q, 2 q + 1
           const uint32_t wg = *reinterpret_cast<const uint32_t*>(lg + ((q ^ grp) << 4));
-          const uint32_t wu = *reinterpret_cast<const uint32_t*>(lg + 8 * 128 + ((q ^ grp) << 4));
+          const uint32_t wu = *reinterpret_cast<const uint32_t*>(lg + kIs * 128 + ((q ^ grp) << 4));
           const uint4 xb = *reinterpret_cast<const uint4*>(xc + 64 * q);
           const uint32_t sg = __byte_perm(e4m3x2_to_f16x2((&sgv.x)[q >> 1] >> (16 * (q & 1))), 0u, ssel);
           const uint32_t su = __byte_perm(e4m3x2_to_f16x2((&suv.x)[q >> 1] >> (16 * (q & 1))), 0u, ssel);
@@ -616,187 +519,184 @@ __global__ void __launch_bounds__(kFdThreads, 1) decode_fused_kernel(const __gri
           mma16816(d[(q & 1) * 2 + 1], gr[2], ur[2], gr[3], ur[3], xb.z, xb.w);
         }
       }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) p[r] = (d[0][r] + d[1][r]) + (d[2][r] + d[3][r]);
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
     }
-    // the two halves meet: half 1 leaves its sums in SMEM, half 0 adds them (fixed order)
-    if (half == 1) *reinterpret_cast<float4*>(&sm->red[slot][4 * lane]) = make_float4(p[0], p[1], p[2], p[3]);
-    asm volatile("bar.sync %0, 64;" ::"r"(2 + slot) : "memory");
-    if (half == 0 && ok) {
-      const float4 o = *reinterpret_cast<const float4*>(&sm->red[slot][4 * lane]);
+    float p[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) p[r] = (d[0][r] + d[1][r]) + (d[2][r] + d[3][r]);
+    // the two K halves meet (fixed order), then h[n][8 mt + grp] = bf16(SiLU(g) * u) for the
+    // lane's tokens n = 2 tig, 2 tig + 1
+    if (kh == 1) *reinterpret_cast<float4*>(&sm->red[mt][4 * lane]) = make_float4(p[0], p[1], p[2], p[3]);
+    named_sync(1, kDkCThreads);
+    if (kh == 0) {
+      const float4 o = *reinterpret_cast<const float4*>(&sm->red[mt][4 * lane]);
       p[0] += o.x;
       p[1] += o.y;
       p[2] += o.z;
       p[3] += o.w;
-      // h[row0 + n, j0 + grp] = SiLU(g) * u for the lane's columns n = 2 tig, 2 tig + 1
+      const float s2 = __ldg(a.gu_scale2 + g);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
-        const int col = 2 * tig + c2;
-        if (col < nt) {
-          const int t = (g == E) ? col : sm->sorted[row0 + col] / k;
+        const int n = 2 * tig + c2;
+        if (n < nt) {
+          const int t = (g == E) ? n : sm->sorted[row0 + n] / k;
           const float f = s2 * sm->xfac[t];
-          a.h[static_cast<int64_t>(row0 + col) * I + j0 + grp] =
-              f32_to_bf16_bits(silu_f32(p[c2] * f) * (p[2 + c2] * f));
+          sm->htile[n][8 * mt + grp] = f32_to_bf16_bits(silu_f32(p[c2] * f) * (p[2 + c2] * f));
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
-    // the unit counts on its expert's readiness: half 0 signals its h stores with a non-blocking
-    // arrive and goes on; half 1 (otherwise idle until its next unit's data) waits for that and
-    // publishes them with its release, which the barrier makes cover half 0's stores
-    if (half == 0) {
-      asm volatile("bar.arrive %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
-    } else {
-      asm volatile("bar.sync %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
-      if (lane == 0 && ok) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ready + gi) : "memory");
+    named_sync(1, kDkCThreads);
+    // ---- down B operand: token column grp, the slice's h as f16 scaled by 2^-e (e from the
+    // token's maximum over the slice); lane tig holds elements 8 tig .. 8 tig + 7 of both pieces
+    uint4 hb[2];
+    float fac0, fac1;
+    {
+      const uint16_t* hrow = sm->htile[cb];
+      const uint4 v0 = *reinterpret_cast<const uint4*>(hrow + 8 * tig);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(hrow + 32 + 8 * tig);
+      float mx = absmax_bf16x8(absmax_bf16x8(0.0f, v0), v1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const int e = row_exponent(mx);
+      const float inv = pow2i(-e);
+      const uint4 vv[2] = {v0, v1};
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        hb[q] = make_uint4(f32x2_to_f16x2(bf16_lo(vv[q].x) * inv, bf16_hi(vv[q].x) * inv),
+                           f32x2_to_f16x2(bf16_lo(vv[q].y) * inv, bf16_hi(vv[q].y) * inv),
+                           f32x2_to_f16x2(bf16_lo(vv[q].z) * inv, bf16_hi(vv[q].z) * inv),
+                           f32x2_to_f16x2(bf16_lo(vv[q].w) * inv, bf16_hi(vv[q].w) * inv));
+      const float f = pow2i(e);
+      fac0 = __shfl_sync(0xffffffffu, f, (2 * tig) * 4);
+      fac1 = __shfl_sync(0xffffffffu, f, (2 * tig + 1) * 4);
     }
-  }
-
-  // phase C: down units.  The unit's 64 rows are four MMA tiles (rows 16 r + grp, + 8); half h
-  // takes tiles 2 h and 2 h + 1.  Column n is h row row0 + n, staged as f16 scaled by 2^-e_n with
-  // e_n from that row's maximum.
-  const int i0 = consumer ? nB_cta + ((my_slot - nB_cta) % NS + NS) % NS : n_cta;   // first i >= nB_cta in my slot
-  for (int i = i0; i < n_cta; i += NS) {
-    const int u = blockIdx.x + i * gridDim.x;
-    const int slot = my_slot;
-    const int blk = (u - nB) % dn_per_group;
-    if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (i / NS) & 1, sm, a.status));
-    const int gi = (u - nB) / dn_per_group;
-    const int g = sm->act[gi];
-    const int row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
-    uint8_t* sl = ring + slot * slot_bytes;
-    uint16_t* hs = reinterpret_cast<uint16_t*>(g == E ? sh_h : sl + h_off);   // h rows [nt][I]
-    if (ok) {
-      // each h row, in place, as f16(h * 2^-e) with e from the row's maximum (half h takes the
-      // rows te with te % 2 == h); 2^e goes to hfac for the epilogue
-      for (int te = half; te < nt; te += 2) {
-        uint4* hr = reinterpret_cast<uint4*>(hs + te * I);
-        constexpr int kMaxV = 1024 / 256;   // uint4 per lane for I <= 1024
-        uint4 v[kMaxV];
-        float m = 0.0f;
+    const float s2d = __ldg(a.dn_scale2 + g);
+    const int tiles = a.dn_rows / (16 * kDkCompute);   // MMA tiles of a down chunk per warp
+    // ---- down: output rows 16 (tiles w + t) + grp (+ 8) of each chunk; partial over the slice
+    for (int c = 0; c < n_dn; ++c, ++it) {
+      const int slot = it % NS;
+      if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, &sm->abort_flag, a.status));
+      if (ok) {
+        const uint8_t* sl = ring + slot * kSlotBytes;
+        for (int t = 0; t < tiles; ++t) {
+          const int ra = 16 * (tiles * warp + t) + grp;   // rows ra and ra + 8 (32-byte swizzle: piece ^= (row >> 2) & 1)
+          const uint32_t sw = (ra >> 2) & 1u;
+          const uint32_t sca = *reinterpret_cast<const uint32_t*>(sl + kDnScaleOff + 4 * ra);
+          const uint32_t scb = *reinterpret_cast<const uint32_t*>(sl + kDnScaleOff + 4 * (ra + 8));
+          float acc[2][4];
 #pragma unroll
-        for (int q = 0; q < kMaxV; ++q)
-          if (q < I / 256) {
-            v[q] = hr[q * 32 + lane];
-            m = absmax_bf16x8(m, v[q]);
-          }
+          for (int q = 0; q < 2; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-        const int e = row_exponent(m);
-        const float inv = pow2i(-e);
-#pragma unroll
-        for (int q = 0; q < kMaxV; ++q)
-          if (q < I / 256)
-            hr[q * 32 + lane] = make_uint4(f32x2_to_f16x2(bf16_lo(v[q].x) * inv, bf16_hi(v[q].x) * inv),
-                                           f32x2_to_f16x2(bf16_lo(v[q].y) * inv, bf16_hi(v[q].y) * inv),
-                                           f32x2_to_f16x2(bf16_lo(v[q].z) * inv, bf16_hi(v[q].z) * inv),
-                                           f32x2_to_f16x2(bf16_lo(v[q].w) * inv, bf16_hi(v[q].w) * inv));
-        if (lane == 0) sm->hfac[slot][te] = pow2i(e);
-      }
-    }
-    // both halves' rows converted (executed by both warps whatever their status, so that neither
-    // waits for a partner that skipped it)
-    asm volatile("bar.sync %0, 64;" ::"r"(2 + slot) : "memory");
-    if (ok) {
-      const float s2 = __ldg(a.dn_scale2 + g);
-      const uint8_t* sc = sl + w_b;   // scales [64][I/16]
-      const float fac0 = (2 * tig < nt) ? sm->hfac[slot][2 * tig] : 0.0f;
-      const float fac1 = (2 * tig + 1 < nt) ? sm->hfac[slot][2 * tig + 1] : 0.0f;
-      const uint8_t* hb = reinterpret_cast<const uint8_t*>(hs + ((grp < nt) ? grp : 0) * I) + 16 * tig;
-      float acc[2][2][4];   // [tile 2 half + r][piece parity]
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) acc[r][e2][0] = acc[r][e2][1] = acc[r][e2][2] = acc[r][e2][3] = 0.0f;
-      for (int c = 0; c < I / 256; ++c) {
-#pragma unroll 2
-        for (int q = 0; q < 8; ++q) {   // piece q of line c: blocks 16 c + 2 q, + 1
-          const uint4 xb = *reinterpret_cast<const uint4*>(hb + 512 * c + 64 * q);
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int ra = 16 * (2 * half + r) + grp;   // rows ra and ra + 8 (both stored with swizzle grp)
-            const uint8_t* la = sl + (c * kFdDnRows + ra) * 128 + ((q ^ grp) << 4) + 4 * tig;
-            const uint32_t wa = *reinterpret_cast<const uint32_t*>(la);
-            const uint32_t wb = *reinterpret_cast<const uint32_t*>(la + 8 * 128);
-            const uint32_t sa = __byte_perm(
-                e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc + ra * (I / 16) + 16 * c + 2 * q)), 0u, ssel);
-            const uint32_t sb = __byte_perm(
-                e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc + (ra + 8) * (I / 16) + 16 * c + 2 * q)), 0u, ssel);
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(sl + ra * 32 + ((q ^ sw) << 4) + 4 * tig);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(sl + (ra + 8) * 32 + ((q ^ sw) << 4) + 4 * tig);
+            const uint32_t sa = __byte_perm(e4m3x2_to_f16x2(sca >> (16 * q)), 0u, ssel);
+            const uint32_t sb = __byte_perm(e4m3x2_to_f16x2(scb >> (16 * q)), 0u, ssel);
             uint32_t ar[4], br[4];
             piece_frag(wa, sa, ar);
             piece_frag(wb, sb, br);
-            mma16816(acc[r][q & 1], ar[0], br[0], ar[1], br[1], xb.x, xb.y);
-            mma16816(acc[r][q & 1], ar[2], br[2], ar[3], br[3], xb.z, xb.w);
+            mma16816(acc[q], ar[0], br[0], ar[1], br[1], hb[q].x, hb[q].y);
+            mma16816(acc[q], ar[2], br[2], ar[3], br[3], hb[q].z, hb[q].w);
+          }
+          // yp[m][row0 + n][col] for the lane's tokens n = 2 tig, 2 tig + 1
+          const int col = c * a.dn_rows + ra;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int n = 2 * tig + c2;
+            if (n < nt) {
+              const float f = s2d * (c2 ? fac1 : fac0);
+              float* yr = a.yp + (static_cast<int64_t>(m) * (S + T) + row0 + n) * H + col;
+              yr[0] = (acc[0][c2] + acc[1][c2]) * f;
+              yr[8] = (acc[0][2 + c2] + acc[1][2 + c2]) * f;
+            }
           }
         }
       }
-      // y[row0 + n, 64 blk + row] for the lane's columns n = 2 tig, 2 tig + 1
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int col = 2 * tig + c2;
-        if (col < nt) {
-          const float f = s2 * (c2 ? fac1 : fac0);
-          float* yr = a.y + static_cast<int64_t>(row0 + col) * H + blk * kFdDnRows + 32 * half + grp;
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            yr[16 * r] = (acc[r][0][c2] + acc[r][1][c2]) * f;
-            yr[16 * r + 8] = (acc[r][0][2 + c2] + acc[r][1][2 + c2]) * f;
-          }
-        }
-      }
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
     }
-    // the in-place h conversion (generic stores) is ordered before the next unit's copy into the
-    // slot; the warp's y stores before lane 0's release below
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
-    // the unit's arrival on its 64-column block (n_act in all), by half 1 once half 0's y stores
-    // are ordered before it (half 0 goes on); the last arrival runs the combine
-    unsigned last = 0;
-    if (half == 0) {
-      asm volatile("bar.arrive %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
-    } else {
-      asm volatile("bar.sync %0, 64;" ::"r"(2 + kFdMaxSlots + slot) : "memory");
-      if (lane == 0 && ok) {
-        unsigned old;
-        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(old) : "l"(ccnt + blk) : "memory");
-        last = old == static_cast<unsigned>(n_act) - 1u;
-      }
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      // every active expert's y of columns [64 blk, 64 blk + 64) is final: the fixed-order combine
-      // out[t, n] = sum_j w[t, j] * y[slot_pos[t*k + j], n] + y[S + t, n], lane l: n = 64 blk + 2 l, + 1
+  }
+
+  // ------------------------------------------------------------ phase C: reduce + combine
+  // every CTA's partials are published by its arrival on the launch's counter (release), and
+  // the reduction starts once all CTAs have arrived (acquire)
+  named_sync(1, kDkCThreads);
+  if (threadIdx.x == 0) {
+    if (ok) {
       __threadfence();
-      const int n = blk * kFdDnRows + 2 * lane;
-#pragma unroll 4
-      for (int t = 0; t < T; ++t) {
-        float ax = 0.0f, ay = 0.0f;
-        for (int j = 0; j < k; ++j) {
-          const float wj = sm->w[t * k + j];
-          const float2 yv = __ldcg(reinterpret_cast<const float2*>(a.y + static_cast<int64_t>(sm->slot_pos[t * k + j]) * H + n));
-          ax = fmaf(wj, yv.x, ax);
-          ay = fmaf(wj, yv.y, ay);
-        }
-        if (a.has_shared) {
-          const float2 yv = __ldcg(reinterpret_cast<const float2*>(a.y + static_cast<int64_t>(S + t) * H + n));
-          ax += yv.x;
-          ay += yv.y;
-        }
-        if (a.out_is_fp32) {
-          *reinterpret_cast<float2*>(static_cast<float*>(a.out) + t * H + n) = make_float2(ax, ay);
-        } else {
-          *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(a.out) + t * H + n) =
-              static_cast<uint32_t>(f32_to_bf16_bits(ax)) | (static_cast<uint32_t>(f32_to_bf16_bits(ay)) << 16);
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(done) : "memory");
+      const uint64_t t0 = now_ns();
+      for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(done) : "memory");
+        if (v >= gridDim.x) break;
+        if ((i & 63u) == 63u && now_ns() - t0 > kFdTimeoutNs) {
+          report_device_error(a.status, kDevTimeout);
+          sm->abort_flag = 1;
+          break;
         }
       }
+    } else {
+      sm->abort_flag = 1;
     }
+  }
+  named_sync(1, kDkCThreads);
+  if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return;
+  // column blocks of 16: task (t, j', c4) sums the slice partials of output t's expert j'
+  // (j' = k is the shared expert) over 4 columns into SMEM, then (t, c4) combines in order
+  const int J = k + a.has_shared;
+  float4* red2 = reinterpret_cast<float4*>(ring);   // [T][J][4]
+  for (int b = blockIdx.x; b < H / kRedCols; b += gridDim.x) {
+    const int col0 = b * kRedCols;
+    for (int task = threadIdx.x; task < T * J * 4; task += kDkCThreads) {
+      const int c4 = task & 3, tj = task >> 2, t = tj / J, j = tj % J;
+      const int row = (j < k) ? sm->slot_pos[t * k + j] : S + t;
+      const float* src = a.yp + static_cast<int64_t>(row) * H + col0 + 4 * c4;
+      float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int m = 0; m < nslice; ++m) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(m) * (S + T) * H));
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
+      red2[tj * 4 + c4] = s;
+    }
+    named_sync(1, kDkCThreads);
+    for (int task = threadIdx.x; task < T * 4; task += kDkCThreads) {
+      const int t = task >> 2, c4 = task & 3;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int j = 0; j < k; ++j) {
+        const float wj = sm->w[t * k + j];
+        const float4 v = red2[(t * J + j) * 4 + c4];
+        acc.x = fmaf(wj, v.x, acc.x);
+        acc.y = fmaf(wj, v.y, acc.y);
+        acc.z = fmaf(wj, v.z, acc.z);
+        acc.w = fmaf(wj, v.w, acc.w);
+      }
+      if (a.has_shared) {
+        const float4 v = red2[(t * J + k) * 4 + c4];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      const int64_t o = static_cast<int64_t>(t) * H + col0 + 4 * c4;
+      if (a.out_is_fp32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = acc;
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + o) =
+            make_uint2(static_cast<uint32_t>(f32_to_bf16_bits(acc.x)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.y)) << 16),
+                       static_cast<uint32_t>(f32_to_bf16_bits(acc.z)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.w)) << 16));
+      }
+    }
+    named_sync(1, kDkCThreads);
   }
 }
 
 struct FdPlan {
-  int x_pitch, x_bytes, smem_off, sh_off, ring_off, ring_bytes, n_slots_worst;
+  int x_pitch, x_bytes, ctl_off, ring_off, n_slots, dn_rows;
   size_t smem_total;
 };
 
@@ -804,18 +704,14 @@ bool fd_plan(const moe_shape_t& s, FdPlan* p) {
   if (s.T < 1 || s.T > kFdMaxT || s.H % 512 || s.H > 4096 || s.I % 256 || s.I > 1024) return false;
   p->x_pitch = 2 * s.H + 64;   // the 64 extra bytes put the 8 rows of an MMA's B loads in distinct banks
   p->x_bytes = ((s.T * p->x_pitch + 127) / 128) * 128;
-  p->smem_off = p->x_bytes;
-  p->sh_off = ((p->smem_off + static_cast<int>(sizeof(FdSmem)) + 127) / 128) * 128;
-  const int sh_bytes = s.has_shared ? s.T * s.I * 2 : 0;   // the shared expert's h rows
-  p->ring_off = ((p->sh_off + sh_bytes + 1023) / 1024) * 1024;
-  p->ring_bytes = kFdSmemLimit - 1024 - p->ring_off;
-  const int w_b = std::max(2 * kFdGuPairs * (s.H / 2), kFdDnRows * (s.I / 2));
-  const int sc_b = std::max(2 * kFdGuPairs * (s.H / 16), kFdDnRows * (s.I / 16));
-  // the kernel sizes its slots after routing; at worst a routed expert holds all T rows
-  const int worst = ((w_b + sc_b + s.T * s.I * 2 + 1023) / 1024) * 1024;
-  p->n_slots_worst = std::min(kFdMaxSlots, p->ring_bytes / worst);
-  p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->ring_bytes);
-  return p->n_slots_worst >= 3;
+  p->ctl_off = p->x_bytes;
+  p->ring_off = ((p->ctl_off + static_cast<int>(sizeof(FdSmem)) + 1023) / 1024) * 1024;
+  p->n_slots = std::min(kDkMaxSlots, (kFdSmemLimit - 1024 - p->ring_off) / kSlotBytes);
+  p->dn_rows = (s.H % 1024 == 0) ? 1024 : 512;   // down chunk: 32 KB (16 KB when H is an odd multiple of 512)
+  p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * kSlotBytes;
+  // the reduction's [T][k + 1][4] float4 fit in the ring
+  const size_t red_bytes = static_cast<size_t>(s.T) * (s.k + 1) * 4 * 16;
+  return p->n_slots >= 3 && red_bytes <= static_cast<size_t>(p->n_slots) * kSlotBytes;
 }
 
 template <int EPL>
@@ -825,13 +721,12 @@ cudaError_t launch_fd(const FdMaps& maps, const FdArgs& args, const FdPlan& plan
   if (e != cudaSuccess) return e;
   int n_sm = 0, per_sm = 0;
   if ((e = current_sm_count(&n_sm)) != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFdThreads, plan.smem_total);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDkThreads, plan.smem_total);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-  if (n_sm < args.H / kFdDnRows) return cudaErrorInvalidValue;   // one shared-expert down unit per CTA at most
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_sm);
-  cfg.blockDim = dim3(kFdThreads);
+  cfg.blockDim = dim3(kDkThreads);
   cfg.dynamicSmemBytes = plan.smem_total;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -854,6 +749,12 @@ bool decode_fused_supported(const moe_shape_t& s) {
   return fd_plan(s, &p);
 }
 
+size_t fd_partial_bytes(const moe_shape_t& s) {
+  if (!decode_fused_supported(s)) return 0;
+  const size_t R = static_cast<size_t>(s.T) * s.k + s.T;
+  return static_cast<size_t>(s.I / kFdSlice) * R * s.H * sizeof(float);
+}
+
 cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   const moe_shape_t& s = d.shape;
   FdPlan plan;
@@ -861,10 +762,7 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   FdArgs a;
   a.x = d.x;
   a.logits = d.logits;
-  a.gu_packed = d.gate_up.packed;
-  a.gu_scales = d.gate_up.scales;
   a.gu_scale2 = d.gate_up.scale2;
-  a.dn_packed = d.down.packed;
   a.dn_scales = d.down.scales;
   a.dn_scale2 = d.down.scale2;
   a.T = s.T;
@@ -879,34 +777,37 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   a.offsets = d.offsets;
   a.sorted_slot = d.sorted_slot;
   a.slot_pos = d.slot_pos;
-  a.h = d.h;
-  a.y = d.y;
+  a.yp = d.yp;
   a.out = d.out;
   a.out_is_fp32 = d.out_is_fp32;
-  a.grid_ctr = reinterpret_cast<unsigned long long*>(d.grid_bar);
-  a.ccnt = d.sync;
+  a.grid_ctr = d.grid_ctr;
+  a.done = d.sync;
   a.status = d.status;
   a.x_pitch = plan.x_pitch;
-  a.smem_off = plan.smem_off;
+  a.ctl_off = plan.ctl_off;
   a.ring_off = plan.ring_off;
-  a.sh_off = plan.sh_off;
-  a.ring_bytes = plan.ring_bytes;
+  a.n_slots = plan.n_slots;
+  a.dn_rows = plan.dn_rows;
   FdMaps maps;
-  const uint64_t gu_dims[4] = {128, static_cast<uint64_t>(d.gate_up.G) * 2 * s.I, 2, static_cast<uint64_t>(s.H) / 256};
-  const uint64_t gu_strides[3] = {static_cast<uint64_t>(s.H) / 2, static_cast<uint64_t>(s.I) * (s.H / 2), 128};
-  const uint32_t gu_box[4] = {128, kFdGuPairs, 2, static_cast<uint32_t>(s.H) / 256};
-  const uint64_t dn_dims[3] = {128, static_cast<uint64_t>(d.down.G) * s.H, static_cast<uint64_t>(s.I) / 256};
-  const uint64_t dn_strides[2] = {static_cast<uint64_t>(s.I) / 2, 128};
-  const uint32_t dn_box[3] = {128, kFdDnRows, static_cast<uint32_t>(s.I) / 256};
-  const uint64_t gus_dims[3] = {static_cast<uint64_t>(s.H) / 16, static_cast<uint64_t>(d.gate_up.G) * 2 * s.I, 2};
-  const uint64_t gus_strides[2] = {static_cast<uint64_t>(s.H) / 16, static_cast<uint64_t>(s.I) * (s.H / 16)};
-  const uint32_t gus_box[3] = {static_cast<uint32_t>(s.H) / 16, kFdGuPairs, 2};
+  const uint64_t G = static_cast<uint64_t>(d.gate_up.G);
+  const uint64_t H = static_cast<uint64_t>(s.H), I = static_cast<uint64_t>(s.I);
+  // gate_up packed {128 B, rows, half, line}; rows stop I early so an up box stays inside
+  const uint64_t gu_dims[4] = {128, G * 2 * I - I, 2, H / 256};
+  const uint64_t gu_strides[3] = {H / 2, I * (H / 2), 128};
+  const uint32_t gu_box[4] = {128, static_cast<uint32_t>(kIs), 2, 2};
+  const uint64_t gus_dims[3] = {H / 16, G * 2 * I - I, 2};
+  const uint64_t gus_strides[2] = {H / 16, I * (H / 16)};
+  const uint32_t gus_box[3] = {32, static_cast<uint32_t>(kIs), 2};
+  // down packed {I/2 B, row in a block of 256, block}
+  const uint64_t dn_dims[3] = {I / 2, 256, static_cast<uint64_t>(d.down.G) * H / 256};
+  const uint64_t dn_strides[2] = {I / 2, 256 * (I / 2)};
+  const uint32_t dn_box[3] = {static_cast<uint32_t>(kIs / 2), 256, static_cast<uint32_t>(plan.dn_rows / 256)};
   if (!make_tensor_map(&maps.gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, d.gate_up.packed, gu_dims, gu_strides, gu_box,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map(&maps.gus, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.gate_up.scales, gus_dims, gus_strides,
                        gus_box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_tensor_map(&maps.dn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.down.packed, dn_dims, dn_strides, dn_box,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
+                       CU_TENSOR_MAP_SWIZZLE_32B))
     return cudaErrorInvalidValue;
   if (s.E <= 256) return launch_fd<8>(maps, a, plan, st);
   if (s.E <= 512) return launch_fd<16>(maps, a, plan, st);

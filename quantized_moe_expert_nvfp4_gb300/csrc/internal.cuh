@@ -19,19 +19,17 @@ constexpr int kSimtTileRows = 64;      // rows per work item of the SIMT grouped
 constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutation
 constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 grouped GEMM
 constexpr int kFdMaxT = 8;             // the fused single-launch decode kernel handles T <= 8
-constexpr int kFdMaxBlocks = 64;       // 64-column output blocks of the one-launch decode kernel
-constexpr int kFdMaxActive = kFdMaxT * kMaxK + 1;   // active groups of one decode launch
-// its sync words, two sets alternating between launches: an arrival counter per output block,
-// then a readiness counter per active group (gate_up units done)
-constexpr int kFdSyncWords = 2 * (kFdMaxBlocks + kFdMaxActive);
+constexpr int kFdSlice = 64;           // intermediate columns of one work unit of that kernel
+// its sync words: two units-done counters, one per launch parity (each launch zeroes the other)
+constexpr int kFdSyncWords = 64;
 
 // ------------------------------------------------------------------ workspace layout
 // All offsets are in bytes from the workspace base and 256-byte aligned.
 struct WsLayout {
   size_t status;       // int32 device status word (+ padding)
   size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] 64-bit launch count
-  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: block arrival and group
-                       // readiness counters, two sets (each launch zeroes the next launch's set)
+  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: its two units-done
+                       // counters (each launch zeroes the next launch's)
   size_t ids;          // int32 [S]
   size_t w;            // fp32  [S]
   size_t counts;       // int32 [E]
@@ -46,6 +44,7 @@ struct WsLayout {
   size_t xe;           // fp32  [S + T]    2^e of each row of xf
   size_t hf;           // f16   [S + T, I]  tensor-core arm: scaled copy of h, and its row exponents
   size_t he;           // fp32  [S + T]    2^e of each row of hf
+  size_t yp;           // fp32  [I/64][S + T][H] one-launch decode arm: partial expert outputs
   size_t total;
   int64_t max_tiles;
   int64_t n_chunks;
@@ -195,15 +194,16 @@ struct DecodeFusedArgs {
   int32_t* offsets;
   int32_t* sorted_slot;
   int32_t* slot_pos;
-  uint16_t* h;
-  unsigned* sync;     // [kFdSyncWords] arrival and readiness counters (the kernel zeroes them itself)
-  float* y;
+  float* yp;                        // [I/64][S + T][H] partial expert outputs (fd_partial_bytes)
+  unsigned* sync;                   // [kFdSyncWords] its counters (the kernel zeroes them itself)
   void* out;
   int out_is_fp32;
-  unsigned* grid_bar;
+  unsigned long long* grid_ctr;     // 64-bit launch count (zero in a new workspace)
   int32_t* status;
 };
 bool decode_fused_supported(const moe_shape_t& s);
+// Bytes of partial expert outputs the one-launch decode kernel needs (0 if unsupported).
+size_t fd_partial_bytes(const moe_shape_t& s);
 // One warp running the decode kernel's bounded wait on a barrier nothing arrives at (test hook).
 cudaError_t launch_fd_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st);

@@ -90,3 +90,41 @@ def test_arm_selection_on_the_host(lib):
     assert arm(T=9) == 2 and arm(T=64) == 2 and arm(T=65) == 2 and arm(T=4096) == 2
     assert arm(T=65, I=128) == 3
     assert arm(H=100) == -1
+
+
+def test_static_scratch_rejects_shapes_that_do_not_fit(lib):
+    """The no-allocation entry point's size rule, on the host only: a one-launch decode shape
+    whose scratch (dominated by the partial expert outputs, (I/64) * T * (k+1) * H * 4 bytes)
+    exceeds the 16 MiB array is rejected with MOE_ERR_UNSUPPORTED_SHAPE before any CUDA call; a
+    shape that fits passes the size check (and then fails here only for want of a device).
+    Skipped where a GPU is visible: fake pointers must never reach a launch."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check; needs a machine without a GPU")
+    moe, L = lib
+    fn = L.moe_forward_decode_static_scratch
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(moe.MoeWeights),
+                   ctypes.POINTER(moe.MoeWeights), ctypes.POINTER(moe.MoeShape), ctypes.c_void_p,
+                   ctypes.c_int32, ctypes.c_void_p]
+    fn.restype = ctypes.c_int32
+    limit, small = 16 << 20, 64 << 10
+    seen = {"fit": 0, "reject": 0}
+    for T in (1, 3, 8):
+        for H in (512, 2048, 4096):
+            for I in (256, 512, 1024):
+                for k in (1, 10, 16):
+                    E = 64
+                    sh = moe.Shape(T=T, H=H, I=I, E=E, k=k, has_shared=1)
+                    assert moe.forward_arm(sh) == 0
+                    gu = moe.MoeWeights(0x200000, 0x300000, 0x400000, E + 1, 2 * I, H)
+                    dn = moe.MoeWeights(0x200000, 0x300000, 0x400000, E + 1, H, I)
+                    st = fn(0x100000, 0x100000, ctypes.byref(gu), ctypes.byref(dn), ctypes.byref(sh.c()),
+                            0x100000, 0, None)
+                    partial = (I // 64) * T * (k + 1) * H * 4
+                    if partial > limit:
+                        assert st == -2, (T, H, I, k, st)
+                        seen["reject"] += 1
+                    elif partial + small <= limit:
+                        assert st != -2, (T, H, I, k, st)
+                        seen["fit"] += 1
+    assert seen["fit"] > 10 and seen["reject"] >= 4
