@@ -59,6 +59,7 @@ def _declare(L):
     L.orc_e4m3_encode.argtypes, L.orc_e4m3_encode.restype = [F], I32
     L.orc_quantize.argtypes, L.orc_quantize.restype = [P, I64, I64, I64, P, P, P], I32
     L.orc_dequantize.argtypes, L.orc_dequantize.restype = [P, P, P, I64, I64, I64, P], I32
+    L.orc_router_logits.argtypes, L.orc_router_logits.restype = [P, P, P, P, I32, I32, I32, P], I32
     L.orc_route.argtypes, L.orc_route.restype = [P, I32, I32, I32, P, P], I32
     L.orc_permute.argtypes, L.orc_permute.restype = [P, I32, I32, I32, P, P, P, P], I32
     L.orc_moe_forward.argtypes = [P] * 8 + [I32] * 6 + [P, I32, P, P, P, I32]
@@ -127,6 +128,18 @@ def dequantize(packed, scales, scale2) -> np.ndarray:
     out = np.empty((G, N, 2 * K2), np.float64)
     _check(lib().orc_dequantize(_ptr(packed), _ptr(scales), _ptr(scale2), G, N, 2 * K2, _ptr(out)),
            "dequantize")
+    return out
+
+
+def router_logits(x, router) -> np.ndarray:
+    """fp64 [T, E] router logits of bf16 x [T, H] against one NVFP4 projection
+    router = (packed [1, E, H/2] or [E, H/2], scales [.., E, H/16], scale2 [1])."""
+    xb = _np(x, np.uint16)
+    p, s_, z = _np(router[0], np.uint8), _np(router[1], np.uint8), _np(router[2], np.float32)
+    T, H = xb.shape
+    E = p.shape[-2]
+    out = np.empty((T, E), np.float64)
+    _check(lib().orc_router_logits(_ptr(xb), _ptr(p), _ptr(s_), _ptr(z), T, H, E, _ptr(out)), "router_logits")
     return out
 
 

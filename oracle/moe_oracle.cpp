@@ -188,6 +188,26 @@ int orc_dequantize(const uint8_t* packed, const uint8_t* scales, const float* sc
   return 0;
 }
 
+// Router GEMM: logit[t, e] = sum_h x[t, h] * w[e, h] in fp64, w dequantized exactly (one group of E
+// rows), each row's products summed in h order.
+int orc_router_logits(const uint16_t* x, const uint8_t* packed, const uint8_t* scales, const float* scale2,
+                      int T, int H, int E, double* logits) {
+  if (!x || !packed || !scales || !scale2 || !logits || T < 0 || H <= 0 || H % 16 || E <= 0) return -1;
+  std::vector<double> w(static_cast<size_t>(E) * H);
+  dequant_matrix(packed, scales, scale2[0], E, H, w.data());
+  std::vector<double> xv(H);
+  for (int t = 0; t < T; ++t) {
+    for (int c = 0; c < H; ++c) xv[c] = bf16_value(x[static_cast<int64_t>(t) * H + c]);
+    for (int e = 0; e < E; ++e) {
+      double s = 0.0;
+      const double* we = &w[static_cast<size_t>(e) * H];
+      for (int c = 0; c < H; ++c) s += we[c] * xv[c];
+      logits[static_cast<int64_t>(t) * E + e] = s;
+    }
+  }
+  return 0;
+}
+
 // Routing: softmax over all E logits, top-k by (logit descending, index ascending) with NaN
 // counted as -inf, then the k probabilities renormalised to sum to 1.  Selection is made on
 // the logits themselves (softmax is monotone).  Where the softmax has no value (every logit

@@ -43,6 +43,14 @@ int orc_quantize(const float* w, int64_t G, int64_t N, int64_t K,
 int orc_dequantize(const uint8_t* packed, const uint8_t* scales, const float* scale2,
                    int64_t G, int64_t N, int64_t K, double* out);
 
+/* --- router GEMM: logits fp64 [T, E] = x (bf16 bit patterns [T, H]) . deq(W_r)^T, with the
+ *     router weights one NVFP4 projection (packed [E, H/2], scales [E, H/16], scale2 [1]), the
+ *     layout of the experts' weights.  The "long-context cold prefill" issue of the Atlas project
+ *     counts the router GEMM among the MoE's logit-changing operations, and its nsys table times
+ *     the router as a W4A16 GEMM.  H % 16 == 0. --- */
+int orc_router_logits(const uint16_t* x, const uint8_t* packed, const uint8_t* scales, const float* scale2,
+                      int T, int H, int E, double* logits);
+
 /* --- routing: logits fp32 [T, E] -> ids int32 [T, k] (rank order), w fp64 [T, k] --- */
 int orc_route(const float* logits, int T, int E, int k, int32_t* ids, double* w);
 

@@ -410,3 +410,50 @@ def test_layer_invariants():
     # a token subset gives the same rows as the full evaluation, and threading does not matter
     sub = oracle.moe_forward(x, logits, gu, d, shape.k, tokens=[4, 1], n_threads=1)
     np.testing.assert_array_equal(sub, base[[4, 1]])
+
+
+# ----------------------------------------------------------------------------- router GEMM
+
+def _golden_case(tag):
+    for line in open(os.path.join(os.path.dirname(__file__), "golden", "hand_layer.txt")):
+        if line.startswith(tag + " "):
+            return dict(kv.split("=") for kv in line.split()[1:])
+    raise KeyError(tag)
+
+
+def test_router_constant_rows_closed_form():
+    g = _golden_case("caseR1")
+    H, E = int(g["H"]), int(g["E"])
+    x = torch.tensor([[c / 16 for c in range(H)]], dtype=torch.bfloat16)
+    p, sc, _ = _const_weights([[(1, 1.0), (1, -0.5), (1, 6.0)]], E, H)
+    logits = oracle.router_logits(x, (p, sc, np.array([0.25], np.float32)))
+    want = [float(g["l0"]), float(g["l1"]), float(g["l2"])]
+    np.testing.assert_array_equal(logits[0], want)
+
+
+def test_router_single_weights_pin_row_column_nibble_and_scale():
+    g = _golden_case("caseR2")
+    H, E, c0, c1 = int(g["H"]), int(g["E"]), int(g["c0"]), int(g["c1"])
+    x = synth.activations(3, H, seed=31)
+    xv = x.float().double().numpy()
+    p = np.zeros((E, H // 2), np.uint8)
+    sc = np.full((E, H // 16), 0x38, np.uint8)
+    p[0, c0 // 2] = 3 << 4           # 1.5 in the high nibble (odd column)
+    sc[0, c0 // 16] = 0x40           # that block's scale 2.0
+    p[1, c1 // 2] = 14               # -4.0 in the low nibble (even column)
+    logits = oracle.router_logits(x, (p, sc, np.ones(1, np.float32)))
+    np.testing.assert_array_equal(logits[:, 0], 3.0 * xv[:, c0])
+    np.testing.assert_array_equal(logits[:, 1], -4.0 * xv[:, c1])
+
+
+def test_router_is_linear_in_scale2_and_permutes_with_rows():
+    H, E, T = 64, 8, 5
+    x = synth.activations(T, H, seed=32)
+    w = synth.expert_weight(E, H, seed=33, layer=0, group=0, proj="gate_up")
+    p, sc, s2 = oracle.quantize(w.numpy()[None])
+    a = oracle.router_logits(x, (p[0], sc[0], s2))
+    b = oracle.router_logits(x, (p[0], sc[0], 2 * s2))
+    np.testing.assert_array_equal(b, 2 * a)
+    perm = np.array([3, 0, 7, 1, 6, 2, 5, 4])
+    c = oracle.router_logits(x, (p[0][perm], sc[0][perm], s2))
+    np.testing.assert_array_equal(c, a[:, perm])
