@@ -451,6 +451,45 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
         layer = {"achieved": layer_ach, "unit": "TFLOP/s", "frac": layer_ach / roofline["peak"],
                  "algorithmic_flops_per_step": acc["fwd_flops"] / steps}
 
+    # the layer from x alone: the router GEMM (NVFP4 router weights) in front of the same layer,
+    # timed the same way, and the router GEMM by itself
+    for L in layers:
+        L["rw"] = moe.quantize_nvfp4(synth.router_weights(w.shape(L["T"]), 17, device=device))
+        L["rlog"] = torch.empty(L["T"], E, dtype=torch.float32, device=device)
+    rgraphs, rogs = [], []
+    for p in range(pool):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for L in layers:
+                moe.forward_routed(L["xs"][p], L["rw"], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+        rgraphs.append(g)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for L in layers:
+                moe.router_logits(L["xs"][p], L["rw"], L["ms"], L["ws"], logits=L["rlog"])
+        rogs.append(g)
+    with torch.cuda.stream(stream):
+        for gs in (rgraphs, rogs):
+            for p in range(pool):
+                gs[p].replay()
+        stream.synchronize()
+        r0, r1, r2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        r0.record(stream)
+        for i in range(steps):
+            rgraphs[i % pool].replay()
+        r1.record(stream)
+        for i in range(steps):
+            rogs[i % pool].replay()
+        r2.record(stream)
+        r2.synchronize()
+    routed_ms = slowest_rank_ms(r0.elapsed_time(r1), dist, device) / steps
+    router_ms = slowest_rank_ms(r1.elapsed_time(r2), dist, device) / steps
+    with_router = {"value": replica_throughput(world, 1, tokens_per_step, routed_ms), "unit": UNIT,
+                   "ms_per_step": routed_ms, "router_us_per_layer": 1e3 * router_ms / len(layers),
+                   "what": "moe_forward_routed: logits = x . deq(W_r)^T (NVFP4 router, E x H) computed in front of "
+                           "the same layer, timed like the headline steps; router_us_per_layer: the router GEMM alone"}
+    del rgraphs, rogs
+
     # end to end through host buffers: H2D of x and logits from pinned memory, the C-ABI call,
     # D2H of the output, every step.
     e2e_steps = min(steps, 200)
@@ -488,6 +527,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
                    else ["route+permute", "gate_up", "down", "combine"])
     res = {"value": value, "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
            "config": describe(name), "roofline": roofline, "layer_roofline": layer, "e2e": e2e,
+           "with_router": with_router,
            "gpu_launches": steps * launches, "clocks": clk.summary(),
            "arm": sorted({moe.ARM_NAMES[a] for a in arms}),
            "method": {"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh input "
@@ -550,7 +590,7 @@ def run_ours(args):
                 "config": main["config"], "roofline": main["roofline"], "e2e": main["e2e"],
                 "gpu_launches": main["gpu_launches"], "clocks": main["clocks"],
                 "parallelism": f"replicas x{world}"}
-        for key in ("cpu_baseline", "layer_roofline", "arm", "method", "stages_us_per_forward",
+        for key in ("cpu_baseline", "layer_roofline", "with_router", "arm", "method", "stages_us_per_forward",
                     "distinct_experts_mean"):
             if key in main:
                 line[key] = main[key]

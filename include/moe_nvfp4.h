@@ -156,6 +156,24 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                                   void* out, int out_is_fp32, void* ws, size_t ws_bytes,
                                   void* stream, void* const* stage_events);
 
+/* Router GEMM in front of the top-k (the issue's list of logit-changing operations includes the
+ * router GEMM; its nsys table times the router as a W4A16 GEMM):
+ *   logits[t, e] = scale2 * (x[t] . deq(W_r[e])), accumulated in fp32, written fp32 [T, E].
+ *   router: one NVFP4 projection of the experts' layout with G = 1, N = E rows, K = H.
+ * Batches above 8 tokens with E % 128 == 0 and H % 256 == 0 run on the tcgen05 grouped GEMM
+ * (x converted to f16 rows scaled by a power of two, as in that arm); other shapes on a CUDA-core
+ * kernel.  ws as for moe_forward (its size covers this call). */
+moe_status_t moe_router_logits(const uint16_t* x, const moe_nvfp4_weights_t* router, const moe_shape_t* shape,
+                               float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_router_logits into the workspace, then moe_forward on those logits: the layer from x
+ * alone.  Same numerics and arms as moe_forward; the routing decisions are taken on the fp32
+ * logits the router GEMM produced. */
+moe_status_t moe_forward_routed(const uint16_t* x, const moe_nvfp4_weights_t* router,
+                                const moe_nvfp4_weights_t* gate_up, const moe_nvfp4_weights_t* down,
+                                const moe_shape_t* shape, void* out, int out_is_fp32, void* ws, size_t ws_bytes,
+                                void* stream);
+
 /* The one-launch decode forward (moe_forward_arm == 0 shapes: T <= 8, H % 512 == 0, H <= 4096,
  * I % 256 == 0, I <= 1024) for callers that cannot allocate device memory -- code running where
  * cudaMalloc is not allowed or not available, such as inside a framework's memory-planning phase,

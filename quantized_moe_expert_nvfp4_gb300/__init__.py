@@ -81,6 +81,8 @@ def _declare(L):
         "moe_get_device_status": ([P, ctypes.POINTER(I32), P], I32),
         "moe_status_string": ([I32], ctypes.c_char_p),
         "moe_forward_arm": ([SH], I32),
+        "moe_router_logits": ([P, W, SH, P, P, SZ, P], I32),
+        "moe_forward_routed": ([P, W, W, W, SH, P, I32, P, SZ, P], I32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -243,6 +245,27 @@ def forward_profiled(x, logits, gate_up: NVFP4Weights, down: NVFP4Weights, shape
     return out
 
 
+def router_logits(x, router: NVFP4Weights, shape: Shape, ws, logits=None, stream=None):
+    """fp32 [T, E] router logits of bf16 x against one NVFP4 projection (G = 1, N = E, K = H)."""
+    logits = logits if logits is not None else torch.empty(shape.T, shape.E, dtype=torch.float32, device=x.device)
+    _check("moe_router_logits", load().moe_router_logits(
+        _ptr(x, torch.bfloat16, "x"), ctypes.byref(router.c()), ctypes.byref(shape.c()),
+        _ptr(logits, torch.float32, "logits"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return logits
+
+
+def forward_routed(x, router: NVFP4Weights, gate_up: NVFP4Weights, down: NVFP4Weights, shape: Shape, ws,
+                   out=None, out_fp32: bool = False, stream=None):
+    """The layer from x alone: router GEMM, then forward() on its logits."""
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    out = out if out is not None else torch.empty(shape.T, shape.H, dtype=dt, device=x.device)
+    _check("moe_forward_routed", load().moe_forward_routed(
+        _ptr(x, torch.bfloat16, "x"), ctypes.byref(router.c()), ctypes.byref(gate_up.c()),
+        ctypes.byref(down.c()), ctypes.byref(shape.c()), _ptr(out, dt, "out"), int(out_fp32),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return out
+
+
 def device_status(ws: torch.Tensor, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("moe_get_device_status", load().moe_get_device_status(
@@ -276,4 +299,4 @@ def status_string(status: int) -> str:
 
 __all__ = ["Shape", "NVFP4Weights", "MoeError", "load", "workspace_size", "workspace",
            "quantize_nvfp4", "route_topk", "permute", "grouped_gate_up", "grouped_down", "combine",
-           "forward", "forward_profiled", "forward_arm", "ARM_NAMES", "device_status", "status_string", "DECODE_MAX_T", "LIB_PATH"]
+           "forward", "forward_profiled", "forward_arm", "router_logits", "forward_routed", "ARM_NAMES", "device_status", "status_string", "DECODE_MAX_T", "LIB_PATH"]

@@ -93,6 +93,9 @@ struct Ws {
   float* xe;
   uint16_t* hf;
   float* he;
+  uint16_t* rxf;
+  float* rxe;
+  float* rlogits;
   WsLayout L;
 };
 
@@ -116,6 +119,9 @@ Ws carve(void* ws, const moe_shape_t& s) {
   r.xe = reinterpret_cast<float*>(b + r.L.xe);
   r.hf = reinterpret_cast<uint16_t*>(b + r.L.hf);
   r.he = reinterpret_cast<float*>(b + r.L.he);
+  r.rxf = reinterpret_cast<uint16_t*>(b + r.L.rxf);
+  r.rxe = reinterpret_cast<float*>(b + r.L.rxe);
+  r.rlogits = reinterpret_cast<float*>(b + r.L.rlogits);
   return r;
 }
 
@@ -191,6 +197,16 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   return a;
 }
 
+// The router GEMM runs on the tcgen05 grouped GEMM (one group of E weight rows) for batches
+// above the decode sizes when E and H fit its tiles, else on the CUDA-core kernel.
+bool router_on_tc(const moe_shape_t& s) { return s.T > kFdMaxT && s.E % 128 == 0 && s.H % 256 == 0; }
+
+moe_status_t check_router(const moe_nvfp4_weights_t* r, const moe_shape_t& s) {
+  if (!r || !aligned16(r->packed) || !aligned16(r->scales) || !aligned16(r->scale2)) return MOE_ERR_INVALID_ARG;
+  if (r->G != 1 || r->N != s.E || r->K != s.H) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
 }  // namespace
 
 // Work items of a shape: sum_e ceil(c_e / R) <= S / R + (number of non-empty experts), and the
@@ -223,20 +239,63 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.slot_pos = take(4 * S);
   L.max_tiles = std::max(max_tiles_for(s, kSimtTileRows), max_tiles_for(s, kDecodeMaxT));
   L.tiles = take(16 * static_cast<size_t>(L.max_tiles));
-  L.n_chunks = (S + kScatterChunk - 1) / kScatterChunk;
-  L.hist = take(4 * static_cast<size_t>(std::max<int64_t>(1, L.n_chunks)) * s.E);
-  L.h = take(2 * static_cast<size_t>(R) * s.I);
-  L.y = take(4 * static_cast<size_t>(R) * s.H);
+  L.hist = take(4 * static_cast<size_t>(kPermuteMaxGrid) * s.E);
+  // moe_forward's intermediates, by arm: h for arms 1-3, fp32 y for arms 2-3, the f16 operands
+  // for arm 2, the partial outputs for arm 0
+  const int arm = forward_arm(s);
+  L.h = take(arm != 0 ? 2 * static_cast<size_t>(R) * s.I : 0);
+  L.y = take(arm >= 2 ? 4 * static_cast<size_t>(R) * s.H : 0);
   const size_t tc_rows = arm_for(s) == Arm::kTc ? static_cast<size_t>(R) : 0;   // tensor-core arm only
   L.xf = take(2 * tc_rows * s.H);
   L.xe = take(4 * tc_rows);
   L.hf = take(2 * tc_rows * s.I);
   L.he = take(4 * tc_rows);
-  L.yp = take(s.T <= kFdMaxT ? fd_partial_bytes(s) : 0);
+  L.yp = take(arm == 0 ? fd_partial_bytes(s) : 0);
+  // the router GEMM (moe_router_logits, moe_forward_routed)
+  L.rxf = take(router_on_tc(s) ? 2 * static_cast<size_t>(s.T) * s.H : 0);
+  L.rxe = take(router_on_tc(s) ? 4 * static_cast<size_t>(s.T) : 0);
+  L.rlogits = take(4 * static_cast<size_t>(s.T) * s.E);
   L.total = off;
   return L;
 }
 
+}  // namespace moe
+
+namespace moe {
+namespace {
+
+// logits [T, E] of the router; ws is a checked workspace of the shape.
+cudaError_t launch_router(const uint16_t* x, const moe_nvfp4_weights_t& r, const moe_shape_t& s, float* logits,
+                          const Ws& w, cudaStream_t cs) {
+  if (!router_on_tc(s)) return launch_router_simt(x, r, s.T, s.H, s.E, logits, cs);
+  // one group of E weight rows against the T rows of x, f16 operands (x scaled per row)
+  uint16_t* xf = w.rxf;
+  float* xe = w.rxe;
+  cudaError_t e = launch_act_to_f16(x, xf, xe, s.T, s.H, cs);
+  if (e == cudaSuccess) e = launch_dense_tiles(s.T, kTcTileRows, w.tiles, w.meta, cs);
+  if (e != cudaSuccess) return e;
+  GroupedArgs a;
+  a.packed = r.packed;
+  a.scales = r.scales;
+  a.scale2 = r.scale2;
+  a.N = s.E;
+  a.K = s.H;
+  a.act = xf;
+  a.sorted_slot = nullptr;
+  a.T = s.T;
+  a.k = 0;
+  a.S = 0;
+  a.E = 0;   // one group
+  a.tiles = w.tiles;
+  a.meta = w.meta;
+  a.max_tiles = (s.T + kTcTileRows - 1) / kTcTileRows;
+  a.out = logits;
+  a.status = w.status;
+  a.act_factor = xe;
+  return launch_down_tc(a, cs);
+}
+
+}  // namespace
 }  // namespace moe
 
 using namespace moe;
@@ -281,8 +340,9 @@ moe_status_t moe_permute(const int32_t* topk_ids, const moe_shape_t* shape, int3
     return cuda_status(launch_route_permute_small(nullptr, topk_ids, s.T, s.E, s.k, s.has_shared,
                                                   nullptr, nullptr, counts, offsets, sorted_slot,
                                                   slot_pos, w.tiles, w.meta, kDecodeMaxT, cs));
-  return cuda_status(launch_permute_large(topk_ids, s.T, s.E, s.k, counts, offsets, sorted_slot,
-                                          slot_pos, w.hist, w.L.n_chunks, cs));
+  return cuda_status(launch_route_permute_large(nullptr, topk_ids, s.T, s.E, s.k, s.has_shared, nullptr,
+                                                nullptr, counts, offsets, sorted_slot, slot_pos, w.hist,
+                                                w.tiles, w.meta, tile_rows_for(s), w.status, cs));
 }
 
 moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
@@ -434,17 +494,10 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     if (e == cudaSuccess) e = mark(4);
     return cuda_status(e);
   }
-  // grouped-GEMM arms: routing, then permutation and work list (one CTA for a small batch)
-  e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, cs);
-  if (e == cudaSuccess && s.T <= kDecodeMaxT)
-    e = launch_route_permute_small(nullptr, w.ids, s.T, s.E, s.k, s.has_shared, nullptr, nullptr, w.counts,
-                                   w.offsets, w.sorted_slot, w.slot_pos, w.tiles, w.meta, tile_rows_for(s), cs);
-  if (e == cudaSuccess && s.T > kDecodeMaxT)
-    e = launch_permute_large(w.ids, s.T, s.E, s.k, w.counts, w.offsets, w.sorted_slot, w.slot_pos,
-                             w.hist, w.L.n_chunks, cs);
-  if (e == cudaSuccess && s.T > kDecodeMaxT)
-    e = launch_build_tiles(w.offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s), w.tiles,
-                           w.meta, w.status, cs);
+  // grouped-GEMM arms: routing, permutation and work list in one cooperative launch
+  e = launch_route_permute_large(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w, w.counts,
+                                 w.offsets, w.sorted_slot, w.slot_pos, w.hist, w.tiles, w.meta,
+                                 tile_rows_for(s), w.status, cs);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
     e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, w, cs);
@@ -456,6 +509,38 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                        w.status, cs);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
+}
+
+
+moe_status_t moe_router_logits(const uint16_t* x, const moe_nvfp4_weights_t* router, const moe_shape_t* shape,
+                               float* logits, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(logits)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_router(router, *shape)) != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_device(stream)) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  Ws w = carve(ws, *shape);
+  return cuda_status(launch_router(x, *router, *shape, logits, w, cs));
+}
+
+moe_status_t moe_forward_routed(const uint16_t* x, const moe_nvfp4_weights_t* router,
+                                const moe_nvfp4_weights_t* gate_up, const moe_nvfp4_weights_t* down,
+                                const moe_shape_t* shape, void* out, int out_is_fp32, void* ws, size_t ws_bytes,
+                                void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (!aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_router(router, *shape)) != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if (shape->T == 0) return MOE_OK;
+  if ((st = check_device(stream)) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  Ws w = carve(ws, *shape);
+  if (launch_router(x, *router, *shape, w.rlogits, w, cs) != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_forward(x, w.rlogits, gate_up, down, shape, out, out_is_fp32, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,

@@ -207,12 +207,18 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<const uint32_t*>(&p);
 }
-// Two e4m3 codes (the low 16 bits, the lower byte first) -> f16x2, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
-  uint32_t r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(v));
-  return r;
+// The e4m3 byte that `sel` picks out of w (sel = 0x0404 | byte * 0x1010), as an f16x2 splat of its
+// value times 2^-8, with integer operations only (the conversion pipe is this kernel's tightest
+// resource): the byte's seven low bits placed at f16 bits 7..13 make the f16 exponent field the
+// e4m3 exponent and the f16 mantissa's top bits the e4m3 mantissa, so every finite code,
+// subnormals included, maps exactly to its value x 2^-8 (the biases differ by 8); the sign goes
+// to bit 15.  The epilogues multiply by 2^8.
+__device__ __forceinline__ uint32_t e4m3_splat_f16x2_2m8(uint32_t w, uint32_t sel) {
+  const uint32_t b = __byte_perm(w, 0u, sel);   // [0, byte, 0, byte]: the byte in each half's high byte
+  return (b & 0x80008000u) | ((b >> 1) & 0x3FFF3FFFu);
 }
+constexpr float kScaleUnbias = 256.0f;   // 2^8, undoes the scales' 2^-8
+
 // Two fp32 -> f16x2 (round to nearest; exact for the power-of-two-scaled bf16 values used here).
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -433,17 +439,26 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
     }
   }
   __syncthreads();
-  // stable scatter: slot s goes after the earlier slots of its expert
-  for (int s = threadIdx.x; s < S; s += blockDim.x) {
-    const int e = sm->ids[s];
-    int rank = 0;
-    for (int s2 = 0; s2 < s; ++s2) rank += sm->ids[s2] == e;
-    const int p = sm->cnt[e] + rank;
-    sm->sorted[p] = s;
-    sm->slot_pos[s] = p;
-    if (blockIdx.x == 0) {
-      a.sorted_slot[p] = s;
-      a.slot_pos[s] = p;
+  // stable scatter by warp 0, 32 slots a step: slot s goes after the earlier slots of its expert
+  // (its rank among the step's slots of the same expert, then the expert's cursor advances)
+  if (warp == 0) {
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int s = s0 + lane;
+      const int e = (s < S) ? sm->ids[s] : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      if (s < S) {
+        const int p = sm->cnt[e] + rank;
+        sm->sorted[p] = s;
+        sm->slot_pos[s] = p;
+        if (blockIdx.x == 0) {
+          a.sorted_slot[p] = s;
+          a.slot_pos[s] = p;
+        }
+      }
+      __syncwarp();
+      if (s < S && rank == 0) sm->cnt[e] += __popc(same);
+      __syncwarp();
     }
   }
   __syncthreads();
@@ -481,7 +496,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   // ------------------------------------------------------------ compute warps
   bool ok = true;
   const int grp = lane >> 2, tig = lane & 3;
-  const uint32_t ssel = (tig >> 1) ? 0x3232u : 0x1010u;   // this lane's block of a piece: 2 q + tig / 2
+  // this lane's scale byte of piece q (block 2 q + tig / 2): byte 2 (q % 2) + tig / 2 of the
+  // piece's scale word (gate_up: word q / 2 of a 16-byte scale row; down: the row's one word)
+  const uint32_t bsel = 0x0404u | (tig >> 1) * 0x1010u;   // + 0x2020 for the odd pieces' bytes 2, 3
   const int mt = warp & 7, kh = warp >> 3;                 // gate_up: MMA tile and 128-byte line
   uint32_t it = 0;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -510,8 +527,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
           const uint32_t wg = *reinterpret_cast<const uint32_t*>(lg + ((q ^ grp) << 4));
           const uint32_t wu = *reinterpret_cast<const uint32_t*>(lg + kIs * 128 + ((q ^ grp) << 4));
           const uint4 xb = *reinterpret_cast<const uint4*>(xc + 64 * q);
-          const uint32_t sg = __byte_perm(e4m3x2_to_f16x2((&sgv.x)[q >> 1] >> (16 * (q & 1))), 0u, ssel);
-          const uint32_t su = __byte_perm(e4m3x2_to_f16x2((&suv.x)[q >> 1] >> (16 * (q & 1))), 0u, ssel);
+          const uint32_t sg = e4m3_splat_f16x2_2m8((&sgv.x)[q >> 1], bsel + ((q & 1) ? 0x2020u : 0u));
+          const uint32_t su = e4m3_splat_f16x2_2m8((&suv.x)[q >> 1], bsel + ((q & 1) ? 0x2020u : 0u));
           uint32_t gr[4], ur[4];
           piece_frag(wg, sg, gr);
           piece_frag(wu, su, ur);
@@ -541,7 +558,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
         const int n = 2 * tig + c2;
         if (n < nt) {
           const int t = (g == E) ? n : sm->sorted[row0 + n] / k;
-          const float f = s2 * sm->xfac[t];
+          const float f = s2 * sm->xfac[t] * kScaleUnbias;
           sm->htile[n][8 * mt + grp] = f32_to_bf16_bits(silu_f32(p[c2] * f) * (p[2 + c2] * f));
         }
       }
@@ -591,8 +608,8 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
           for (int q = 0; q < 2; ++q) {
             const uint32_t wa = *reinterpret_cast<const uint32_t*>(sl + ra * 32 + ((q ^ sw) << 4) + 4 * tig);
             const uint32_t wb = *reinterpret_cast<const uint32_t*>(sl + (ra + 8) * 32 + ((q ^ sw) << 4) + 4 * tig);
-            const uint32_t sa = __byte_perm(e4m3x2_to_f16x2(sca >> (16 * q)), 0u, ssel);
-            const uint32_t sb = __byte_perm(e4m3x2_to_f16x2(scb >> (16 * q)), 0u, ssel);
+            const uint32_t sa = e4m3_splat_f16x2_2m8(sca, bsel + (q ? 0x2020u : 0u));
+            const uint32_t sb = e4m3_splat_f16x2_2m8(scb, bsel + (q ? 0x2020u : 0u));
             uint32_t ar[4], br[4];
             piece_frag(wa, sa, ar);
             piece_frag(wb, sb, br);
@@ -605,7 +622,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
           for (int c2 = 0; c2 < 2; ++c2) {
             const int n = 2 * tig + c2;
             if (n < nt) {
-              const float f = s2d * (c2 ? fac1 : fac0);
+              const float f = s2d * (c2 ? fac1 : fac0) * kScaleUnbias;
               float* yr = a.yp + (static_cast<int64_t>(m) * (S + T) + row0 + n) * H + col;
               yr[0] = (acc[0][c2] + acc[1][c2]) * f;
               yr[8] = (acc[0][2 + c2] + acc[1][2 + c2]) * f;
@@ -653,13 +670,23 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
       const int c4 = task & 3, tj = task >> 2, t = tj / J, j = tj % J;
       const int row = (j < k) ? sm->slot_pos[t * k + j] : S + t;
       const float* src = a.yp + static_cast<int64_t>(row) * H + col0 + 4 * c4;
+      // the slices' loads in groups of 8 issued together, summed in slice order
       float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      for (int m = 0; m < nslice; ++m) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(m) * (S + T) * H));
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
+      for (int m0 = 0; m0 < nslice; m0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+          if (m0 + m < nslice)
+            v[m] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(m0 + m) * (S + T) * H));
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          if (m0 + m < nslice) {
+            s.x += v[m].x;
+            s.y += v[m].y;
+            s.z += v[m].z;
+            s.w += v[m].w;
+          }
+        }
       }
       red2[tj * 4 + c4] = s;
     }

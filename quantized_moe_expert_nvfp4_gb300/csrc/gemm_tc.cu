@@ -7,7 +7,7 @@
 //
 // Swap-AB: the MMA's M dimension is 128 weight rows of one expert, N is up to 128 of that
 // expert's tokens, so a small expert group still fills M.  Per CTA (one per SM, persistent):
-//   warp 0       TMA producer of the packed e2m1 + e4m3 scale tiles (K = 256 per stage)
+//   warp 0       TMA producer of the packed e2m1 tiles (K = 256 per stage)
 //   warp 1       MMA issuer: the whole warp waits, one elected lane issues tcgen05.mma kind::f16
 //                with A from TMEM and B from SMEM
 //   warps 2-9    dequant: one weight row per thread (two warps per TMEM lane quarter, taking
@@ -17,6 +17,8 @@
 //   warp 10      TMA producer of the activation tiles (K = 256 per stage)
 //   warps 11-14  epilogue: tcgen05.ld of the fp32 accumulator, x scale2 x 2^e (the activation
 //                row's exponent), SiLU(gate)*up (gate_up)
+//   warp 15      TMA producer of the e4m3 scale tiles (a second issuing thread: each thread
+//                keeps only a few bulk copies in flight, so the packed tiles get their own)
 // The MMA is kind::f16 with f16 operands: the activations arrive as f16 rows in expert order,
 // scaled by a power of two per row (exact for every element above 2^-31 of the row maximum), so
 // the dequantization is one conversion and one packed multiply per pair of weights, and the
@@ -52,10 +54,10 @@ static_assert(kACol + kGStages * (kGK / 2) <= kTmemCols, "TMEM budget");
 static_assert(kBN == 128, "the epilogue holds four 32-column groups of row factors");
 static_assert(kGK / kBK == 4, "a group is four 64-wide chunks");
 
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpTmaB = 10, kWarpEpi = 11;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpTmaB = 10, kWarpEpi = 11, kWarpTmaS = 15;
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 15 * 32;
+constexpr int kThreads = 16 * 32;
 constexpr uint32_t kSpinLimit = 1u << 24;      // drain loops only
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: no legitimate wait comes close
 
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&sm->a_full[s], 1);
+      mbar_init(&sm->a_full[s], 2);   // the packed tile's producer and the scales' producer
       mbar_init(&sm->a_free[s], kDeqWarps);
     }
     for (int s = 0; s < kGStages; ++s) {
@@ -318,13 +320,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int st = ia % kAStages;
           if (!(ok = mbar_wait(&sm->a_free[st], ((ia / kAStages) & 1) ^ 1, sm, a.status))) break;
           uint8_t* dA = sA + st * kAStageBytes;
-          mbar_expect_tx(&sm->a_full[st], kAStageBytes);
+          mbar_expect_tx(&sm->a_full[st], kAPackedBytes);
           if (kGateUp) {
             tma_load_3d(dA, &maps.a, g * (kGK / 2), r0, 0, &sm->a_full[st]);
-            tma_load_3d(dA + kAPackedBytes, &maps.s, g * (kGK / 16), r0, 0, &sm->a_full[st]);
           } else {
             tma_load_2d(dA, &maps.a, g * (kGK / 2), r0, &sm->a_full[st]);
-            tma_load_2d(dA + kAPackedBytes, &maps.s, g * (kGK / 16), r0, &sm->a_full[st]);
+          }
+        }
+      }
+      if (!ok) {  // let copies already issued land before the CTA winds down (bounded)
+        for (int j = 0; j < kAStages && ia > 0; ++j, --ia) {
+          const uint32_t q = ia - 1;
+          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->a_full[q % kAStages], (q / kAStages) & 1); ++i) {
+          }
+        }
+      }
+    }
+  } else if (warp == kWarpTmaS) {
+    if (lane == 0) {
+      // the stages' e4m3 scales: a second issuing thread, so that the packed tiles' copies and
+      // these small ones are not queued behind each other (a thread keeps only a few bulk copies
+      // in flight); it arrives on the stage's barrier with its own byte count
+      const int box_rows = kGateUp ? kBM / 2 : kBM;
+      uint32_t ia = 0;
+      bool ok = true;
+      int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const int4 td = td_next;
+        td_next = load_tile(a, item + gridDim.x, n_items, MB);
+        const int mb = item % MB;
+        const int r0 = td.x * a.Nw + mb * box_rows;
+        for (int g = 0; g < KG; ++g, ++ia) {
+          const int st = ia % kAStages;
+          if (!(ok = mbar_wait(&sm->a_free[st], ((ia / kAStages) & 1) ^ 1, sm, a.status))) break;
+          uint8_t* dS = sA + st * kAStageBytes + kAPackedBytes;
+          mbar_expect_tx(&sm->a_full[st], kAScaleBytes);
+          if (kGateUp) {
+            tma_load_3d(dS, &maps.s, g * (kGK / 16), r0, 0, &sm->a_full[st]);
+          } else {
+            tma_load_2d(dS, &maps.s, g * (kGK / 16), r0, &sm->a_full[st]);
           }
         }
       }

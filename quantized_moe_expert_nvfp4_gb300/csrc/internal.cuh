@@ -16,8 +16,8 @@ constexpr int kMaxK = 16;
 constexpr int kMaxE = 1024;
 constexpr int kDecodeMaxT = 64;        // moe_forward uses the grouped-GEMV arm up to this T
 constexpr int kSimtTileRows = 64;      // rows per work item of the SIMT grouped GEMM
-constexpr int kScatterChunk = 2048;    // slots per CTA of the large-T permutation
 constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 grouped GEMM
+constexpr int kPermuteMaxGrid = 256;   // CTAs of the one-launch permutation (histogram rows)
 constexpr int kFdMaxT = 8;             // the fused single-launch decode kernel handles T <= 8
 constexpr int kFdSlice = 64;           // intermediate columns of one work unit of that kernel
 // its sync words: two units-done counters, one per launch parity (each launch zeroes the other)
@@ -37,17 +37,19 @@ struct WsLayout {
   size_t sorted_slot;  // int32 [S]
   size_t slot_pos;     // int32 [S]
   size_t tiles;        // int4  [max_tiles] work items {group, row_begin, rows, 0}
-  size_t hist;         // int32 [n_chunks, E] per-chunk expert histogram / bases
-  size_t h;            // bf16  [S + T, I]
-  size_t y;            // fp32  [S + T, H]
+  size_t hist;         // int32 [kPermuteMaxGrid, E] per-CTA expert histograms of the permutation
+  size_t h;            // bf16  [S + T, I]  (moe_forward on arms 1-3)
+  size_t y;            // fp32  [S + T, H]  (moe_forward on arms 2-3)
   size_t xf;           // f16   [S + T, H]  tensor-core arm: scaled rows of x in expert order
   size_t xe;           // fp32  [S + T]    2^e of each row of xf
   size_t hf;           // f16   [S + T, I]  tensor-core arm: scaled copy of h, and its row exponents
   size_t he;           // fp32  [S + T]    2^e of each row of hf
   size_t yp;           // fp32  [I/64][S + T][H] one-launch decode arm: partial expert outputs
+  size_t rxf;          // f16   [T, H]  router GEMM on the tensor cores: scaled rows of x
+  size_t rxe;          // fp32  [T]     and their factors 2^e
+  size_t rlogits;      // fp32  [T, E]  moe_forward_routed: the router's logits
   size_t total;
   int64_t max_tiles;
-  int64_t n_chunks;
 };
 
 WsLayout ws_layout(const moe_shape_t& s);
@@ -121,10 +123,14 @@ cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_i
                                        int32_t* counts, int32_t* offsets, int32_t* sorted_slot,
                                        int32_t* slot_pos, int4* tiles, int32_t* meta,
                                        int tile_rows, cudaStream_t st);
-// Multi-CTA permutation for any T.
-cudaError_t launch_permute_large(const int32_t* ids, int T, int E, int k, int32_t* counts,
-                                 int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
-                                 int32_t* hist, int64_t n_chunks, cudaStream_t st);
+// One cooperative launch for any T: routing (logits != NULL) or given ids, counts, offsets, the
+// stable permutation and the work list.  hist: [kPermuteMaxGrid, E]; meta[4..5] is its barrier
+// counter (zero in a new workspace).
+cudaError_t launch_route_permute_large(const float* logits, const int32_t* ids_in, int T, int E, int k,
+                                      int has_shared, int32_t* ids, float* w, int32_t* counts,
+                                      int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
+                                      int32_t* hist, int4* tiles, int32_t* meta, int tile_rows,
+                                      int32_t* status, cudaStream_t st);
 // Work list from offsets: one item per (group, run of <= tile_rows rows).
 // Offsets that are not a valid exclusive prefix (offsets[0] = 0, non-decreasing, offsets[E] = S)
 // produce no routed work and record kDevBadIndex.
@@ -211,6 +217,12 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st);
 cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
                            int32_t* status, cudaStream_t st);
+// Router GEMM on the CUDA cores: logits [T, E] fp32 = scale2 * x . deq(W)^T, W one NVFP4
+// projection of E rows of H (H % 16 == 0).
+cudaError_t launch_router_simt(const uint16_t* x, const moe_nvfp4_weights_t& w, int T, int H, int E, float* logits,
+                               cudaStream_t st);
+// Work list of a one-group GEMM over rows [0, rows) in items of tile_rows (meta[0] = count).
+cudaError_t launch_dense_tiles(int rows, int tile_rows, int4* tiles, int32_t* meta, cudaStream_t st);
 
 cudaError_t launch_quantize(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,
                             uint8_t* scales, float* scale2, cudaStream_t st);

@@ -6,6 +6,8 @@
 // index asc), a NaN never wins.  The permutation is the issue's "token permutation": slots
 // grouped by expert, stable in slot order, with counts and exclusive prefix offsets, computed
 // here by warp-level match/scan so that nothing returns to the host.
+#include <algorithm>
+
 #include "internal.cuh"
 #include "topk.cuh"
 
@@ -163,78 +165,108 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(
   write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
 }
 
-// Large T, pass 1: per-chunk expert histogram.
-__global__ void __launch_bounds__(256) permute_hist_kernel(const int32_t* __restrict__ ids, int S,
-                                                           int E, int32_t* __restrict__ hist) {
-  __shared__ int s_cnt[kMaxE];
+// Any T, one cooperative launch of up to kPermuteMaxGrid CTAs of 1024 threads: routing (or given
+// ids), per-CTA expert histograms of contiguous token ranges, a grid-wide barrier, every CTA's
+// stable placement base per expert (the histograms of the CTAs before it plus the expert's
+// offset), the stable scatter of its range, and (CTA 0) the work list.  The barrier is a
+// monotonic 64-bit arrival counter in the workspace (every launch on a workspace uses the same
+// grid), waited for with a bound.
+__device__ __forceinline__ uint64_t rp_now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ ids_in, int T, int E, int k,
+    int has_shared, int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot, int32_t* __restrict__ slot_pos,
+    int32_t* __restrict__ hist, int4* __restrict__ tiles, int32_t* __restrict__ meta, int tile_rows,
+    unsigned long long* __restrict__ bar, int32_t* __restrict__ status) {
+  __shared__ int s_cnt[kMaxE];   // this CTA's histogram, then its placement cursors
+  __shared__ int s_tot[kMaxE];   // expert counts (for the work list)
+  __shared__ int s_off[kMaxE];   // expert offsets
+  __shared__ int s_warp[32];
+  __shared__ int s_ok;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int S = T * k, G = gridDim.x, b = blockIdx.x;
+  const int per = (T + G - 1) / G;
+  const int t0 = min(T, b * per), t1 = min(T, t0 + per);
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  const int64_t s0 = static_cast<int64_t>(blockIdx.x) * kScatterChunk;
-  const int n = static_cast<int>(min(static_cast<int64_t>(kScatterChunk), static_cast<int64_t>(S) - s0));
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const int e = ids[s0 + i];
-    if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+  // routing of this CTA's tokens (warp per token) and its histogram
+  if (logits) {
+    for (int t = t0 + warp; t < t1; t += 32) {
+      int my_id;
+      float my_w;
+      warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w);
+      if (lane < k) {
+        ids[static_cast<int64_t>(t) * k + lane] = my_id;
+        w[static_cast<int64_t>(t) * k + lane] = my_w;
+        atomicAdd(&s_cnt[my_id], 1);
+      }
+    }
+  } else {
+    for (int64_t s = static_cast<int64_t>(t0) * k + threadIdx.x; s < static_cast<int64_t>(t1) * k; s += blockDim.x) {
+      const int e = ids_in[s];
+      if (e >= 0 && e < E) atomicAdd(&s_cnt[e], 1);
+      else report_device_error(status, kDevBadIndex);
+    }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    hist[static_cast<int64_t>(blockIdx.x) * E + e] = s_cnt[e];
-}
-
-// Large T, pass 2 (one CTA of 1024 threads): counts, offsets, and per-chunk bases
-// hist[c, e] <- offsets[e] + sum_{c' < c} hist[c', e].
-__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist,
-                                                            int64_t n_chunks, int E, int S,
-                                                            int32_t* __restrict__ counts,
-                                                            int32_t* __restrict__ offsets) {
-  __shared__ int s_warp[32];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(b) * E + e] = s_cnt[e];
+  // grid-wide barrier (all histograms written)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned long long old = atomicAdd(bar, 1ull);
+    const unsigned long long target = (old / G + 1) * G;
+    const uint64_t ts = rp_now_ns();
+    int ok = 1;
+    for (uint32_t i = 0;; ++i) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(bar) : "memory");
+      if (v >= target) break;
+      if ((i & 63u) == 63u && rp_now_ns() - ts > 1000000000ull) {
+        report_device_error(status, kDevTimeout);
+        ok = 0;
+        break;
+      }
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  // counts, offsets and this CTA's bases: thread e sums column e of the histograms
   const int e = threadIdx.x;
-  int run = 0;
+  int before = 0, total = 0;
   if (e < E) {
-    for (int64_t c = 0; c < n_chunks; ++c) {
-      const int v = hist[c * E + e];
-      hist[c * E + e] = run;
-      run += v;
+#pragma unroll 8
+    for (int c = 0; c < G; ++c) {
+      const int v = __ldcg(hist + static_cast<int64_t>(c) * E + e);
+      total += v;
+      before += (c < b) ? v : 0;
     }
   }
-  const int off = block_exclusive_scan(run, s_warp, nullptr);
+  const int off = block_exclusive_scan(e < E ? total : 0, s_warp, nullptr);
   if (e < E) {
-    counts[e] = run;
-    offsets[e] = off;
-    for (int64_t c = 0; c < n_chunks; ++c) hist[c * E + e] += off;
-  }
-  if (e == 0) offsets[E] = S;
-}
-
-// Large T, pass 3: stable scatter.  Warp w of the CTA places the w-th eighth of the chunk.
-__global__ void __launch_bounds__(256) permute_scatter_kernel(const int32_t* __restrict__ ids,
-                                                              int S, int E,
-                                                              const int32_t* __restrict__ hist,
-                                                              int32_t* __restrict__ sorted_slot,
-                                                              int32_t* __restrict__ slot_pos) {
-  constexpr int kWarps = 8;
-  constexpr int kSub = kScatterChunk / kWarps;
-  __shared__ int s_cur[kWarps][kMaxE];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kWarps * kMaxE; i += blockDim.x) (&s_cur[0][0])[i] = 0;
-  __syncthreads();
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kScatterChunk;
-  const int64_t w0 = c0 + static_cast<int64_t>(warp) * kSub;
-  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(kSub), static_cast<int64_t>(S) - w0)));
-  for (int i = lane; i < n; i += 32) {
-    const int e = ids[w0 + i];
-    if (e >= 0 && e < E) atomicAdd(&s_cur[warp][e], 1);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = hist[static_cast<int64_t>(blockIdx.x) * E + e];
-    for (int q = 0; q < kWarps; ++q) {
-      const int v = s_cur[q][e];
-      s_cur[q][e] = run;
-      run += v;
+    s_cnt[e] = off + before;
+    s_tot[e] = total;
+    s_off[e] = off;
+    if (b == 0) {
+      counts[e] = total;
+      offsets[e] = off;
     }
   }
+  if (b == 0 && threadIdx.x == 0) offsets[E] = S;
   __syncthreads();
-  warp_stable_scatter(ids, static_cast<int>(w0), n, E, s_cur[warp], sorted_slot, slot_pos);
+  // stable placement of the CTA's slots (its own ids, written above or given)
+  if (warp == 0) {
+    const int32_t* src = logits ? ids : ids_in;
+    warp_stable_scatter(src, t0 * k, (t1 - t0) * k, E, s_cnt, sorted_slot, slot_pos);
+  }
+  if (b == 0) write_tiles_block(E, S, T, has_shared, tile_rows, s_tot, s_off, tiles, meta, s_warp);
 }
 
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
@@ -289,15 +321,28 @@ cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_i
   return cudaGetLastError();
 }
 
-cudaError_t launch_permute_large(const int32_t* ids, int T, int E, int k, int32_t* counts,
-                                 int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
-                                 int32_t* hist, int64_t n_chunks, cudaStream_t st) {
-  const int S = T * k;
-  permute_hist_kernel<<<static_cast<unsigned>(n_chunks), 256, 0, st>>>(ids, S, E, hist);
-  permute_scan_kernel<<<1, 1024, 0, st>>>(hist, n_chunks, E, S, counts, offsets);
-  permute_scatter_kernel<<<static_cast<unsigned>(n_chunks), 256, 0, st>>>(ids, S, E, hist,
-                                                                          sorted_slot, slot_pos);
-  return cudaGetLastError();
+cudaError_t launch_route_permute_large(const float* logits, const int32_t* ids_in, int T, int E, int k,
+                                      int has_shared, int32_t* ids, float* w, int32_t* counts,
+                                      int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,
+                                      int32_t* hist, int4* tiles, int32_t* meta, int tile_rows,
+                                      int32_t* status, cudaStream_t st) {
+  int n_sm = 0;
+  cudaError_t e = current_sm_count(&n_sm);
+  if (e != cudaSuccess) return e;
+  auto kern = (E <= 256) ? route_permute_large_kernel<8>
+             : (E <= 512) ? route_permute_large_kernel<16> : route_permute_large_kernel<32>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::min(n_sm, kPermuteMaxGrid));
+  cfg.blockDim = dim3(1024);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  unsigned long long* bar = reinterpret_cast<unsigned long long*>(meta + 4);
+  return cudaLaunchKernelEx(&cfg, kern, logits, ids_in, T, E, k, has_shared, ids, w, counts, offsets,
+                            sorted_slot, slot_pos, hist, tiles, meta, tile_rows, bar, status);
 }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,

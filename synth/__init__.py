@@ -38,7 +38,7 @@ def _splitmix64(z: int) -> int:
     return z ^ (z >> 31)
 
 
-_TAGS = {"x": 1, "logits": 2, "bias": 3, "outliers": 4, "perm": 5, "gate_up": 6, "down": 7, "w": 8}
+_TAGS = {"x": 1, "logits": 2, "bias": 3, "outliers": 4, "perm": 5, "gate_up": 6, "down": 7, "w": 8, "router": 9}
 
 
 def _generator(device, seed: int, layer: int, tag: str, group: int = 0) -> torch.Generator:
@@ -154,6 +154,13 @@ def projection_weights(shape: Shape, seed: int, layer: int, proj: str, groups=No
     return out
 
 
+def router_weights(shape: Shape, seed: int, layer: int = 0, device="cpu", std: float = 0.02) -> torch.Tensor:
+    """fp32 [1, E, H] router weights drawn N(0, std^2) (one projection of E rows; with x ~ N(0,1)
+    and H = 2048 the logits come out near N(0, 0.8))."""
+    g = _generator(device, seed, layer, "router")
+    return std * torch.randn(1, shape.E, shape.H, generator=g, device=device, dtype=torch.float32)
+
+
 def random_floats(n: int, seed: int, device="cpu", scale: float = 1.0) -> torch.Tensor:
     """n fp32 values N(0, scale^2) for format and encoder sweeps."""
     g = _generator(device, seed, 0, "w", n)
@@ -165,4 +172,4 @@ def ceil_div(a: int, b: int) -> int:
 
 
 __all__ = ["Shape", "Workload", "WORKLOADS", "layer_seed", "activations", "router_logits",
-           "expert_weight", "projection_weights", "random_floats", "ceil_div", "math"]
+           "expert_weight", "projection_weights", "router_weights", "random_floats", "ceil_div", "math"]
