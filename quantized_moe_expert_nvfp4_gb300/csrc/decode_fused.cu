@@ -203,19 +203,17 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
-  return *reinterpret_cast<const uint32_t*>(&p);
-}
-// The e4m3 byte that `sel` picks out of w (sel = 0x0404 | byte * 0x1010), as an f16x2 splat of its
-// value times 2^-8, with integer operations only (the conversion pipe is this kernel's tightest
-// resource): the byte's seven low bits placed at f16 bits 7..13 make the f16 exponent field the
-// e4m3 exponent and the f16 mantissa's top bits the e4m3 mantissa, so every finite code,
-// subnormals included, maps exactly to its value x 2^-8 (the biases differ by 8); the sign goes
-// to bit 15.  The epilogues multiply by 2^8.
-__device__ __forceinline__ uint32_t e4m3_splat_f16x2_2m8(uint32_t w, uint32_t sel) {
-  const uint32_t b = __byte_perm(w, 0u, sel);   // [0, byte, 0, byte]: the byte in each half's high byte
-  return (b & 0x80008000u) | ((b >> 1) & 0x3FFF3FFFu);
+// Two e4m3 bytes of w as an f16x2 pair of their values times 2^-8 (sel = 0x0404 | lo << 4 |
+// hi << 12 puts byte lo into the low half and byte hi into the high half), with integer
+// operations only (the conversion pipe is this kernel's tightest resource): a byte's seven low
+// bits placed at f16 bits 7..13 make the f16 exponent field the e4m3 exponent and the f16
+// mantissa's top bits the e4m3 mantissa, so every finite code, subnormals included, maps exactly
+// to its value x 2^-8 (the biases differ by 8); the sign goes to bit 15.  The epilogues multiply
+// by 2^8.  The products below broadcast one half of the pair.
+__device__ __forceinline__ __half2 e4m3_pair_f16x2_2m8(uint32_t w, uint32_t sel) {
+  const uint32_t b = __byte_perm(w, 0u, sel);   // [0, lo, 0, hi]: each byte in its half's high byte
+  const uint32_t f = (b & 0x80008000u) | ((b >> 1) & 0x3FFF3FFFu);
+  return *reinterpret_cast<const __half2*>(&f);
 }
 constexpr float kScaleUnbias = 256.0f;   // 2^8, undoes the scales' 2^-8
 
@@ -229,12 +227,15 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
 // first MMA of the piece uses 8 tig .. + 3 as its K positions (2 tig, 2 tig + 1 | 2 tig + 8,
 // 2 tig + 9) and the second MMA 8 tig + 4 .. + 7.  The B operand (activation rows) is read in the
 // same order, so each dot product is the pieces' own; the lane's elements all lie in block
-// 2 q + tig / 2 of piece q and share one scale.  w: the lane's word of the row, s: the scale as an
-// f16x2 splat; r[0], r[1] feed the first MMA, r[2], r[3] the second (e2m1 x e4m3 is exact in f16).
-__device__ __forceinline__ void piece_frag(uint32_t w, uint32_t s, uint32_t (&r)[4]) {
+// 2 q + tig / 2 of piece q and share one scale.  w: the lane's word of the row, s: the scale in
+// both halves; r[0], r[1] feed the first MMA, r[2], r[3] the second (e2m1 x e4m3 is exact in f16).
+__device__ __forceinline__ void piece_frag(uint32_t w, __half2 s, uint32_t (&r)[4]) {
   e2m1x8_to_f16x2(w, r);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) r[i] = hmul2(r[i], s);
+  for (int i = 0; i < 4; ++i) {
+    const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&r[i]), s);
+    r[i] = *reinterpret_cast<const uint32_t*>(&p);
+  }
 }
 // Row exponent of the f16 staging: floor(log2(max)) - 14 puts the row maximum in [2^14, 2^15)
 // (kept >= -126 so that 2^-e is a normal float; such a row is then scaled less than it could be).
@@ -496,9 +497,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   // ------------------------------------------------------------ compute warps
   bool ok = true;
   const int grp = lane >> 2, tig = lane & 3;
-  // this lane's scale byte of piece q (block 2 q + tig / 2): byte 2 (q % 2) + tig / 2 of the
-  // piece's scale word (gate_up: word q / 2 of a 16-byte scale row; down: the row's one word)
-  const uint32_t bsel = 0x0404u | (tig >> 1) * 0x1010u;   // + 0x2020 for the odd pieces' bytes 2, 3
+  // this lane's scale bytes of the piece pair 2 p, 2 p + 1 (piece q's lane block is 2 q + tig / 2):
+  // bytes tig / 2 and 2 + tig / 2 of the pair's scale word (gate_up: word p of a 16-byte scale
+  // row; down: the row's one word), into the low and the high half
+  const uint32_t psel = 0x0404u | ((tig >> 1) << 4) | ((2u + (tig >> 1)) << 12);
   const int mt = warp & 7, kh = warp >> 3;                 // gate_up: MMA tile and 128-byte line
   uint32_t it = 0;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
@@ -527,11 +529,11 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
           const uint32_t wg = *reinterpret_cast<const uint32_t*>(lg + ((q ^ grp) << 4));
           const uint32_t wu = *reinterpret_cast<const uint32_t*>(lg + kIs * 128 + ((q ^ grp) << 4));
           const uint4 xb = *reinterpret_cast<const uint4*>(xc + 64 * q);
-          const uint32_t sg = e4m3_splat_f16x2_2m8((&sgv.x)[q >> 1], bsel + ((q & 1) ? 0x2020u : 0u));
-          const uint32_t su = e4m3_splat_f16x2_2m8((&suv.x)[q >> 1], bsel + ((q & 1) ? 0x2020u : 0u));
+          const __half2 sgp = e4m3_pair_f16x2_2m8((&sgv.x)[q >> 1], psel);
+          const __half2 sup = e4m3_pair_f16x2_2m8((&suv.x)[q >> 1], psel);
           uint32_t gr[4], ur[4];
-          piece_frag(wg, sg, gr);
-          piece_frag(wu, su, ur);
+          piece_frag(wg, (q & 1) ? __high2half2(sgp) : __low2half2(sgp), gr);
+          piece_frag(wu, (q & 1) ? __high2half2(sup) : __low2half2(sup), ur);
           mma16816(d[(q & 1) * 2], gr[0], ur[0], gr[1], ur[1], xb.x, xb.y);
           mma16816(d[(q & 1) * 2 + 1], gr[2], ur[2], gr[3], ur[3], xb.z, xb.w);
         }
@@ -604,15 +606,15 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
           float acc[2][4];
 #pragma unroll
           for (int q = 0; q < 2; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
+          const __half2 sap = e4m3_pair_f16x2_2m8(sca, psel);
+          const __half2 sbp = e4m3_pair_f16x2_2m8(scb, psel);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const uint32_t wa = *reinterpret_cast<const uint32_t*>(sl + ra * 32 + ((q ^ sw) << 4) + 4 * tig);
             const uint32_t wb = *reinterpret_cast<const uint32_t*>(sl + (ra + 8) * 32 + ((q ^ sw) << 4) + 4 * tig);
-            const uint32_t sa = e4m3_splat_f16x2_2m8(sca, bsel + (q ? 0x2020u : 0u));
-            const uint32_t sb = e4m3_splat_f16x2_2m8(scb, bsel + (q ? 0x2020u : 0u));
             uint32_t ar[4], br[4];
-            piece_frag(wa, sa, ar);
-            piece_frag(wb, sb, br);
+            piece_frag(wa, q ? __high2half2(sap) : __low2half2(sap), ar);
+            piece_frag(wb, q ? __high2half2(sbp) : __low2half2(sbp), br);
             mma16816(acc[q], ar[0], br[0], ar[1], br[1], hb[q].x, hb[q].y);
             mma16816(acc[q], ar[2], br[2], ar[3], br[3], hb[q].z, hb[q].w);
           }

@@ -31,33 +31,46 @@ __global__ void __launch_bounds__(kRtWarps * 32) router_simt_kernel(const uint16
   const uint8_t* prow = packed + static_cast<int64_t>(e) * (H / 2);
   const uint8_t* srow = scales + static_cast<int64_t>(e) * nblk;
   float acc[kRtTokens] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int b = lane; b < nblk; b += 32) {
-    const uint2 q = __ldg(reinterpret_cast<const uint2*>(prow) + b);
-    const float s = e4m3_to_f32(__ldg(srow + b));
-    float w[16];
-    {
-      float lo[8], hi[8];
-      e2m1x8_to_f32(q.x, lo);
-      e2m1x8_to_f32(q.y, hi);
+  // four blocks per lane and pass, their weight and scale loads issued together
+  for (int b0 = lane; b0 < nblk; b0 += 4 * 32) {
+    uint2 q[4];
+    uint32_t sb[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        w[i] = lo[i];
-        w[8 + i] = hi[i];
-      }
+    for (int u = 0; u < 4; ++u) {
+      const int b = b0 + 32 * u;
+      q[u] = b < nblk ? __ldg(reinterpret_cast<const uint2*>(prow) + b) : make_uint2(0u, 0u);
+      sb[u] = b < nblk ? __ldg(srow + b) : 0u;
     }
 #pragma unroll
-    for (int t = 0; t < kRtTokens; ++t) {
-      if (t < nt) {
-        const uint4* xp = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t0 + t) * H + 16 * b);
-        const uint4 a0 = __ldg(xp), a1 = __ldg(xp + 1);
-        const uint32_t u[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        float d = 0.0f;
+    for (int u = 0; u < 4; ++u) {
+      const int b = b0 + 32 * u;
+      if (b >= nblk) break;
+      const float s = e4m3_to_f32(sb[u]);
+      float w[16];
+      {
+        float lo[8], hi[8];
+        e2m1x8_to_f32(q[u].x, lo);
+        e2m1x8_to_f32(q[u].y, hi);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          d = fmaf(w[2 * i], bf16_bits_to_f32(u[i] & 0xffffu), d);
-          d = fmaf(w[2 * i + 1], bf16_bits_to_f32(u[i] >> 16), d);
+          w[i] = lo[i];
+          w[8 + i] = hi[i];
         }
-        acc[t] = fmaf(d, s, acc[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < kRtTokens; ++t) {
+        if (t < nt) {
+          const uint4* xp = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t0 + t) * H + 16 * b);
+          const uint4 a0 = __ldg(xp), a1 = __ldg(xp + 1);
+          const uint32_t v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          float d = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            d = fmaf(w[2 * i], bf16_bits_to_f32(v[i] & 0xffffu), d);
+            d = fmaf(w[2 * i + 1], bf16_bits_to_f32(v[i] >> 16), d);
+          }
+          acc[t] = fmaf(d, s, acc[t]);
+        }
       }
     }
   }

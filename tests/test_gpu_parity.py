@@ -112,8 +112,10 @@ def test_forward_arm_selection(cuda_lib):
 
 
 def test_forward_deterministic_and_matches_stages(cuda_lib):
+    """Repeated forwards are bit-identical, and on the grouped-GEMM arms moe_forward equals the
+    staged calls (route, permute, gate_up, down, combine) bit for bit."""
     moe = cuda_lib
-    for case in (SMALL[2], SMALL[5]):
+    for case in (SMALL[2], SMALL[5], SMALL[12], SMALL[14], SMALL[15], SMALL[16]):
         L = _small_layer(case)
         ms = moe_shape(moe, L.shape)
         gu, dn = L.gpu_weights(moe)
@@ -122,6 +124,19 @@ def test_forward_deterministic_and_matches_stages(cuda_lib):
         a = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
         b = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
         assert torch.equal(a, b)
+        if moe.forward_arm(ms) < 2:
+            continue
+        ids, w = moe.route_topk(logits, ms)
+        _, offsets, sorted_slot, slot_pos = moe.permute(ids, ms, ws)
+        h = moe.grouped_gate_up(x, sorted_slot, offsets, gu, ms, ws)
+        y = moe.grouped_down(h, offsets, dn, ms, ws)
+        for fp32 in (True, False):
+            staged = moe.combine(y, slot_pos, w, ms, out_fp32=fp32)
+            fused = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=fp32)
+            torch.cuda.synchronize()
+            assert moe.device_status(ws) == 0
+            assert torch.equal(fused.view(torch.int16 if not fp32 else torch.int32),
+                               staged.view(torch.int16 if not fp32 else torch.int32)), (case, fp32)
 
 
 def test_one_launch_consecutive_calls(cuda_lib):

@@ -17,13 +17,16 @@ from moe_cases import Layer, check_layer_close, moe_shape, to_np
 
 pytestmark = pytest.mark.gpu
 
-# (T, H, E, k, I, seed): the CUDA-core router (T <= 8, or E not a multiple of 128) and the
-# tensor-core one (ragged token tiles, several tiles, the full prefill chunk)
+# (T, H, E, k, I, seed): the CUDA-core router (T <= 32, or E not a multiple of 128) and the
+# tensor-core one (ragged token tiles, several tiles, the full prefill chunk), both sides of the
+# boundary
 CASES = [
     (4, 256, 16, 2, 128, 300),
     (1, 2048, 512, 10, 512, 301),
     (8, 2048, 512, 10, 512, 302),
     (9, 384, 48, 3, 256, 303),
+    (32, 2048, 512, 10, 512, 307),
+    (33, 512, 256, 8, 256, 308),
     (64, 2048, 512, 10, 512, 304),
     (300, 512, 256, 8, 256, 305),
     (4096, 2048, 512, 10, 512, 306),
