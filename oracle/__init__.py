@@ -64,6 +64,10 @@ def _declare(L):
     L.orc_permute.argtypes, L.orc_permute.restype = [P, I32, I32, I32, P, P, P, P], I32
     L.orc_moe_forward.argtypes = [P] * 8 + [I32] * 6 + [P, I32, P, P, P, I32]
     L.orc_moe_forward.restype = I32
+    L.orc_quant_rows_e4m3.argtypes, L.orc_quant_rows_e4m3.restype = [P, I64, I64, P, P], I32
+    L.orc_prepare_fp8.argtypes, L.orc_prepare_fp8.restype = [P, P, I64, I64, I64, P, P], I32
+    L.orc_moe_forward_fp8.argtypes = [P] * 8 + [I32] * 6 + [P, I32, P, P, P, I32]
+    L.orc_moe_forward_fp8.restype = I32
 
 
 def _ptr(a: np.ndarray):
@@ -197,4 +201,57 @@ def moe_forward(x, logits, gate_up, down, k: int, has_shared: int = 1, tokens=No
                                None if h is None else _ptr(h), None if y is None else _ptr(y),
                                int(n_threads))
     _check(rc, "moe_forward")
+    return (out, h, y) if dumps else out
+
+
+def quant_rows_e4m3(v) -> tuple[np.ndarray, np.ndarray]:
+    """fp32 [rows, K] -> (e4m3 codes u8 [rows, K], row scales f32 [rows]) by the row rule of the
+    FP8-activation arm (see moe_oracle.h)."""
+    v = _np(v, np.float32)
+    rows, K = v.shape
+    codes = np.empty((rows, K), np.uint8)
+    scale = np.empty((rows,), np.float32)
+    _check(lib().orc_quant_rows_e4m3(_ptr(v), rows, K, _ptr(codes), _ptr(scale)), "quant_rows_e4m3")
+    return codes, scale
+
+
+def prepare_fp8(packed, scales) -> tuple[np.ndarray, np.ndarray]:
+    """NVFP4 (packed [G, N, K/2], scales [G, N, K/16]) -> (e4m3 codes [G, N, K], row scales [G, N])."""
+    packed, scales = _np(packed, np.uint8), _np(scales, np.uint8)
+    G, N, K2 = packed.shape
+    codes = np.empty((G, N, 2 * K2), np.uint8)
+    rs = np.empty((G, N), np.float32)
+    _check(lib().orc_prepare_fp8(_ptr(packed), _ptr(scales), G, N, 2 * K2, _ptr(codes), _ptr(rs)), "prepare_fp8")
+    return codes, rs
+
+
+def moe_forward_fp8(x, logits, gate_up, down, k: int, has_shared: int = 1, tokens=None,
+                    dumps: bool = False, n_threads: int = 0):
+    """fp64 output of the FP8-activation arm for the listed tokens (default all).
+
+    gate_up / down: (codes [G, N, K] u8, row_scale [G, N] f32, scale2 [G] f32) as prepare_fp8
+    gives them plus the NVFP4 scale2.  Returns out [n, H] (and h [n, k+1, I], y [n, k+1, H]
+    when dumps=True)."""
+    xb = _np(x, np.uint16)
+    lg = _np(logits, np.float32)
+    T, H = xb.shape
+    E = lg.shape[1]
+    gc, gr, g2 = (_np(gate_up[0], np.uint8), _np(gate_up[1], np.float32), _np(gate_up[2], np.float32))
+    dc, dr, d2 = (_np(down[0], np.uint8), _np(down[1], np.float32), _np(down[2], np.float32))
+    I = gc.shape[1] // 2
+    if tokens is None:
+        tok, n = None, T
+    else:
+        tok = np.ascontiguousarray(np.asarray(tokens, np.int32))
+        n = tok.shape[0]
+    J = k + (1 if has_shared else 0)
+    out = np.empty((n, H), np.float64)
+    h = np.empty((n, J, I), np.float64) if dumps else None
+    y = np.empty((n, J, H), np.float64) if dumps else None
+    rc = lib().orc_moe_forward_fp8(_ptr(xb), _ptr(lg), _ptr(gc), _ptr(gr), _ptr(g2), _ptr(dc), _ptr(dr),
+                                   _ptr(d2), T, H, I, E, k, int(has_shared),
+                                   None if tok is None else _ptr(tok), n, _ptr(out),
+                                   None if h is None else _ptr(h), None if y is None else _ptr(y),
+                                   int(n_threads))
+    _check(rc, "moe_forward_fp8")
     return (out, h, y) if dumps else out

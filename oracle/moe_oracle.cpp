@@ -364,3 +364,170 @@ int orc_moe_forward(const uint16_t* x, const float* logits, const uint8_t* gu_pa
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// FP8-activation arm.  The "long-context cold prefill" issue of the Atlas project describes
+// its transposed prefill kernels as e4m3 x e4m3: the weights re-quantized to e4m3 (a second
+// rounding of the NVFP4 values) and the activations in e4m3; its fix option (a) scales each
+// token row into the e4m3 range (row absmax, computed in the gather) and applies the scale in
+// the f32 epilogue.  Readings (the issue leaves them open): the weights are re-quantized per
+// output row with the same rule as an activation row, from their exact values e2m1 x e4m3
+// block scale (scale2 stays the group's fp32 factor); the SiLU(g) * u intermediate is rounded to
+// bf16 as on the W4A16 path and then quantized per row like x before the down projection.
+// ---------------------------------------------------------------------------------------
+
+// e4m3 quantization of one row of fp32 values: amax = max |v|; inv = 448 / amax and
+// scale = amax / 448, one fp32 division each (a row whose amax is 0 or not finite gets
+// inv = scale = 1); code = e4m3 round-to-nearest-even, saturating at 448, of the fp32 product
+// v * inv.  The row's value is then scale * e4m3(code).
+void quant_row_e4m3(const float* v, int64_t K, uint8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < K; ++i) amax = std::max(amax, std::fabs(v[i]));
+  float inv = 1.0f, sc = 1.0f;
+  if (amax > 0.0f && std::isfinite(amax)) {
+    inv = 448.0f / amax;
+    sc = amax / 448.0f;
+  }
+  for (int64_t i = 0; i < K; ++i) {
+    const float q = v[i] * inv;
+    codes[i] = static_cast<uint8_t>(e4m3_encode(q));
+  }
+  *scale = sc;
+}
+
+// Round a double to bf16 (8 significant bits, ties to even), returned as a double.
+double round_bf16(double a) {
+  if (a == 0.0 || !std::isfinite(a)) return a;
+  const double tiny = std::ldexp(1.0, -126);
+  if (std::fabs(a) < tiny) {   // bf16 subnormals: multiples of 2^-133
+    const double q = std::ldexp(1.0, -133);
+    return std::nearbyint(a / q) * q;
+  }
+  int e = 0;
+  const double m = std::frexp(a, &e);   // a = m 2^e, 0.5 <= |m| < 1
+  return std::ldexp(std::nearbyint(std::ldexp(m, 8)), e - 8);
+}
+
+extern "C" {
+
+int orc_quant_rows_e4m3(const float* v, int64_t rows, int64_t K, uint8_t* codes, float* scale) {
+  if (!v || !codes || !scale || rows < 0 || K <= 0) return -1;
+  for (int64_t r = 0; r < rows; ++r) quant_row_e4m3(v + r * K, K, codes + r * K, scale + r);
+  return 0;
+}
+
+int orc_prepare_fp8(const uint8_t* packed, const uint8_t* scales, int64_t G, int64_t N, int64_t K,
+                    uint8_t* codes, float* row_scale) {
+  if (!packed || !scales || !codes || !row_scale || G <= 0 || N <= 0 || K <= 0 || K % 16) return -1;
+  const Tables& tb = tables();
+  std::vector<float> w(static_cast<size_t>(K));
+  for (int64_t r = 0; r < G * N; ++r) {
+    const uint8_t* pr = packed + r * (K / 2);
+    const uint8_t* sr = scales + r * (K / 16);
+    for (int64_t c = 0; c < K; ++c) {
+      const unsigned code = (c & 1) ? (pr[c / 2] >> 4) : (pr[c / 2] & 0xF);
+      // e2m1 x e4m3 has at most 6 significant bits: exact in fp32
+      w[c] = static_cast<float>(tb.e2m1_all[code] * tb.e4m3_all[sr[c / 16]]);
+    }
+    quant_row_e4m3(w.data(), K, codes + r * K, row_scale + r);
+  }
+  return 0;
+}
+
+int orc_moe_forward_fp8(const uint16_t* x, const float* logits, const uint8_t* gu_codes,
+                        const float* gu_rs, const float* gu_scale2, const uint8_t* dn_codes,
+                        const float* dn_rs, const float* dn_scale2, int T, int H, int I, int E, int k,
+                        int has_shared, const int32_t* tokens, int n_tok, double* out, double* h,
+                        double* y, int n_threads) {
+  if (!x || !logits || !gu_codes || !gu_rs || !gu_scale2 || !dn_codes || !dn_rs || !dn_scale2 ||
+      !out || T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E)
+    return -1;
+  std::vector<int32_t> tok;
+  if (tokens) {
+    tok.assign(tokens, tokens + n_tok);
+    for (int32_t t : tok)
+      if (t < 0 || t >= T) return -1;
+  } else {
+    tok.resize(T);
+    for (int t = 0; t < T; ++t) tok[t] = t;
+  }
+  const int64_t n = static_cast<int64_t>(tok.size());
+  const int J = k + (has_shared ? 1 : 0);
+  std::vector<int32_t> ids(static_cast<size_t>(T) * k);
+  std::vector<double> rw(static_cast<size_t>(T) * k);
+  if (orc_route(logits, T, E, k, ids.data(), rw.data())) return -1;
+  const int G = E + (has_shared ? 1 : 0);
+  std::vector<std::vector<std::pair<int64_t, int>>> work(G);
+  for (int64_t i = 0; i < n; ++i) {
+    for (int j = 0; j < k; ++j) work[ids[static_cast<size_t>(tok[i]) * k + j]].push_back({i, j});
+    if (has_shared) work[E].push_back({i, k});
+  }
+  // x rows quantized once per evaluated token (every expert of the token sees the same codes)
+  std::vector<uint8_t> xq(static_cast<size_t>(n) * H);
+  std::vector<float> xs(static_cast<size_t>(n));
+  {
+    std::vector<float> xf(H);
+    for (int64_t i = 0; i < n; ++i) {
+      const uint16_t* xr = x + static_cast<int64_t>(tok[i]) * H;
+      for (int c = 0; c < H; ++c) xf[c] = static_cast<float>(bf16_value(xr[c]));
+      quant_row_e4m3(xf.data(), H, &xq[static_cast<size_t>(i) * H], &xs[i]);
+    }
+  }
+  std::vector<double> ybuf(static_cast<size_t>(n) * J * H, 0.0);
+  std::vector<double> hbuf(h ? static_cast<size_t>(n) * J * I : 0, 0.0);
+  const Tables& tb = tables();
+  constexpr size_t kChunk = 64;
+  std::vector<std::pair<int, size_t>> tasks;
+  for (int g = 0; g < G; ++g)
+    for (size_t b = 0; b < work[g].size(); b += kChunk) tasks.push_back({g, b});
+  parallel_for(static_cast<int64_t>(tasks.size()), thread_count(n_threads), [&](int64_t ti) {
+    const int64_t g = tasks[ti].first;
+    const size_t b0 = tasks[ti].second, b1 = std::min(work[g].size(), b0 + kChunk);
+    const uint8_t* wgu = gu_codes + g * (2LL * I) * H;
+    const uint8_t* wdn = dn_codes + g * static_cast<int64_t>(H) * I;
+    std::vector<double> xv(H), a(I);
+    std::vector<float> hf(I);
+    std::vector<uint8_t> hq(I);
+    for (size_t wi = b0; wi < b1; ++wi) {
+      const int64_t i = work[g][wi].first;
+      const int j = work[g][wi].second;
+      for (int c = 0; c < H; ++c) xv[c] = tb.e4m3_all[xq[static_cast<size_t>(i) * H + c]];
+      for (int r = 0; r < I; ++r) {
+        double gsum = 0.0, usum = 0.0;
+        const uint8_t* wg = wgu + static_cast<int64_t>(r) * H;
+        const uint8_t* wu = wgu + static_cast<int64_t>(I + r) * H;
+        for (int c = 0; c < H; ++c) gsum += tb.e4m3_all[wg[c]] * xv[c];
+        for (int c = 0; c < H; ++c) usum += tb.e4m3_all[wu[c]] * xv[c];
+        const double gv = gsum * gu_rs[g * 2LL * I + r] * xs[i] * gu_scale2[g];
+        const double uv = usum * gu_rs[g * 2LL * I + I + r] * xs[i] * gu_scale2[g];
+        a[r] = silu(gv) * uv;
+      }
+      if (h) std::memcpy(&hbuf[(static_cast<size_t>(i) * J + j) * I], a.data(), sizeof(double) * I);
+      // h as bf16, then quantized per row like x
+      for (int r = 0; r < I; ++r) hf[r] = static_cast<float>(round_bf16(a[r]));
+      float hs = 1.0f;
+      quant_row_e4m3(hf.data(), I, hq.data(), &hs);
+      double* yr = &ybuf[(static_cast<size_t>(i) * J + j) * H];
+      for (int r = 0; r < H; ++r) {
+        double s = 0.0;
+        const uint8_t* wd = wdn + static_cast<int64_t>(r) * I;
+        for (int c = 0; c < I; ++c) s += tb.e4m3_all[wd[c]] * tb.e4m3_all[hq[c]];
+        yr[r] = s * dn_rs[g * static_cast<int64_t>(H) + r] * hs * dn_scale2[g];
+      }
+    }
+  });
+  for (int64_t i = 0; i < n; ++i) {
+    for (int c = 0; c < H; ++c) {
+      double acc = 0.0;
+      for (int j = 0; j < k; ++j)
+        acc += rw[static_cast<size_t>(tok[i]) * k + j] * ybuf[(static_cast<size_t>(i) * J + j) * H + c];
+      if (has_shared) acc += ybuf[(static_cast<size_t>(i) * J + k) * H + c];
+      out[i * H + c] = acc;
+    }
+  }
+  if (h) std::memcpy(h, hbuf.data(), sizeof(double) * hbuf.size());
+  if (y) std::memcpy(y, ybuf.data(), sizeof(double) * ybuf.size());
+  return 0;
+}
+
+}  // extern "C"

@@ -74,6 +74,28 @@ int orc_moe_forward(const uint16_t* x, const float* logits,
                     const int32_t* tokens, int n_tok, double* out, double* h, double* y,
                     int n_threads);
 
+/* --- FP8-activation arm (the "long-context cold prefill" issue: its transposed prefill kernels run
+ * e4m3 x e4m3 with the weights re-quantized to e4m3, and its option (a) gives each token row an
+ * e4m3 scale, applied in the f32 epilogue).
+ * Row rule: amax = max |v|, inv = 448 / amax and scale = amax / 448 (fp32 divisions; amax 0 or
+ * not finite -> inv = scale = 1), code = e4m3 nearest-even saturating of the fp32 product v * inv.
+ * orc_quant_rows_e4m3: v fp32 [rows, K] -> codes [rows, K], scale [rows].
+ * orc_prepare_fp8: NVFP4 packed/scales [G, N, ..] -> codes [G, N, K], row_scale [G, N]: each row's
+ *   exact values e2m1 x e4m3(block scale) under the row rule (scale2 stays the group factor).
+ * orc_moe_forward_fp8: the layer of orc_moe_forward with x rows quantized by the row rule,
+ *   gate/up = scale2 * row_scale * x_scale * sum(e4m3 w * e4m3 x) in fp64, h = SiLU(g) * u
+ *   rounded to bf16 and quantized by the row rule, y = scale2 * row_scale * h_scale *
+ *   sum(e4m3 w * e4m3 h), combine as orc_moe_forward.  Dumps: h before rounding, y. --- */
+int orc_quant_rows_e4m3(const float* v, int64_t rows, int64_t K, uint8_t* codes, float* scale);
+int orc_prepare_fp8(const uint8_t* packed, const uint8_t* scales, int64_t G, int64_t N, int64_t K,
+                    uint8_t* codes, float* row_scale);
+int orc_moe_forward_fp8(const uint16_t* x, const float* logits,
+                        const uint8_t* gu_codes, const float* gu_rs, const float* gu_scale2,
+                        const uint8_t* dn_codes, const float* dn_rs, const float* dn_scale2,
+                        int T, int H, int I, int E, int k, int has_shared,
+                        const int32_t* tokens, int n_tok, double* out, double* h, double* y,
+                        int n_threads);
+
 #ifdef __cplusplus
 }
 #endif

@@ -457,3 +457,116 @@ def test_router_is_linear_in_scale2_and_permutes_with_rows():
     perm = np.array([3, 0, 7, 1, 6, 2, 5, 4])
     c = oracle.router_logits(x, (p[0][perm], sc[0][perm], s2))
     np.testing.assert_array_equal(c, a[:, perm])
+
+
+# ----------------------------------------------------------------------------- FP8-activation arm
+# (the "long-context cold prefill" issue: e4m3 x e4m3 transposed kernels, weights re-quantized to
+# e4m3, option (a) a per-token-row e4m3 activation scale applied in the f32 epilogue)
+
+def test_fp8_row_rule_closed_form():
+    # amax 4: inv = 448 / 4 = 112 and scale = 4 / 448; every product is an e4m3 value
+    codes, scale = oracle.quant_rows_e4m3(np.array([[1.0, 2.0, -4.0, 0.5]], np.float32))
+    assert codes.tolist() == [[0x6E, 0x76, 0xFE, 0x66]]           # 112, 224, -448, 56
+    assert scale[0] == np.float32(4.0) / np.float32(448.0)
+    # amax 448: inv = scale = 1, so the codes are the nearest-even e4m3 of the values:
+    # 38 is the midpoint of 36 (0x61) and 40 (0x62) -> the even code; 37.9 -> 36; 2^-9 is the
+    # smallest subnormal; 2^-10 is the midpoint of 0 and 2^-9 -> 0
+    row = np.array([[448.0, 38.0, -38.0, 37.9, 2.0 ** -9, 2.0 ** -10, 0.0, -448.0]], np.float32)
+    codes, scale = oracle.quant_rows_e4m3(row)
+    assert codes.tolist() == [[0x7E, 0x62, 0xE2, 0x61, 0x01, 0x00, 0x00, 0xFE]]
+    assert scale[0] == 1.0
+    # an all-zero row keeps scale 1 and codes 0
+    codes, scale = oracle.quant_rows_e4m3(np.zeros((1, 16), np.float32))
+    assert not codes.any() and scale[0] == 1.0
+
+
+def test_fp8_row_rule_matches_torch_float8_on_random_rows():
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-20, 20, (64, 1)))).astype(np.float32)
+    v[3, 17] *= 40.0                                              # an outlier row
+    codes, scale = oracle.quant_rows_e4m3(v)
+    amax = np.abs(v).max(axis=1)
+    inv = (np.float32(448.0) / amax).astype(np.float32)
+    q = (v * inv[:, None]).astype(np.float32)                     # one fp32 multiply
+    ref = torch.from_numpy(np.minimum(np.abs(q), 448.0) * np.sign(q)).to(torch.float8_e4m3fn)
+    assert np.array_equal(codes, ref.view(torch.uint8).numpy())
+    assert np.array_equal(scale, (amax / np.float32(448.0)).astype(np.float32))
+
+
+def _fp8_exact_nvfp4(G, N, K, seed):
+    """NVFP4 weights whose values are e4m3-exact with row amax 448 (so the re-quantization is
+    lossless with row scale 1): e2m1 codes of one significant bit (0, 0.5, 1, 2, 4) times normal
+    e4m3 block scales <= 112, and element 0 of every row is 4 x 112 = 448."""
+    rng = np.random.default_rng(seed)
+    one_bit = [0, 1, 2, 4, 6, 9, 10, 12, 14]                      # 0, +-0.5, +-1, +-2, +-4
+    codes = rng.choice(one_bit, size=(G, N, K))
+    scl = rng.choice([c for c in range(0x10, 0x6F)], size=(G, N, K // 16))   # 2^-5 .. 112
+    codes[:, :, 0] = 6
+    scl[:, :, 0] = 0x6E
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    return packed, scl.astype(np.uint8)
+
+
+def test_fp8_weight_requant_lossless_on_e4m3_exact_weights():
+    packed, scl = _fp8_exact_nvfp4(2, 8, 64, 11)
+    codes, rs = oracle.prepare_fp8(packed, scl)
+    assert np.all(rs == 1.0)
+    deq = oracle.dequantize(packed, scl, np.ones(2, np.float32))
+    vals = np.vectorize(oracle.e4m3_value)(codes.astype(int))
+    assert np.array_equal(vals, deq)
+
+
+def test_fp8_weight_requant_is_the_row_rule_on_dequantized_rows():
+    shape = synth.Shape(T=1, H=128, E=3, k=1, I=32)
+    p, s_, _ = oracle.quantize(synth.projection_weights(shape, 4, 0, "gate_up"))
+    codes, rs = oracle.prepare_fp8(p, s_)
+    deq = oracle.dequantize(p, s_, np.ones(p.shape[0], np.float32)).astype(np.float32)   # exact in fp32
+    c2, s2 = oracle.quant_rows_e4m3(deq.reshape(-1, deq.shape[-1]))
+    assert np.array_equal(codes.reshape(c2.shape), c2) and np.array_equal(rs.reshape(-1), s2)
+
+
+def _bf16_rne(a):
+    """Round fp64 values to bf16 (8 significant bits, ties to even) with numpy."""
+    m, e = np.frexp(a)
+    return np.ldexp(np.round(np.ldexp(m, 8)), e - 8)   # np.round: half to even
+
+
+def test_fp8_layer_gate_up_equals_w4a16_on_exact_inputs_and_down_wiring():
+    """With e4m3-exact weights (row scale 1) and x rows whose quantization is exact (values e4m3
+    x 2^-8 with amax 1.75, so inv = 256 and scale = 2^-8), the FP8 layer's SiLU(g)*u equals the
+    W4A16 layer's.  Down weights 448 x a permutation (output n reads h element n mod I) then make
+    y[n] = 448 * scale2 * (the e4m3-quantized bf16 h)[n mod I], checked through the row rule."""
+    T, H, E, k, I = 5, 64, 3, 2, 32
+    G = E + 1
+    rng = np.random.default_rng(3)
+    gp, gs = _fp8_exact_nvfp4(G, 2 * I, H, 12)
+    g2 = np.array([0.5, 0.25, 1.0, 2.0], np.float32)
+    # down: row n has the single value 448 = 4 x 112 at column n mod I
+    dcodes = np.zeros((G, H, I), np.int64)
+    dscl = np.full((G, H, I // 16), 0x38, np.int64)
+    for n in range(H):
+        dcodes[:, n, n % I] = 6
+        dscl[:, n, (n % I) // 16] = 0x6E
+    dp = (dcodes[..., 0::2] | (dcodes[..., 1::2] << 4)).astype(np.uint8)
+    ds = dscl.astype(np.uint8)
+    d2 = np.array([1.0, 0.5, 2.0, 0.25], np.float32)
+    ev = np.array([oracle.e4m3_value(c) for c in range(0x08, 0x7F)])   # positive normal e4m3
+    xv = rng.choice(ev, size=(T, H)) * rng.choice([-1.0, 1.0], size=(T, H))
+    xv[:, 0] = 448.0
+    xv = xv * 2.0 ** -8
+    x = torch.from_numpy(xv.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(x.float().double(), torch.from_numpy(xv))
+    logits = torch.from_numpy(rng.standard_normal((T, E)).astype(np.float32))
+    gc, gr = oracle.prepare_fp8(gp, gs)
+    dc, dr = oracle.prepare_fp8(dp, ds)
+    assert np.all(gr == 1.0) and np.all(dr == 1.0)
+    _, h8, y8 = oracle.moe_forward_fp8(x, logits, (gc, gr, g2), (dc, dr, d2), k, 1, dumps=True)
+    _, h16, _ = oracle.moe_forward(x, logits, (gp, gs, g2), (dp, ds, d2), k, 1, dumps=True)
+    np.testing.assert_allclose(h8, h16, rtol=1e-12, atol=0)
+    ids, _ = oracle.route(logits, k)
+    groups = np.concatenate([ids, np.full((T, 1), E)], axis=1)     # rank j's group, shared last
+    hq, hs = oracle.quant_rows_e4m3(_bf16_rne(h8.reshape(-1, I)).astype(np.float32))
+    hval = np.vectorize(oracle.e4m3_value)(hq.astype(int)) * hs[:, None].astype(np.float64)
+    hval = hval.reshape(T, k + 1, I)
+    want = 448.0 * d2[groups][:, :, None] * hval[:, :, np.arange(H) % I]
+    np.testing.assert_allclose(y8, want, rtol=1e-15, atol=0)
