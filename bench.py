@@ -490,6 +490,44 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
                            "the same layer, timed like the headline steps; router_us_per_layer: the router GEMM alone"}
     del rgraphs, rogs
 
+    # the FP8-activation arm (its own numerics: e4m3 weights re-quantized once, e4m3 activation
+    # rows with fp32 scales), timed the same way on the same inputs
+    fp8_arm = None
+    if all(a == 2 for a in arms) and not hbm_bound:
+        for L in layers:
+            L["gu8"], L["dn8"] = moe.prepare_fp8(L["gu"]), moe.prepare_fp8(L["dn"])
+        fgraphs = []
+        for p in range(pool):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for L in layers:
+                    moe.forward_fp8(L["xs"][p], L["lgs"][p], L["gu8"], L["dn8"], L["ms"], L["ws"], out=L["out"])
+            fgraphs.append(g)
+        with torch.cuda.stream(stream):
+            for p in range(pool):
+                fgraphs[p].replay()
+            stream.synchronize()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for i in range(steps):
+                fgraphs[i % pool].replay()
+            f1.record(stream)
+            f1.synchronize()
+        fp8_ms = slowest_rank_ms(f0.elapsed_time(f1), dist, device) / steps
+        fp8_peak = 2.0 * roofline["peak"]
+        fl = acc["fwd_flops"] / steps
+        fp8_arm = {"value": replica_throughput(world, 1, tokens_per_step, fp8_ms), "unit": UNIT,
+                   "ms_per_step": fp8_ms,
+                   "layer_roofline": {"bound": "tensor", "achieved": fl / (fp8_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                                      "peak": fp8_peak, "frac": fl / (fp8_ms / 1e3) / 1e12 / fp8_peak,
+                                      "peak_source": roofline["peak_source"] + " x 2 (nominal fp8 / bf16 ratio)"},
+                   "numerics": "e4m3 x e4m3 tcgen05 (kind::f8f6f4): weights re-quantized to e4m3 per row at load, "
+                               "x and h rows quantized to e4m3 with one fp32 scale each, fp32 accumulation and epilogue",
+                   "what": "moe_forward_fp8 on the same inputs, timed like the headline steps"}
+        for L in layers:
+            del L["gu8"], L["dn8"]
+        del fgraphs
+
     # end to end through host buffers: H2D of x and logits from pinned memory, the C-ABI call,
     # D2H of the output, every step.
     e2e_steps = min(steps, 200)
@@ -528,6 +566,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     res = {"value": value, "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
            "config": describe(name), "roofline": roofline, "layer_roofline": layer, "e2e": e2e,
            "with_router": with_router,
+           "fp8_arm": fp8_arm,
            "gpu_launches": steps * launches, "clocks": clk.summary(),
            "arm": sorted({moe.ARM_NAMES[a] for a in arms}),
            "method": {"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh input "
@@ -590,7 +629,7 @@ def run_ours(args):
                 "config": main["config"], "roofline": main["roofline"], "e2e": main["e2e"],
                 "gpu_launches": main["gpu_launches"], "clocks": main["clocks"],
                 "parallelism": f"replicas x{world}"}
-        for key in ("cpu_baseline", "layer_roofline", "with_router", "arm", "method", "stages_us_per_forward",
+        for key in ("cpu_baseline", "layer_roofline", "with_router", "fp8_arm", "arm", "method", "stages_us_per_forward",
                     "distinct_experts_mean"):
             if key in main:
                 line[key] = main[key]

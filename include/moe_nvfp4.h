@@ -221,6 +221,48 @@ moe_status_t moe_get_device_status(void* ws, int32_t* status, void* stream);
  * with moe_get_device_status. */
 moe_status_t moe_debug_timeout_probe(void* ws, uint64_t limit_ns, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * FP8-activation prefill arm (a separate arm with its own numerics).  The "long-context cold
+ * prefill to SGLang parity" issue runs its transposed prefill kernels as e4m3 x e4m3 (weights
+ * re-quantized to e4m3, a second rounding) and lists as fix (a) a per-token-row e4m3 activation
+ * scale computed in the gather and applied in the f32 epilogue.  Every e4m3 operand row here
+ * carries one fp32 scale under one rule:
+ *   amax = max |v| over the row; inv = 448 / amax, scale = amax / 448 (IEEE fp32 divisions; a row
+ *   whose amax is 0 or not finite gets inv = scale = 1); code = e4m3 round-to-nearest-even,
+ *   saturating at 448, of the fp32 product v * inv.  The row's value is scale * e4m3(code).
+ * Weight rows are re-quantized from their exact NVFP4 values (e2m1 x e4m3 block scale; scale2
+ * stays the group's factor); x rows are quantized per token; h = SiLU(g) * u is rounded to bf16
+ * as on the W4A16 path and then quantized per row before down.
+ * ------------------------------------------------------------------------------------------- */
+
+/* One e4m3 projection of every group (device pointers, caller-owned). */
+typedef struct {
+  const uint8_t* codes;      /* [G, N, K] e4m3, row-major */
+  const float* row_scale;    /* [G, N] fp32 */
+  const float* scale2;       /* [G] fp32, the NVFP4 projection's own */
+  int32_t G, N, K;
+} moe_fp8_weights_t;
+
+/* Load-time re-quantization of an NVFP4 projection: codes [G, N, K] and row_scale [G, N] (the
+ * caller's device buffers, 16-byte aligned) by the row rule above; scale2 is not touched (point
+ * the fp8 weights at the NVFP4 scale2).  K % 256 == 0.  Asynchronous on stream. */
+moe_status_t moe_prepare_fp8(const moe_nvfp4_weights_t* w, uint8_t* codes, float* row_scale, void* stream);
+
+/* The row rule on bf16 rows: x [rows, K] -> codes [rows, K] e4m3, scale [rows] fp32 (the
+ * quantization the FP8 arm applies to activation rows).  K % 256 == 0. */
+moe_status_t moe_quantize_rows_e4m3(const uint16_t* x, int64_t rows, int32_t K, uint8_t* codes, float* scale,
+                                    void* stream);
+
+/* The whole layer on the FP8-activation arm: route and permute as moe_forward, x rows
+ * quantized per token and gathered into expert order, e4m3 x e4m3 grouped gate_up on the tensor
+ * cores (fp32 accumulation, epilogue x scale2 x weight-row scale x x-row scale, SiLU(g) * u ->
+ * bf16 h), h rows quantized, grouped down (-> fp32 y), then moe_combine's fixed-order sum.
+ * Shapes of moe_forward_arm 2 only (T > 8, H and I multiples of 256); the workspace is
+ * moe_workspace_size(shape). */
+moe_status_t moe_forward_fp8(const uint16_t* x, const float* logits, const moe_fp8_weights_t* gate_up,
+                             const moe_fp8_weights_t* down, const moe_shape_t* shape, void* out, int out_is_fp32,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* Which kernels moe_forward runs for a shape (-1 for an unsupported shape):
  *   0  T <= 8 (H % 512 == 0, H <= 4096, I % 256 == 0, I <= 1024, and room in shared memory for
  *      a ring of three slots): one cooperative launch that routes, streams the active experts'

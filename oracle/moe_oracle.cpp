@@ -420,17 +420,21 @@ int orc_prepare_fp8(const uint8_t* packed, const uint8_t* scales, int64_t G, int
                     uint8_t* codes, float* row_scale) {
   if (!packed || !scales || !codes || !row_scale || G <= 0 || N <= 0 || K <= 0 || K % 16) return -1;
   const Tables& tb = tables();
-  std::vector<float> w(static_cast<size_t>(K));
-  for (int64_t r = 0; r < G * N; ++r) {
-    const uint8_t* pr = packed + r * (K / 2);
-    const uint8_t* sr = scales + r * (K / 16);
-    for (int64_t c = 0; c < K; ++c) {
-      const unsigned code = (c & 1) ? (pr[c / 2] >> 4) : (pr[c / 2] & 0xF);
-      // e2m1 x e4m3 has at most 6 significant bits: exact in fp32
-      w[c] = static_cast<float>(tb.e2m1_all[code] * tb.e4m3_all[sr[c / 16]]);
+  // rows are independent: blocks of 64 rows over the threads
+  const int64_t rows = G * N, nb = (rows + 63) / 64;
+  parallel_for(nb, thread_count(0), [&](int64_t b) {
+    std::vector<float> w(static_cast<size_t>(K));
+    for (int64_t r = b * 64; r < std::min(rows, b * 64 + 64); ++r) {
+      const uint8_t* pr = packed + r * (K / 2);
+      const uint8_t* sr = scales + r * (K / 16);
+      for (int64_t c = 0; c < K; ++c) {
+        const unsigned code = (c & 1) ? (pr[c / 2] >> 4) : (pr[c / 2] & 0xF);
+        // e2m1 x e4m3 has at most 6 significant bits: exact in fp32
+        w[c] = static_cast<float>(tb.e2m1_all[code] * tb.e4m3_all[sr[c / 16]]);
+      }
+      quant_row_e4m3(w.data(), K, codes + r * K, row_scale + r);
     }
-    quant_row_e4m3(w.data(), K, codes + r * K, row_scale + r);
-  }
+  });
   return 0;
 }
 

@@ -45,6 +45,11 @@ class MoeWeights(ctypes.Structure):
                 ("G", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32)]
 
 
+class MoeFp8Weights(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("row_scale", ctypes.c_void_p), ("scale2", ctypes.c_void_p),
+                ("G", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -67,7 +72,7 @@ def load() -> ctypes.CDLL:
 
 def _declare(L):
     P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-    SH, W = ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights)
+    SH, W, W8 = ctypes.POINTER(MoeShape), ctypes.POINTER(MoeWeights), ctypes.POINTER(MoeFp8Weights)
     sigs = {
         "moe_workspace_size": ([SH], SZ),
         "moe_route_topk": ([P, SH, P, P, P], I32),
@@ -83,6 +88,9 @@ def _declare(L):
         "moe_forward_arm": ([SH], I32),
         "moe_router_logits": ([P, W, SH, P, P, SZ, P], I32),
         "moe_forward_routed": ([P, W, W, W, SH, P, I32, P, SZ, P], I32),
+        "moe_prepare_fp8": ([W, P, P, P], I32),
+        "moe_quantize_rows_e4m3": ([P, I64, I32, P, P, P], I32),
+        "moe_forward_fp8": ([P, P, W8, W8, SH, P, I32, P, SZ, P], I32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -144,6 +152,22 @@ class NVFP4Weights:
             _ptr(t, dt, name)
         return MoeWeights(self.packed.data_ptr(), self.scales.data_ptr(), self.scale2.data_ptr(),
                           G, N, 2 * K2)
+
+
+@dataclass
+class FP8Weights:
+    """One projection of every group re-quantized to e4m3 (FP8-activation arm): codes u8
+    [G, N, K], row_scale fp32 [G, N], scale2 fp32 [G] (the NVFP4 projection's own)."""
+    codes: torch.Tensor
+    row_scale: torch.Tensor
+    scale2: torch.Tensor
+
+    def c(self) -> MoeFp8Weights:
+        G, N, K = self.codes.shape
+        for name, t, dt in (("codes", self.codes, torch.uint8), ("row_scale", self.row_scale, torch.float32),
+                            ("scale2", self.scale2, torch.float32)):
+            _ptr(t, dt, name)
+        return MoeFp8Weights(self.codes.data_ptr(), self.row_scale.data_ptr(), self.scale2.data_ptr(), G, N, K)
 
 
 def workspace_size(shape: Shape) -> int:
@@ -266,6 +290,37 @@ def forward_routed(x, router: NVFP4Weights, gate_up: NVFP4Weights, down: NVFP4We
     return out
 
 
+def prepare_fp8(w: NVFP4Weights, stream=None) -> FP8Weights:
+    """Load-time re-quantization of an NVFP4 projection to e4m3 rows with fp32 row scales."""
+    G, N, K2 = w.packed.shape
+    codes = torch.empty(G, N, 2 * K2, dtype=torch.uint8, device=w.packed.device)
+    rs = torch.empty(G, N, dtype=torch.float32, device=w.packed.device)
+    _check("moe_prepare_fp8", load().moe_prepare_fp8(ctypes.byref(w.c()), _ptr(codes), _ptr(rs), _stream(stream)))
+    return FP8Weights(codes, rs, w.scale2)
+
+
+def quantize_rows_e4m3(x: torch.Tensor, stream=None):
+    """bf16 [rows, K] -> (e4m3 codes u8 [rows, K], row scales fp32 [rows])."""
+    rows, K = x.shape
+    codes = torch.empty(rows, K, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check("moe_quantize_rows_e4m3", load().moe_quantize_rows_e4m3(
+        _ptr(x, torch.bfloat16, "x"), rows, K, _ptr(codes), _ptr(scale), _stream(stream)))
+    return codes, scale
+
+
+def forward_fp8(x, logits, gate_up: FP8Weights, down: FP8Weights, shape: Shape, ws, out=None,
+                out_fp32: bool = False, stream=None):
+    """The layer on the FP8-activation arm (e4m3 x e4m3 grouped GEMMs with row scales)."""
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    out = out if out is not None else torch.empty(shape.T, shape.H, dtype=dt, device=x.device)
+    _check("moe_forward_fp8", load().moe_forward_fp8(
+        _ptr(x, torch.bfloat16, "x"), _ptr(logits, torch.float32, "logits"), ctypes.byref(gate_up.c()),
+        ctypes.byref(down.c()), ctypes.byref(shape.c()), _ptr(out, dt, "out"), int(out_fp32),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)))
+    return out
+
+
 def device_status(ws: torch.Tensor, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check("moe_get_device_status", load().moe_get_device_status(
@@ -299,4 +354,6 @@ def status_string(status: int) -> str:
 
 __all__ = ["Shape", "NVFP4Weights", "MoeError", "load", "workspace_size", "workspace",
            "quantize_nvfp4", "route_topk", "permute", "grouped_gate_up", "grouped_down", "combine",
-           "forward", "forward_profiled", "forward_arm", "router_logits", "forward_routed", "ARM_NAMES", "device_status", "status_string", "DECODE_MAX_T", "LIB_PATH"]
+           "forward", "forward_profiled", "forward_arm", "router_logits", "forward_routed", "FP8Weights",
+           "prepare_fp8", "quantize_rows_e4m3", "forward_fp8", "ARM_NAMES", "device_status", "status_string",
+           "DECODE_MAX_T", "LIB_PATH"]

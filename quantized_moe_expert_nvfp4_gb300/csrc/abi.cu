@@ -155,10 +155,14 @@ int tile_rows_for(const moe_shape_t& s) {
 }
 
 // The tensor-core arm takes its activations as f16 rows with power-of-two row exponents, in
-// expert order: x is gathered and converted into the workspace first (h already is in order).
-cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaStream_t cs) {
+// expert order: x is converted into the workspace first (h already is in order), token-major
+// from the inverse map when the caller has it (slot_pos, moe_forward), else gathered by
+// sorted_slot.
+cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, const int32_t* slot_pos,
+                           cudaStream_t cs) {
   if (arm_for(s) != Arm::kTc) return launch_gate_up_simt(a, cs);
-  cudaError_t e = launch_act_gather_f16(a.act, a.sorted_slot, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs);
+  cudaError_t e = slot_pos ? launch_act_scatter_f16(a.act, slot_pos, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs)
+                           : launch_act_gather_f16(a.act, a.sorted_slot, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs);
   if (e != cudaSuccess) return e;
   a.act = ws.xf;
   a.act_factor = ws.xe;
@@ -366,7 +370,7 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
   cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
                                      w.tiles, w.meta, w.status, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, w, cs));
+  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, w, nullptr, cs));
 }
 
 moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
@@ -503,7 +507,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
                                  tile_rows_for(s), w.status, cs);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess)
-    e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, w, cs);
+    e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, w, w.slot_pos, cs);
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) e = launch_down(grouped_args(*down, s, w.h, nullptr, w, w.y), s, w, cs);
   if (e == cudaSuccess) e = mark(3);
@@ -544,6 +548,90 @@ moe_status_t moe_forward_routed(const uint16_t* x, const moe_nvfp4_weights_t* ro
   Ws w = carve(ws, *shape);
   if (launch_router(x, *router, *shape, w.rlogits, w, cs) != cudaSuccess) return MOE_ERR_CUDA;
   return moe_forward(x, w.rlogits, gate_up, down, shape, out, out_is_fp32, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_prepare_fp8(const moe_nvfp4_weights_t* w, uint8_t* codes, float* row_scale, void* stream) {
+  if (!w || !aligned16(w->packed) || !aligned16(w->scales) || !aligned16(codes) || !aligned16(row_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (w->G < 1 || w->N < 1 || w->K < 256 || w->K % 256 || w->K > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status_t st = check_device(stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_prepare_fp8(w->packed, w->scales, static_cast<int64_t>(w->G) * w->N, w->K, codes,
+                                        row_scale, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_quantize_rows_e4m3(const uint16_t* x, int64_t rows, int32_t K, uint8_t* codes, float* scale,
+                                    void* stream) {
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(scale)) return MOE_ERR_INVALID_ARG;
+  if (rows < 0 || K < 256 || K % 256 || K > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MOE_OK;
+  moe_status_t st = check_device(stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_act_quant_fp8(x, nullptr, 0, 1, rows, K, codes, scale, nullptr,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+moe_status_t check_fp8_weights(const moe_fp8_weights_t* w, const moe_shape_t& s, bool gate_up) {
+  if (!w || !aligned16(w->codes) || !aligned16(w->row_scale) || !aligned16(w->scale2)) return MOE_ERR_INVALID_ARG;
+  const int N = gate_up ? 2 * s.I : s.H, K = gate_up ? s.H : s.I;
+  if (w->G != s.E + s.has_shared || w->N != N || w->K != K) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+GroupedFp8Args fp8_args(const moe_fp8_weights_t& w, const moe_shape_t& s, const Ws& ws, const uint8_t* act,
+                        const float* act_scale, void* out) {
+  GroupedFp8Args a;
+  a.codes = w.codes;
+  a.row_scale = w.row_scale;
+  a.scale2 = w.scale2;
+  a.N = w.N;
+  a.K = w.K;
+  a.act = act;
+  a.act_scale = act_scale;
+  a.T = s.T;
+  a.k = s.k;
+  a.S = s.T * s.k;
+  a.E = s.E;
+  a.tiles = ws.tiles;
+  a.meta = ws.meta;
+  a.max_tiles = max_tiles_for(s, kTcTileRows);
+  a.out = out;
+  a.status = ws.status;
+  return a;
+}
+}  // namespace
+
+moe_status_t moe_forward_fp8(const uint16_t* x, const float* logits, const moe_fp8_weights_t* gate_up,
+                             const moe_fp8_weights_t* down, const moe_shape_t* shape, void* out, int out_is_fp32,
+                             void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (arm_for(*shape) != Arm::kTc) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(logits) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (out_is_fp32 != 0 && out_is_fp32 != 1) return MOE_ERR_INVALID_ARG;
+  if ((st = check_fp8_weights(gate_up, *shape, true)) != MOE_OK) return st;
+  if ((st = check_fp8_weights(down, *shape, false)) != MOE_OK) return st;
+  if ((st = check_ws(ws, ws_bytes, *shape)) != MOE_OK) return st;
+  if ((st = check_device(stream)) != MOE_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const moe_shape_t& s = *shape;
+  Ws w = carve(ws, s);
+  // the e4m3 operands reuse the f16 operands' regions (one byte per element instead of two)
+  uint8_t* xq = reinterpret_cast<uint8_t*>(w.xf);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(w.hf);
+  const int S = s.T * s.k;
+  const int64_t R = static_cast<int64_t>(S) + s.T;
+  cudaError_t e = launch_route_permute_large(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w, w.counts,
+                                             w.offsets, w.sorted_slot, w.slot_pos, w.hist, w.tiles, w.meta,
+                                             kTcTileRows, w.status, cs);
+  if (e == cudaSuccess) e = launch_act_scatter_fp8(x, w.slot_pos, s.T, s.k, s.H, xq, w.xe, w.status, cs);
+  if (e == cudaSuccess) e = launch_gate_up_fp8(fp8_args(*gate_up, s, w, xq, w.xe, w.h), cs);
+  if (e == cudaSuccess) e = launch_act_quant_fp8(w.h, nullptr, 0, 1, R, s.I, hq, w.he, w.status, cs);
+  if (e == cudaSuccess) e = launch_down_fp8(fp8_args(*down, s, w, hq, w.he, w.y), cs);
+  if (e == cudaSuccess)
+    e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs);
+  return cuda_status(e);
 }
 
 moe_status_t moe_quantize_nvfp4(const float* w, int64_t G, int64_t N, int64_t K, uint8_t* packed,

@@ -69,7 +69,71 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
   }
 }
 
+// Token-major version of the expert-order gather: one warp per token reads its row once and
+// writes the f16 row to every expert-ordered row that holds the token (slot_pos[t k + j] for its
+// k ranks, and S + t for the shared expert).  Each token row is read from memory once instead of
+// k + 1 times (a 32k-token batch of x is larger than L2).
+__global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __restrict__ src,
+                                                              const int32_t* __restrict__ slot_pos, int T, int k,
+                                                              uint16_t* __restrict__ dst, float* __restrict__ factor,
+                                                              int K, int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int t = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (t >= T) return;
+  const int S = T * k;
+  // destination rows: lane j < k holds rank j's row, lane k the shared expert's row S + t
+  int p = -1;
+  if (lane < k) {
+    p = __ldg(slot_pos + static_cast<int64_t>(t) * k + lane);
+    if (static_cast<unsigned>(p) >= static_cast<unsigned>(S)) {
+      report_device_error(status, kDevBadIndex);
+      p = -1;
+    }
+  } else if (lane == k) {
+    p = S + t;
+  }
+  const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * K);
+  float m = 0.0f;
+  for (int c = lane; c < K / 8; c += 32) {
+    const uint4 v = __ldg(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+      m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const int e = (m > 0.0f && m <= 3.4e38f) ? max(ilogbf(m) - 14, -126) : 0;
+  const float inv = __int_as_float((127 - e) << 23);
+  if (p >= 0) factor[p] = __int_as_float((127 + e) << 23);
+  for (int c = lane; c < K / 8; c += 32) {
+    const uint4 v = __ldg(s + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[i] << 16) * inv, __uint_as_float(w[i] & 0xffff0000u) * inv);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int j = 0; j <= k; ++j) {
+      const int pj = __shfl_sync(0xffffffffu, p, j);
+      if (pj >= 0) reinterpret_cast<uint4*>(dst + static_cast<int64_t>(pj) * K)[c] = ov;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_act_scatter_f16(const uint16_t* x, const int32_t* slot_pos, int T, int k, int K, uint16_t* dst,
+                                   float* factor, int32_t* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  act_scatter_f16_kernel<<<static_cast<unsigned>((static_cast<int64_t>(T) + 7) / 8), 256, 0, st>>>(
+      x, slot_pos, T, k, dst, factor, K, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K,
                               cudaStream_t st) {

@@ -31,10 +31,13 @@
 // mbarrier wait is bounded; on timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // workspace status word and winds down.
 #include "internal.cuh"
+#include "tc_common.cuh"
 #include "tensor_map.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int kBM = 128;                      // weight rows per tile (MMA M)
 constexpr int kBN = kTcTileRows;              // tokens per tile at most (MMA N, rounded up to 16)
@@ -96,84 +99,14 @@ struct Smem {
   int abort_flag;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false when the CTA is aborting (another role timed out) or this wait timed out.
-// The warp_ variant gives every lane of the warp the same answer, as the .sync.aligned tcgen05
-// instructions that follow it need the whole warp converged.
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
+// Bounded waits on this kernel's barriers (the CTA's abort flag lives in Smem).
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Smem* sm, int32_t* status) {
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try(b, parity)) return true;
-    if ((i & 255u) == 255u) {
-      if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return false;
-      const uint64_t now = global_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > kWaitTimeoutNs) {
-        report_device_error(status, kDevTimeout);
-        *reinterpret_cast<volatile int*>(&sm->abort_flag) = 1;
-        return false;
-      }
-    }
-  }
+  return tc::mbar_wait_flag(b, parity, &sm->abort_flag, status, kWaitTimeoutNs);
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, Smem* sm, int32_t* status) {
   const bool ok = mbar_wait(b, parity, sm, status);
   return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_commit(uint64_t* b) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(b))
-               : "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -185,17 +118,8 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// K-major bf16 operand in SMEM, 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-         (static_cast<uint64_t>(2) << 61);
-}
-
 // Instruction descriptor: D f32, A f16, B f16, both K-major, M = 128, N.
-__device__ __forceinline__ uint32_t make_idesc(int n) {
-  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(kBM >> 4) << 24);
-}
+__device__ __forceinline__ uint32_t make_idesc(int n) { return tc::idesc_f32acc(kBM, n); }
 
 #define TC_ST32(taddr, r)                                                                          \
   asm volatile(                                                                                    \
@@ -206,16 +130,6 @@ __device__ __forceinline__ uint32_t make_idesc(int n) {
       "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),          \
       "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),          \
       "r"(r[30]), "r"(r[31])                                                                       \
-      : "memory")
-
-#define TC_LD16(taddr, v)                                                                          \
-  asm volatile(                                                                                    \
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}," \
-      " [%16];"                                                                                    \
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),       \
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),   \
-        "=r"(v[14]), "=r"(v[15])                                                                   \
-      : "r"(taddr)                                                                                 \
       : "memory")
 
 // Eight e2m1 codes (one 32-bit word, element i in bits 4i..4i+3) times the block scale ->
@@ -246,14 +160,6 @@ __device__ __forceinline__ void tc_mma_acc(uint32_t d_tmem, uint32_t a_tmem, uin
   asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc),
                "r"(idesc)
                : "memory");
-}
-
-// One lane of a converged warp (the MMA issue is cheaper from a converged warp than from a lane
-// branched off on its own).
-__device__ __forceinline__ bool elect_one() {
-  uint32_t p;
-  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
-  return p != 0;
 }
 
 // Tile descriptor of a work item (zeros past the end).  Every role loads the next item's

@@ -162,12 +162,45 @@ cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor,
 // sorted_slot[p] / k of x, row S + t is token t (out-of-range slots are reported as kDevBadIndex).
 cudaError_t launch_act_gather_f16(const uint16_t* x, const int32_t* sorted_slot, int T, int k, int K,
                                   uint16_t* dst, float* factor, int32_t* status, cudaStream_t st);
+// The same rows written token-major from the inverse map (slot_pos): every x row is read once.
+// k < 32.
+cudaError_t launch_act_scatter_f16(const uint16_t* x, const int32_t* slot_pos, int T, int k, int K, uint16_t* dst,
+                                   float* factor, int32_t* status, cudaStream_t st);
 // tcgen05 grouped GEMM (work items from a tile list built with kTcTileRows rows); act is the
 // expert-ordered f16 operand [S + T, K] (launch_act_gather_f16 for gate_up, launch_act_to_f16
 // of h for down) and act_factor its row factors 2^e.
 bool tc_supported(const moe_shape_t& s);
 cudaError_t launch_gate_up_tc(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_tc(const GroupedArgs& a, cudaStream_t st);
+
+// FP8-activation arm: e4m3 rows with one fp32 scale each (fp8_quant.cu) on tcgen05 kind::f8f6f4
+// (gemm_fp8.cu).  Same work list as the f16 tensor-core arm.
+struct GroupedFp8Args {
+  const uint8_t* codes;         // weights [G, N, K] e4m3
+  const float* row_scale;       // [G, N]
+  const float* scale2;          // [G]
+  int N, K;
+  const uint8_t* act;           // expert-ordered activation codes [S + T, K]
+  const float* act_scale;       // [S + T]
+  int T, k, S, E;
+  const int4* tiles;
+  const int32_t* meta;
+  int64_t max_tiles;
+  void* out;                    // h [S + T, I] bf16 (gate_up) or y [S + T, H] fp32 (down)
+  int32_t* status;
+};
+cudaError_t launch_gate_up_fp8(const GroupedFp8Args& a, cudaStream_t st);
+cudaError_t launch_down_fp8(const GroupedFp8Args& a, cudaStream_t st);
+// Weight rows [rows, K] (NVFP4 packed/scales) -> e4m3 codes [rows, K] and row scales [rows].
+cudaError_t launch_prepare_fp8(const uint8_t* packed, const uint8_t* scales, int64_t rows, int K, uint8_t* codes,
+                               float* row_scale, cudaStream_t st);
+// bf16 rows -> e4m3 codes + row scales; with sorted_slot, gathered into expert order as
+// launch_act_gather_f16 does.
+cudaError_t launch_act_quant_fp8(const uint16_t* src, const int32_t* sorted_slot, int S, int k, int64_t rows, int K,
+                                 uint8_t* dst, float* scale, int32_t* status, cudaStream_t st);
+// Token-major from slot_pos, as launch_act_scatter_f16.  k < 32.
+cudaError_t launch_act_scatter_fp8(const uint16_t* x, const int32_t* slot_pos, int T, int k, int K, uint8_t* dst,
+                                   float* scale, int32_t* status, cudaStream_t st);
 
 struct DownCombineArgs {
   const uint8_t* packed;

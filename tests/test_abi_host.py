@@ -128,3 +128,30 @@ def test_static_scratch_rejects_shapes_that_do_not_fit(lib):
                         assert st != -2, (T, H, I, k, st)
                         seen["fit"] += 1
     assert seen["fit"] > 10 and seen["reject"] >= 4
+
+
+def test_fp8_arm_host_validation(lib):
+    """The FP8-activation arm's calls reject bad arguments before any CUDA call."""
+    moe, L = lib
+    P = ctypes.c_void_p
+    fake, mis = P(0x100000), P(0x100008)
+    shape = _shape(moe, T=4096)
+    need = L.moe_workspace_size(ctypes.byref(shape))
+    gu8 = moe.MoeFp8Weights(0x200000, 0x300000, 0x400000, 513, 1024, 2048)
+    dn8 = moe.MoeFp8Weights(0x200000, 0x300000, 0x400000, 513, 2048, 512)
+    call = lambda **o: L.moe_forward_fp8(o.get("x", fake), fake, ctypes.byref(o.get("gu", gu8)),
+                                         ctypes.byref(o.get("dn", dn8)), ctypes.byref(o.get("shape", shape)),
+                                         fake, o.get("fp32", 0), fake, o.get("ws", need), None)
+    assert call(shape=_shape(moe, T=8)) == -2                      # decode batches: not this arm
+    assert call(shape=_shape(moe, T=4096, I=128)) == -2            # I not a multiple of 256
+    assert call(x=mis) == -1
+    assert call(gu=moe.MoeFp8Weights(0x200000, 0x300000, 0x400000, 512, 1024, 2048)) == -1   # wrong G
+    assert call(dn=moe.MoeFp8Weights(0x200000, 0x300008, 0x400000, 513, 2048, 512)) == -1   # misaligned
+    assert call(fp32=2) == -1
+    assert call(ws=need - 1) == -3
+    w = moe.MoeWeights(0x200000, 0x300000, 0x400000, 513, 1024, 2048)
+    assert L.moe_prepare_fp8(ctypes.byref(w), fake, mis, None) == -1
+    assert L.moe_prepare_fp8(ctypes.byref(moe.MoeWeights(0x200000, 0x300000, 0x400000, 513, 1024, 200)),
+                             fake, fake, None) == -2
+    assert L.moe_quantize_rows_e4m3(fake, 4, 100, fake, fake, None) == -2
+    assert L.moe_quantize_rows_e4m3(mis, 4, 256, fake, fake, None) == -1

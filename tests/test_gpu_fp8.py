@@ -1,0 +1,129 @@
+"""GPU parity of the FP8-activation arm (needs a GB300).
+
+The "long-context cold prefill to SGLang parity" issue runs its transposed prefill kernels as
+e4m3 x e4m3 (weights re-quantized to e4m3) and gives, as fix (a), every token row an e4m3 scale
+applied in the f32 epilogue.  The integer decisions of that arm are taken in fp32 on both sides
+by the same row rule, so the load-time weight codes and the activation-row codes are bit-exact
+against the oracle; the layer output is checked against the oracle's FP8 layer with the layer
+tolerance (the fp32 accumulation order differs, and the bf16 h that is quantized before down can
+round differently in rare elements).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from moe_cases import Layer, bf16_round_bits, check_layer_close, moe_shape, to_np
+
+pytestmark = pytest.mark.gpu
+
+# (T, H, E, k, I, has_shared, logit bias, seed): ragged token tiles, several tiles per expert,
+# no shared expert, the N tail of a single 16-column step, H = 1024 with I = 512
+CASES = [
+    (9, 256, 16, 2, 256, 1, "none", 401),
+    (48, 512, 32, 4, 256, 1, "zipf", 402),
+    (129, 256, 8, 2, 256, 0, "none", 403),
+    (1000, 512, 64, 8, 256, 1, "zipf", 404),
+    (700, 1024, 32, 6, 512, 1, "normal", 405),
+]
+
+
+def _layer(case, gen_device="cpu"):
+    T, H, E, k, I, sh, bias, seed = case
+    return Layer(synth.Shape(T=T, H=H, E=E, k=k, I=I, has_shared=sh), seed, logit_bias=bias,
+                 gen_device=gen_device)
+
+
+def _weights(moe, L, groups=None):
+    """GPU NVFP4 weights (checked byte-equal to the oracle's quantization of the same fp32
+    tensors) and both sides' e4m3 re-quantizations: the GPU's from its own NVFP4 bytes, the
+    oracle's from its own."""
+    gu, dn = L.gpu_weights(moe)
+    ogu, odn = L.oracle_weights(groups)
+    groups = list(range(L.G)) if groups is None else sorted(set(groups))
+    gi = torch.tensor(groups, device="cuda")
+    for q, o in ((gu, ogu), (dn, odn)):
+        assert np.array_equal(q.packed[gi].cpu().numpy(), o[0][groups])
+        assert np.array_equal(q.scales[gi].cpu().numpy(), o[1][groups])
+    gu8, dn8 = moe.prepare_fp8(gu), moe.prepare_fp8(dn)
+    o8 = []
+    for o in (ogu, odn):
+        c, rs = oracle.prepare_fp8(o[0], o[1])
+        o8.append((c, rs, o[2]))
+    return gu8, dn8, o8[0], o8[1], groups
+
+
+@pytest.mark.parametrize("case", CASES[:3], ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}_I{c[4]}")
+def test_weight_requantization_bit_exact(cuda_lib, case):
+    moe = cuda_lib
+    L = _layer(case)
+    gu8, dn8, ogu8, odn8, groups = _weights(moe, L)
+    torch.cuda.synchronize()
+    for q8, o8 in ((gu8, ogu8), (dn8, odn8)):
+        assert np.array_equal(q8.codes.cpu().numpy(), o8[0])
+        assert np.array_equal(q8.row_scale.cpu().numpy(), o8[1])
+
+
+def test_activation_rows_bit_exact(cuda_lib):
+    """Seeded rows with outliers, an all-zero row, a row of tiny values (2^-100 scale) and a row
+    holding one huge value: codes and scales bit-exact."""
+    moe = cuda_lib
+    x = synth.activations(64, 1024, 406, 0, 0.05).float()
+    x[3] = 0.0
+    x[7] *= 2.0 ** -100
+    x[11] = 0.0
+    x[11, 5] = 3.0e38
+    x = x.to(torch.bfloat16)
+    codes, scale = moe.quantize_rows_e4m3(x.cuda())
+    torch.cuda.synchronize()
+    oc, os_ = oracle.quant_rows_e4m3(x.float().numpy())
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(scale.cpu().numpy(), os_)
+
+
+def _check_forward(moe, L, gu8, dn8, ogu8, odn8, tokens=None):
+    s = L.shape
+    ms = moe_shape(moe, s)
+    ws = moe.workspace(ms)
+    x, logits = L.x.cuda(), L.logits.cuda()
+    out32 = moe.forward_fp8(x, logits, gu8, dn8, ms, ws, out_fp32=True)
+    out = moe.forward_fp8(x, logits, gu8, dn8, ms, ws)
+    again = moe.forward_fp8(x, logits, gu8, dn8, ms, ws, out_fp32=True)
+    torch.cuda.synchronize()
+    assert moe.device_status(ws) == 0
+    assert torch.equal(out32, again), "not deterministic"
+    assert torch.equal(out.view(torch.int16), bf16_round_bits(out32)), "bf16 output != rounded fp32 output"
+    ref = oracle.moe_forward_fp8(L.x.cpu(), L.logits.cpu(), ogu8, odn8, s.k, s.has_shared, tokens=tokens)
+    sel = slice(None) if tokens is None else torch.tensor(tokens, device="cuda")
+    check_layer_close(to_np(out32[sel]), ref, "forward_fp8 fp32")
+    check_layer_close(to_np(out[sel]), ref, "forward_fp8 bf16", rounded_bf16=True)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_I{c[4]}_sh{c[5]}")
+def test_forward_fp8_matches_oracle(cuda_lib, case):
+    moe = cuda_lib
+    L = _layer(case)
+    gu8, dn8, ogu8, odn8, _ = _weights(moe, L)
+    _check_forward(moe, L, gu8, dn8, ogu8, odn8)
+
+
+def test_forward_fp8_prefill_chunk_every_row(cuda_lib):
+    """The T = 4096 prefill chunk (1% outlier rows x30), every row."""
+    moe = cuda_lib
+    w = synth.WORKLOADS["prefill"]
+    L = Layer(w.shape(4096), synth.layer_seed(w, w.seeds[0], 0), logit_bias=w.logit_bias,
+              outlier_frac=w.outlier_frac, gen_device="cuda")
+    gu8, dn8, ogu8, odn8, _ = _weights(moe, L)
+    _check_forward(moe, L, gu8, dn8, ogu8, odn8)
+
+
+def test_forward_fp8_rejects_decode_shapes(cuda_lib):
+    moe = cuda_lib
+    L = _layer(CASES[0])
+    gu8, dn8, _, _, _ = _weights(moe, L)
+    ms = moe.Shape(T=8, H=256, I=256, E=16, k=2)
+    ws = moe.workspace(ms)
+    with pytest.raises(moe.MoeError):
+        moe.forward_fp8(torch.zeros(8, 256, dtype=torch.bfloat16, device="cuda"),
+                        torch.zeros(8, 16, device="cuda"), gu8, dn8, ms, ws)
