@@ -298,10 +298,9 @@ def build_layer(moe, w, T, seed, pool, device):
 
 def launches_per_forward(arm, T):
     """Kernels one moe_forward launches: arm 0 one; arm 1 route+permute, gate_up, down+combine;
-    arm 2 route, the permutation (one kernel up to 64 tokens, else three plus the work list),
-    the activation gather, gate_up, the h conversion, down, combine; arm 3 the same without the
-    two f16 conversions."""
-    return {0: 1, 1: 3, 2: 7 if T <= 64 else 10, 3: 5 if T <= 64 else 8}[arm]
+    arm 2 route+permute (one cooperative kernel), the expert-ordered f16 copy of x, gate_up, the
+    f16 copy of h, down, combine; arm 3 route+permute, gate_up, down, combine."""
+    return {0: 1, 1: 3, 2: 6, 3: 4}[arm]
 
 
 def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds, cpu_baseline):
@@ -562,7 +561,8 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     if any(status):
         raise RuntimeError(f"{name}: device status {status}")
     stage_names = (["whole layer (one launch)", "-", "-", "-"] if all(a == 0 for a in arms)
-                   else ["route+permute", "gate_up", "down", "combine"])
+                   else ["route+permute+x gather", "gate_up GEMM", "h conversion+down GEMM", "combine"]
+                   if all(a == 2 for a in arms) else ["route+permute", "gate_up", "down", "combine"])
     res = {"value": value, "unit": UNIT, "steps": steps, "warmup": warmup, "ms_per_step": ms_per_step,
            "config": describe(name), "roofline": roofline, "layer_roofline": layer, "e2e": e2e,
            "with_router": with_router,

@@ -146,7 +146,8 @@ moe_status_t moe_forward(const uint16_t* x, const float* logits,
 /* moe_forward with per-stage timing (the per-stage microsecond hooks of the handover briefs'
  * measure-first steps, as CUDA events).  stage_events, when not NULL, points to 5 cudaEvent_t
  * (created with timing enabled) that are recorded on `stream`: [0] before routing, [1] after
- * the permutation and work list, [2] after gate_up, [3] after down, [4] after combine.  On the
+ * the permutation and work list (on arm 2 also the expert-ordered f16 copy of x), [2] after the
+ * gate_up GEMM, [3] after down (on arm 2 with the f16 conversion of h), [4] after combine.  On the
  * decode arm down and combine are one kernel, so [3] and [4] are recorded together; on arm 0
  * (see moe_forward_arm) the whole layer is one kernel and [1]..[4] follow it.  With
  * stage_events == NULL this is moe_forward. */

@@ -155,14 +155,11 @@ int tile_rows_for(const moe_shape_t& s) {
 }
 
 // The tensor-core arm takes its activations as f16 rows with power-of-two row exponents, in
-// expert order: x is converted into the workspace first (h already is in order), token-major
-// from the inverse map when the caller has it (slot_pos, moe_forward), else gathered by
-// sorted_slot.
-cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, const int32_t* slot_pos,
-                           cudaStream_t cs) {
+// expert order: x is gathered by sorted_slot and converted into the workspace first (h already
+// is in order).  moe_forward writes the same rows token-major from the inverse map instead.
+cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaStream_t cs) {
   if (arm_for(s) != Arm::kTc) return launch_gate_up_simt(a, cs);
-  cudaError_t e = slot_pos ? launch_act_scatter_f16(a.act, slot_pos, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs)
-                           : launch_act_gather_f16(a.act, a.sorted_slot, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs);
+  cudaError_t e = launch_act_gather_f16(a.act, a.sorted_slot, s.T, s.k, s.H, ws.xf, ws.xe, ws.status, cs);
   if (e != cudaSuccess) return e;
   a.act = ws.xf;
   a.act_factor = ws.xe;
@@ -370,7 +367,7 @@ moe_status_t moe_grouped_gate_up(const uint16_t* x, const int32_t* sorted_slot,
   cudaError_t e = launch_build_tiles(offsets, s.T, s.E, s.k, s.has_shared, tile_rows_for(s),
                                      w.tiles, w.meta, w.status, cs);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, w, nullptr, cs));
+  return cuda_status(launch_gate_up(grouped_args(*gate_up, s, x, sorted_slot, w, h), s, w, cs));
 }
 
 moe_status_t moe_grouped_down(const uint16_t* h, const int32_t* offsets,
@@ -502,12 +499,24 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     return cuda_status(e);
   }
   // grouped-GEMM arms: routing, permutation and work list in one cooperative launch
+  // (on the tensor-core arm also the expert-ordered f16 rows of x, written token-major from the
+  // inverse map so that each x row is read once; stage event 1 follows them)
+  const bool tc = arm_for(s) == Arm::kTc;
   e = launch_route_permute_large(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w, w.counts,
                                  w.offsets, w.sorted_slot, w.slot_pos, w.hist, w.tiles, w.meta,
                                  tile_rows_for(s), w.status, cs);
+  if (e == cudaSuccess && tc) e = launch_act_scatter_f16(x, w.slot_pos, s.T, s.k, s.H, w.xf, w.xe, w.status, cs);
   if (e == cudaSuccess) e = mark(1);
-  if (e == cudaSuccess)
-    e = launch_gate_up(grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h), s, w, w.slot_pos, cs);
+  if (e == cudaSuccess) {
+    GroupedArgs ga = grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h);
+    if (tc) {
+      ga.act = w.xf;
+      ga.act_factor = w.xe;
+      e = launch_gate_up_tc(ga, cs);
+    } else {
+      e = launch_gate_up_simt(ga, cs);
+    }
+  }
   if (e == cudaSuccess) e = mark(2);
   if (e == cudaSuccess) e = launch_down(grouped_args(*down, s, w.h, nullptr, w, w.y), s, w, cs);
   if (e == cudaSuccess) e = mark(3);
