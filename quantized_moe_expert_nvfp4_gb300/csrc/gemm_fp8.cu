@@ -280,25 +280,38 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp8_kernel(const __g
           // a gate lane finishes columns c0..c0+7 and its up partner (lane ^ 16) c0+8..c0+15,
           // each receiving the other's scaled half by one exchange
           const int cb = is_gate ? 0 : 8;
+          float gv[8], uv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const float mine0 = __uint_as_float(v[i]) * rowf, mine1 = __uint_as_float(v[8 + i]) * rowf;
             const float other = __shfl_xor_sync(0xffffffffu, is_gate ? mine1 : mine0, 16);
             const float sc = __shfl_sync(0xffffffffu, colf, (c0 & 31) + cb + i);
-            const int col = c0 + cb + i;
-            if (col < td.z) {
-              const float g = (is_gate ? mine0 : other) * sc;
-              const float u = (is_gate ? other : mine1) * sc;
-              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + j] =
-                  f32_to_bf16_bits(silu_f32(g) * u);
-            }
+            gv[i] = (is_gate ? mine0 : other) * sc;
+            uv[i] = (is_gate ? other : mine1) * sc;
+          }
+          uint16_t* hcol = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(td.y + c0 + cb) * a.out_ld + j;
+          if (c0 + 16 <= td.z) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hcol[static_cast<int64_t>(i) * a.out_ld] = f32_to_bf16_bits(silu_f32(gv[i]) * uv[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c0 + cb + i < td.z) hcol[static_cast<int64_t>(i) * a.out_ld] = f32_to_bf16_bits(silu_f32(gv[i]) * uv[i]);
           }
         } else {
+          // the column factors first, then the stores: unguarded for a full 16-column chunk (a
+          // store guarded per element inside the shuffle sequence cost as much as the MMAs)
           float* yrow = static_cast<float*>(a.out) + static_cast<int64_t>(td.y + c0) * a.out_ld + wrow;
+          float sc[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float sc = __shfl_sync(0xffffffffu, colf, (c0 & 31) + i);
-            if (c0 + i < td.z) yrow[static_cast<int64_t>(i) * a.out_ld] = __uint_as_float(v[i]) * rowf * sc;
+          for (int i = 0; i < 16; ++i) sc[i] = __shfl_sync(0xffffffffu, colf, (c0 & 31) + i) * rowf;
+          if (c0 + 16 <= td.z) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) yrow[static_cast<int64_t>(i) * a.out_ld] = __uint_as_float(v[i]) * sc[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c0 + i < td.z) yrow[static_cast<int64_t>(i) * a.out_ld] = __uint_as_float(v[i]) * sc[i];
           }
         }
       }

@@ -456,17 +456,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool is_gate = lane < 16;
           const int j = mb * 64 + q * 16 + (lane & 15);
           const int cb = is_gate ? 0 : 8;
+          float gv[8], uv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t other = __shfl_xor_sync(0xffffffffu, is_gate ? v[8 + i] : v[i], 16);
             const float sc = __shfl_sync(0xffffffffu, colf, (c0 & 31) + cb + i);
-            const int col = c0 + cb + i;
-            if (col < td.z) {
-              const float g = __uint_as_float(is_gate ? v[i] : other) * sc;
-              const float u = __uint_as_float(is_gate ? other : v[8 + i]) * sc;
-              static_cast<uint16_t*>(a.out)[static_cast<int64_t>(td.y + col) * a.out_ld + j] =
-                  f32_to_bf16_bits(silu_f32(g) * u);
-            }
+            gv[i] = __uint_as_float(is_gate ? v[i] : other) * sc;
+            uv[i] = __uint_as_float(is_gate ? other : v[8 + i]) * sc;
+          }
+          // unguarded stores for a full 16-column chunk
+          uint16_t* hcol = static_cast<uint16_t*>(a.out) + static_cast<int64_t>(td.y + c0 + cb) * a.out_ld + j;
+          if (c0 + 16 <= td.z) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hcol[static_cast<int64_t>(i) * a.out_ld] = f32_to_bf16_bits(silu_f32(gv[i]) * uv[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c0 + cb + i < td.z) hcol[static_cast<int64_t>(i) * a.out_ld] = f32_to_bf16_bits(silu_f32(gv[i]) * uv[i]);
           }
         } else {
           float* yrow = static_cast<float*>(a.out) + static_cast<int64_t>(td.y + c0) * a.out_ld + mb * kBM +
