@@ -60,6 +60,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--warmup-seconds", type=float, default=1.0,
                    help="keep warming up (whole steps) at least this long, for steady clocks")
+    p.add_argument("--fp8", action="store_true", help="with --one-forward: the FP8-activation arm")
     p.add_argument("--one-forward", type=int, default=None, metavar="LAYER",
                    help="profiling aid: build layer LAYER of the workload, run four forwards, exit "
                         "(no timing, no JSON line)")
@@ -601,8 +602,13 @@ def run_ours(args):
         w = synth.WORKLOADS[head]
         T, seed = workload_entries(head)[args.one_forward]
         L = build_layer(moe, w, T, seed, 1, device)
+        if args.fp8:
+            gu8, dn8 = moe.prepare_fp8(L["gu"]), moe.prepare_fp8(L["dn"])
         for _ in range(4):
-            moe.forward(L["xs"][0], L["lgs"][0], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+            if args.fp8:
+                moe.forward_fp8(L["xs"][0], L["lgs"][0], gu8, dn8, L["ms"], L["ws"], out=L["out"])
+            else:
+                moe.forward(L["xs"][0], L["lgs"][0], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
         torch.cuda.synchronize()
         if moe.device_status(L["ws"]) != 0:
             raise RuntimeError(f"device status {moe.device_status(L['ws'])}")
