@@ -198,6 +198,13 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   return a;
 }
 
+// Routing, permutation and work list of the grouped-GEMM arms: one cooperative launch.
+cudaError_t launch_route_permute(const float* logits, const moe_shape_t& s, const Ws& w, int tile_rows,
+                                 cudaStream_t cs) {
+  return launch_route_permute_large(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w, w.counts, w.offsets,
+                                    w.sorted_slot, w.slot_pos, w.hist, w.tiles, w.meta, tile_rows, w.status, cs);
+}
+
 // The router GEMM runs on the tcgen05 grouped GEMM (one group of E weight rows) for batches
 // above the decode sizes when E and H fit its tiles, else on the CUDA-core kernel.
 // The CUDA-core router up to 32 tokens (measured on GB300 at H = 2048, E = 512: 5.8 us against
@@ -502,9 +509,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
   // (on the tensor-core arm also the expert-ordered f16 rows of x, written token-major from the
   // inverse map so that each x row is read once; stage event 1 follows them)
   const bool tc = arm_for(s) == Arm::kTc;
-  e = launch_route_permute_large(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w, w.counts,
-                                 w.offsets, w.sorted_slot, w.slot_pos, w.hist, w.tiles, w.meta,
-                                 tile_rows_for(s), w.status, cs);
+  e = launch_route_permute(logits, s, w, tile_rows_for(s), cs);
   if (e == cudaSuccess && tc) e = launch_act_scatter_f16(x, w.slot_pos, s.T, s.k, s.H, w.xf, w.xe, w.status, cs);
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess) {
@@ -631,9 +636,7 @@ moe_status_t moe_forward_fp8(const uint16_t* x, const float* logits, const moe_f
   uint8_t* hq = reinterpret_cast<uint8_t*>(w.hf);
   const int S = s.T * s.k;
   const int64_t R = static_cast<int64_t>(S) + s.T;
-  cudaError_t e = launch_route_permute_large(logits, nullptr, s.T, s.E, s.k, s.has_shared, w.ids, w.w, w.counts,
-                                             w.offsets, w.sorted_slot, w.slot_pos, w.hist, w.tiles, w.meta,
-                                             kTcTileRows, w.status, cs);
+  cudaError_t e = launch_route_permute(logits, s, w, kTcTileRows, cs);
   if (e == cudaSuccess) e = launch_act_scatter_fp8(x, w.slot_pos, s.T, s.k, s.H, xq, w.xe, w.status, cs);
   if (e == cudaSuccess) e = launch_gate_up_fp8(fp8_args(*gate_up, s, w, xq, w.xe, w.h), cs);
   if (e == cudaSuccess) e = launch_act_quant_fp8(w.h, nullptr, 0, 1, R, s.I, hq, w.he, w.status, cs);

@@ -69,16 +69,19 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
   }
 }
 
-// Token-major version of the expert-order gather: one warp per token reads its row once and
-// writes the f16 row to every expert-ordered row that holds the token (slot_pos[t k + j] for its
-// k ranks, and S + t for the shared expert).  Each token row is read from memory once instead of
-// k + 1 times (a 32k-token batch of x is larger than L2).
+// Token-major version of the expert-order gather: a warp reads its token's row and writes the
+// f16 row to every expert-ordered row that holds the token (slot_pos[t k + j] for its k ranks,
+// and S + t for the shared expert).  Each token row is read from memory once instead of k + 1
+// times (a 32k-token batch of x is larger than L2).  For small batches `slices` warps share a
+// token, each taking the row maximum over the whole row and then converting and writing its
+// 1 / slices of the columns (K / 256 divisible by slices).
 __global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __restrict__ src,
                                                               const int32_t* __restrict__ slot_pos, int T, int k,
                                                               uint16_t* __restrict__ dst, float* __restrict__ factor,
-                                                              int K, int32_t* status) {
+                                                              int K, int slices, int32_t* status) {
   const int lane = threadIdx.x & 31;
-  const int t = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int t = static_cast<int>(gw / slices), sl = static_cast<int>(gw % slices);
   if (t >= T) return;
   const int S = T * k;
   // destination rows: lane j < k holds rank j's row, lane k the shared expert's row S + t
@@ -107,8 +110,9 @@ __global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   const int e = (m > 0.0f && m <= 3.4e38f) ? max(ilogbf(m) - 14, -126) : 0;
   const float inv = __int_as_float((127 - e) << 23);
-  if (p >= 0) factor[p] = __int_as_float((127 + e) << 23);
-  for (int c = lane; c < K / 8; c += 32) {
+  if (p >= 0 && sl == 0) factor[p] = __int_as_float((127 + e) << 23);
+  const int per = K / 8 / slices;   // uint4 columns of this warp's slice
+  for (int c = sl * per + lane; c < (sl + 1) * per; c += 32) {
     const uint4 v = __ldg(s + c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[4];
@@ -130,8 +134,13 @@ __global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __
 cudaError_t launch_act_scatter_f16(const uint16_t* x, const int32_t* slot_pos, int T, int k, int K, uint16_t* dst,
                                    float* factor, int32_t* status, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
-  act_scatter_f16_kernel<<<static_cast<unsigned>((static_cast<int64_t>(T) + 7) / 8), 256, 0, st>>>(
-      x, slot_pos, T, k, dst, factor, K, status);
+  // slices per token: enough warps for about 16 per SM on a 152-SM GPU, at most K / 256
+  int slices = 1;
+  while (slices * 2 <= K / 256 && static_cast<int64_t>(T) * slices < 152 * 16) slices *= 2;
+  while ((K / 256) % slices) slices /= 2;
+  const int64_t warps = static_cast<int64_t>(T) * slices;
+  act_scatter_f16_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(x, slot_pos, T, k, dst, factor, K,
+                                                                                slices, status);
   return cudaGetLastError();
 }
 

@@ -238,12 +238,14 @@ __global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
   }
   __syncthreads();
   if (!s_ok) return;
-  // counts, offsets and this CTA's bases: thread e sums column e of the histograms
+  // counts, offsets and this CTA's bases: thread e sums column e of the histograms (of the CTAs
+  // that own tokens: with T < G the others' are zero)
   const int e = threadIdx.x;
+  const int g_used = per > 0 ? (T + per - 1) / per : 0;
   int before = 0, total = 0;
   if (e < E) {
 #pragma unroll 8
-    for (int c = 0; c < G; ++c) {
+    for (int c = 0; c < g_used; ++c) {
       const int v = __ldcg(hist + static_cast<int64_t>(c) * E + e);
       total += v;
       before += (c < b) ? v : 0;
@@ -332,7 +334,7 @@ cudaError_t launch_route_permute_large(const float* logits, const int32_t* ids_i
   auto kern = (E <= 256) ? route_permute_large_kernel<8>
              : (E <= 512) ? route_permute_large_kernel<16> : route_permute_large_kernel<32>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(std::min(n_sm, kPermuteMaxGrid));
+  cfg.gridDim = dim3(std::min(n_sm, kPermuteMaxGrid));   // fixed per device: the barrier count is monotonic
   cfg.blockDim = dim3(1024);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
