@@ -149,7 +149,7 @@ int forward_arm(const moe_shape_t& s) {
 int tile_rows_for(const moe_shape_t& s) {
   switch (arm_for(s)) {
     case Arm::kDecode: return kDecodeMaxT;
-    case Arm::kTc: return kTcTileRows;
+    case Arm::kTc: return s.T <= kDecodeMaxT ? 64 : kTcTileRows;   // 64-row tiles for small batches
     default: return kSimtTileRows;
   }
 }
@@ -192,6 +192,7 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   a.tiles = ws.tiles;
   a.meta = ws.meta;
   a.max_tiles = max_tiles_for(s, tile_rows_for(s));
+  a.tile_rows = tile_rows_for(s);
   a.out = out;
   a.status = ws.status;
   a.act_factor = nullptr;

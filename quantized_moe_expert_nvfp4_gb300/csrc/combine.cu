@@ -30,17 +30,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    int64_t p = __ldg(slot_pos + static_cast<int64_t>(t) * k + j);
-    if (p < 0 || p >= S) {  // caller-provided index
-      if (status) report_device_error(status, kDevBadIndex);
-      p = 0;
-    }
-    const float wj = __ldg(topk_w + static_cast<int64_t>(t) * k + j);
-    float v[8];
-    load8(y + p * H + c, v);
+  // ranks in groups of four: the group's row loads are issued together, then summed in rank order
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    float v[4][8], wj[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, v[i], acc[i]);
+    for (int q = 0; q < 4; ++q) {
+      if (j0 + q < k) {
+        int64_t p = __ldg(slot_pos + static_cast<int64_t>(t) * k + j0 + q);
+        if (p < 0 || p >= S) {  // caller-provided index
+          if (status) report_device_error(status, kDevBadIndex);
+          p = 0;
+        }
+        wj[q] = __ldg(topk_w + static_cast<int64_t>(t) * k + j0 + q);
+        load8(y + p * H + c, v[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (j0 + q < k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[q], v[q][i], acc[i]);
   }
   if (has_shared) {
     float v[8];

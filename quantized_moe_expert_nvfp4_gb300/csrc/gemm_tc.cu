@@ -40,22 +40,33 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128;                      // weight rows per tile (MMA M)
-constexpr int kBN = kTcTileRows;              // tokens per tile at most (MMA N, rounded up to 16)
 constexpr int kBK = 64;                       // K per 128-byte swizzled operand row
 constexpr int kGK = 256;                      // K per pipeline group
 constexpr int kAStages = 4;                   // packed-weight ring (SMEM), one group per stage
-constexpr int kGStages = 2;                   // group ring: dequantized A (TMEM) + activations (SMEM)
 constexpr int kAPackedBytes = kBM * kGK / 2;  // 16 KB: 128 rows x 128 B, 128B swizzle
 constexpr int kAScaleBytes = kBM * kGK / 16;  // 2 KB: 128 rows x 16 B
 constexpr int kAStageBytes = kAPackedBytes + kAScaleBytes;
-constexpr int kBSubBytes = kBN * kBK * 2;     // 16 KB: 128 rows x 128 B, 128B swizzle
-constexpr int kBStageBytes = (kGK / kBK) * kBSubBytes;   // 64 KB: four 64-wide sub-tiles
 constexpr int kTmemCols = 512;
-constexpr int kDCol = 0;                      // accumulators: 2 x kBN columns
-constexpr int kACol = 2 * kBN;                // A stages: kGStages x kGK / 2 columns
-static_assert(kACol + kGStages * (kGK / 2) <= kTmemCols, "TMEM budget");
-static_assert(kBN == 128, "the epilogue holds four 32-column groups of row factors");
+constexpr int kGStagesMax = 3, kBStagesMax = 4;
 static_assert(kGK / kBK == 4, "a group is four 64-wide chunks");
+
+// Per-tile-size layout.  kBN = the tile's token rows at most (MMA N, rounded up to 16): 128 for
+// prefill; 64 for small batches, where the smaller accumulators leave TMEM room for a third
+// dequantized A stage and the smaller activation stages for four of them in the same SMEM (the
+// activation stage's load is otherwise exposed once per group at a few tokens per expert).
+template <int kBNt>
+struct TcCfg {
+  static constexpr int kBN = kBNt;
+  static constexpr int kGStages = kBNt == 64 ? 3 : 2;          // dequantized A stages (TMEM)
+  static constexpr int kBStages = kBNt == 64 ? 4 : 2;          // activation stages (SMEM)
+  static constexpr int kBSubBytes = kBN * kBK * 2;             // kBN rows x 128 B, 128B swizzle
+  static constexpr int kBStageBytes = (kGK / kBK) * kBSubBytes;  // four 64-wide sub-tiles
+  static constexpr int kDCol = 0;                              // accumulators: 2 x kBN columns
+  static constexpr int kACol = 2 * kBN;                        // A stages: kGStages x kGK / 2 columns
+  static_assert(kBN == 64 || kBN == 128, "tile rows");
+  static_assert(kACol + kGStages * (kGK / 2) <= kTmemCols, "TMEM budget");
+  static_assert(kGStages <= kGStagesMax && kBStages <= kBStagesMax, "barrier arrays");
+};
 
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq = 2, kWarpTmaB = 10, kWarpEpi = 11, kWarpTmaS = 15;
 constexpr int kDeqWarps = 8;
@@ -72,7 +83,7 @@ constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s: no legitimate wait c
 struct TcMaps {
   CUtensorMap a;                // packed e2m1
   CUtensorMap s;                // e4m3 scales
-  CUtensorMap b[kBN / 16];      // f16 activations
+  CUtensorMap b[kTcTileRows / 16];   // f16 activations (the 64-row tiles use the first four)
 };
 
 struct TcArgs {
@@ -89,9 +100,10 @@ struct TcArgs {
 struct Smem {
   uint64_t a_full[kAStages];     // packed tile + scales landed (TMA transaction)
   uint64_t a_free[kAStages];     // every dequant warp is done reading the stage
-  uint64_t g_full[kGStages];     // a group's A is in TMEM (one arrival per dequant warp) and its
-                                 // activations have landed (the producer's arrival + transaction)
-  uint64_t g_free[kGStages];     // the MMAs reading that group's TMEM and SMEM stages completed
+  uint64_t g_full[kGStagesMax];  // a group's A is in TMEM (one arrival per dequant warp)
+  uint64_t g_free[kGStagesMax];  // the MMAs reading that TMEM stage completed
+  uint64_t b_full[kBStagesMax];  // a group's activations landed (the producer's transaction)
+  uint64_t b_free[kBStagesMax];  // the MMAs reading that activation stage completed
   uint64_t acc_full[2];
   uint64_t acc_empty[2];         // one arrival per epilogue warp
   uint64_t drain;
@@ -168,13 +180,16 @@ __device__ __forceinline__ int4 load_tile(const TcArgs& a, int item, int n_items
   return item < n_items ? __ldg(a.tiles + item / MB) : make_int4(0, 0, 0, 0);
 }
 
-template <bool kGateUp>
+template <bool kGateUp, int kBNt>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs a) {
+  using C = TcCfg<kBNt>;
+  constexpr int kBN = C::kBN, kGStages = C::kGStages, kBStages = C::kBStages;
+  constexpr int kBStageBytes = C::kBStageBytes, kDCol = C::kDCol, kACol = C::kACol;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sB = base;                                   // kGStages x 64 KB (1024-aligned)
-  uint8_t* sA = base + kGStages * kBStageBytes;         // kAStages x 18 KB (1024-aligned)
+  uint8_t* sB = base;                                   // kBStages activation stages (1024-aligned)
+  uint8_t* sA = base + kBStages * kBStageBytes;         // kAStages x 18 KB (1024-aligned)
   Smem* sm = reinterpret_cast<Smem*>(sA + kAStages * kAStageBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -188,8 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->a_free[s], kDeqWarps);
     }
     for (int s = 0; s < kGStages; ++s) {
-      mbar_init(&sm->g_full[s], kDeqWarps + 1);
+      mbar_init(&sm->g_full[s], kDeqWarps);
       mbar_init(&sm->g_free[s], 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(&sm->b_full[s], 1);
+      mbar_init(&sm->b_free[s], 1);
     }
     for (int d = 0; d < 2; ++d) {
       mbar_init(&sm->acc_full[d], 1);
@@ -291,16 +310,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n16 = (td.z + 15) >> 4;                 // 16-row blocks of the tile
         const CUtensorMap* mb_map = &maps.b[n16 - 1];
         for (int g = 0; g < KG; ++g, ++ib) {
-          const int sb = ib % kGStages;
-          if (!(ok = mbar_wait(&sm->g_free[sb], ((ib / kGStages) & 1) ^ 1, sm, a.status))) break;
-          mbar_expect_tx(&sm->g_full[sb], (kGK / kBK) * n16 * 16 * kBK * 2);
-          tma_load_3d(sB + sb * kBStageBytes, mb_map, 0, td.y, g * (kGK / kBK), &sm->g_full[sb]);
+          const int sb = ib % kBStages;
+          if (!(ok = mbar_wait(&sm->b_free[sb], ((ib / kBStages) & 1) ^ 1, sm, a.status))) break;
+          mbar_expect_tx(&sm->b_full[sb], (kGK / kBK) * n16 * 16 * kBK * 2);
+          tma_load_3d(sB + sb * kBStageBytes, mb_map, 0, td.y, g * (kGK / kBK), &sm->b_full[sb]);
         }
       }
       if (!ok) {  // let the copies in flight land: the last stages' transactions (bounded)
-        for (int j = 0; j < kGStages && ib > 0; ++j, --ib) {
+        for (int j = 0; j < kBStages && ib > 0; ++j, --ib) {
           const uint32_t q = ib - 1;
-          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->g_full[q % kGStages], (q / kGStages) & 1); ++i) {
+          for (uint32_t i = 0; i < (1u << 16) && !mbar_try(&sm->b_full[q % kBStages], (q / kBStages) & 1); ++i) {
           }
         }
       }
@@ -321,15 +340,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem + kDCol + d * kBN;
       for (int g = 0; g < KG; ++g, ++ig) {
-        const int gs = ig % kGStages;
+        const int gs = ig % kGStages, bs = ig % kBStages;
         if (!(ok = warp_wait(&sm->g_full[gs], (ig / kGStages) & 1, sm, a.status))) break;
+        if (!(ok = warp_wait(&sm->b_full[bs], (ig / kBStages) & 1, sm, a.status))) break;
         tc_fence_after();
         if (elect_one()) {
           const uint32_t a_tmem = tmem + kACol + gs * (kGK / 2);
 #pragma unroll
           for (int c = 0; c < kGK / kBK; ++c) {       // 64-wide chunk c of the group
             // sub-tile c of the stage starts c * n rows (n * 128 B, a multiple of 2 KB) in
-            const uint32_t b_addr = smem_u32(sB + gs * kBStageBytes + c * n * (kBK * 2));
+            const uint32_t b_addr = smem_u32(sB + bs * kBStageBytes + c * n * (kBK * 2));
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
               const uint32_t at = a_tmem + c * (kBK / 2) + kk * 8;
@@ -341,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_commit(&sm->g_free[gs]);
+          tc_commit(&sm->b_free[bs]);
         }
         __syncwarp();
       }
@@ -447,7 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         TC_LD16(t_lane + kDCol + d * kBN + c0, v);
         // scale of column c0 + i: lane (c0 & 31) + i of register c0 / 32
         const int cr = c0 >> 5;
-        const float colf = s2 * (cr == 0 ? cf[0] : cr == 1 ? cf[1] : cr == 2 ? cf[2] : cf[3]);
+        float colf = cf[0];
+#pragma unroll
+        for (int i = 1; i < kBN / 32; ++i)
+          if (cr == i) colf = cf[i];
+        colf *= s2;
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         if (kGateUp) {
           // lanes 0-15 hold gate rows j, lanes 16-31 the up rows j (j = mb*64 + 16q + lane%16);
@@ -523,13 +548,20 @@ bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const v
   return make_tensor_map(m, dt, 2, ptr, dims, strides, box, sw);
 }
 
-constexpr size_t kSmemBytes = 1024 + kGStages * kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+template <int kBNt>
+constexpr size_t smem_bytes() {
+  return 1024 + TcCfg<kBNt>::kBStages * TcCfg<kBNt>::kBStageBytes + kAStages * kAStageBytes + sizeof(Smem);
+}
+static_assert(smem_bytes<128>() <= 232448 && smem_bytes<64>() <= 232448, "shared memory per CTA");
 
 template <bool kGateUp>
 cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
-  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp>),
-                                      static_cast<int>(kSmemBytes));
+  const bool small = g.tile_rows == 64;
+  const void* kern = small ? reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 64>)
+                           : reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 128>);
+  const size_t smem = small ? smem_bytes<64>() : smem_bytes<128>();
+  if (g.tile_rows != 64 && g.tile_rows != kTcTileRows) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_dynamic_smem(kern, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   int n_sm = 0;
   if ((e = current_sm_count(&n_sm)) != cudaSuccess) return e;
@@ -553,7 +585,7 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
                            CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   // activations viewed as {64 columns, rows, K / 64 chunks}: chunk z of row y at y * 2K + 128 z bytes
-  for (int i = 0; ok && i < kBN / 16; ++i)
+  for (int i = 0; ok && i < g.tile_rows / 16; ++i)
     ok = make_map_3d(&maps.b[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.act, kBK, act_rows, g.K / kBK,
                      static_cast<uint64_t>(g.K) * 2, kBK * 2, kBK, 16 * (i + 1), kGK / kBK,
                      CU_TENSOR_MAP_SWIZZLE_128B);
@@ -570,7 +602,10 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.status = g.status;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, n_sm));
-  grouped_gemm_tc_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(maps, a);
+  if (small)
+    grouped_gemm_tc_kernel<kGateUp, 64><<<grid, kThreads, smem, st>>>(maps, a);
+  else
+    grouped_gemm_tc_kernel<kGateUp, 128><<<grid, kThreads, smem, st>>>(maps, a);
   return cudaGetLastError();
 }
 

@@ -152,6 +152,7 @@ struct GroupedArgs {
   void* out;                    // h [S + T, I] bf16 (gate_up) or y [S + T, H] fp32 (down)
   int32_t* status;              // device status word (bad indices are clamped and reported)
   const float* act_factor;      // tensor-core arm: 2^e of each f16 act row
+  int tile_rows = kTcTileRows;  // tensor-core arm: rows per work item of the list (64 or 128)
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
