@@ -3,6 +3,8 @@
 #include <algorithm>
 #include <atomic>
 
+#include <cmath>
+
 #include "internal.cuh"
 
 namespace moe {
@@ -524,11 +526,27 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     }
   }
   if (e == cudaSuccess) e = mark(2);
-  if (e == cudaSuccess) e = launch_down(grouped_args(*down, s, w.h, nullptr, w, w.y), s, w, cs);
+  // The tensor-core arm hands y to the combine compact: f16 of the raw down accumulator times
+  // 2^-c, c fixed by the accumulator's bound (|e2m1 x e4m3| <= 2688 and the f16 rows of h below
+  // 2^15, so |acc| <= I * 2688 * 2^15 and |acc| * 2^-c stays below f16's maximum); the values keep
+  // f16's 11 significant bits, and the combine multiplies them by scale2 * (h row factor) * 2^c.
+  const int64_t R = static_cast<int64_t>(s.T) * s.k + s.T;
+  uint16_t* y16 = tc ? reinterpret_cast<uint16_t*>(w.y) : nullptr;
+  float* rowf = tc ? reinterpret_cast<float*>(y16 + R * s.H) : nullptr;   // after the f16 rows, in the y region
+  if (e == cudaSuccess) {
+    GroupedArgs da = grouped_args(*down, s, w.h, nullptr, w, w.y);
+    if (tc) {
+      const int c = static_cast<int>(std::ceil(std::log2(static_cast<double>(s.I) * 2688.0 * 32768.0 / 65504.0)));
+      da.y16 = y16;
+      da.y16_scale = std::ldexp(1.0f, -c);
+      da.y16_rowf = rowf;
+    }
+    e = launch_down(da, s, w, cs);
+  }
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
-    e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32,
-                       w.status, cs);
+    e = tc ? launch_combine_y16(y16, rowf, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs)
+           : launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
 }
@@ -641,9 +659,20 @@ moe_status_t moe_forward_fp8(const uint16_t* x, const float* logits, const moe_f
   if (e == cudaSuccess) e = launch_act_scatter_fp8(x, w.slot_pos, s.T, s.k, s.H, xq, w.xe, w.status, cs);
   if (e == cudaSuccess) e = launch_gate_up_fp8(fp8_args(*gate_up, s, w, xq, w.xe, w.h), cs);
   if (e == cudaSuccess) e = launch_act_quant_fp8(w.h, nullptr, 0, 1, R, s.I, hq, w.he, w.status, cs);
-  if (e == cudaSuccess) e = launch_down_fp8(fp8_args(*down, s, w, hq, w.he, w.y), cs);
+  // y compact as on the W4A16 tensor-core arm: f16(acc * weight-row scale * 2^-c), with
+  // |acc| <= I * 448^2 and the row scale <= 2688 / 448 (an NVFP4 row's largest value over 448)
+  const int c = static_cast<int>(std::ceil(std::log2(static_cast<double>(s.I) * 448.0 * 448.0 * 6.0 / 65504.0)));
+  uint16_t* y16 = reinterpret_cast<uint16_t*>(w.y);
+  float* rowf = reinterpret_cast<float*>(y16 + R * s.H);
+  if (e == cudaSuccess) {
+    GroupedFp8Args da = fp8_args(*down, s, w, hq, w.he, w.y);
+    da.y16 = y16;
+    da.y16_scale = std::ldexp(1.0f, -c);
+    da.y16_rowf = rowf;
+    e = launch_down_fp8(da, cs);
+  }
   if (e == cudaSuccess)
-    e = launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs);
+    e = launch_combine_y16(y16, rowf, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs);
   return cuda_status(e);
 }
 

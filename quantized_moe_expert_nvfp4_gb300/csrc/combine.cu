@@ -72,7 +72,87 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
+// The same sum over the compact y of the tensor-core down (one thread per (token, 8 columns)):
+// row p's values are f16 * rowf[p], rowf written by the down epilogue (the factor the fp32 path
+// applies to the accumulator, times the power of two the compact form removed).
+__global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __restrict__ y16,
+                                                          const float* __restrict__ rowf,
+                                                          const int32_t* __restrict__ slot_pos,
+                                                          const float* __restrict__ topk_w, int T, int H, int k,
+                                                          int has_shared, void* out, int out_is_fp32,
+                                                          int32_t* status) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int cpr = H / 8;
+  if (idx >= static_cast<int64_t>(T) * cpr) return;
+  const int t = static_cast<int>(idx / cpr);
+  const int c = static_cast<int>(idx % cpr) * 8;
+  const int64_t S = static_cast<int64_t>(T) * k;
+  auto load8 = [&](int64_t row, float (&f)[8]) {
+    const uint4 h = __ldg(reinterpret_cast<const uint4*>(y16 + row * H + c));
+    const float fr = __ldg(rowf + row);
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xffffu))) * fr;
+      f[2 * i + 1] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * fr;
+    }
+  };
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    float v[4][8], wj[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (j0 + q < k) {
+        const int64_t s = static_cast<int64_t>(t) * k + j0 + q;
+        int64_t p = __ldg(slot_pos + s);
+        if (p < 0 || p >= S) {
+          if (status) report_device_error(status, kDevBadIndex);
+          p = 0;
+        }
+        wj[q] = __ldg(topk_w + s);
+        load8(p, v[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (j0 + q < k)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[q], v[q][i], acc[i]);
+  }
+  if (has_shared) {
+    float v[8];
+    load8(S + t, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+  }
+  const int64_t o = static_cast<int64_t>(t) * H + c;
+  if (out_is_fp32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  } else {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * i])) |
+             (static_cast<uint32_t>(f32_to_bf16_bits(acc[2 * i + 1])) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_combine_y16(const uint16_t* y16, const float* rowf, const int32_t* slot_pos, const float* topk_w,
+                               int T, int H, int k, int has_shared, void* out, int out_is_fp32, int32_t* status,
+                               cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(T) * (H / 8);
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  combine_y16_kernel<<<blocks, 256, 0, st>>>(y16, rowf, slot_pos, topk_w, T, H, k, has_shared, out, out_is_fp32,
+                                             status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,

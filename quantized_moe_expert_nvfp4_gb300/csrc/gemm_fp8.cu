@@ -61,6 +61,9 @@ struct F8Args {
   int out_ld;
   const float* act_scale;        // [S + T] activation-row scales (expert order)
   int32_t* status;
+  uint16_t* y16;                 // down: compact y, f16(accumulator * row scale * y16_scale), when set,
+  float y16_scale;               // and per row the factor that restores it
+  float* y16_rowf;
 };
 
 struct F8Smem {
@@ -266,6 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp8_kernel(const __g
       float cf[kBN / 32];
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) cf[i] = (32 * i + lane < td.z) ? __ldg(a.act_scale + td.y + 32 * i + lane) : 0.0f;
+      if (!kGateUp && a.y16 && mb == 0 && q == 0) {   // the tile's row factors for the combine
+        const float s2 = __ldg(a.scale2 + td.x);
+#pragma unroll
+        for (int i = 0; i < kBN / 32; ++i)
+          if (32 * i + lane < td.z) a.y16_rowf[td.y + 32 * i + lane] = s2 * cf[i] / a.y16_scale;
+      }
       if (!(ok = warp_wait(&sm->acc_full[d], (ic >> 1) & 1, sm, a.status))) break;
       tc_fence_after();
       const int n = (td.z + 15) & ~15;
@@ -297,6 +306,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_fp8_kernel(const __g
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (c0 + cb + i < td.z) hcol[static_cast<int64_t>(i) * a.out_ld] = f32_to_bf16_bits(silu_f32(gv[i]) * uv[i]);
+          }
+        } else if (a.y16) {
+          // compact y: the accumulator times the weight row's scale and a fixed power of two, as
+          // f16 (the combine applies scale2 and the activation row's scale)
+          const float f = __ldg(a.row_scale + static_cast<int64_t>(td.x) * a.Nw + wrow) * a.y16_scale;
+          uint16_t* yh = a.y16 + static_cast<int64_t>(td.y + c0) * a.out_ld + wrow;
+          if (c0 + 16 <= td.z) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              yh[static_cast<int64_t>(i) * a.out_ld] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i]) * f));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c0 + i < td.z)
+                yh[static_cast<int64_t>(i) * a.out_ld] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i]) * f));
           }
         } else {
           // the column factors first, then the stores: unguarded for a full 16-column chunk (a
@@ -381,6 +405,9 @@ cudaError_t launch_fp8(const GroupedFp8Args& g, cudaStream_t st) {
   a.out_ld = kGateUp ? g.N / 2 : g.N;
   a.act_scale = g.act_scale;
   a.status = g.status;
+  a.y16 = kGateUp ? nullptr : g.y16;
+  a.y16_scale = g.y16_scale;
+  a.y16_rowf = g.y16_rowf;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, n_sm));
   grouped_gemm_fp8_kernel<kGateUp><<<grid, kThreads, kSmemBytes, st>>>(maps, a);

@@ -95,6 +95,9 @@ struct TcArgs {
   int out_ld;
   const float* act_factor;      // 2^e of each f16 activation row (expert order)
   int32_t* status;
+  uint16_t* y16;                // down: compact y, f16(accumulator * y16_scale), when set,
+  float y16_scale;              // and per row the factor that restores it
+  float* y16_rowf;
 };
 
 struct Smem {
@@ -459,6 +462,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kBN / 32; ++i) cf[i] = cf_next[i];
       const int mb = item % MB;
       const int d = ic & 1;
+      if (!kGateUp && a.y16 && mb == 0 && q == 0) {   // the tile's row factors for the combine
+#pragma unroll
+        for (int i = 0; i < kBN / 32; ++i)
+          if (32 * i + lane < td.z) a.y16_rowf[td.y + 32 * i + lane] = s2 * cf[i] / a.y16_scale;
+      }
       if (!(ok = warp_wait(&sm->acc_full[d], (ic >> 1) & 1, sm, a.status))) break;
       tc_fence_after();
       const int n = (td.z + 15) & ~15;
@@ -498,6 +506,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (c0 + cb + i < td.z) hcol[static_cast<int64_t>(i) * a.out_ld] = f32_to_bf16_bits(silu_f32(gv[i]) * uv[i]);
+          }
+        } else if (a.y16) {
+          // compact y: the raw accumulator times a fixed power of two, as f16 (the combine applies
+          // scale2 and the row factor); two operations per element, half the bytes of fp32
+          uint16_t* yh = a.y16 + static_cast<int64_t>(td.y + c0) * a.out_ld + mb * kBM + q * 32 + lane;
+          if (c0 + 16 <= td.z) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              yh[static_cast<int64_t>(i) * a.out_ld] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i]) * a.y16_scale));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (c0 + i < td.z)
+                yh[static_cast<int64_t>(i) * a.out_ld] = __half_as_ushort(__float2half_rn(__uint_as_float(v[i]) * a.y16_scale));
           }
         } else {
           float* yrow = static_cast<float*>(a.out) + static_cast<int64_t>(td.y + c0) * a.out_ld + mb * kBM +
@@ -600,6 +622,9 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.out_ld = kGateUp ? g.N / 2 : g.N;
   a.act_factor = g.act_factor;
   a.status = g.status;
+  a.y16 = kGateUp ? nullptr : g.y16;
+  a.y16_scale = g.y16_scale;
+  a.y16_rowf = g.y16_rowf;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, n_sm));
   if (small)

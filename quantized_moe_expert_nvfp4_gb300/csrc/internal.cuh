@@ -153,6 +153,12 @@ struct GroupedArgs {
   int32_t* status;              // device status word (bad indices are clamped and reported)
   const float* act_factor;      // tensor-core arm: 2^e of each f16 act row
   int tile_rows = kTcTileRows;  // tensor-core arm: rows per work item of the list (64 or 128)
+  // tensor-core down inside moe_forward: y stored compact as f16(acc * y16_scale), the raw fp32
+  // accumulator times a power of two fixed by its bound, and per row the factor that restores it
+  // (scale2 * activation row factor / y16_scale), for launch_combine_y16
+  uint16_t* y16 = nullptr;
+  float y16_scale = 0.0f;
+  float* y16_rowf = nullptr;
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
@@ -189,6 +195,11 @@ struct GroupedFp8Args {
   int64_t max_tiles;
   void* out;                    // h [S + T, I] bf16 (gate_up) or y [S + T, H] fp32 (down)
   int32_t* status;
+  // down inside moe_forward_fp8: y compact as f16(accumulator * weight-row scale * y16_scale),
+  // and per row the factor that restores it (scale2 * activation row scale / y16_scale)
+  uint16_t* y16 = nullptr;
+  float y16_scale = 0.0f;
+  float* y16_rowf = nullptr;
 };
 cudaError_t launch_gate_up_fp8(const GroupedFp8Args& a, cudaStream_t st);
 cudaError_t launch_down_fp8(const GroupedFp8Args& a, cudaStream_t st);
@@ -251,6 +262,10 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st);
 cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,
                            int H, int k, int has_shared, void* out, int out_is_fp32,
                            int32_t* status, cudaStream_t st);
+// The same sum over the tensor-core down's compact y: row p's values are f16 * rowf[p].
+cudaError_t launch_combine_y16(const uint16_t* y16, const float* rowf, const int32_t* slot_pos, const float* topk_w,
+                               int T, int H, int k, int has_shared, void* out, int out_is_fp32, int32_t* status,
+                               cudaStream_t st);
 // Router GEMM on the CUDA cores: logits [T, E] fp32 = scale2 * x . deq(W)^T, W one NVFP4
 // projection of E rows of H (H % 16 == 0).
 cudaError_t launch_router_simt(const uint16_t* x, const moe_nvfp4_weights_t& w, int T, int H, int E, float* logits,

@@ -111,11 +111,27 @@ def test_forward_arm_selection(cuda_lib):
     assert arm(H=100) == -1
 
 
+def _compact_y_bound(y, slot_pos, w, ms, staged):
+    """Largest difference the tensor-core forward's compact y allows against the staged combine
+    over fp32 y: every y value is rounded once to f16 (relative error at most 2^-11, taken as
+    2^-10 with the products' roundings) before it is weighted and summed, plus fp32 rounding of
+    the sums and the absolute error of values in f16's subnormal range."""
+    S, T, k = ms.S, ms.T, ms.k
+    valid = y if ms.has_shared else y[:S]     # rows S.. hold the shared expert's outputs only if it exists
+    rows = slot_pos.view(T, k).long()
+    b = (w.abs()[:, :, None] * valid.abs()[rows]).sum(1)
+    if ms.has_shared:
+        b = b + y[S:].abs()
+    return 2.0 ** -10 * b + 1e-6 * staged.abs() + 1e-6 * valid.abs().max() + 1e-30
+
+
 def test_forward_deterministic_and_matches_stages(cuda_lib):
-    """Repeated forwards are bit-identical, and on the grouped-GEMM arms moe_forward equals the
-    staged calls (route, permute, gate_up, down, combine) bit for bit."""
+    """Repeated forwards are bit-identical, and moe_forward matches the staged calls (route,
+    permute, gate_up, down, combine over fp32 y): bit for bit on the CUDA-core grouped arm; on the
+    tensor-core arm, which hands y to the combine as f16 of the raw accumulator, within one f16
+    rounding of each weighted y value."""
     moe = cuda_lib
-    for case in (SMALL[2], SMALL[5], SMALL[12], SMALL[14], SMALL[15], SMALL[16]):
+    for case in (SMALL[2], SMALL[4], SMALL[5], SMALL[7], SMALL[12], SMALL[14], SMALL[15], SMALL[16]):
         L = _small_layer(case)
         ms = moe_shape(moe, L.shape)
         gu, dn = L.gpu_weights(moe)
@@ -130,13 +146,16 @@ def test_forward_deterministic_and_matches_stages(cuda_lib):
         _, offsets, sorted_slot, slot_pos = moe.permute(ids, ms, ws)
         h = moe.grouped_gate_up(x, sorted_slot, offsets, gu, ms, ws)
         y = moe.grouped_down(h, offsets, dn, ms, ws)
-        for fp32 in (True, False):
-            staged = moe.combine(y, slot_pos, w, ms, out_fp32=fp32)
-            fused = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=fp32)
-            torch.cuda.synchronize()
-            assert moe.device_status(ws) == 0
-            assert torch.equal(fused.view(torch.int16 if not fp32 else torch.int32),
-                               staged.view(torch.int16 if not fp32 else torch.int32)), (case, fp32)
+        staged = moe.combine(y, slot_pos, w, ms, out_fp32=True)
+        fused = moe.forward(x, logits, gu, dn, ms, ws, out_fp32=True)
+        torch.cuda.synchronize()
+        assert moe.device_status(ws) == 0
+        if moe.forward_arm(ms) == 2:
+            bound = _compact_y_bound(y, slot_pos, w, ms, staged)
+            err = (fused - staged).abs()
+            assert (err <= bound).all(), (case, float((err / bound).max()))
+        else:
+            assert torch.equal(fused.view(torch.int32), staged.view(torch.int32)), case
 
 
 def test_one_launch_consecutive_calls(cuda_lib):
