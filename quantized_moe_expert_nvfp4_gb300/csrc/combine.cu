@@ -87,23 +87,24 @@ __global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __rest
   const int t = static_cast<int>(idx / cpr);
   const int c = static_cast<int>(idx % cpr) * 8;
   const int64_t S = static_cast<int64_t>(T) * k;
-  auto load8 = [&](int64_t row, float (&f)[8]) {
-    const uint4 h = __ldg(reinterpret_cast<const uint4*>(y16 + row * H + c));
-    const float fr = __ldg(rowf + row);
-    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xffffu))) * fr;
-      f[2 * i + 1] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * fr;
-    }
-  };
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j0 = 0; j0 < k; j0 += 4) {
-    float v[4][8], wj[4];
+  // ranks in groups of eight: the group's row loads (raw f16 words and the row factors) are
+  // issued together, then decoded and summed in rank order
+  auto fma8 = [&](const uint4& h, float fr, float wj) {
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = fmaf(wj, __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xffffu))) * fr, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj, __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * fr, acc[2 * i + 1]);
+    }
+  };
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    uint4 hv[8];
+    float fr[8], wj[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
       if (j0 + q < k) {
         const int64_t s = static_cast<int64_t>(t) * k + j0 + q;
         int64_t p = __ldg(slot_pos + s);
@@ -112,20 +113,23 @@ __global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __rest
           p = 0;
         }
         wj[q] = __ldg(topk_w + s);
-        load8(p, v[q]);
+        hv[q] = __ldg(reinterpret_cast<const uint4*>(y16 + p * H + c));
+        fr[q] = __ldg(rowf + p);
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (j0 + q < k)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[q], v[q][i], acc[i]);
+    for (int q = 0; q < 8; ++q)
+      if (j0 + q < k) fma8(hv[q], fr[q], wj[q]);
   }
   if (has_shared) {
-    float v[8];
-    load8(S + t, v);
+    const uint4 h = __ldg(reinterpret_cast<const uint4*>(y16 + (S + t) * H + c));
+    const float fr = __ldg(rowf + S + t);
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] += __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xffffu))) * fr;
+      acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * fr;
+    }
   }
   const int64_t o = static_cast<int64_t>(t) * H + c;
   if (out_is_fp32) {
