@@ -529,17 +529,20 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
         del fgraphs
 
     # end to end through host buffers: every layer call of every step copies its x and logits in
-    # from pinned host memory, runs the C-ABI call and copies its output back to pinned memory.
-    # Three streams: the copies in of call n+1 and out of call n-1 run while call n computes
-    # (device buffers double-buffered per layer); every copy is inside the timed region.
+    # from pinned host memory, runs the C-ABI call and copies its output back to pinned memory, all
+    # inside the timed region.  For batches of 64 tokens and more the copies run on their own
+    # streams (the copies in of call n+1 and out of call n-1 overlap call n; device buffers
+    # double-buffered per layer); for decode batches, whose calls take microseconds, the event
+    # handshakes between streams would cost more than they hide, so all of it runs on one stream.
     e2e_steps = min(steps, 200)
+    overlap = min(L["T"] for L in layers) >= 64
     hx = [[L["xs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
     hl = [[L["lgs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
     ho = [[torch.empty(L["T"], H, dtype=torch.bfloat16).pin_memory() for _ in range(2)] for L in layers]
     dx = [[torch.empty_like(L["xs"][0]) for _ in range(2)] for L in layers]
     dl = [[torch.empty_like(L["lgs"][0]) for _ in range(2)] for L in layers]
     do = [[torch.empty_like(L["out"]) for _ in range(2)] for L in layers]
-    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    h2d_s, d2h_s = (torch.cuda.Stream(device), torch.cuda.Stream(device)) if overlap else (stream, stream)
     in_ready = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
     done = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
     out_read = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
@@ -548,19 +551,25 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
         p, b = i % pool, i % 2
         for li, L in enumerate(layers):
             with torch.cuda.stream(h2d_s):
-                h2d_s.wait_event(done[li][b])          # the call two steps back has read these buffers
+                if overlap:
+                    h2d_s.wait_event(done[li][b])      # the call two steps back has read these buffers
                 dx[li][b].copy_(hx[li][p], non_blocking=True)
                 dl[li][b].copy_(hl[li][p], non_blocking=True)
-                in_ready[li][b].record(h2d_s)
+                if overlap:
+                    in_ready[li][b].record(h2d_s)
             with torch.cuda.stream(stream):
-                stream.wait_event(in_ready[li][b])
-                stream.wait_event(out_read[li][b])     # its output buffer has been copied out
+                if overlap:
+                    stream.wait_event(in_ready[li][b])
+                    stream.wait_event(out_read[li][b])  # its output buffer has been copied out
                 moe.forward(dx[li][b], dl[li][b], L["gu"], L["dn"], L["ms"], L["ws"], out=do[li][b])
-                done[li][b].record(stream)
+                if overlap:
+                    done[li][b].record(stream)
             with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(done[li][b])
+                if overlap:
+                    d2h_s.wait_event(done[li][b])
                 ho[li][b].copy_(do[li][b], non_blocking=True)
-                out_read[li][b].record(d2h_s)
+                if overlap:
+                    out_read[li][b].record(d2h_s)
 
     for i in range(2):   # untimed: the buffers' first use
         e2e_step(i)
@@ -581,8 +590,9 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     d2h = sum(L["T"] * H * 2 for L in layers)
     e2e = {"value": replica_throughput(world, e2e_steps, tokens_per_step, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "method": "moe_forward per layer call with pinned-host x/logits copied in and the output copied "
-                     "out every call; copies on their own streams overlap the neighbouring calls' compute"}
+           "method": ("moe_forward per layer call with pinned-host x/logits copied in and the output copied out "
+                      "every call; " + ("copies on their own streams overlap the neighbouring calls' compute"
+                                        if overlap else "copies and calls in order on one stream"))}
     torch.cuda.synchronize(device)
 
     status = [moe.device_status(L["ws"]) for L in layers]

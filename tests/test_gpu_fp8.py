@@ -127,3 +127,13 @@ def test_forward_fp8_rejects_decode_shapes(cuda_lib):
     with pytest.raises(moe.MoeError):
         moe.forward_fp8(torch.zeros(8, 256, dtype=torch.bfloat16, device="cuda"),
                         torch.zeros(8, 16, device="cuda"), gu8, dn8, ms, ws)
+
+
+def test_forward_fp8_zipf_8192_every_row(cuda_lib):
+    """One Zipf-routed layer of the long-prefill shape at T = 8192 (hot experts span many tiles),
+    every row."""
+    moe = cuda_lib
+    w = synth.WORKLOADS["long"]
+    L = Layer(w.shape(8192), 7_901, layer=0, logit_bias="zipf", gen_device="cuda")
+    gu8, dn8, ogu8, odn8, _ = _weights(moe, L)
+    _check_forward(moe, L, gu8, dn8, ogu8, odn8)
