@@ -5,8 +5,11 @@ e4m3 x e4m3 (weights re-quantized to e4m3) and gives, as fix (a), every token ro
 applied in the f32 epilogue.  The integer decisions of that arm are taken in fp32 on both sides
 by the same row rule, so the load-time weight codes and the activation-row codes are bit-exact
 against the oracle; the layer output is checked against the oracle's FP8 layer with the layer
-tolerance (the fp32 accumulation order differs, and the bf16 h that is quantized before down can
-round differently in rare elements).
+tolerance's mean bound, and with a max-element bound of 4e-2 of the row RMS instead of 2e-2: the h
+that is quantized before down carries the fp32 (GPU) versus fp64 (oracle) accumulation
+difference, so where it lies on an e4m3 rounding boundary the two sides pick neighbouring codes,
+one e4m3 step (up to 12.5% of that element) apart; a flipped code near a row's maximum moves an
+expert output by about 1% of its RMS, and a Zipf-routed token can carry two of them.
 """
 import numpy as np
 import pytest
@@ -17,6 +20,8 @@ import synth
 from moe_cases import Layer, bf16_round_bits, check_layer_close, moe_shape, to_np
 
 pytestmark = pytest.mark.gpu
+
+FP8_ROW_RMS_TOL = 4e-2   # max-element bound of the FP8 arm (see the module docstring)
 
 # (T, H, E, k, I, has_shared, logit bias, seed): ragged token tiles, several tiles per expert,
 # no shared expert, the N tail of a single 16-column step, H = 1024 with I = 512
@@ -96,8 +101,8 @@ def _check_forward(moe, L, gu8, dn8, ogu8, odn8, tokens=None):
     assert torch.equal(out.view(torch.int16), bf16_round_bits(out32)), "bf16 output != rounded fp32 output"
     ref = oracle.moe_forward_fp8(L.x.cpu(), L.logits.cpu(), ogu8, odn8, s.k, s.has_shared, tokens=tokens)
     sel = slice(None) if tokens is None else torch.tensor(tokens, device="cuda")
-    check_layer_close(to_np(out32[sel]), ref, "forward_fp8 fp32")
-    check_layer_close(to_np(out[sel]), ref, "forward_fp8 bf16", rounded_bf16=True)
+    check_layer_close(to_np(out32[sel]), ref, "forward_fp8 fp32", row_rms_tol=FP8_ROW_RMS_TOL)
+    check_layer_close(to_np(out[sel]), ref, "forward_fp8 bf16", rounded_bf16=True, row_rms_tol=FP8_ROW_RMS_TOL)
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_I{c[4]}_sh{c[5]}")
