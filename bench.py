@@ -528,6 +528,48 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
             del L["gu8"], L["dn8"]
         del fgraphs
 
+    # the per-expert register arm inside the tcgen05 grouped GEMMs (expert groups of at most 8
+    # token rows on mma.sync in the same launch), timed the same way; the headline steps keep the
+    # library default (every item on tcgen05)
+    register_arm = None
+    if all(a == 2 for a in arms):
+        share = []
+        for L in layers:
+            ids = torch.topk(L["lgs"][0], w.k, dim=1).indices.reshape(-1)
+            cnt = torch.bincount(ids, minlength=E).tolist() + ([L["T"]] if w.shape(L["T"]).has_shared else [])
+            tile = 64 if L["T"] <= moe.DECODE_MAX_T else 128
+            rows = [min(c - i, tile) for c in cnt for i in range(0, c, tile)]
+            share.append(sum(r <= 8 for r in rows) / max(len(rows), 1))
+        moe.set_narrow_rows(8)
+        try:
+            ngraphs = []
+            for p in range(pool):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for L in layers:
+                        moe.forward(L["xs"][p], L["lgs"][p], L["gu"], L["dn"], L["ms"], L["ws"], out=L["out"])
+                ngraphs.append(g)
+        finally:
+            moe.set_narrow_rows(-1)
+        with torch.cuda.stream(stream):
+            for p in range(pool):
+                ngraphs[p].replay()
+            stream.synchronize()
+            n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n0.record(stream)
+            for i in range(steps):
+                ngraphs[i % pool].replay()
+            n1.record(stream)
+            n1.synchronize()
+        nar_ms = slowest_rank_ms(n0.elapsed_time(n1), dist, device) / steps
+        register_arm = {"value": replica_throughput(world, 1, tokens_per_step, nar_ms), "unit": UNIT,
+                        "ms_per_step": nar_ms, "narrow_rows": 8,
+                        "narrow_item_share": [round(x, 3) for x in share],
+                        "what": "moe_forward with moe_set_narrow_rows(8): work items of at most 8 token rows run on "
+                                "the dequant warps' mma.sync register arm inside the same tcgen05 launch, timed like "
+                                "the headline steps (the headline keeps every item on tcgen05)"}
+        del ngraphs
+
     # end to end through host buffers: every layer call of every step copies its x and logits in
     # from pinned host memory, runs the C-ABI call and copies its output back to pinned memory, all
     # inside the timed region.  For batches of 64 tokens and more the copies run on their own
@@ -605,6 +647,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
            "config": describe(name), "roofline": roofline, "layer_roofline": layer, "e2e": e2e,
            "with_router": with_router,
            "fp8_arm": fp8_arm,
+           "register_arm": register_arm,
            "gpu_launches": steps * launches, "clocks": clk.summary(),
            "arm": sorted({moe.ARM_NAMES[a] for a in arms}),
            "method": {"l2": "inputs larger than L2: every layer's NVFP4 weights (907 MB) resident, a fresh input "
@@ -672,7 +715,7 @@ def run_ours(args):
                 "config": main["config"], "roofline": main["roofline"], "e2e": main["e2e"],
                 "gpu_launches": main["gpu_launches"], "clocks": main["clocks"],
                 "parallelism": f"replicas x{world}"}
-        for key in ("cpu_baseline", "layer_roofline", "with_router", "fp8_arm", "arm", "method", "stages_us_per_forward",
+        for key in ("cpu_baseline", "layer_roofline", "with_router", "fp8_arm", "register_arm", "arm", "method", "stages_us_per_forward",
                     "distinct_experts_mean"):
             if key in main:
                 line[key] = main[key]

@@ -274,6 +274,19 @@ moe_status_t moe_forward_fp8(const uint16_t* x, const float* logits, const moe_f
  *   3  T > 64 otherwise: CUDA-core grouped GEMMs. */
 int moe_forward_arm(const moe_shape_t* shape);
 
+/* Per-expert choice inside the arm-2 grouped GEMMs (the handover briefs' MoE decode-arm brief
+ * wants the grouped arm to engage only where a group is wide and tiny groups to take a GEMV-like
+ * path, decided on the device): a work item whose expert group has at most `rows` token rows runs
+ * on the dequant warps of the same persistent launch as a register-operand mma.sync product with
+ * the group's tokens as the 8 MMA columns, instead of TMEM staging and tcgen05; wider groups stay
+ * on tcgen05.  The choice is made per item on the device from the permutation's counts.
+ *   rows  0 (every item on tcgen05), 1..8, or -1 (the library's default for the shape).
+ * Process-wide; takes effect for calls issued afterwards (a captured CUDA graph keeps the value
+ * it was captured with).  Returns MOE_ERR_INVALID_ARG outside [-1, 8].  Numerics are those of
+ * the grouped GEMMs (exact f16 operands, fp32 accumulation); only the accumulation order of the
+ * MMA differs between the two arms. */
+moe_status_t moe_set_narrow_rows(int rows);
+
 /* Static description of a status code. */
 const char* moe_status_string(moe_status_t status);
 

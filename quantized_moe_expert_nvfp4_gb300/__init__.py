@@ -91,6 +91,7 @@ def _declare(L):
         "moe_prepare_fp8": ([W, P, P, P], I32),
         "moe_quantize_rows_e4m3": ([P, I64, I32, P, P, P], I32),
         "moe_forward_fp8": ([P, P, W8, W8, SH, P, I32, P, SZ, P], I32),
+        "moe_set_narrow_rows": ([I32], I32),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -348,6 +349,13 @@ def forward_arm(shape: Shape) -> int:
     return load().moe_forward_arm(ctypes.byref(shape.c()))
 
 
+def set_narrow_rows(rows: int) -> None:
+    """Row bound of the register arm inside the tcgen05 grouped GEMMs (moe_set_narrow_rows):
+    expert groups of at most `rows` tokens run on mma.sync in the same launch; 0 = none, -1 =
+    the library's default."""
+    _check("moe_set_narrow_rows", load().moe_set_narrow_rows(int(rows)))
+
+
 def status_string(status: int) -> str:
     return load().moe_status_string(status).decode()
 
@@ -356,4 +364,4 @@ __all__ = ["Shape", "NVFP4Weights", "MoeError", "load", "workspace_size", "works
            "quantize_nvfp4", "route_topk", "permute", "grouped_gate_up", "grouped_down", "combine",
            "forward", "forward_profiled", "forward_arm", "router_logits", "forward_routed", "FP8Weights",
            "prepare_fp8", "quantize_rows_e4m3", "forward_fp8", "ARM_NAMES", "device_status", "status_string",
-           "DECODE_MAX_T", "LIB_PATH"]
+           "set_narrow_rows", "DECODE_MAX_T", "LIB_PATH"]

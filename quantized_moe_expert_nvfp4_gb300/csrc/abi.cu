@@ -156,6 +156,18 @@ int tile_rows_for(const moe_shape_t& s) {
   }
 }
 
+// Row bound of the tensor-core arm's register arm (tiles of at most this many rows run on the
+// dequant warps with mma.sync; set by moe_set_narrow_rows, -1 = the library's default).
+std::atomic<int> g_narrow_rows{-1};
+constexpr int kNarrowMaxRows = 8;
+
+int narrow_rows_for(const moe_shape_t& s) {
+  if (arm_for(s) != Arm::kTc) return 0;
+  const int set = g_narrow_rows.load(std::memory_order_relaxed);
+  if (set >= 0) return set;
+  return 0;
+}
+
 // The tensor-core arm takes its activations as f16 rows with power-of-two row exponents, in
 // expert order: x is gathered by sorted_slot and converted into the workspace first (h already
 // is in order).  moe_forward writes the same rows token-major from the inverse map instead.
@@ -195,6 +207,7 @@ GroupedArgs grouped_args(const moe_nvfp4_weights_t& w, const moe_shape_t& s, con
   a.meta = ws.meta;
   a.max_tiles = max_tiles_for(s, tile_rows_for(s));
   a.tile_rows = tile_rows_for(s);
+  a.narrow_rows = narrow_rows_for(s);
   a.out = out;
   a.status = ws.status;
   a.act_factor = nullptr;
@@ -315,6 +328,12 @@ cudaError_t launch_router(const uint16_t* x, const moe_nvfp4_weights_t& r, const
 using namespace moe;
 
 extern "C" {
+
+moe_status_t moe_set_narrow_rows(int rows) {
+  if (rows < -1 || rows > kNarrowMaxRows) return MOE_ERR_INVALID_ARG;
+  g_narrow_rows.store(rows, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 size_t moe_workspace_size(const moe_shape_t* shape) {
   if (check_shape(shape) != MOE_OK) return 0;

@@ -36,6 +36,7 @@
 #include <algorithm>
 
 #include "internal.cuh"
+#include "mma_frag.cuh"
 #include "tensor_map.cuh"
 #include "topk.cuh"
 
@@ -191,51 +192,10 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
-// One m16n8k16 tensor-core step, D += A * B with f16 operands and fp32 accumulators.  Fragment
-// layout (lane = 4 * grp + tig): A registers {row grp, K 2tig..+1}, {row grp + 8, same K},
-// {row grp, K 2tig + 8..+9}, {row grp + 8, same K}; B registers {K 2tig..+1, column grp},
-// {K 2tig + 8..+9, column grp}; D {row grp, columns 2tig, 2tig + 1}, {row grp + 8, same}.
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// Two e4m3 bytes of w as an f16x2 pair of their values times 2^-8 (sel = 0x0404 | lo << 4 |
-// hi << 12 puts byte lo into the low half and byte hi into the high half), with integer
-// operations only (the conversion pipe is this kernel's tightest resource): a byte's seven low
-// bits placed at f16 bits 7..13 make the f16 exponent field the e4m3 exponent and the f16
-// mantissa's top bits the e4m3 mantissa, so every finite code, subnormals included, maps exactly
-// to its value x 2^-8 (the biases differ by 8); the sign goes to bit 15.  The epilogues multiply
-// by 2^8.  The products below broadcast one half of the pair.
-__device__ __forceinline__ __half2 e4m3_pair_f16x2_2m8(uint32_t w, uint32_t sel) {
-  const uint32_t b = __byte_perm(w, 0u, sel);   // [0, lo, 0, hi]: each byte in its half's high byte
-  const uint32_t f = (b & 0x80008000u) | ((b >> 1) & 0x3FFF3FFFu);
-  return *reinterpret_cast<const __half2*>(&f);
-}
-constexpr float kScaleUnbias = 256.0f;   // 2^8, undoes the scales' 2^-8
-
 // Two fp32 -> f16x2 (round to nearest; exact for the power-of-two-scaled bf16 values used here).
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-// K order of the MMAs.  A 16-byte piece of a weight row holds 32 elements (two NVFP4 blocks);
-// lane tig of a quad takes the piece's word tig, i.e. elements 8 tig .. 8 tig + 7, of which the
-// first MMA of the piece uses 8 tig .. + 3 as its K positions (2 tig, 2 tig + 1 | 2 tig + 8,
-// 2 tig + 9) and the second MMA 8 tig + 4 .. + 7.  The B operand (activation rows) is read in the
-// same order, so each dot product is the pieces' own; the lane's elements all lie in block
-// 2 q + tig / 2 of piece q and share one scale.  w: the lane's word of the row, s: the scale in
-// both halves; r[0], r[1] feed the first MMA, r[2], r[3] the second (e2m1 x e4m3 is exact in f16).
-__device__ __forceinline__ void piece_frag(uint32_t w, __half2 s, uint32_t (&r)[4]) {
-  e2m1x8_to_f16x2(w, r);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2 p = __hmul2(*reinterpret_cast<const __half2*>(&r[i]), s);
-    r[i] = *reinterpret_cast<const uint32_t*>(&p);
-  }
 }
 // Row exponent of the f16 staging: floor(log2(max)) - 14 puts the row maximum in [2^14, 2^15)
 // (kept >= -126 so that 2^-e is a normal float; such a row is then scaled less than it could be).
@@ -500,7 +460,7 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   // this lane's scale bytes of the piece pair 2 p, 2 p + 1 (piece q's lane block is 2 q + tig / 2):
   // bytes tig / 2 and 2 + tig / 2 of the pair's scale word (gate_up: word p of a 16-byte scale
   // row; down: the row's one word), into the low and the high half
-  const uint32_t psel = 0x0404u | ((tig >> 1) << 4) | ((2u + (tig >> 1)) << 12);
+  const uint32_t psel = scale_pair_sel(tig);
   const int mt = warp & 7, kh = warp >> 3;                 // gate_up: MMA tile and 128-byte line
   uint32_t it = 0;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {

@@ -31,6 +31,7 @@
 // mbarrier wait is bounded; on timeout the kernel records MOE_ERR_DEVICE_TIMEOUT in the
 // workspace status word and winds down.
 #include "internal.cuh"
+#include "mma_frag.cuh"
 #include "tc_common.cuh"
 #include "tensor_map.cuh"
 
@@ -98,6 +99,7 @@ struct TcArgs {
   uint16_t* y16;                // down: compact y, f16(accumulator * y16_scale), when set,
   float y16_scale;              // and per row the factor that restores it
   float* y16_rowf;
+  int narrow_rows;              // items of at most this many rows take the register arm (0: none)
 };
 
 struct Smem {
@@ -110,6 +112,7 @@ struct Smem {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];         // one arrival per epilogue warp
   uint64_t drain;
+  uint32_t nb_done[kBStagesMax];   // register arm: dequant warps done with an activation stage
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -183,7 +186,102 @@ __device__ __forceinline__ int4 load_tile(const TcArgs& a, int item, int n_items
   return item < n_items ? __ldg(a.tiles + item / MB) : make_int4(0, 0, 0, 0);
 }
 
+// The register arm of one work item whose tile has at most 8 rows (a tiny expert group): the eight
+// dequant warps multiply the packed stages straight from shared memory with mma.sync, 16 weight
+// rows per warp (gate_up: 8 gate rows and the matching 8 up rows, so a lane holds both halves of
+// its h columns; down: 16 consecutive output rows) against the tile's tokens as the 8 MMA columns,
+// and write the item's outputs themselves; the TMEM stages, the MMA warp and the epilogue warps
+// skip the item.  The packed and activation stages are consumed in the rings' order like the
+// tensor-core items'; the last dequant warp done with an activation stage releases it.  The
+// dequant warps wait on every group's activation stage, tensor-core groups included, so that their
+// parity waits never run two phases ahead of the loads (the MMA warp, which waits only on its own
+// groups' stages, first waits for their dequantized A, i.e. after the dequant warps' waits).  ia
+// advances by the item's groups.  Returns false when a wait ran out or the CTA is aborting.
 template <bool kGateUp, int kBNt>
+__device__ __forceinline__ bool narrow_item(const TcArgs& a, Smem* sm, const uint8_t* sA, const uint8_t* sB, const int4 td,
+                                         int mb, int KG, uint32_t& ia) {
+  using C = TcCfg<kBNt>;
+  constexpr int kBStages = C::kBStages, kBStageBytes = C::kBStageBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = warp - kWarpDeq, grp = lane >> 2, tig = lane & 3;
+  const int ra = kGateUp ? 8 * w + grp : 16 * w + grp;                  // stage rows of MMA rows grp
+  const int rb = kGateUp ? kBM / 2 + 8 * w + grp : 16 * w + grp + 8;    // and grp + 8
+  const uint32_t psel = scale_pair_sel(tig);
+  const int nb = (td.z + 15) & ~15;             // rows of each 64-wide activation sub-tile
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.0f;
+  for (int g = 0; g < KG; ++g, ++ia) {
+    const int st = ia % kAStages, sb = ia % kBStages;
+    if (!warp_wait(&sm->a_full[st], (ia / kAStages) & 1, sm, a.status)) return false;
+    if (!warp_wait(&sm->b_full[sb], (ia / kBStages) & 1, sm, a.status)) return false;
+    const uint8_t* stage = sA + st * kAStageBytes;
+    const uint4 sca = *reinterpret_cast<const uint4*>(stage + kAPackedBytes + ra * (kGK / 16));
+    const uint4 scb = *reinterpret_cast<const uint4*>(stage + kAPackedBytes + rb * (kGK / 16));
+    const uint8_t* rowa = stage + ra * (kGK / 2);
+    const uint8_t* rowb = stage + rb * (kGK / 2);
+    const uint8_t* brow = sB + sb * kBStageBytes + grp * (kBK * 2);   // token column grp
+#pragma unroll
+    for (int p = 0; p < kGK / 32; ++p) {   // piece p: K 32 p .. 32 p + 31, 16 bytes of a packed row
+      // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+      const uint32_t wa = *reinterpret_cast<const uint32_t*>(rowa + ((p ^ (ra & 7)) << 4) + 4 * tig);
+      const uint32_t wb = *reinterpret_cast<const uint32_t*>(rowb + ((p ^ (rb & 7)) << 4) + 4 * tig);
+      // the lane's 8 activations at K 32 p + 8 tig: sub-tile p / 2, chunk 4 (p & 1) + tig
+      const uint4 xb = *reinterpret_cast<const uint4*>(brow + (p >> 1) * nb * (kBK * 2) +
+                                                       (((4 * (p & 1) + tig) ^ (grp & 7)) << 4));
+      const __half2 spa = e4m3_pair_f16x2_2m8((&sca.x)[p >> 1], psel);
+      const __half2 spb = e4m3_pair_f16x2_2m8((&scb.x)[p >> 1], psel);
+      uint32_t ar[4], br[4];
+      piece_frag(wa, (p & 1) ? __high2half2(spa) : __low2half2(spa), ar);
+      piece_frag(wb, (p & 1) ? __high2half2(spb) : __low2half2(spb), br);
+      mma16816(acc[(p & 1) * 2], ar[0], br[0], ar[1], br[1], xb.x, xb.y);
+      mma16816(acc[(p & 1) * 2 + 1], ar[2], br[2], ar[3], br[3], xb.z, xb.w);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&sm->a_free[st]);
+      __threadfence_block();
+      if (atomicAdd(&sm->nb_done[sb], 1u) == static_cast<uint32_t>(kDeqWarps - 1)) {
+        sm->nb_done[sb] = 0;
+        __threadfence_block();
+        mbar_arrive(&sm->b_free[sb]);
+      }
+    }
+  }
+  float d[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) d[r] = (acc[0][r] + acc[1][r]) + (acc[2][r] + acc[3][r]);
+  // D: d[c2] is MMA row grp and token 2 tig + c2, d[2 + c2] MMA row grp + 8 and the same token
+  const float s2 = __ldg(a.scale2 + td.x);
+#pragma unroll
+  for (int c2 = 0; c2 < 2; ++c2) {
+    const int n = 2 * tig + c2;
+    if (n >= td.z) continue;
+    const float cf = __ldg(a.act_factor + td.y + n);
+    const int64_t orow = static_cast<int64_t>(td.y + n) * a.out_ld;
+    if (kGateUp) {
+      const float f = s2 * cf * kScaleUnbias;
+      static_cast<uint16_t*>(a.out)[orow + mb * (kBM / 2) + 8 * w + grp] =
+          f32_to_bf16_bits(silu_f32(d[c2] * f) * (d[2 + c2] * f));
+    } else if (a.y16) {
+      const float ys = a.y16_scale * kScaleUnbias;
+      uint16_t* yr = a.y16 + orow + mb * kBM + 16 * w + grp;
+      yr[0] = __half_as_ushort(__float2half_rn(d[c2] * ys));
+      yr[8] = __half_as_ushort(__float2half_rn(d[2 + c2] * ys));
+      if (mb == 0 && w == 0 && grp == 0) a.y16_rowf[td.y + n] = s2 * cf / a.y16_scale;
+    } else {
+      const float f = s2 * cf * kScaleUnbias;
+      float* yr = static_cast<float*>(a.out) + orow + mb * kBM + 16 * w + grp;
+      yr[0] = d[c2] * f;
+      yr[8] = d[2 + c2] * f;
+    }
+  }
+  return true;
+}
+
+// kNarrow: whether the launch has the register arm (a separate instantiation, so that the
+// tensor-core-only kernel keeps its own register allocation).
+template <bool kGateUp, int kBNt, bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ TcMaps maps, TcArgs a) {
   using C = TcCfg<kBNt>;
@@ -218,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm->acc_empty[d], kEpiWarps);
     }
     mbar_init(&sm->drain, 1);
+    for (int s = 0; s < kBStagesMax; ++s) sm->nb_done[s] = 0;
     sm->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -330,22 +429,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // The whole warp waits (converged) once per group; one elected lane issues the group's 16
     // MMAs and the commit that releases its TMEM and activation stages.
-    uint32_t ig = 0, ic = 0;
+    // ig counts the groups of tensor-core items (TMEM stages), ib every group (activation ring)
+    uint32_t ig = 0, ib = 0, ic = 0;
     bool ok = true;
     int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       const int4 td = td_next;
       td_next = load_tile(a, item + gridDim.x, n_items, MB);
+      if (kNarrow && td.z <= a.narrow_rows) {   // the dequant warps' register arm takes this item
+        ib += KG;
+        continue;
+      }
       const int n = (td.z + 15) & ~15;
       const uint32_t idesc = make_idesc(n);
       const int d = ic & 1;
       if (!(ok = warp_wait(&sm->acc_empty[d], ((ic >> 1) & 1) ^ 1, sm, a.status))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem + kDCol + d * kBN;
-      for (int g = 0; g < KG; ++g, ++ig) {
-        const int gs = ig % kGStages, bs = ig % kBStages;
+      for (int g = 0; g < KG; ++g, ++ig, ++ib) {
+        const int gs = ig % kGStages, bs = ib % kBStages;
         if (!(ok = warp_wait(&sm->g_full[gs], (ig / kGStages) & 1, sm, a.status))) break;
-        if (!(ok = warp_wait(&sm->b_full[bs], (ig / kBStages) & 1, sm, a.status))) break;
+        if (!(ok = warp_wait(&sm->b_full[bs], (ib / kBStages) & 1, sm, a.status))) break;
         tc_fence_after();
         if (elect_one()) {
           const uint32_t a_tmem = tmem + kACol + gs * (kGK / 2);
@@ -372,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (elect_one()) tc_commit(&sm->acc_full[d]);
         __syncwarp();
       }
+      ++ic;
     }
     // every MMA issued must have completed before TMEM is released (bounded)
     if (elect_one()) {
@@ -391,12 +496,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       srow = q * 32 + lane;
     }
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t ia = 0;
+    uint32_t ia = 0, iw = 0;   // every group (packed-weight and activation rings); tensor-core groups
     bool ok = true;
+    int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      for (int g = 0; g < KG; ++g, ++ia) {
-        const int st = ia % kAStages, ts = ia % kGStages;
+      const int4 td = td_next;
+      td_next = load_tile(a, item + gridDim.x, n_items, MB);
+      if (kNarrow && td.z <= a.narrow_rows) {
+        ok = narrow_item<kGateUp, kBNt>(a, sm, sA, sB, td, item % MB, KG, ia);
+        continue;
+      }
+      for (int g = 0; g < KG; ++g, ++ia, ++iw) {
+        const int st = ia % kAStages, ts = iw % kGStages;
         if (!(ok = warp_wait(&sm->a_full[st], (ia / kAStages) & 1, sm, a.status))) break;
+        // with the register arm the dequant warps observe every activation stage's phase in order
+        // (a parity wait only tells two consecutive phases apart, and the register arm's waits on
+        // these barriers must not run two phases ahead of the loads)
+        if (kNarrow && !(ok = warp_wait(&sm->b_full[ia % kBStages], (ia / kBStages) & 1, sm, a.status))) break;
         const uint8_t* stage = sA + st * kAStageBytes;
         const uint8_t* rowp = stage + srow * (kGK / 2);
         const uint4 sc = *reinterpret_cast<const uint4*>(stage + kAPackedBytes + srow * (kGK / 16));
@@ -412,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->a_free[st]);
-        if (!(ok = warp_wait(&sm->g_free[ts], ((ia / kGStages) & 1) ^ 1, sm, a.status))) break;
+        if (!(ok = warp_wait(&sm->g_free[ts], ((iw / kGStages) & 1) ^ 1, sm, a.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
@@ -453,13 +569,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int4 td_next = load_tile(a, blockIdx.x, n_items, MB);
     if (blockIdx.x < n_items) fetch_scales(td_next);
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ic) {
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       const int4 td = td_next;
       td_next = load_tile(a, item + gridDim.x, n_items, MB);
       const float s2 = s2_next;
       float cf[kBN / 32];
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) cf[i] = cf_next[i];
+      if (kNarrow && td.z <= a.narrow_rows) {   // written by the dequant warps' register arm
+        if (item + static_cast<int>(gridDim.x) < n_items) fetch_scales(td_next);
+        continue;
+      }
       const int mb = item % MB;
       const int d = ic & 1;
       if (!kGateUp && a.y16 && mb == 0 && q == 0) {   // the tile's row factors for the combine
@@ -541,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->acc_empty[d]);
       if (item + static_cast<int>(gridDim.x) < n_items) fetch_scales(td_next);
+      ++ic;
     }
   }
 
@@ -579,8 +700,11 @@ static_assert(smem_bytes<128>() <= 232448 && smem_bytes<64>() <= 232448, "shared
 template <bool kGateUp>
 cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   const bool small = g.tile_rows == 64;
-  const void* kern = small ? reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 64>)
-                           : reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 128>);
+  const bool narrow = g.narrow_rows > 0;
+  const void* kern = small ? (narrow ? reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 64, true>)
+                                     : reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 64, false>))
+                           : (narrow ? reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 128, true>)
+                                     : reinterpret_cast<const void*>(grouped_gemm_tc_kernel<kGateUp, 128, false>));
   const size_t smem = small ? smem_bytes<64>() : smem_bytes<128>();
   if (g.tile_rows != 64 && g.tile_rows != kTcTileRows) return cudaErrorInvalidValue;
   cudaError_t e = ensure_dynamic_smem(kern, static_cast<int>(smem));
@@ -625,12 +749,21 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   a.y16 = kGateUp ? nullptr : g.y16;
   a.y16_scale = g.y16_scale;
   a.y16_rowf = g.y16_rowf;
+  a.narrow_rows = g.narrow_rows;
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, n_sm));
-  if (small)
-    grouped_gemm_tc_kernel<kGateUp, 64><<<grid, kThreads, smem, st>>>(maps, a);
-  else
-    grouped_gemm_tc_kernel<kGateUp, 128><<<grid, kThreads, smem, st>>>(maps, a);
+  if (g.narrow_rows < 0 || g.narrow_rows > 8) return cudaErrorInvalidValue;   // one MMA column block
+  if (small) {
+    if (narrow)
+      grouped_gemm_tc_kernel<kGateUp, 64, true><<<grid, kThreads, smem, st>>>(maps, a);
+    else
+      grouped_gemm_tc_kernel<kGateUp, 64, false><<<grid, kThreads, smem, st>>>(maps, a);
+  } else {
+    if (narrow)
+      grouped_gemm_tc_kernel<kGateUp, 128, true><<<grid, kThreads, smem, st>>>(maps, a);
+    else
+      grouped_gemm_tc_kernel<kGateUp, 128, false><<<grid, kThreads, smem, st>>>(maps, a);
+  }
   return cudaGetLastError();
 }
 

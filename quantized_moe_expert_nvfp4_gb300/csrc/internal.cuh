@@ -159,6 +159,9 @@ struct GroupedArgs {
   uint16_t* y16 = nullptr;
   float y16_scale = 0.0f;
   float* y16_rowf = nullptr;
+  // tensor-core arm: work items of at most this many rows (<= 8) run on the dequant warps'
+  // register arm inside the same launch (0: every item on tcgen05)
+  int narrow_rows = 0;
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
@@ -200,6 +203,9 @@ struct GroupedFp8Args {
   uint16_t* y16 = nullptr;
   float y16_scale = 0.0f;
   float* y16_rowf = nullptr;
+  // tensor-core arm: work items of at most this many rows (<= 8) run on the dequant warps'
+  // register arm inside the same launch (0: every item on tcgen05)
+  int narrow_rows = 0;
 };
 cudaError_t launch_gate_up_fp8(const GroupedFp8Args& a, cudaStream_t st);
 cudaError_t launch_down_fp8(const GroupedFp8Args& a, cudaStream_t st);

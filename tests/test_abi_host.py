@@ -155,3 +155,13 @@ def test_fp8_arm_host_validation(lib):
                              fake, fake, None) == -2
     assert L.moe_quantize_rows_e4m3(fake, 4, 100, fake, fake, None) == -2
     assert L.moe_quantize_rows_e4m3(mis, 4, 256, fake, fake, None) == -1
+
+
+def test_register_arm_row_bound_is_checked(lib):
+    """moe_set_narrow_rows is host state (no CUDA call): -1..8 accepted, anything else rejected."""
+    moe, L = lib
+    for bad in (-2, 9, 64):
+        with pytest.raises(moe.MoeError):
+            moe.set_narrow_rows(bad)
+    for ok in (0, 8, 3, -1):
+        moe.set_narrow_rows(ok)
