@@ -299,8 +299,9 @@ def build_layer(moe, w, T, seed, pool, device):
 
 def launches_per_forward(arm, T):
     """Kernels one moe_forward launches: arm 0 one; arm 1 route+permute, gate_up, down+combine;
-    arm 2 route+permute (one cooperative kernel), the expert-ordered f16 copy of x, gate_up, the
-    f16 copy of h, down, combine; arm 3 route+permute, gate_up, down, combine."""
+    arm 2 route+permute (one cooperative kernel; up to 64 tokens the top-k, then permutation and
+    gather in one kernel) and the expert-ordered f16 copy of x, gate_up, the f16 copy of h, down,
+    combine; arm 3 route+permute, gate_up, down, combine."""
     return {0: 1, 1: 3, 2: 6, 3: 4}[arm]
 
 

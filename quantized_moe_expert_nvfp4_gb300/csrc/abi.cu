@@ -530,9 +530,19 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
   // grouped-GEMM arms: routing, permutation and work list in one cooperative launch
   // (on the tensor-core arm also the expert-ordered f16 rows of x, written token-major from the
   // inverse map so that each x row is read once; stage event 1 follows them)
+  // (batches of up to kDecodeMaxT tokens on the tensor-core arm: the top-k, then permutation, work
+  // list and the f16 rows of x in one launch whose CTAs each place the whole batch, with no
+  // grid-wide wait)
   const bool tc = arm_for(s) == Arm::kTc;
-  e = launch_route_permute(logits, s, w, tile_rows_for(s), cs);
-  if (e == cudaSuccess && tc) e = launch_act_scatter_f16(x, w.slot_pos, s.T, s.k, s.H, w.xf, w.xe, w.status, cs);
+  if (tc && s.T <= kDecodeMaxT) {
+    e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, cs);
+    if (e == cudaSuccess)
+      e = launch_permute_gather_small(w.ids, x, s.T, s.E, s.k, s.has_shared, s.H, w.counts, w.offsets, w.sorted_slot,
+                                      w.slot_pos, w.tiles, w.meta, tile_rows_for(s), w.xf, w.xe, w.status, cs);
+  } else {
+    e = launch_route_permute(logits, s, w, tile_rows_for(s), cs);
+    if (e == cudaSuccess && tc) e = launch_act_scatter_f16(x, w.slot_pos, s.T, s.k, s.H, w.xf, w.xe, w.status, cs);
+  }
   if (e == cudaSuccess) e = mark(1);
   if (e == cudaSuccess) {
     GroupedArgs ga = grouped_args(*gate_up, s, x, w.sorted_slot, w, w.h);

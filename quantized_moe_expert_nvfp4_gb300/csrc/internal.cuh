@@ -126,6 +126,13 @@ cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_i
 // One cooperative launch for any T: routing (logits != NULL) or given ids, counts, offsets, the
 // stable permutation and the work list.  hist: [kPermuteMaxGrid, E]; meta[4..5] is its barrier
 // counter (zero in a new workspace).
+// After the top-k of a batch of T <= kDecodeMaxT tokens: permutation, work list and the
+// expert-ordered f16 rows of x (as act_scatter_f16) in one launch of min(T, SMs) CTAs without a
+// grid-wide wait.
+cudaError_t launch_permute_gather_small(const int32_t* ids, const uint16_t* x, int T, int E, int k, int has_shared,
+                                        int H, int32_t* counts, int32_t* offsets, int32_t* sorted_slot,
+                                        int32_t* slot_pos, int4* tiles, int32_t* meta, int tile_rows, uint16_t* xf,
+                                        float* xe, int32_t* status, cudaStream_t st);
 cudaError_t launch_route_permute_large(const float* logits, const int32_t* ids_in, int T, int E, int k,
                                       int has_shared, int32_t* ids, float* w, int32_t* counts,
                                       int32_t* offsets, int32_t* sorted_slot, int32_t* slot_pos,

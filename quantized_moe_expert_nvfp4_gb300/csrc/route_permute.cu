@@ -165,6 +165,119 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(
   write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
 }
 
+// Batched decode on the tensor-core arm (T <= kDecodeMaxT), after the top-k: permutation, work
+// list and the expert-ordered f16 rows of x in one launch with no grid-wide wait.  Every CTA reads
+// the batch's S = T k expert ids, builds the counts, offsets and the stable placement in shared
+// memory, and then converts its share of the tokens (token b, b + gridDim, ...): each x row is read
+// once, scaled by 2^-e (e = floor(log2 max|row|) - 14, at least -126) and written as f16 to the k
+// expert-ordered rows that hold the token and to the shared expert's row S + t, with the factor
+// 2^e per row -- the rows act_scatter_f16 writes.  CTA 0 also writes the permutation and the work
+// list for the later stages.
+__global__ void __launch_bounds__(1024) permute_gather_small_kernel(
+    const int32_t* __restrict__ ids, const uint16_t* __restrict__ x, int T, int E, int k, int has_shared, int H,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot,
+    int32_t* __restrict__ slot_pos, int4* __restrict__ tiles, int32_t* __restrict__ meta, int tile_rows,
+    uint16_t* __restrict__ xf, float* __restrict__ xe, int32_t* __restrict__ status) {
+  __shared__ int s_ids[kDecodeMaxT * kMaxK];
+  __shared__ int s_pos[kDecodeMaxT * kMaxK];
+  __shared__ int s_cnt[kMaxE];
+  __shared__ int s_off[kMaxE];
+  __shared__ int s_cur[kMaxE];
+  __shared__ int s_warp[32];
+  __shared__ float s_max[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool lead = blockIdx.x == 0;
+  const int S = T * k;
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    int e = __ldg(ids + s);
+    if (e < 0 || e >= E) {   // written by the library's top-k; a bad value is reported and clamped
+      if (lead) report_device_error(status, kDevBadIndex);
+      e = 0;
+    }
+    s_ids[s] = e;
+  }
+  for (int e = threadIdx.x; e < kMaxE; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) atomicAdd(&s_cnt[s_ids[s]], 1);
+  __syncthreads();
+  const int my = (threadIdx.x < E) ? s_cnt[threadIdx.x] : 0;
+  const int off = block_exclusive_scan(my, s_warp, nullptr);
+  if (threadIdx.x < E) {
+    s_off[threadIdx.x] = off;
+    s_cur[threadIdx.x] = off;
+    if (lead) {
+      counts[threadIdx.x] = my;
+      offsets[threadIdx.x] = off;
+    }
+  }
+  if (lead && threadIdx.x == 0) offsets[E] = S;
+  __syncthreads();
+  // stable placement by warp 0, 32 slots a step: a slot goes after the earlier slots of its expert
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b = 0; b < S; b += 32) {
+      const int s = b + lane;
+      const int e = (s < S) ? s_ids[s] : -1;
+      const unsigned same = __match_any_sync(kFull, e);
+      const int rank = __popc(same & lt);
+      if (e >= 0) {
+        const int pos = s_cur[e] + rank;
+        s_pos[s] = pos;
+        if (lead) {
+          sorted_slot[pos] = s;
+          slot_pos[s] = pos;
+        }
+      }
+      __syncwarp();
+      if (e >= 0 && rank == 0) s_cur[e] += __popc(same);
+      __syncwarp();
+    }
+  }
+  if (lead) write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+  __syncthreads();
+  // this CTA's tokens: f16 rows scaled by the row's power of two, to every row that holds the token
+  const int nv = H / 8;   // 16-byte columns of a row
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H);
+    float m = 0.0f;
+    for (int c = threadIdx.x; c < nv; c += blockDim.x) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(q[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(q[i] & 0xffff0000u)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    if (lane == 0) s_max[warp] = m;
+    __syncthreads();
+    m = (lane < static_cast<int>(blockDim.x >> 5)) ? s_max[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+    const int ex = (m > 0.0f && m <= 3.4e38f) ? max(ilogbf(m) - 14, -126) : 0;
+    const float inv = __int_as_float((127 - ex) << 23);
+    if (threadIdx.x <= k) xe[threadIdx.x < k ? s_pos[t * k + threadIdx.x] : S + t] = __int_as_float((127 + ex) << 23);
+    for (int c = threadIdx.x; c < nv; c += blockDim.x) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(__uint_as_float(q[i] << 16) * inv, __uint_as_float(q[i] & 0xffff0000u) * inv);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int j = 0; j <= k; ++j) {
+        const int64_t p = (j < k) ? s_pos[t * k + j] : S + t;
+        reinterpret_cast<uint4*>(xf + p * H)[c] = ov;
+      }
+    }
+    __syncthreads();   // s_max is reused by the next token
+  }
+}
+
 // Any T, one cooperative launch of up to kPermuteMaxGrid CTAs of 1024 threads: routing (or given
 // ids), per-CTA expert histograms of contiguous token ranges, a grid-wide barrier, every CTA's
 // stable placement base per expert (the histograms of the CTAs before it plus the expert's
@@ -345,6 +458,20 @@ cudaError_t launch_route_permute_large(const float* logits, const int32_t* ids_i
   unsigned long long* bar = reinterpret_cast<unsigned long long*>(meta + 4);
   return cudaLaunchKernelEx(&cfg, kern, logits, ids_in, T, E, k, has_shared, ids, w, counts, offsets,
                             sorted_slot, slot_pos, hist, tiles, meta, tile_rows, bar, status);
+}
+
+cudaError_t launch_permute_gather_small(const int32_t* ids, const uint16_t* x, int T, int E, int k, int has_shared,
+                                        int H, int32_t* counts, int32_t* offsets, int32_t* sorted_slot,
+                                        int32_t* slot_pos, int4* tiles, int32_t* meta, int tile_rows, uint16_t* xf,
+                                        float* xe, int32_t* status, cudaStream_t st) {
+  if (T < 1 || T > kDecodeMaxT || H % 8) return cudaErrorInvalidValue;
+  int n_sm = 0;
+  cudaError_t e = current_sm_count(&n_sm);
+  if (e != cudaSuccess) return e;
+  permute_gather_small_kernel<<<std::min(T, n_sm), 1024, 0, st>>>(ids, x, T, E, k, has_shared, H, counts, offsets,
+                                                                  sorted_slot, slot_pos, tiles, meta, tile_rows, xf,
+                                                                  xe, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,

@@ -248,6 +248,32 @@ def test_route_edge_rows(cuda_lib):
     np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
 
 
+
+@pytest.mark.parametrize("E,k", [(512, 10), (1024, 16), (64, 8), (24, 3)])
+def test_route_rows_with_clustered_winners(cuda_lib, E, k):
+    """Rows whose largest logits sit in a few lanes of the ranking warp (entries e, e + 32, ...
+    share a lane), so that more than 32 entries reach the lane-maxima threshold and the ranking
+    takes its k-round path; rows with ties inside one lane; random rows.  Every routing call
+    (moe_route_topk, and the forward's own routing on each arm) against the oracle."""
+    moe = cuda_lib
+    rng = np.random.default_rng(E + k)
+    T = 12
+    l = rng.standard_normal((T, E)).astype(np.float32)
+    l[0, ::32] += 50.0                                   # lane 0 holds the top entries
+    l[1, 5::32] = 7.0                                    # ties within lane 5
+    l[2, ::32] += 50.0
+    l[2, 1::32] += 49.0                                  # two lanes hold them
+    l[3, :] = np.float32(1.0)
+    l[3, 31::32] = np.float32(1.0000001)                 # lane 31 just above the rest
+    l[4, ::16] = np.nan
+    l[4, 3::32] = np.inf
+    ms = moe.Shape(T=T, H=256, I=256, E=E, k=k)
+    ids, w = moe.route_topk(torch.from_numpy(l).cuda(), ms)
+    oids, ow = oracle.route(l, k)
+    assert np.array_equal(ids.cpu().numpy(), oids)
+    np.testing.assert_allclose(w.cpu().numpy(), ow, rtol=2e-6, atol=1e-7)
+
+
 def test_empty_batch_is_a_noop(cuda_lib):
     moe = cuda_lib
     L = _small_layer(SMALL[0])
@@ -398,3 +424,22 @@ def test_zipf_prefill_8192_every_row(cuda_lib):
     w = synth.WORKLOADS["long"]
     L = Layer(w.shape(8192), 7_900, layer=0, logit_bias="zipf", gen_device="cuda")
     _check_full(cuda_lib, L, list(range(8192)))
+
+
+# batches of 9..64 tokens on the tensor-core arm: routing, permutation, work list and the
+# expert-ordered f16 rows of x come from one launch whose CTAs each rank the whole batch;
+# E = 1024 with k = 16 fills its shared-memory slot table (64 x 16)
+SMALL_BATCH = [
+    (9, 512, 16, 2, 256, 1, "normal", 141),
+    (33, 512, 1024, 16, 256, 0, "zipf", 142),
+    (64, 512, 1024, 16, 256, 1, "normal", 143),
+    (64, 256, 8, 8, 256, 1, "none", 144),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_BATCH, ids=lambda c: f"T{c[0]}_H{c[1]}_E{c[2]}_k{c[3]}_I{c[4]}_sh{c[5]}")
+def test_small_batch_tensor_core_forward(cuda_lib, case):
+    T, H, E, k, I, sh, bias, seed = case
+    L = Layer(synth.Shape(T=T, H=H, E=E, k=k, I=I, has_shared=sh), seed, logit_bias=bias, gen_device="cuda")
+    assert cuda_lib.forward_arm(moe_shape(cuda_lib, L.shape)) == 2
+    _check_full(cuda_lib, L, list(range(T)))
