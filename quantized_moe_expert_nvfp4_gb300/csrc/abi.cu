@@ -182,7 +182,7 @@ cudaError_t launch_gate_up(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cu
 
 cudaError_t launch_down(GroupedArgs a, const moe_shape_t& s, const Ws& ws, cudaStream_t cs) {
   if (arm_for(s) != Arm::kTc) return launch_down_simt(a, cs);
-  cudaError_t e = launch_act_to_f16(a.act, ws.hf, ws.he, static_cast<int64_t>(s.T) * s.k + s.T, s.I, cs);
+  cudaError_t e = launch_act_to_f16(a.act, ws.hf, ws.he, static_cast<int64_t>(s.T) * s.k + s.T, s.I, a.pdl, cs);
   if (e != cudaSuccess) return e;
   a.act = ws.hf;
   a.act_factor = ws.he;
@@ -298,7 +298,7 @@ cudaError_t launch_router(const uint16_t* x, const moe_nvfp4_weights_t& r, const
   // one group of E weight rows against the T rows of x, f16 operands (x scaled per row)
   uint16_t* xf = w.rxf;
   float* xe = w.rxe;
-  cudaError_t e = launch_act_to_f16(x, xf, xe, s.T, s.H, cs);
+  cudaError_t e = launch_act_to_f16(x, xf, xe, s.T, s.H, false, cs);
   if (e == cudaSuccess) e = launch_dense_tiles(s.T, kTcTileRows, w.tiles, w.meta, cs);
   if (e != cudaSuccess) return e;
   GroupedArgs a;
@@ -347,7 +347,7 @@ moe_status_t moe_route_topk(const float* logits, const moe_shape_t* shape, int32
   if (!aligned16(logits) || !aligned16(topk_ids) || !aligned16(topk_w)) return MOE_ERR_INVALID_ARG;
   if (shape->T == 0) return MOE_OK;
   if ((st = check_device(stream)) != MOE_OK) return st;
-  return cuda_status(launch_route_topk(logits, shape->T, shape->E, shape->k, topk_ids, topk_w,
+  return cuda_status(launch_route_topk(logits, shape->T, shape->E, shape->k, topk_ids, topk_w, false,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -534,8 +534,9 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
   // list and the f16 rows of x in one launch whose CTAs each place the whole batch, with no
   // grid-wide wait)
   const bool tc = arm_for(s) == Arm::kTc;
-  if (tc && s.T <= kDecodeMaxT) {
-    e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, cs);
+  const bool small_tc = tc && s.T <= kDecodeMaxT;   // its kernels launch with programmatic dependencies
+  if (small_tc) {
+    e = launch_route_topk(logits, s.T, s.E, s.k, w.ids, w.w, true, cs);
     if (e == cudaSuccess)
       e = launch_permute_gather_small(w.ids, x, s.T, s.E, s.k, s.has_shared, s.H, w.counts, w.offsets, w.sorted_slot,
                                       w.slot_pos, w.tiles, w.meta, tile_rows_for(s), w.xf, w.xe, w.status, cs);
@@ -549,6 +550,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     if (tc) {
       ga.act = w.xf;
       ga.act_factor = w.xe;
+      ga.pdl = small_tc;
       e = launch_gate_up_tc(ga, cs);
     } else {
       e = launch_gate_up_simt(ga, cs);
@@ -569,12 +571,14 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
       da.y16 = y16;
       da.y16_scale = std::ldexp(1.0f, -c);
       da.y16_rowf = rowf;
+      da.pdl = small_tc;
     }
     e = launch_down(da, s, w, cs);
   }
   if (e == cudaSuccess) e = mark(3);
   if (e == cudaSuccess)
-    e = tc ? launch_combine_y16(y16, rowf, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs)
+    e = tc ? launch_combine_y16(y16, rowf, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status,
+                                small_tc, cs)
            : launch_combine(w.y, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs);
   if (e == cudaSuccess) e = mark(4);
   return cuda_status(e);
@@ -701,7 +705,8 @@ moe_status_t moe_forward_fp8(const uint16_t* x, const float* logits, const moe_f
     e = launch_down_fp8(da, cs);
   }
   if (e == cudaSuccess)
-    e = launch_combine_y16(y16, rowf, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, cs);
+    e = launch_combine_y16(y16, rowf, w.slot_pos, w.w, s.T, s.H, s.k, s.has_shared, out, out_is_fp32, w.status, false,
+                           cs);
   return cuda_status(e);
 }
 

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
                                                          int S, int k, uint16_t* __restrict__ dst,
                                                          float* __restrict__ factor, int64_t rows,
                                                          int K, int32_t* status) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (r >= rows) return;
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __
                                                               const int32_t* __restrict__ slot_pos, int T, int k,
                                                               uint16_t* __restrict__ dst, float* __restrict__ factor,
                                                               int K, int slices, int32_t* status) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int t = static_cast<int>(gw / slices), sl = static_cast<int>(gw % slices);
@@ -139,18 +141,16 @@ cudaError_t launch_act_scatter_f16(const uint16_t* x, const int32_t* slot_pos, i
   while (slices * 2 <= K / 256 && static_cast<int64_t>(T) * slices < 152 * 16) slices *= 2;
   while ((K / 256) % slices) slices /= 2;
   const int64_t warps = static_cast<int64_t>(T) * slices;
-  act_scatter_f16_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, st>>>(x, slot_pos, T, k, dst, factor, K,
-                                                                                slices, status);
-  return cudaGetLastError();
+  return launch_pdl(false, act_scatter_f16_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0, st, x, slot_pos,
+                    T, k, dst, factor, K, slices, status);
 }
 
-cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K,
+cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K, bool pdl,
                               cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
-  act_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, nullptr, 0, 1, dst, factor, rows, K,
-                                                                     nullptr);
-  return cudaGetLastError();
+  return launch_pdl(pdl, act_to_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, src,
+                    static_cast<const int32_t*>(nullptr), 0, 1, dst, factor, rows, K, static_cast<int32_t*>(nullptr));
 }
 
 cudaError_t launch_act_gather_f16(const uint16_t* x, const int32_t* sorted_slot, int T, int k, int K,

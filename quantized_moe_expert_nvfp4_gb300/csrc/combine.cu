@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __rest
                                                           const float* __restrict__ topk_w, int T, int H, int k,
                                                           int has_shared, void* out, int out_is_fp32,
                                                           int32_t* status) {
+  pdl_wait();
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int cpr = H / 8;
   if (idx >= static_cast<int64_t>(T) * cpr) return;
@@ -150,12 +151,11 @@ __global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __rest
 
 cudaError_t launch_combine_y16(const uint16_t* y16, const float* rowf, const int32_t* slot_pos, const float* topk_w,
                                int T, int H, int k, int has_shared, void* out, int out_is_fp32, int32_t* status,
-                               cudaStream_t st) {
+                               bool pdl, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(T) * (H / 8);
   const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
-  combine_y16_kernel<<<blocks, 256, 0, st>>>(y16, rowf, slot_pos, topk_w, T, H, k, has_shared, out, out_is_fp32,
-                                             status);
-  return cudaGetLastError();
+  return launch_pdl(pdl, combine_y16_kernel, dim3(blocks), dim3(256), 0, st, y16, rowf, slot_pos, topk_w, T, H, k, has_shared,
+                    out, out_is_fp32, status);
 }
 
 cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float* topk_w, int T,

@@ -296,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MB = a.Nw / kBM;                           // m-blocks per group
   const int KG = a.K / kGK;                            // pipeline groups per item
-  const int n_items = __ldg(a.meta) * MB;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -329,6 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm->tmem_base;
+  pdl_wait_then_release();   // the work list and the activations come from earlier launches
+  const int n_items = __ldg(a.meta) * MB;
 
   if (warp == kWarpTma) {
     if (lane == 0) {
@@ -753,18 +754,11 @@ cudaError_t launch_tc(const GroupedArgs& g, cudaStream_t st) {
   const int64_t items_max = g.max_tiles * (g.N / kBM);
   const int grid = static_cast<int>(std::min<int64_t>(items_max, n_sm));
   if (g.narrow_rows < 0 || g.narrow_rows > 8) return cudaErrorInvalidValue;   // one MMA column block
-  if (small) {
-    if (narrow)
-      grouped_gemm_tc_kernel<kGateUp, 64, true><<<grid, kThreads, smem, st>>>(maps, a);
-    else
-      grouped_gemm_tc_kernel<kGateUp, 64, false><<<grid, kThreads, smem, st>>>(maps, a);
-  } else {
-    if (narrow)
-      grouped_gemm_tc_kernel<kGateUp, 128, true><<<grid, kThreads, smem, st>>>(maps, a);
-    else
-      grouped_gemm_tc_kernel<kGateUp, 128, false><<<grid, kThreads, smem, st>>>(maps, a);
-  }
-  return cudaGetLastError();
+  if (small)
+    return narrow ? launch_pdl(g.pdl, grouped_gemm_tc_kernel<kGateUp, 64, true>, dim3(grid), dim3(kThreads), smem, st, maps, a)
+                  : launch_pdl(g.pdl, grouped_gemm_tc_kernel<kGateUp, 64, false>, dim3(grid), dim3(kThreads), smem, st, maps, a);
+  return narrow ? launch_pdl(g.pdl, grouped_gemm_tc_kernel<kGateUp, 128, true>, dim3(grid), dim3(kThreads), smem, st, maps, a)
+                : launch_pdl(g.pdl, grouped_gemm_tc_kernel<kGateUp, 128, false>, dim3(grid), dim3(kThreads), smem, st, maps, a);
 }
 
 }  // namespace

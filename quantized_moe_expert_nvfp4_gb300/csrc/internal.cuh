@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <utility>
 
 #include "moe_nvfp4.h"
 
@@ -100,6 +101,40 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
   return __half2float(__half(hr));
 }
 
+// Programmatic dependent launch (the kernels of one layer call follow each other on a stream):
+// a kernel launched with launch_pdl may start while the previous kernel drains; before touching
+// global memory it waits for that kernel's completion and the visibility of its writes
+// (griddepcontrol.wait, a no-op when the launch has no programmatic dependency).  Kernels of a
+// single wave of CTAs (the persistent GEMMs, the small routing kernels) then let their successor
+// be scheduled at once (pdl_wait_then_release), so that its launch and shared-memory / TMEM set-up
+// overlap their work; kernels of many waves do not (pdl_wait), because a successor scheduled early
+// would take the SM resources their later waves need.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches kern, with a programmatic dependency on the stream's previous kernel when pdl is set
+// (moe_forward sets it for batches of up to kDecodeMaxT tokens, where launch latency is a visible
+// share of the layer; on larger batches the early-resident successors cost the GEMMs more than the
+// overlap gains, measured on GB300).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
 __device__ __forceinline__ void report_device_error(int32_t* status, int32_t code) {
@@ -115,7 +150,7 @@ cudaError_t ensure_dynamic_smem(const void* kernel, int bytes);
 
 // ------------------------------------------------------------------ launchers
 // Each returns cudaGetLastError() of its launches.
-cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, bool pdl,
                               cudaStream_t st);
 // Single-CTA routing + permutation + work list for small T (decode arm).
 cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_in, int T, int E,
@@ -169,11 +204,12 @@ struct GroupedArgs {
   // tensor-core arm: work items of at most this many rows (<= 8) run on the dequant warps'
   // register arm inside the same launch (0: every item on tcgen05)
   int narrow_rows = 0;
+  bool pdl = false;             // launched with a programmatic dependency (see launch_pdl)
 };
 cudaError_t launch_gate_up_simt(const GroupedArgs& a, cudaStream_t st);
 cudaError_t launch_down_simt(const GroupedArgs& a, cudaStream_t st);
 // bf16 rows -> f16 rows scaled by 2^-e[row] (e = floor(log2 max|row|) - 14), for the f16 MMAs.
-cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K,
+cudaError_t launch_act_to_f16(const uint16_t* src, uint16_t* dst, float* factor, int64_t rows, int K, bool pdl,
                               cudaStream_t st);
 // The same for the gate_up operand, gathered into expert order: row p < S of dst is token
 // sorted_slot[p] / k of x, row S + t is token t (out-of-range slots are reported as kDevBadIndex).
@@ -210,9 +246,6 @@ struct GroupedFp8Args {
   uint16_t* y16 = nullptr;
   float y16_scale = 0.0f;
   float* y16_rowf = nullptr;
-  // tensor-core arm: work items of at most this many rows (<= 8) run on the dequant warps'
-  // register arm inside the same launch (0: every item on tcgen05)
-  int narrow_rows = 0;
 };
 cudaError_t launch_gate_up_fp8(const GroupedFp8Args& a, cudaStream_t st);
 cudaError_t launch_down_fp8(const GroupedFp8Args& a, cudaStream_t st);
@@ -278,7 +311,7 @@ cudaError_t launch_combine(const float* y, const int32_t* slot_pos, const float*
 // The same sum over the tensor-core down's compact y: row p's values are f16 * rowf[p].
 cudaError_t launch_combine_y16(const uint16_t* y16, const float* rowf, const int32_t* slot_pos, const float* topk_w,
                                int T, int H, int k, int has_shared, void* out, int out_is_fp32, int32_t* status,
-                               cudaStream_t st);
+                               bool pdl, cudaStream_t st);
 // Router GEMM on the CUDA cores: logits [T, E] fp32 = scale2 * x . deq(W)^T, W one NVFP4
 // projection of E rows of H (H % 16 == 0).
 cudaError_t launch_router_simt(const uint16_t* x, const moe_nvfp4_weights_t& w, int T, int H, int E, float* logits,

@@ -20,6 +20,7 @@ template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
+  pdl_wait_then_release();
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -185,6 +186,7 @@ __global__ void __launch_bounds__(1024) permute_gather_small_kernel(
   __shared__ int s_cur[kMaxE];
   __shared__ int s_warp[32];
   __shared__ float s_max[32];
+  pdl_wait_then_release();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool lead = blockIdx.x == 0;
   const int S = T * k;
@@ -412,16 +414,11 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
 
 }  // namespace
 
-cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+cudaError_t launch_route_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, bool pdl,
                               cudaStream_t st) {
   const int blocks = (T + 7) / 8;
-  if (E <= 256)
-    route_topk_kernel<8><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
-  else if (E <= 512)
-    route_topk_kernel<16><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
-  else
-    route_topk_kernel<32><<<blocks, 256, 0, st>>>(logits, T, E, k, ids, w);
-  return cudaGetLastError();
+  auto kern = (E <= 256) ? route_topk_kernel<8> : (E <= 512) ? route_topk_kernel<16> : route_topk_kernel<32>;
+  return launch_pdl(pdl, kern, dim3(blocks), dim3(256), 0, st, logits, T, E, k, ids, w);
 }
 
 cudaError_t launch_route_permute_small(const float* logits, const int32_t* ids_in, int T, int E,
@@ -468,10 +465,8 @@ cudaError_t launch_permute_gather_small(const int32_t* ids, const uint16_t* x, i
   int n_sm = 0;
   cudaError_t e = current_sm_count(&n_sm);
   if (e != cudaSuccess) return e;
-  permute_gather_small_kernel<<<std::min(T, n_sm), 1024, 0, st>>>(ids, x, T, E, k, has_shared, H, counts, offsets,
-                                                                  sorted_slot, slot_pos, tiles, meta, tile_rows, xf,
-                                                                  xe, status);
-  return cudaGetLastError();
+  return launch_pdl(true, permute_gather_small_kernel, dim3(std::min(T, n_sm)), dim3(1024), 0, st, ids, x, T, E, k,
+                    has_shared, H, counts, offsets, sorted_slot, slot_pos, tiles, meta, tile_rows, xf, xe, status);
 }
 
 cudaError_t launch_build_tiles(const int32_t* offsets, int T, int E, int k, int has_shared,
