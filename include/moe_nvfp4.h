@@ -180,13 +180,14 @@ moe_status_t moe_forward_routed(const uint16_t* x, const moe_nvfp4_weights_t* ro
  * cudaMalloc is not allowed or not available, such as inside a framework's memory-planning phase,
  * a host callback, or a plugin whose host application owns every device allocation and only
  * passes in tensor pointers.  No workspace argument: the scratch (routing results, permutation,
- * the partial expert outputs, the status word and the decode kernel's counters) lives in one
- * 16 MiB array in device global memory that the library declares at file scope; every GPU that
+ * the layer's h and expert outputs, the status word and the decode kernel's counters) lives in
+ * one 4 MiB array in device global memory that the library declares at file scope; every GPU that
  * loads the library holds it until the library is unloaded.  The pages have no counterpart to
  * this call; it is a deployment aid.
  *   - Inputs, weights and out are as for moe_forward; nothing is allocated or freed.
- *   - Shapes whose scratch exceeds 16 MiB (the partial outputs take (I/64) * T * (k+1) * H * 4
- *     bytes), and shapes outside arm 0, return MOE_ERR_UNSUPPORTED_SHAPE.
+ *   - Shapes outside arm 0 return MOE_ERR_UNSUPPORTED_SHAPE, and so would a shape whose scratch
+ *     exceeded 4 MiB (h and the expert outputs take T (k+1) (2 I + 4 H) bytes, at most 2.5 MB on
+ *     arm-0 shapes, so every arm-0 shape fits).
  *   - All calls on a device share the array: calls that overlap on the GPU (other streams or
  *     threads) race and corrupt each other; serialize them.
  *   - The first call on a device looks up the array's device address, and looks it up again

@@ -277,7 +277,7 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.xe = take(4 * tc_rows);
   L.hf = take(2 * tc_rows * s.I);
   L.he = take(4 * tc_rows);
-  L.yp = take(arm == 0 ? fd_partial_bytes(s) : 0);
+  L.fdscr = take(arm == 0 ? fd_scratch_bytes(s) : 0);
   // the router GEMM (moe_router_logits, moe_forward_routed)
   L.rxf = take(router_on_tc(s) ? 2 * static_cast<size_t>(s.T) * s.H : 0);
   L.rxe = take(router_on_tc(s) ? 4 * static_cast<size_t>(s.T) : 0);
@@ -482,7 +482,7 @@ moe_status_t moe_forward_profiled(const uint16_t* x, const float* logits,
     f.offsets = w.offsets;
     f.sorted_slot = w.sorted_slot;
     f.slot_pos = w.slot_pos;
-    f.yp = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + w.L.yp);
+    f.scratch = reinterpret_cast<char*>(ws) + w.L.fdscr;
     f.sync = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(ws) + w.L.fdsync);
     f.out = out;
     f.out_is_fp32 = out_is_fp32;

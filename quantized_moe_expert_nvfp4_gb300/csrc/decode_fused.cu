@@ -4,28 +4,30 @@
 // the selected experts' bytes (bandwidth floor = bytes of the active experts / stream bandwidth,
 // done when within 1.3x of it), the routed top-k and the shared expert in one launch per
 // projection, gate+up fused and silu+down fused, and no host round trip.  Here one launch does
-// all of it, split so that no CTA ever waits for another one's intermediate:
+// all of it:
 //   phase A  every CTA routes the T tokens itself (one warp per token), builds the permutation
 //            in shared memory with block-wide scans, and stages x as f16 rows scaled by a power
 //            of two per row (exact for every element of at least 2^-31 of the row maximum);
-//   phase B  work units: one active expert (the shared expert first) and one 64-wide slice of
-//            its intermediate dimension.  A unit streams the slice's 64 gate rows, their 64 up
-//            rows and the down projection's 64 matching columns (every output row's 32 bytes
-//            of the slice), computes h = SiLU(g) * u for its 64 columns on chip (rounded to
-//            bf16), and multiplies it by its down columns: a partial expert output over the
-//            slice, written in fp32.  Down is thereby split along I (split-K) instead of
-//            waiting for other CTAs' h;
-//   phase C  once every unit of the launch is done (one counter), each CTA sums, for a block
-//            of output columns, the I/64 partials of every (token, expert) in slice order and
-//            combines the experts in the fixed order out[t] = sum_j w[t,j] y[t,j] + y_shared[t],
-//            in fp32.
+//   phase B  work units of two kinds, all gate_up units of the launch before all down units:
+//            a gate_up unit is one active expert (the shared expert first) and one 64-wide slice
+//            of its intermediate dimension -- it streams the slice's 64 gate rows and their 64 up
+//            rows, computes h = SiLU(g) * u for its 64 columns (rounded to bf16), writes them to
+//            the expert's rows of h in global memory and counts itself done for the expert; a
+//            down unit is one active expert and 256 output rows -- it streams those rows' whole
+//            down weights (contiguous 128-byte lines), waits until every slice of its expert's h
+//            is written, stages that h as f16 and writes the 256 outputs of every token row
+//            of the expert (y, fp32);
+//   phase C  once every unit of the launch is done (one counter), each CTA combines a block of
+//            output columns in the fixed order out[t] = sum_j w[t,j] y[t,j] + y_shared[t], fp32.
+// A down unit's weights do not depend on h, so its CTA streams them while the gate_up units it
+// waits for finish elsewhere; a CTA reaches its first down unit only after its own gate_up
+// units, so no wait can close a cycle (all CTAs are co-resident: cooperative launch).
 // A producer warp streams each CTA's units into a ring of shared-memory slots with large copies
 // (a GB300 SM keeps only a few bulk copies in flight, so its stream rate grows with the copy
 // size): a gate_up chunk is one 32 KB TMA tensor copy (128 rows x 512 K, 128-byte swizzle) and
-// one copy of its 4 KB of scales; a down chunk is one 32 KB tensor copy (1024 output rows x the
-// slice's 32 bytes, 32-byte swizzle), its 4-byte scale words fetched by the producer lanes with
-// cp.async.  All 16 compute warps consume every chunk (each takes its share of the rows or of
-// K), so the ring is consumed in order and its depth does not depend on the warp count.
+// one copy of its 4 KB of scales; a down chunk one 32 KB copy (256 rows x 256 K) and one of its
+// 4 KB of scales.  All 16 compute warps consume every chunk (each takes its share of the rows or
+// of K), so the ring is consumed in order and its depth does not depend on the warp count.
 // Products run on the tensor cores (mma.sync m16n8k16, f16 operands, fp32 accumulation): the
 // weights are dequantized exactly into f16 (e2m1 x e4m3 has at most 6 significant bits and lies
 // in [2^-10, 2688]) and the MMA columns are the expert's tokens (up to 8).
@@ -53,7 +55,9 @@ constexpr int kIs = kFdSlice;                  // intermediate columns of one un
 constexpr int kGuK = 512;                      // K of one gate_up chunk (two 128-byte lines per row)
 constexpr int kGuPacked = 2 * kIs * kGuK / 2;  // 32 KB: [line 2][gate|up][64 rows][128 B]
 constexpr int kGuScales = 2 * kIs * kGuK / 16; // 4 KB:  [gate|up][64 rows][32 B]
-constexpr int kDnScaleOff = 32 * 1024;         // down chunk: packed [rows][32 B], then [rows][4 B] scales
+constexpr int kDnRows = 256;                   // output rows of a down unit
+constexpr int kDnK = 256;                      // K of one down chunk (one 128-byte line per row)
+constexpr int kDnScaleOff = 32 * 1024;         // down chunk: packed [256 rows][128 B], then [256 rows][16 B] scales
 constexpr int kSlotBytes = 36 * 1024;
 constexpr int kDkMaxSlots = 8;
 constexpr int kFdMaxS = kFdMaxT * kMaxK;
@@ -61,27 +65,29 @@ constexpr int kFdSmemLimit = 227 * 1024;
 constexpr uint64_t kFdTimeoutNs = 1000000000ull;
 constexpr int kRedCols = 16;                   // output columns per reduction block
 
-static_assert(kIs == 64, "a unit's h slice is 8 MMA tiles of 8 gate + 8 up rows, and 32 bytes of a down row");
+static_assert(kIs == 64, "a gate_up unit's h slice is 8 MMA tiles of 8 gate + 8 up rows");
+static_assert(kDnRows == 16 * kDkCompute, "a down chunk gives each compute warp one MMA tile of rows");
+static_assert(2 * kFdMaxAct + 2 <= kFdSyncWords, "sync words: units-done counters and per-expert h counters");
 
 // TMA descriptors:
 //   gu   packed gate_up {128 B, row of [G * 2I - I], gate/up half (stride I rows), 128-byte line
 //        (stride 128 B)}: a box of 64 rows x 2 halves x 2 lines is one gate_up chunk
 //   gus  gate_up scales {H/16 B, row of [G * 2I - I], gate/up half}: a box of 32 B x 64 x 2
-//   dn   packed down {I/2 B, row in a block of 256, block of 256 rows of [G * H]}: a box of
-//        32 B x 256 x (rows / 256) is one down chunk
+//   dn   packed down {I/2 B, row of [G * H]}: a box of 128 B x 256 rows is one down chunk
+//   dns  down scales {I/16 B, row of [G * H]}: a box of 16 B x 256 rows
 // (the row dimension of the gate_up maps stops I rows early, so that the up half of every box
 // stays inside the tensor and the out-of-range fill would cover a bad coordinate)
 struct FdMaps {
   CUtensorMap gu;
   CUtensorMap gus;
   CUtensorMap dn;
+  CUtensorMap dns;
 };
 
 struct FdArgs {
   const uint16_t* x;
   const float* logits;
   const float* gu_scale2;
-  const uint8_t* dn_scales;
   const float* dn_scale2;
   int T, H, I, E, k, has_shared;
   int32_t* ids;
@@ -90,13 +96,15 @@ struct FdArgs {
   int32_t* offsets;
   int32_t* sorted_slot;
   int32_t* slot_pos;
-  float* yp;                      // [I/64][S + T][H] partial expert outputs
+  uint16_t* h;                    // [S + T][I] bf16, expert-ordered rows (gate_up units -> down units)
+  float* y;                       // [S + T][H] fp32 expert outputs (down units -> combine)
   void* out;
   int out_is_fp32;
   unsigned long long* grid_ctr;   // launch count: one arrival per CTA and launch, monotonic
   unsigned* done;                 // [2] units-done counters (CTAs), one per launch parity
+  unsigned* hdone;                // [2][kFdMaxAct] gate_up units done per active expert, per parity
   int32_t* status;
-  int x_pitch, ctl_off, ring_off, n_slots, dn_rows;
+  int x_pitch, hb_pitch, ctl_off, ring_off, n_slots;
 };
 
 struct FdSmem {
@@ -114,7 +122,7 @@ struct FdSmem {
   int wnz[kDkCompute];
   float xfac[kFdMaxT];         // 2^e of each staged f16 activation row
   alignas(16) float red[8][32 * 4];            // gate_up: the second K half's sums, per MMA tile
-  alignas(16) uint16_t htile[kFdMaxT][kIs + 8];   // the unit's h (bf16), one row per token
+  float hfac[kFdMaxT];         // 2^e of each staged f16 row of h (down units)
   int n_act;
   int abort_flag;
   int ep;                      // this launch's counter set (parity of the launch count)
@@ -173,6 +181,13 @@ __global__ void __launch_bounds__(32) fd_timeout_probe_kernel(int32_t* status, u
   fd_wait(&bar, 0, &abort_flag, status, limit_ns);
 }
 
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
@@ -187,9 +202,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* tm, in
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
       : "memory");
-}
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
 // Two fp32 -> f16x2 (round to nearest; exact for the power-of-two-scaled bf16 values used here).
@@ -217,47 +229,41 @@ template <int EPL>
 __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __grid_constant__ FdMaps maps, FdArgs a) {
   extern __shared__ __align__(1024) uint8_t fd_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fd_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* xs = base;   // f16 activation rows, x_pitch bytes apart
+  uint8_t* xs = base;   // f16 activation rows, x_pitch bytes apart (gate_up units)
+  uint8_t* hb = base;   // the same area for a down unit's f16 rows of h, hb_pitch bytes apart
   FdSmem* sm = reinterpret_cast<FdSmem*>(base + a.ctl_off);
   uint8_t* ring = base + a.ring_off;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, I = a.I, E = a.E, k = a.k, S = T * k;
   const int NS = a.n_slots;
-  const int nslice = I / kIs;
-  const int n_gu = H / kGuK;                 // gate_up chunks of a unit
-  const int n_dn = H / a.dn_rows;            // down chunks of a unit
-  const int n_chunk = n_gu + n_dn;
+  const int nslice = I / kIs;                // gate_up units per active expert
+  const int nrb = H / kDnRows;               // down units per active expert
+  const int n_gu = H / kGuK;                 // chunks of a gate_up unit
+  const int n_dnc = I / kDnK;                // chunks of a down unit
 
-  // The producer warp issues chunk c of unit (group g, slice m) into ring position it (warp-wide:
-  // the down chunk's scale words are fetched by all 32 lanes).
-  auto issue = [&](int g, int m, int c, uint32_t it) {
+  // Lane 0 of the producer warp issues chunk c of a gate_up unit (group g, slice m), or of a down
+  // unit (group g, 256-row block rb), into ring position it.
+  auto issue_gu = [&](int g, int m, int c, uint32_t it) {
     const int slot = it % NS;
     uint8_t* dst = ring + slot * kSlotBytes;
     uint64_t* bar = &sm->full[slot];
-    if (c < n_gu) {
-      if (lane == 0) {
-        const int r0 = g * 2 * I + m * kIs;   // first gate row of the slice; its up row is + I
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                     "r"(kGuPacked + kGuScales)
-                     : "memory");
-        tma_load_4d(dst, &maps.gu, 0, r0, 0, 2 * c, bar);
-        tma_load_3d(dst + kGuPacked, &maps.gus, 32 * c, r0, 0, bar);
-      }
-    } else {
-      const int d = c - n_gu;
-      const int64_t row0 = static_cast<int64_t>(g) * H + static_cast<int64_t>(d) * a.dn_rows;
-      const uint8_t* src = a.dn_scales + row0 * (I / 16) + 4 * m;
-      for (int r = lane; r < a.dn_rows; r += 32) cp_async4(dst + kDnScaleOff + 4 * r, src + static_cast<int64_t>(r) * (I / 16));
-      // each lane's arrive (pending count +1 now, -1 once its copies land) before lane 0's
-      asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
-      __syncwarp();
-      if (lane == 0) {
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                     "r"(a.dn_rows * (kIs / 2))
-                     : "memory");
-        tma_load_3d(dst, &maps.dn, (kIs / 2) * m, 0, static_cast<int>(row0 / 256), bar);
-      }
-    }
+    const int r0 = g * 2 * I + m * kIs;   // first gate row of the slice; its up row is + I
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(kGuPacked + kGuScales)
+                 : "memory");
+    tma_load_4d(dst, &maps.gu, 0, r0, 0, 2 * c, bar);
+    tma_load_3d(dst + kGuPacked, &maps.gus, 32 * c, r0, 0, bar);
+  };
+  auto issue_dn = [&](int g, int rb, int c, uint32_t it) {
+    const int slot = it % NS;
+    uint8_t* dst = ring + slot * kSlotBytes;
+    uint64_t* bar = &sm->full[slot];
+    const int r0 = g * H + rb * kDnRows;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(kDnRows * (kDnK / 2 + kDnK / 16))
+                 : "memory");
+    tma_load_2d(dst, &maps.dn, c * (kDnK / 2), r0, bar);
+    tma_load_2d(dst + kDnScaleOff, &maps.dns, c * (kDnK / 16), r0, bar);
   };
 
   // ------------------------------------------------------------ phase A: route + permute
@@ -274,8 +280,9 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
     __syncwarp();
     // the shared expert is active group 0: this CTA's first unit is known before routing
     if (a.has_shared && static_cast<int>(blockIdx.x) < nslice) {
-      early = static_cast<uint32_t>(min(n_chunk, NS));
-      for (uint32_t c = 0; c < early; ++c) issue(E, blockIdx.x, c, c);
+      early = static_cast<uint32_t>(min(n_gu, NS));
+      if (lane == 0)
+        for (uint32_t c = 0; c < early; ++c) issue_gu(E, blockIdx.x, c, c);
     }
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) sm->cnt[e] = 0;
@@ -321,7 +328,10 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   if (threadIdx.x == 32) sm->ep = static_cast<int>((launch_n / gridDim.x) & 1ull);
   __syncthreads();
   const int ep = sm->ep;
-  if (blockIdx.x == 0 && threadIdx.x == 0) a.done[ep ^ 1] = 0u;   // the next launch's counter
+  if (blockIdx.x == 0) {   // the next launch's counters
+    if (threadIdx.x == 0) a.done[ep ^ 1] = 0u;
+    for (int i = threadIdx.x; i < kFdMaxAct; i += blockDim.x) a.hdone[(ep ^ 1) * kFdMaxAct + i] = 0u;
+  }
   if (warp < T && lane < k) {
     sm->ids[warp * k + lane] = my_id;
     sm->w[warp * k + lane] = my_w;
@@ -424,16 +434,21 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   }
   __syncthreads();
 
-  const int n_units = sm->n_act * nslice;
+  const int n_gu_units = sm->n_act * nslice;
+  const int n_units = n_gu_units + sm->n_act * nrb;
   unsigned* const done = a.done + ep;
+  unsigned* const hdone = a.hdone + ep * kFdMaxAct;
 
   if (warp == kDkProducer) {
     // ------------------------------------------------------------ producer
     uint32_t it = early;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const int g = sm->act[u / nslice], m = u % nslice;
-      for (int c = (u == static_cast<int>(blockIdx.x)) ? static_cast<int>(early) : 0; c < n_chunk; ++c, ++it) {
+      const bool gu = u < n_gu_units;
+      const int v = gu ? u : u - n_gu_units, per = gu ? nslice : nrb;
+      const int g = sm->act[v / per], sub = v % per;
+      const int nch = gu ? n_gu : n_dnc;
+      for (int c = (u == static_cast<int>(blockIdx.x)) ? static_cast<int>(early) : 0; c < nch; ++c, ++it) {
         const int slot = it % NS;
         if (it >= static_cast<uint32_t>(NS)) {   // the slot's previous chunk must be consumed
           bool got = true;
@@ -441,7 +456,12 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
           ok = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
           if (!ok) break;
         }
-        issue(g, m, c, it);
+        if (lane == 0) {
+          if (gu)
+            issue_gu(g, sub, c, it);
+          else
+            issue_dn(g, sub, c, it);
+        }
       }
     }
     if (!ok && lane == 0) {   // let copies already issued land before the CTA winds down (bounded)
@@ -458,148 +478,177 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   bool ok = true;
   const int grp = lane >> 2, tig = lane & 3;
   // this lane's scale bytes of the piece pair 2 p, 2 p + 1 (piece q's lane block is 2 q + tig / 2):
-  // bytes tig / 2 and 2 + tig / 2 of the pair's scale word (gate_up: word p of a 16-byte scale
-  // row; down: the row's one word), into the low and the high half
+  // bytes tig / 2 and 2 + tig / 2 of the pair's scale word, into the low and the high half
   const uint32_t psel = scale_pair_sel(tig);
   const int mt = warp & 7, kh = warp >> 3;                 // gate_up: MMA tile and 128-byte line
   uint32_t it = 0;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int gi = u / nslice, m = u % nslice;
-    const int g = sm->act[gi], row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
-    // B column grp is the expert's token grp (columns past its count repeat token 0, ignored)
-    const int cb = (grp < nt) ? grp : 0;
-    const int tb = (g == E) ? cb : sm->sorted[row0 + cb] / k;
-    const uint8_t* xr = xs + tb * a.x_pitch + 16 * tig;
-    // ---- gate_up: rows 8 mt + grp of the slice's gate half and of its up half; this warp takes
-    // line kh (K 256 kh .. 256 kh + 255) of every chunk
-    float d[4][4];
+    if (u < n_gu_units) {
+      // ======== gate_up unit: active group gi, intermediate columns 64 m .. 64 m + 63
+      const int gi = u / nslice, m = u % nslice;
+      const int g = sm->act[gi], row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
+      // B column grp is the expert's token grp (columns past its count repeat token 0, ignored)
+      const int cb = (grp < nt) ? grp : 0;
+      const int tb = (g == E) ? cb : sm->sorted[row0 + cb] / k;
+      const uint8_t* xr = xs + tb * a.x_pitch + 16 * tig;
+      // rows 8 mt + grp of the slice's gate half and of its up half; this warp takes line kh
+      // (K 256 kh .. 256 kh + 255) of every chunk
+      float d[4][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.0f;
-    for (int c = 0; c < n_gu; ++c, ++it) {
-      const int slot = it % NS;
-      if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, &sm->abort_flag, a.status));
-      if (ok) {
-        const uint8_t* sl = ring + slot * kSlotBytes;
-        const uint8_t* lg = sl + kh * (2 * kIs * 128) + (8 * mt + grp) * 128 + 4 * tig;   // gate row; up 64 rows on
-        const uint4 sgv = *reinterpret_cast<const uint4*>(sl + kGuPacked + (8 * mt + grp) * 32 + 16 * kh);
-        const uint4 suv = *reinterpret_cast<const uint4*>(sl + kGuPacked + (kIs + 8 * mt + grp) * 32 + 16 * kh);
-        const uint8_t* xc = xr + 2 * (kGuK * c + 256 * kh);
+      for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.0f;
+      for (int c = 0; c < n_gu; ++c, ++it) {
+        const int slot = it % NS;
+        if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, &sm->abort_flag, a.status));
+        if (ok) {
+          const uint8_t* sl = ring + slot * kSlotBytes;
+          const uint8_t* lg = sl + kh * (2 * kIs * 128) + (8 * mt + grp) * 128 + 4 * tig;   // gate row; up 64 rows on
+          const uint4 sgv = *reinterpret_cast<const uint4*>(sl + kGuPacked + (8 * mt + grp) * 32 + 16 * kh);
+          const uint4 suv = *reinterpret_cast<const uint4*>(sl + kGuPacked + (kIs + 8 * mt + grp) * 32 + 16 * kh);
+          const uint8_t* xc = xr + 2 * (kGuK * c + 256 * kh);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {   // piece q of the line (stored at q ^ grp): blocks 2 q, 2 q + 1
-          const uint32_t wg = *reinterpret_cast<const uint32_t*>(lg + ((q ^ grp) << 4));
-          const uint32_t wu = *reinterpret_cast<const uint32_t*>(lg + kIs * 128 + ((q ^ grp) << 4));
-          const uint4 xb = *reinterpret_cast<const uint4*>(xc + 64 * q);
-          const __half2 sgp = e4m3_pair_f16x2_2m8((&sgv.x)[q >> 1], psel);
-          const __half2 sup = e4m3_pair_f16x2_2m8((&suv.x)[q >> 1], psel);
-          uint32_t gr[4], ur[4];
-          piece_frag(wg, (q & 1) ? __high2half2(sgp) : __low2half2(sgp), gr);
-          piece_frag(wu, (q & 1) ? __high2half2(sup) : __low2half2(sup), ur);
-          mma16816(d[(q & 1) * 2], gr[0], ur[0], gr[1], ur[1], xb.x, xb.y);
-          mma16816(d[(q & 1) * 2 + 1], gr[2], ur[2], gr[3], ur[3], xb.z, xb.w);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
-    }
-    float p[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) p[r] = (d[0][r] + d[1][r]) + (d[2][r] + d[3][r]);
-    // the two K halves meet (fixed order), then h[n][8 mt + grp] = bf16(SiLU(g) * u) for the
-    // lane's tokens n = 2 tig, 2 tig + 1
-    if (kh == 1) *reinterpret_cast<float4*>(&sm->red[mt][4 * lane]) = make_float4(p[0], p[1], p[2], p[3]);
-    named_sync(1, kDkCThreads);
-    if (kh == 0) {
-      const float4 o = *reinterpret_cast<const float4*>(&sm->red[mt][4 * lane]);
-      p[0] += o.x;
-      p[1] += o.y;
-      p[2] += o.z;
-      p[3] += o.w;
-      const float s2 = __ldg(a.gu_scale2 + g);
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {
-        const int n = 2 * tig + c2;
-        if (n < nt) {
-          const int t = (g == E) ? n : sm->sorted[row0 + n] / k;
-          const float f = s2 * sm->xfac[t] * kScaleUnbias;
-          sm->htile[n][8 * mt + grp] = f32_to_bf16_bits(silu_f32(p[c2] * f) * (p[2 + c2] * f));
-        }
-      }
-    }
-    named_sync(1, kDkCThreads);
-    // ---- down B operand: token column grp, the slice's h as f16 scaled by 2^-e (e from the
-    // token's maximum over the slice); lane tig holds elements 8 tig .. 8 tig + 7 of both pieces
-    uint4 hb[2];
-    float fac0, fac1;
-    {
-      const uint16_t* hrow = sm->htile[cb];
-      const uint4 v0 = *reinterpret_cast<const uint4*>(hrow + 8 * tig);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(hrow + 32 + 8 * tig);
-      float mx = absmax_bf16x8(absmax_bf16x8(0.0f, v0), v1);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const int e = row_exponent(mx);
-      const float inv = pow2i(-e);
-      const uint4 vv[2] = {v0, v1};
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-        hb[q] = make_uint4(f32x2_to_f16x2(bf16_lo(vv[q].x) * inv, bf16_hi(vv[q].x) * inv),
-                           f32x2_to_f16x2(bf16_lo(vv[q].y) * inv, bf16_hi(vv[q].y) * inv),
-                           f32x2_to_f16x2(bf16_lo(vv[q].z) * inv, bf16_hi(vv[q].z) * inv),
-                           f32x2_to_f16x2(bf16_lo(vv[q].w) * inv, bf16_hi(vv[q].w) * inv));
-      const float f = pow2i(e);
-      fac0 = __shfl_sync(0xffffffffu, f, (2 * tig) * 4);
-      fac1 = __shfl_sync(0xffffffffu, f, (2 * tig + 1) * 4);
-    }
-    const float s2d = __ldg(a.dn_scale2 + g);
-    const int tiles = a.dn_rows / (16 * kDkCompute);   // MMA tiles of a down chunk per warp
-    // ---- down: output rows 16 (tiles w + t) + grp (+ 8) of each chunk; partial over the slice
-    for (int c = 0; c < n_dn; ++c, ++it) {
-      const int slot = it % NS;
-      if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, &sm->abort_flag, a.status));
-      if (ok) {
-        const uint8_t* sl = ring + slot * kSlotBytes;
-        for (int t = 0; t < tiles; ++t) {
-          const int ra = 16 * (tiles * warp + t) + grp;   // rows ra and ra + 8 (32-byte swizzle: piece ^= (row >> 2) & 1)
-          const uint32_t sw = (ra >> 2) & 1u;
-          const uint32_t sca = *reinterpret_cast<const uint32_t*>(sl + kDnScaleOff + 4 * ra);
-          const uint32_t scb = *reinterpret_cast<const uint32_t*>(sl + kDnScaleOff + 4 * (ra + 8));
-          float acc[2][4];
-#pragma unroll
-          for (int q = 0; q < 2; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
-          const __half2 sap = e4m3_pair_f16x2_2m8(sca, psel);
-          const __half2 sbp = e4m3_pair_f16x2_2m8(scb, psel);
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t wa = *reinterpret_cast<const uint32_t*>(sl + ra * 32 + ((q ^ sw) << 4) + 4 * tig);
-            const uint32_t wb = *reinterpret_cast<const uint32_t*>(sl + (ra + 8) * 32 + ((q ^ sw) << 4) + 4 * tig);
-            uint32_t ar[4], br[4];
-            piece_frag(wa, q ? __high2half2(sap) : __low2half2(sap), ar);
-            piece_frag(wb, q ? __high2half2(sbp) : __low2half2(sbp), br);
-            mma16816(acc[q], ar[0], br[0], ar[1], br[1], hb[q].x, hb[q].y);
-            mma16816(acc[q], ar[2], br[2], ar[3], br[3], hb[q].z, hb[q].w);
+          for (int q = 0; q < 8; ++q) {   // piece q of the line (stored at q ^ grp): blocks 2 q, 2 q + 1
+            const uint32_t wg = *reinterpret_cast<const uint32_t*>(lg + ((q ^ grp) << 4));
+            const uint32_t wu = *reinterpret_cast<const uint32_t*>(lg + kIs * 128 + ((q ^ grp) << 4));
+            const uint4 xb = *reinterpret_cast<const uint4*>(xc + 64 * q);
+            const __half2 sgp = e4m3_pair_f16x2_2m8((&sgv.x)[q >> 1], psel);
+            const __half2 sup = e4m3_pair_f16x2_2m8((&suv.x)[q >> 1], psel);
+            uint32_t gr[4], ur[4];
+            piece_frag(wg, (q & 1) ? __high2half2(sgp) : __low2half2(sgp), gr);
+            piece_frag(wu, (q & 1) ? __high2half2(sup) : __low2half2(sup), ur);
+            mma16816(d[(q & 1) * 2], gr[0], ur[0], gr[1], ur[1], xb.x, xb.y);
+            mma16816(d[(q & 1) * 2 + 1], gr[2], ur[2], gr[3], ur[3], xb.z, xb.w);
           }
-          // yp[m][row0 + n][col] for the lane's tokens n = 2 tig, 2 tig + 1
-          const int col = c * a.dn_rows + ra;
+        }
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+      }
+      float p[4];
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int n = 2 * tig + c2;
-            if (n < nt) {
-              const float f = s2d * (c2 ? fac1 : fac0) * kScaleUnbias;
-              float* yr = a.yp + (static_cast<int64_t>(m) * (S + T) + row0 + n) * H + col;
-              yr[0] = (acc[0][c2] + acc[1][c2]) * f;
-              yr[8] = (acc[0][2 + c2] + acc[1][2 + c2]) * f;
-            }
+      for (int r = 0; r < 4; ++r) p[r] = (d[0][r] + d[1][r]) + (d[2][r] + d[3][r]);
+      // the two K halves meet (fixed order), then h[row0 + n][64 m + 8 mt + grp] =
+      // bf16(SiLU(g) * u) for the lane's tokens n = 2 tig, 2 tig + 1, written to global memory
+      if (kh == 1) *reinterpret_cast<float4*>(&sm->red[mt][4 * lane]) = make_float4(p[0], p[1], p[2], p[3]);
+      named_sync(1, kDkCThreads);
+      if (kh == 0) {
+        const float4 o = *reinterpret_cast<const float4*>(&sm->red[mt][4 * lane]);
+        p[0] += o.x;
+        p[1] += o.y;
+        p[2] += o.z;
+        p[3] += o.w;
+        const float s2 = __ldg(a.gu_scale2 + g);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int n = 2 * tig + c2;
+          if (n < nt) {
+            const int t = (g == E) ? n : sm->sorted[row0 + n] / k;
+            const float f = s2 * sm->xfac[t] * kScaleUnbias;
+            a.h[static_cast<int64_t>(row0 + n) * I + m * kIs + 8 * mt + grp] =
+                f32_to_bf16_bits(silu_f32(p[c2] * f) * (p[2 + c2] * f));
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+      // every slice of h written by this unit is published before the unit counts as done
+      named_sync(1, kDkCThreads);
+      if (threadIdx.x == 0 && ok) {
+        __threadfence();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(hdone + gi) : "memory");
+      }
+    } else {
+      // ======== down unit: active group gi, output rows 256 rb .. 256 rb + 255
+      const int v = u - n_gu_units;
+      const int gi = v / nrb, rb = v % nrb;
+      const int g = sm->act[gi], row0 = sm->act_row[gi], nt = sm->act_cnt[gi];
+      // wait until every gate_up unit of the group has written its slice of h
+      if (threadIdx.x == 0 && ok) {
+        const uint64_t t0 = now_ns();
+        for (uint32_t i = 0;; ++i) {
+          unsigned c;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(hdone + gi) : "memory");
+          if (c >= static_cast<unsigned>(nslice)) break;
+          if ((i & 63u) == 63u && (*reinterpret_cast<volatile int*>(&sm->abort_flag) || now_ns() - t0 > kFdTimeoutNs)) {
+            if (!*reinterpret_cast<volatile int*>(&sm->abort_flag)) report_device_error(a.status, kDevTimeout);
+            sm->abort_flag = 1;
+            break;
+          }
+        }
+      }
+      named_sync(1, kDkCThreads);
+      if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) ok = false;
+      // the group's rows of h as f16 scaled by 2^-e per row (e from the row's maximum over all I
+      // columns, as for x): warp n stages token row n
+      if (ok && warp < nt) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.h + static_cast<int64_t>(row0 + warp) * I);
+        float mx = 0.0f;
+        for (int c = lane; c < I / 8; c += 32) mx = absmax_bf16x8(mx, __ldcg(src + c));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const int e = row_exponent(mx);
+        const float inv = pow2i(-e);
+        if (lane == 0) sm->hfac[warp] = pow2i(e);
+        uint4* dst = reinterpret_cast<uint4*>(hb + warp * a.hb_pitch);
+        for (int c = lane; c < I / 8; c += 32) {
+          const uint4 hv = __ldcg(src + c);
+          dst[c] = make_uint4(f32x2_to_f16x2(bf16_lo(hv.x) * inv, bf16_hi(hv.x) * inv),
+                              f32x2_to_f16x2(bf16_lo(hv.y) * inv, bf16_hi(hv.y) * inv),
+                              f32x2_to_f16x2(bf16_lo(hv.z) * inv, bf16_hi(hv.z) * inv),
+                              f32x2_to_f16x2(bf16_lo(hv.w) * inv, bf16_hi(hv.w) * inv));
+        }
+      }
+      named_sync(1, kDkCThreads);
+      // this warp's MMA tile: rows ra = 16 warp + grp and ra + 8 of the block, all of K; B column
+      // grp is the group's token grp (columns past its count repeat token 0, never written)
+      const int ra = 16 * warp + grp, rc = ra + 8;
+      const uint8_t* hrow = hb + ((grp < nt) ? grp : 0) * a.hb_pitch + 16 * tig;
+      float acc[2][4];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.0f;
+      for (int c = 0; c < n_dnc; ++c, ++it) {
+        const int slot = it % NS;
+        if (ok) ok = __all_sync(0xffffffffu, fd_wait(&sm->full[slot], (it / NS) & 1, &sm->abort_flag, a.status));
+        if (ok) {
+          const uint8_t* sl = ring + slot * kSlotBytes;
+          const uint8_t* rowa = sl + ra * (kDnK / 2);
+          const uint8_t* rowc = sl + rc * (kDnK / 2);
+          const uint4 sca = *reinterpret_cast<const uint4*>(sl + kDnScaleOff + ra * (kDnK / 16));
+          const uint4 scc = *reinterpret_cast<const uint4*>(sl + kDnScaleOff + rc * (kDnK / 16));
+          const uint8_t* hc = hrow + 2 * kDnK * c;
+#pragma unroll
+          for (int q = 0; q < kDnK / 32; ++q) {   // piece q: K 32 q .. 32 q + 31 (128-byte swizzle)
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(rowa + ((q ^ (ra & 7)) << 4) + 4 * tig);
+            const uint32_t wc = *reinterpret_cast<const uint32_t*>(rowc + ((q ^ (rc & 7)) << 4) + 4 * tig);
+            const uint4 xb = *reinterpret_cast<const uint4*>(hc + 64 * q);
+            const __half2 sap = e4m3_pair_f16x2_2m8((&sca.x)[q >> 1], psel);
+            const __half2 scp = e4m3_pair_f16x2_2m8((&scc.x)[q >> 1], psel);
+            uint32_t ar[4], cr[4];
+            piece_frag(wa, (q & 1) ? __high2half2(sap) : __low2half2(sap), ar);
+            piece_frag(wc, (q & 1) ? __high2half2(scp) : __low2half2(scp), cr);
+            mma16816(acc[q & 1], ar[0], cr[0], ar[1], cr[1], xb.x, xb.y);
+            mma16816(acc[q & 1], ar[2], cr[2], ar[3], cr[3], xb.z, xb.w);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&sm->empty[slot])) : "memory");
+      }
+      // y[row0 + n][256 rb + ra] (and ra + 8) for the lane's tokens n = 2 tig, 2 tig + 1
+      if (ok) {
+        const float s2d = __ldg(a.dn_scale2 + g) * kScaleUnbias;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int n = 2 * tig + c2;
+          if (n < nt) {
+            const float f = s2d * sm->hfac[n];
+            float* yr = a.y + static_cast<int64_t>(row0 + n) * H + rb * kDnRows + ra;
+            yr[0] = (acc[0][c2] + acc[1][c2]) * f;
+            yr[8] = (acc[0][2 + c2] + acc[1][2 + c2]) * f;
+          }
+        }
+      }
     }
   }
 
-  // ------------------------------------------------------------ phase C: reduce + combine
-  // every CTA's partials are published by its arrival on the launch's counter (release), and
-  // the reduction starts once all CTAs have arrived (acquire)
+  // ------------------------------------------------------------ phase C: combine
+  // every CTA's outputs are published by its arrival on the launch's counter (release), and
+  // the combine starts once all CTAs have arrived (acquire)
   named_sync(1, kDkCThreads);
   if (threadIdx.x == 0) {
     if (ok) {
@@ -622,50 +671,24 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   }
   named_sync(1, kDkCThreads);
   if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return;
-  // column blocks of 16: task (t, j', c4) sums the slice partials of output t's expert j'
-  // (j' = k is the shared expert) over 4 columns into SMEM, then (t, c4) combines in order
-  const int J = k + a.has_shared;
-  float4* red2 = reinterpret_cast<float4*>(ring);   // [T][J][4]
+  // columns in blocks of 16: thread (t, c4) sums token t's expert outputs over 4 columns in
+  // rank order, then adds the shared expert's
   for (int b = blockIdx.x; b < H / kRedCols; b += gridDim.x) {
     const int col0 = b * kRedCols;
-    for (int task = threadIdx.x; task < T * J * 4; task += kDkCThreads) {
-      const int c4 = task & 3, tj = task >> 2, t = tj / J, j = tj % J;
-      const int row = (j < k) ? sm->slot_pos[t * k + j] : S + t;
-      const float* src = a.yp + static_cast<int64_t>(row) * H + col0 + 4 * c4;
-      // the slices' loads in groups of 8 issued together, summed in slice order
-      float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      for (int m0 = 0; m0 < nslice; m0 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-          if (m0 + m < nslice)
-            v[m] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(m0 + m) * (S + T) * H));
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          if (m0 + m < nslice) {
-            s.x += v[m].x;
-            s.y += v[m].y;
-            s.z += v[m].z;
-            s.w += v[m].w;
-          }
-        }
-      }
-      red2[tj * 4 + c4] = s;
-    }
-    named_sync(1, kDkCThreads);
     for (int task = threadIdx.x; task < T * 4; task += kDkCThreads) {
       const int t = task >> 2, c4 = task & 3;
       float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       for (int j = 0; j < k; ++j) {
         const float wj = sm->w[t * k + j];
-        const float4 v = red2[(t * J + j) * 4 + c4];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<int64_t>(sm->slot_pos[t * k + j]) * H +
+                                                                col0 + 4 * c4));
         acc.x = fmaf(wj, v.x, acc.x);
         acc.y = fmaf(wj, v.y, acc.y);
         acc.z = fmaf(wj, v.z, acc.z);
         acc.w = fmaf(wj, v.w, acc.w);
       }
       if (a.has_shared) {
-        const float4 v = red2[(t * J + k) * 4 + c4];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<int64_t>(S + t) * H + col0 + 4 * c4));
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -680,27 +703,25 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
                        static_cast<uint32_t>(f32_to_bf16_bits(acc.z)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.w)) << 16));
       }
     }
-    named_sync(1, kDkCThreads);
   }
 }
 
 struct FdPlan {
-  int x_pitch, x_bytes, ctl_off, ring_off, n_slots, dn_rows;
+  int x_pitch, hb_pitch, x_bytes, ctl_off, ring_off, n_slots;
   size_t smem_total;
 };
 
 bool fd_plan(const moe_shape_t& s, FdPlan* p) {
   if (s.T < 1 || s.T > kFdMaxT || s.H % 512 || s.H > 4096 || s.I % 256 || s.I > 1024) return false;
-  p->x_pitch = 2 * s.H + 64;   // the 64 extra bytes put the 8 rows of an MMA's B loads in distinct banks
-  p->x_bytes = ((s.T * p->x_pitch + 127) / 128) * 128;
+  // the 64 extra bytes per row put the 8 rows of an MMA's B loads in distinct banks
+  p->x_pitch = 2 * s.H + 64;   // f16 rows of x (gate_up units)
+  p->hb_pitch = 2 * s.I + 64;  // f16 rows of h (down units), in the same area
+  p->x_bytes = ((s.T * std::max(p->x_pitch, p->hb_pitch) + 127) / 128) * 128;
   p->ctl_off = p->x_bytes;
   p->ring_off = ((p->ctl_off + static_cast<int>(sizeof(FdSmem)) + 1023) / 1024) * 1024;
   p->n_slots = std::min(kDkMaxSlots, (kFdSmemLimit - 1024 - p->ring_off) / kSlotBytes);
-  p->dn_rows = (s.H % 1024 == 0) ? 1024 : 512;   // down chunk: 32 KB (16 KB when H is an odd multiple of 512)
   p->smem_total = 1024 + static_cast<size_t>(p->ring_off) + static_cast<size_t>(p->n_slots) * kSlotBytes;
-  // the reduction's [T][k + 1][4] float4 fit in the ring
-  const size_t red_bytes = static_cast<size_t>(s.T) * (s.k + 1) * 4 * 16;
-  return p->n_slots >= 3 && red_bytes <= static_cast<size_t>(p->n_slots) * kSlotBytes;
+  return p->n_slots >= 3;
 }
 
 template <int EPL>
@@ -738,10 +759,16 @@ bool decode_fused_supported(const moe_shape_t& s) {
   return fd_plan(s, &p);
 }
 
-size_t fd_partial_bytes(const moe_shape_t& s) {
+// h [S + T][I] bf16, then (at a 256-byte boundary) y [S + T][H] fp32.
+size_t fd_h_bytes(const moe_shape_t& s) {
+  const size_t R = static_cast<size_t>(s.T) * s.k + s.T;
+  return (R * s.I * sizeof(uint16_t) + 255) & ~static_cast<size_t>(255);
+}
+
+size_t fd_scratch_bytes(const moe_shape_t& s) {
   if (!decode_fused_supported(s)) return 0;
   const size_t R = static_cast<size_t>(s.T) * s.k + s.T;
-  return static_cast<size_t>(s.I / kFdSlice) * R * s.H * sizeof(float);
+  return fd_h_bytes(s) + R * s.H * sizeof(float);
 }
 
 cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
@@ -752,7 +779,6 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   a.x = d.x;
   a.logits = d.logits;
   a.gu_scale2 = d.gate_up.scale2;
-  a.dn_scales = d.down.scales;
   a.dn_scale2 = d.down.scale2;
   a.T = s.T;
   a.H = s.H;
@@ -766,17 +792,19 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   a.offsets = d.offsets;
   a.sorted_slot = d.sorted_slot;
   a.slot_pos = d.slot_pos;
-  a.yp = d.yp;
+  a.h = static_cast<uint16_t*>(d.scratch);
+  a.y = reinterpret_cast<float*>(static_cast<char*>(d.scratch) + fd_h_bytes(s));
   a.out = d.out;
   a.out_is_fp32 = d.out_is_fp32;
   a.grid_ctr = d.grid_ctr;
   a.done = d.sync;
+  a.hdone = d.sync + 2;
   a.status = d.status;
   a.x_pitch = plan.x_pitch;
+  a.hb_pitch = plan.hb_pitch;
   a.ctl_off = plan.ctl_off;
   a.ring_off = plan.ring_off;
   a.n_slots = plan.n_slots;
-  a.dn_rows = plan.dn_rows;
   FdMaps maps;
   const uint64_t G = static_cast<uint64_t>(d.gate_up.G);
   const uint64_t H = static_cast<uint64_t>(s.H), I = static_cast<uint64_t>(s.I);
@@ -787,16 +815,22 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st) {
   const uint64_t gus_dims[3] = {H / 16, G * 2 * I - I, 2};
   const uint64_t gus_strides[2] = {H / 16, I * (H / 16)};
   const uint32_t gus_box[3] = {32, static_cast<uint32_t>(kIs), 2};
-  // down packed {I/2 B, row in a block of 256, block}
-  const uint64_t dn_dims[3] = {I / 2, 256, static_cast<uint64_t>(d.down.G) * H / 256};
-  const uint64_t dn_strides[2] = {I / 2, 256 * (I / 2)};
-  const uint32_t dn_box[3] = {static_cast<uint32_t>(kIs / 2), 256, static_cast<uint32_t>(plan.dn_rows / 256)};
+  // down packed {I/2 B, row} with boxes of 128 B x 256 rows; scales {I/16 B, row}, 16 B x 256 rows
+  const uint64_t dn_rows = static_cast<uint64_t>(d.down.G) * H;
+  const uint64_t dn_dims[2] = {I / 2, dn_rows};
+  const uint64_t dn_strides[1] = {I / 2};
+  const uint32_t dn_box[2] = {kDnK / 2, kDnRows};
+  const uint64_t dns_dims[2] = {I / 16, dn_rows};
+  const uint64_t dns_strides[1] = {I / 16};
+  const uint32_t dns_box[2] = {kDnK / 16, kDnRows};
   if (!make_tensor_map(&maps.gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, d.gate_up.packed, gu_dims, gu_strides, gu_box,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tensor_map(&maps.gus, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.gate_up.scales, gus_dims, gus_strides,
                        gus_box, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_tensor_map(&maps.dn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, d.down.packed, dn_dims, dn_strides, dn_box,
-                       CU_TENSOR_MAP_SWIZZLE_32B))
+      !make_tensor_map(&maps.dn, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d.down.packed, dn_dims, dn_strides, dn_box,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tensor_map(&maps.dns, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, d.down.scales, dns_dims, dns_strides, dns_box,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (s.E <= 256) return launch_fd<8>(maps, a, plan, st);
   if (s.E <= 512) return launch_fd<16>(maps, a, plan, st);

@@ -21,16 +21,18 @@ constexpr int kTcTileRows = 128;       // tokens per work item of the tcgen05 gr
 constexpr int kPermuteMaxGrid = 256;   // CTAs of the one-launch permutation (histogram rows)
 constexpr int kFdMaxT = 8;             // the fused single-launch decode kernel handles T <= 8
 constexpr int kFdSlice = 64;           // intermediate columns of one work unit of that kernel
-// its sync words: two units-done counters, one per launch parity (each launch zeroes the other)
-constexpr int kFdSyncWords = 64;
+// its sync words: two units-done counters, one per launch parity, then per launch parity one
+// gate_up-units-done counter per active expert (each launch zeroes the other parity's words)
+constexpr int kFdSyncWords = 512;
+constexpr int kFdMaxAct = 160;         // active experts of one decode launch (at most T * k + 1), rounded up
 
 // ------------------------------------------------------------------ workspace layout
 // All offsets are in bytes from the workspace base and 256-byte aligned.
 struct WsLayout {
   size_t status;       // int32 device status word (+ padding)
   size_t meta;         // int32 meta[8]: [0] = number of work tiles, [2..3] 64-bit launch count
-  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: its two units-done
-                       // counters (each launch zeroes the next launch's)
+  size_t fdsync;       // uint32 [kFdSyncWords] one-launch decode arm: its units-done counters
+                       // and per-expert h counters (each launch zeroes the next launch's)
   size_t ids;          // int32 [S]
   size_t w;            // fp32  [S]
   size_t counts;       // int32 [E]
@@ -45,7 +47,7 @@ struct WsLayout {
   size_t xe;           // fp32  [S + T]    2^e of each row of xf
   size_t hf;           // f16   [S + T, I]  tensor-core arm: scaled copy of h, and its row exponents
   size_t he;           // fp32  [S + T]    2^e of each row of hf
-  size_t yp;           // fp32  [I/64][S + T][H] one-launch decode arm: partial expert outputs
+  size_t fdscr;        // one-launch decode arm: h [S + T][I] bf16, then y [S + T][H] fp32
   size_t rxf;          // f16   [T, H]  router GEMM on the tensor cores: scaled rows of x
   size_t rxe;          // fp32  [T]     and their factors 2^e
   size_t rlogits;      // fp32  [T, E]  moe_forward_routed: the router's logits
@@ -291,7 +293,7 @@ struct DecodeFusedArgs {
   int32_t* offsets;
   int32_t* sorted_slot;
   int32_t* slot_pos;
-  float* yp;                        // [I/64][S + T][H] partial expert outputs (fd_partial_bytes)
+  void* scratch;                    // fd_scratch_bytes(shape): h and y of the launch, 256-byte aligned
   unsigned* sync;                   // [kFdSyncWords] its counters (the kernel zeroes them itself)
   void* out;
   int out_is_fp32;
@@ -299,8 +301,9 @@ struct DecodeFusedArgs {
   int32_t* status;
 };
 bool decode_fused_supported(const moe_shape_t& s);
-// Bytes of partial expert outputs the one-launch decode kernel needs (0 if unsupported).
-size_t fd_partial_bytes(const moe_shape_t& s);
+// Bytes of scratch the one-launch decode kernel needs: h [S + T][I] bf16 and y [S + T][H] fp32
+// (0 if unsupported).
+size_t fd_scratch_bytes(const moe_shape_t& s);
 // One warp running the decode kernel's bounded wait on a barrier nothing arrives at (test hook).
 cudaError_t launch_fd_timeout_probe(int32_t* status, uint64_t limit_ns, cudaStream_t st);
 cudaError_t launch_decode_fused(const DecodeFusedArgs& d, cudaStream_t st);

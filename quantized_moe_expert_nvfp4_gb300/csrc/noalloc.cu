@@ -5,15 +5,16 @@
 // not available or not allowed (for example inside a framework's memory-planning phase that
 // forbids new allocations, inside a host callback, or a plugin whose host application owns
 // every device allocation and only passes in tensor pointers).  For them this entry point keeps
-// its scratch (routing results, the permutation, the decode kernel's partial expert outputs, the
+// its scratch (routing results, the permutation, the decode kernel's h and expert outputs, the
 // device status word and the kernel's counters) in one fixed-size array in device global
 // memory, declared below at file scope.  It calls no allocator at all.
 //
 // Costs and rules, in plain terms:
-//  - The array is kNoAllocScratchBytes (16 MiB) and exists on every GPU that loads this library,
-//    for as long as the library stays loaded.  Shapes whose scratch would not fit are rejected;
-//    the partial outputs dominate: (I / 64) x T (k + 1) x H x 4 bytes (5.8 MB for T = 8, k = 10,
-//    I = 512, H = 2048).
+//  - The array is kNoAllocScratchBytes (4 MiB) and exists on every GPU that loads this library,
+//    for as long as the library stays loaded.  h and the expert outputs dominate the scratch:
+//    T (k + 1) (2 I + 4 H) bytes, 0.8 MB for T = 8, k = 10, I = 512, H = 2048 and at most 2.5 MB
+//    for a one-launch decode shape, so every such shape fits (a shape that did not would be
+//    rejected).
 //  - All calls on a device share the one array.  Calls whose work overlaps on the GPU (two
 //    streams, or two host threads) race on it and produce garbage; serialize them.
 //  - The first call on a device looks up the array's device address (cudaGetSymbolAddress), and
@@ -33,7 +34,7 @@
 namespace moe {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t{16} << 20;
+constexpr size_t kNoAllocScratchBytes = size_t{4} << 20;
 
 // The scratch itself.  In host code `g_noalloc_scratch` is only a host-side stand-in for the
 // symbol; its device address comes from cudaGetSymbolAddress.
@@ -42,7 +43,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 size_t up256(size_t x) { return (x + 255) & ~size_t{255}; }
 
 struct Carve {
-  size_t meta, fdsync, ids, w, counts, offsets, sorted, slot_pos, yp, total;
+  size_t meta, fdsync, ids, w, counts, offsets, sorted, slot_pos, fdscr, total;
 };
 
 Carve carve_for(const moe_shape_t& s) {
@@ -62,7 +63,7 @@ Carve carve_for(const moe_shape_t& s) {
   c.offsets = take(4 * static_cast<size_t>(s.E + 1));
   c.sorted = take(4 * S);
   c.slot_pos = take(4 * S);
-  c.yp = take(fd_partial_bytes(s));   // the decode kernel's partial expert outputs
+  c.fdscr = take(fd_scratch_bytes(s));   // the decode kernel's h and expert outputs
   c.total = off;
   return c;
 }
@@ -187,7 +188,7 @@ extern "C" moe_status_t moe_forward_decode_static_scratch(const uint16_t* x, con
   f.offsets = reinterpret_cast<int32_t*>(base + c.offsets);
   f.sorted_slot = reinterpret_cast<int32_t*>(base + c.sorted);
   f.slot_pos = reinterpret_cast<int32_t*>(base + c.slot_pos);
-  f.yp = reinterpret_cast<float*>(base + c.yp);
+  f.scratch = base + c.fdscr;
   f.sync = reinterpret_cast<unsigned*>(base + c.fdsync);
   f.out = out;
   f.out_is_fp32 = out_is_fp32;

@@ -92,12 +92,12 @@ def test_arm_selection_on_the_host(lib):
     assert arm(H=100) == -1
 
 
-def test_static_scratch_rejects_shapes_that_do_not_fit(lib):
-    """The no-allocation entry point's size rule, on the host only: a one-launch decode shape
-    whose scratch (dominated by the partial expert outputs, (I/64) * T * (k+1) * H * 4 bytes)
-    exceeds the 16 MiB array is rejected with MOE_ERR_UNSUPPORTED_SHAPE before any CUDA call; a
-    shape that fits passes the size check (and then fails here only for want of a device).
-    Skipped where a GPU is visible: fake pointers must never reach a launch."""
+def test_static_scratch_fits_every_one_launch_shape(lib):
+    """The no-allocation entry point's size rule, on the host only: its scratch (dominated by h and
+    the expert outputs, T (k+1) (2 I + 4 H) bytes) fits the 4 MiB array for every one-launch decode
+    shape, so a shape of arm 0 passes the size check (and then fails here only for want of a
+    device), while shapes of other arms are rejected with MOE_ERR_UNSUPPORTED_SHAPE before any CUDA
+    call.  Skipped where a GPU is visible: fake pointers must never reach a launch."""
     import torch
     if torch.cuda.is_available():
         pytest.skip("host-only check; needs a machine without a GPU")
@@ -107,8 +107,8 @@ def test_static_scratch_rejects_shapes_that_do_not_fit(lib):
                    ctypes.POINTER(moe.MoeWeights), ctypes.POINTER(moe.MoeShape), ctypes.c_void_p,
                    ctypes.c_int32, ctypes.c_void_p]
     fn.restype = ctypes.c_int32
-    limit, small = 16 << 20, 64 << 10
-    seen = {"fit": 0, "reject": 0}
+    limit = 4 << 20
+    n = 0
     for T in (1, 3, 8):
         for H in (512, 2048, 4096):
             for I in (256, 512, 1024):
@@ -116,18 +116,19 @@ def test_static_scratch_rejects_shapes_that_do_not_fit(lib):
                     E = 64
                     sh = moe.Shape(T=T, H=H, I=I, E=E, k=k, has_shared=1)
                     assert moe.forward_arm(sh) == 0
+                    assert T * (k + 1) * (2 * I + 4 * H) + (64 << 10) <= limit
                     gu = moe.MoeWeights(0x200000, 0x300000, 0x400000, E + 1, 2 * I, H)
                     dn = moe.MoeWeights(0x200000, 0x300000, 0x400000, E + 1, H, I)
                     st = fn(0x100000, 0x100000, ctypes.byref(gu), ctypes.byref(dn), ctypes.byref(sh.c()),
                             0x100000, 0, None)
-                    partial = (I // 64) * T * (k + 1) * H * 4
-                    if partial > limit:
-                        assert st == -2, (T, H, I, k, st)
-                        seen["reject"] += 1
-                    elif partial + small <= limit:
-                        assert st != -2, (T, H, I, k, st)
-                        seen["fit"] += 1
-    assert seen["fit"] > 10 and seen["reject"] >= 4
+                    assert st != -2, (T, H, I, k, st)
+                    n += 1
+    for sh in (moe.Shape(T=9, H=2048, I=512, E=64, k=10), moe.Shape(T=4, H=8192, I=512, E=64, k=10)):
+        assert moe.forward_arm(sh) != 0
+        gu = moe.MoeWeights(0x200000, 0x300000, 0x400000, 65, 2 * sh.I, sh.H)
+        dn = moe.MoeWeights(0x200000, 0x300000, 0x400000, 65, sh.H, sh.I)
+        assert fn(0x100000, 0x100000, ctypes.byref(gu), ctypes.byref(dn), ctypes.byref(sh.c()), 0x100000, 0, None) == -2
+    assert n == 81
 
 
 def test_fp8_arm_host_validation(lib):

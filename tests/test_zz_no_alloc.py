@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 CASES = [
     (3, 2048, 16, 4, 512, 1, "none", 201),
     (8, 2048, 512, 10, 512, 1, "none", 202),
-    # k = 16 at the largest H whose partial outputs still fit the array (8.9 MB of 16 MiB)
-    (8, 4096, 64, 16, 256, 1, "zipf", 203),
+    # k = 16 at the largest H and I of the one-launch arm (h and y: 2.5 MB of the 4 MiB array)
+    (8, 4096, 64, 16, 1024, 1, "zipf", 203),
 ]
 
 
