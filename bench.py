@@ -413,7 +413,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     if all(a == 0 for a in arms):
         t_launch_ms = ms_per_step / len(layers)
         alg = acc["fwd_bytes"] / n_launch
-        kname, kfile = "decode_fused_kernel", ["decode_fused.cu", "topk.cuh", "internal.cuh"]
+        kname, kfile = "decode_fused_kernel", ["decode_fused.cu", "topk.cuh", "internal.cuh", "mma_frag.cuh"]
         roofline = {"bound": "hbm", "achieved": alg / (t_launch_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
                     "kernel": kname + " (the whole layer: route, gate_up, down, combine)",
                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * t_launch_ms,
@@ -424,7 +424,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
         alg = (acc["gu_bytes"] if dom == 1 else acc["dn_bytes"]) / n_launch
         kname = f"grouped_gemm_tc_kernel<{'gate_up' if dom == 1 else 'down'}>" if all(a == 2 for a in arms) \
             else ("grouped_simt_kernel<gate_up>" if dom == 1 else "down_combine_gemv_kernel")
-        kfile = ["gemm_tc.cu", "internal.cuh"] if all(a == 2 for a in arms) else ["grouped_simt.cu"]
+        kfile = ["gemm_tc.cu", "internal.cuh", "mma_frag.cuh"] if all(a == 2 for a in arms) else ["grouped_simt.cu"]
         roofline = {"bound": "hbm", "achieved": alg / (t_launch_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
                     "kernel": kname, "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * t_launch_ms,
                     "timing": "CUDA events around the kernel on its stream (profiled replay of the timed steps)"}
@@ -432,7 +432,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
         t_launch_ms = tot_stage[1] / n_launch
         alg = acc["gu_flops"] / n_launch
         kname = "grouped_gemm_tc_kernel<gate_up>" if all(a == 2 for a in arms) else "grouped_simt_kernel<gate_up>"
-        kfile = ["gemm_tc.cu", "internal.cuh"]
+        kfile = ["gemm_tc.cu", "internal.cuh", "mma_frag.cuh"]
         peak = pk["bf16_sustained"] if long_step else pk["bf16"]
         roofline = {"bound": "tensor", "achieved": alg / (t_launch_ms / 1e3) / 1e12, "peak": peak,
                     "unit": "TFLOP/s", "kernel": kname, "algorithmic_flops_per_launch": alg,
