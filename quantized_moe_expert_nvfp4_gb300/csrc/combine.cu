@@ -91,8 +91,9 @@ __global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __rest
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  // ranks in groups of eight: the group's row loads (raw f16 words and the row factors) are
-  // issued together, then decoded and summed in rank order
+  // every rank's row (raw f16 words and its row factor) and the shared expert's are loaded
+  // before any is used -- up to kMaxK + 1 loads in flight per thread -- then decoded and summed
+  // in rank order
   auto fma8 = [&](const uint4& h, float fr, float wj) {
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
 #pragma unroll
@@ -101,35 +102,44 @@ __global__ void __launch_bounds__(256) combine_y16_kernel(const uint16_t* __rest
       acc[2 * i + 1] = fmaf(wj, __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * fr, acc[2 * i + 1]);
     }
   };
-  for (int j0 = 0; j0 < k; j0 += 8) {
-    uint4 hv[8];
-    float fr[8], wj[8];
+  int64_t p[kMaxK];
+  float wj[kMaxK];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (j0 + q < k) {
-        const int64_t s = static_cast<int64_t>(t) * k + j0 + q;
-        int64_t p = __ldg(slot_pos + s);
-        if (p < 0 || p >= S) {
-          if (status) report_device_error(status, kDevBadIndex);
-          p = 0;
-        }
-        wj[q] = __ldg(topk_w + s);
-        hv[q] = __ldg(reinterpret_cast<const uint4*>(y16 + p * H + c));
-        fr[q] = __ldg(rowf + p);
-      }
+  for (int q = 0; q < kMaxK; ++q) {
+    if (q < k) {
+      const int64_t s = static_cast<int64_t>(t) * k + q;
+      p[q] = __ldg(slot_pos + s);
+      wj[q] = __ldg(topk_w + s);
     }
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (j0 + q < k) fma8(hv[q], fr[q], wj[q]);
   }
+  uint4 hv[kMaxK];
+  float fr[kMaxK];
+#pragma unroll
+  for (int q = 0; q < kMaxK; ++q) {
+    if (q < k) {
+      if (p[q] < 0 || p[q] >= S) {
+        if (status) report_device_error(status, kDevBadIndex);
+        p[q] = 0;
+      }
+      hv[q] = __ldg(reinterpret_cast<const uint4*>(y16 + p[q] * H + c));
+      fr[q] = __ldg(rowf + p[q]);
+    }
+  }
+  uint4 hs = make_uint4(0u, 0u, 0u, 0u);
+  float frs = 0.0f;
   if (has_shared) {
-    const uint4 h = __ldg(reinterpret_cast<const uint4*>(y16 + (S + t) * H + c));
-    const float fr = __ldg(rowf + S + t);
-    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+    hs = __ldg(reinterpret_cast<const uint4*>(y16 + (S + t) * H + c));
+    frs = __ldg(rowf + S + t);
+  }
+#pragma unroll
+  for (int q = 0; q < kMaxK; ++q)
+    if (q < k) fma8(hv[q], fr[q], wj[q]);
+  if (has_shared) {
+    const uint32_t w[4] = {hs.x, hs.y, hs.z, hs.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      acc[2 * i] += __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xffffu))) * fr;
-      acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * fr;
+      acc[2 * i] += __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xffffu))) * frs;
+      acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))) * frs;
     }
   }
   const int64_t o = static_cast<int64_t>(t) * H + c;
