@@ -31,8 +31,8 @@
  *    T * (k + 1) < 2^31.  The shared expert, when present, has the routed experts' I.
  *  - Data types: bf16 tensors are passed as their 16-bit patterns (uint16_t).
  *
- * Weight layout (one projection, all groups), chosen as the resident "[N, K/2]" layout the
- * issue prices ("no dequant, no transpose"):
+ * Weight layout (one projection, all groups): the resident [N, K/2] layout that the issue prices
+ * as the option without a dequantization pass or a transpose:
  *    packed [G, N, K/2] bytes, element k of row n in byte k/2, even k in the low nibble;
  *    scales [G, N, K/16] e4m3 bytes, one per 16 consecutive k of a row;
  *    scale2 [G] fp32, one per group and projection;
@@ -87,7 +87,7 @@ typedef struct {
 /* Bytes of workspace every call below needs for this shape (0 on an unsupported shape). */
 size_t moe_workspace_size(const moe_shape_t* shape);
 
-/* Router top-k ("router/gating GEMM and top-k" of the issue's list of logit-changing ops; the
+/* Router top-k (the top-k after the router GEMM, in the issue's list of logit-changing ops; the
  * tie rule is the handover briefs' device selection: lower index wins, NaN never wins).
  *   logits   fp32 [T, E]
  *   topk_ids int32 [T, k]: experts ordered by (logit descending, index ascending), NaN as -inf

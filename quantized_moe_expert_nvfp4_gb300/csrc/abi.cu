@@ -268,7 +268,7 @@ WsLayout ws_layout(const moe_shape_t& s) {
   L.tiles = take(16 * static_cast<size_t>(L.max_tiles));
   L.hist = take(4 * static_cast<size_t>(kPermuteMaxGrid) * s.E);
   // moe_forward's intermediates, by arm: h for arms 1-3, fp32 y for arms 2-3, the f16 operands
-  // for arm 2, the partial outputs for arm 0
+  // for arm 2, the decode kernel's h and expert outputs for arm 0
   const int arm = forward_arm(s);
   L.h = take(arm != 0 ? 2 * static_cast<size_t>(R) * s.I : 0);
   L.y = take(arm >= 2 ? 4 * static_cast<size_t>(R) * s.H : 0);

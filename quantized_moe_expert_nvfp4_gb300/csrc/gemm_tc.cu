@@ -2,8 +2,8 @@
 //
 // W4A16 as in the untransposed column of the "long-context cold prefill to SGLang parity"
 // issue's kernel table (16-bit MMA, f32 accumulation, scale2 and SiLU(gate)*up in an fp32
-// epilogue), computed over the resident [N, K/2] weight layout the same issue prices ("MoE FP4
-// MMA over the resident decode layout, no dequant pass, no transpose").
+// epilogue), computed over the resident [N, K/2] weight layout that the same issue prices as the
+// option without a separate dequantization pass or transpose.
 //
 // Swap-AB: the MMA's M dimension is 128 weight rows of one expert, N is up to 128 of that
 // expert's tokens, so a small expert group still fills M.  Per CTA (one per SM, persistent):
