@@ -571,20 +571,44 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
                                 "the headline steps (the headline keeps every item on tcgen05)"}
         del ngraphs
 
-    # end to end through host buffers: every layer call of every step copies its x and logits in
-    # from pinned host memory, runs the C-ABI call and copies its output back to pinned memory, all
-    # inside the timed region.  For batches of 64 tokens and more the copies run on their own
-    # streams (the copies in of call n+1 and out of call n-1 overlap call n; device buffers
-    # double-buffered per layer); for decode batches, whose calls take microseconds, the event
-    # handshakes between streams would cost more than they hide, so all of it runs on one stream.
+    # end to end through host buffers: every step copies its inputs in from pinned host memory,
+    # runs the C-ABI calls and copies the results back to pinned memory, all inside the timed
+    # region.  For batches of 64 tokens and more every layer call copies its x and logits in and
+    # its output out on their own streams (the copies in of call n+1 and out of call n-1 overlap
+    # call n; device buffers double-buffered per layer); for decode batches, whose calls take
+    # microseconds, the whole step's inputs (every layer's x and logits, back to back in one pinned
+    # buffer) move in one copy before its calls and its outputs in one copy after them, all on the
+    # calls' stream.
     e2e_steps = min(steps, 200)
     overlap = min(L["T"] for L in layers) >= 64
-    hx = [[L["xs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
-    hl = [[L["lgs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
-    ho = [[torch.empty(L["T"], H, dtype=torch.bfloat16).pin_memory() for _ in range(2)] for L in layers]
-    dx = [[torch.empty_like(L["xs"][0]) for _ in range(2)] for L in layers]
-    dl = [[torch.empty_like(L["lgs"][0]) for _ in range(2)] for L in layers]
-    do = [[torch.empty_like(L["out"]) for _ in range(2)] for L in layers]
+    if overlap:
+        hx = [[L["xs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
+        hl = [[L["lgs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
+        ho = [[torch.empty(L["T"], H, dtype=torch.bfloat16).pin_memory() for _ in range(2)] for L in layers]
+        dx = [[torch.empty_like(L["xs"][0]) for _ in range(2)] for L in layers]
+        dl = [[torch.empty_like(L["lgs"][0]) for _ in range(2)] for L in layers]
+        do = [[torch.empty_like(L["out"]) for _ in range(2)] for L in layers]
+    else:
+        # one pinned buffer per pooled batch: every layer's x, then its logits, back to back
+        xb = [L["T"] * H * 2 for L in layers]
+        lb = [L["T"] * E * 4 for L in layers]
+        ob = [L["T"] * H * 2 for L in layers]
+        in_off = [sum(xb[:i]) + sum(lb[:i]) for i in range(len(layers))]
+        out_off = [sum(ob[:i]) for i in range(len(layers))]
+        hin = []
+        for p in range(pool):
+            buf = torch.empty(sum(xb) + sum(lb), dtype=torch.uint8).pin_memory()
+            for li, L in enumerate(layers):
+                buf[in_off[li]:in_off[li] + xb[li]].copy_(L["xs"][p].cpu().view(torch.uint8).reshape(-1))
+                buf[in_off[li] + xb[li]:in_off[li] + xb[li] + lb[li]].copy_(L["lgs"][p].cpu().view(torch.uint8).reshape(-1))
+            hin.append(buf)
+        hout = torch.empty(sum(ob), dtype=torch.uint8).pin_memory()
+        din = torch.empty(sum(xb) + sum(lb), dtype=torch.uint8, device=device)
+        dout = torch.empty(sum(ob), dtype=torch.uint8, device=device)
+        dviews = [(din[in_off[li]:in_off[li] + xb[li]].view(torch.bfloat16).view(L["T"], H),
+                   din[in_off[li] + xb[li]:in_off[li] + xb[li] + lb[li]].view(torch.float32).view(L["T"], E),
+                   dout[out_off[li]:out_off[li] + ob[li]].view(torch.bfloat16).view(L["T"], H))
+                  for li, L in enumerate(layers)]
     h2d_s, d2h_s = (torch.cuda.Stream(device), torch.cuda.Stream(device)) if overlap else (stream, stream)
     in_ready = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
     done = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
@@ -592,6 +616,13 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
 
     def e2e_step(i):
         p, b = i % pool, i % 2
+        if not overlap:
+            with torch.cuda.stream(stream):
+                din.copy_(hin[p], non_blocking=True)
+                for (x, lg, out), L in zip(dviews, layers):
+                    moe.forward(x, lg, L["gu"], L["dn"], L["ms"], L["ws"], out=out)
+                hout.copy_(dout, non_blocking=True)
+            return
         for li, L in enumerate(layers):
             with torch.cuda.stream(h2d_s):
                 if overlap:
@@ -635,7 +666,8 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "method": ("moe_forward per layer call with pinned-host x/logits copied in and the output copied out "
                       "every call; " + ("copies on their own streams overlap the neighbouring calls' compute"
-                                        if overlap else "copies and calls in order on one stream"))}
+                                        if overlap else "the step's inputs (every layer's) in one copy before its "
+                                        "calls and its outputs in one copy after them, on the calls' stream"))}
     torch.cuda.synchronize(device)
 
     status = [moe.device_status(L["ws"]) for L in layers]
@@ -660,7 +692,7 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
            "distinct_experts_mean": [float(np.mean(L["uniq"])) for L in layers]}
     if cpu_baseline:
         res["cpu_baseline"] = oracle_sample(name, device)
-    del layers, graphs, pgraphs, hx, hl, ho, dx, dl, do
+    del layers, graphs, pgraphs
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
