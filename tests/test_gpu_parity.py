@@ -347,6 +347,8 @@ ONE_LAUNCH = [
     (8, 2048, 64, 8, 512, 1, "zipf", 120),
     (2, 2048, 32, 2, 1024, 1, "normal", 115),
     (4, 4096, 64, 4, 512, 1, "zipf", 119),
+    # rows of h wider than rows of x (I > H): the down units' staging of h sizes the shared area
+    (7, 512, 64, 8, 1024, 1, "zipf", 121),
 ]
 
 
