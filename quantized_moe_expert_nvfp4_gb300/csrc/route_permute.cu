@@ -20,13 +20,14 @@ template <int EPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int32_t* __restrict__ ids,
                                                          float* __restrict__ w) {
+  __shared__ uint2 s_topk[8][32];   // each warp's top-k scratch
   pdl_wait_then_release();
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
   int my_id;
   float my_w;
-  warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w);
+  warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w, s_topk[threadIdx.x >> 5]);
   if (lane < k) {
     ids[static_cast<int64_t>(t) * k + lane] = my_id;
     w[static_cast<int64_t>(t) * k + lane] = my_w;
@@ -91,23 +92,31 @@ __device__ void write_tiles_block(int E, int S, int T, int has_shared, int tile_
 __device__ __forceinline__ void warp_stable_scatter(const int32_t* ids, int s0, int n, int E,
                                                     int* cursor, int32_t* sorted_slot,
                                                     int32_t* slot_pos) {
+  constexpr int kBatch = 8;   // 32-slot steps whose ids are loaded together, ahead of their use
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
-  for (int b = 0; b < n; b += 32) {
-    const int s = s0 + b + lane;
-    const bool live = (b + lane) < n;
-    int e = live ? ids[s] : -1;
-    if (e >= E) e = -2;  // out-of-range ids are ignored (the caller validated them)
-    const unsigned grp = __match_any_sync(kFull, e);
-    const int rank = __popc(grp & lt);
-    if (e >= 0) {
-      const int pos = cursor[e] + rank;
-      sorted_slot[pos] = s;
-      slot_pos[s] = pos;
+  for (int b0 = 0; b0 < n; b0 += 32 * kBatch) {
+    int ev[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) ev[j] = (b0 + 32 * j + lane < n) ? ids[s0 + b0 + 32 * j + lane] : -1;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int b = b0 + 32 * j;
+      if (b >= n) break;
+      const int s = s0 + b + lane;
+      int e = ev[j];
+      if (e >= E) e = -2;  // out-of-range ids are ignored (the caller validated them)
+      const unsigned grp = __match_any_sync(kFull, e);
+      const int rank = __popc(grp & lt);
+      if (e >= 0) {
+        const int pos = cursor[e] + rank;
+        sorted_slot[pos] = s;
+        slot_pos[s] = pos;
+      }
+      __syncwarp();
+      if (e >= 0 && rank == 0) cursor[e] += __popc(grp);
+      __syncwarp();
     }
-    __syncwarp();
-    if (e >= 0 && rank == 0) cursor[e] += __popc(grp);
-    __syncwarp();
   }
 }
 
@@ -121,6 +130,7 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(
     int32_t* __restrict__ slot_pos, int4* __restrict__ tiles, int32_t* __restrict__ meta,
     int tile_rows) {
   __shared__ int s_ids[kDecodeMaxT * kMaxK];
+  __shared__ uint2 s_topk[32][32];   // each warp's top-k scratch
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE];
   __shared__ int s_cur[kMaxE];
@@ -132,7 +142,8 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(
     for (int t = warp; t < T; t += 32) {
       int my_id;
       float my_w;
-      warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w);
+      // (the threshold selection's registers do not fit 1024-thread blocks above 512 experts)
+      warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w, EPL <= 16 ? s_topk[warp] : nullptr);
       if (lane < k) {
         ids[t * k + lane] = my_id;
         w[t * k + lane] = my_w;
@@ -300,6 +311,7 @@ __global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
     int32_t* __restrict__ hist, int4* __restrict__ tiles, int32_t* __restrict__ meta, int tile_rows,
     unsigned long long* __restrict__ bar, int32_t* __restrict__ status) {
   __shared__ int s_cnt[kMaxE];   // this CTA's histogram, then its placement cursors
+  __shared__ uint2 s_topk[32][32];   // each warp's top-k scratch
   __shared__ int s_tot[kMaxE];   // expert counts (for the work list)
   __shared__ int s_off[kMaxE];   // expert offsets
   __shared__ int s_warp[32];
@@ -315,7 +327,8 @@ __global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
     for (int t = t0 + warp; t < t1; t += 32) {
       int my_id;
       float my_w;
-      warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w);
+      // (the threshold selection's registers do not fit 1024-thread blocks above 512 experts)
+      warp_topk<EPL>(logits + static_cast<int64_t>(t) * E, E, k, lane, my_id, my_w, EPL <= 16 ? s_topk[warp] : nullptr);
       if (lane < k) {
         ids[static_cast<int64_t>(t) * k + lane] = my_id;
         w[static_cast<int64_t>(t) * k + lane] = my_w;
@@ -353,18 +366,35 @@ __global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
   }
   __syncthreads();
   if (!s_ok) return;
-  // counts, offsets and this CTA's bases: thread e sums column e of the histograms (of the CTAs
-  // that own tokens: with T < G the others' are zero)
+  // counts, offsets and this CTA's bases: column e of the histograms (of the CTAs that own
+  // tokens: with T < G the others' are zero) summed by thread e, or, when the block has two
+  // threads per expert, by threads e and E + e over the two halves of the CTAs
   const int e = threadIdx.x;
   const int g_used = per > 0 ? (T + per - 1) / per : 0;
+  const bool split = 2 * E <= static_cast<int>(blockDim.x);
+  const int col = (split && e >= E) ? e - E : e;
+  const int c_lo = (split && e >= E) ? g_used / 2 : 0;
+  const int c_hi = (split && e < E) ? g_used / 2 : g_used;
   int before = 0, total = 0;
-  if (e < E) {
+  if (col < E) {
 #pragma unroll 8
-    for (int c = 0; c < g_used; ++c) {
-      const int v = __ldcg(hist + static_cast<int64_t>(c) * E + e);
+    for (int c = c_lo; c < c_hi; ++c) {
+      const int v = __ldcg(hist + static_cast<int64_t>(c) * E + col);
       total += v;
       before += (c < b) ? v : 0;
     }
+  }
+  if (split) {
+    if (e >= E && col < E) {
+      s_tot[col] = total;
+      s_off[col] = before;
+    }
+    __syncthreads();
+    if (e < E) {
+      total += s_tot[e];
+      before += s_off[e];
+    }
+    __syncthreads();
   }
   const int off = block_exclusive_scan(e < E ? total : 0, s_warp, nullptr);
   if (e < E) {
