@@ -64,20 +64,30 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 
 // Work list: for each group with rows, ceil(rows / tile_rows) items {g, row_begin, rows, 0};
 // routed groups first (ascending expert), then the shared group (rows S .. S+T-1).  Called by
-// one whole block of >= E threads; cnt(e) / off(e) come from the caller.
+// one whole block of >= E threads; cnt(e) / off(e) come from the caller (shared memory), and
+// s_base (E entries of shared memory the caller no longer reads) receives each expert's first
+// item.  The items are written by all threads in parallel, item j by thread j mod blockDim: its
+// expert is the last one whose first item is at most j (an expert without rows shares its first
+// item with the next), so one busy expert's many items do not fall to one thread.
 __device__ void write_tiles_block(int E, int S, int T, int has_shared, int tile_rows,
                                   const int* cnt_of, const int* off_of, int4* tiles,
-                                  int32_t* meta, int* s_warp) {
+                                  int32_t* meta, int* s_warp, int* s_base) {
   const int e = threadIdx.x;
   const int c = (e < E) ? cnt_of[e] : 0;
   const int n = (c + tile_rows - 1) / tile_rows;
   int total = 0;
   const int base = block_exclusive_scan(n, s_warp, &total);
-  if (e < E) {
-    for (int i = 0; i < n; ++i) {
-      const int r0 = i * tile_rows;
-      tiles[base + i] = make_int4(e, off_of[e] + r0, min(tile_rows, c - r0), 0);
+  if (e < E) s_base[e] = base;
+  __syncthreads();
+  for (int j = threadIdx.x; j < total; j += blockDim.x) {
+    int lo = 0, hi = E - 1;   // the last expert whose first item is <= j
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_base[mid] <= j) lo = mid;
+      else hi = mid - 1;
     }
+    const int r0 = (j - s_base[lo]) * tile_rows;
+    tiles[j] = make_int4(lo, off_of[lo] + r0, min(tile_rows, cnt_of[lo] - r0), 0);
   }
   const int n_shared = has_shared ? (T + tile_rows - 1) / tile_rows : 0;
   for (int i = threadIdx.x; i < n_shared; i += blockDim.x) {
@@ -92,7 +102,7 @@ __device__ void write_tiles_block(int E, int S, int T, int has_shared, int tile_
 __device__ __forceinline__ void warp_stable_scatter(const int32_t* ids, int s0, int n, int E,
                                                     int* cursor, int32_t* sorted_slot,
                                                     int32_t* slot_pos) {
-  constexpr int kBatch = 8;   // 32-slot steps whose ids are loaded together, ahead of their use
+  constexpr int kBatch = 4;   // 32-slot steps whose ids are loaded together, ahead of their use
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   for (int b0 = 0; b0 < n; b0 += 32 * kBatch) {
@@ -174,7 +184,8 @@ __global__ void __launch_bounds__(1024) route_permute_small_kernel(
   if (threadIdx.x == 0) offsets[E] = S;
   __syncthreads();
   if (warp == 0) warp_stable_scatter(s_ids, 0, S, E, s_cur, sorted_slot, slot_pos);
-  write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+  // (s_cur is free once the work list's scan has passed its barriers: warp 0 has placed every slot)
+  write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp, s_cur);
 }
 
 // Batched decode on the tensor-core arm (T <= kDecodeMaxT), after the top-k: permutation, work
@@ -246,7 +257,7 @@ __global__ void __launch_bounds__(1024) permute_gather_small_kernel(
       __syncwarp();
     }
   }
-  if (lead) write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+  if (lead) write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp, s_cur);
   __syncthreads();
   // this CTA's tokens: f16 rows scaled by the row's power of two, to every row that holds the token
   const int nv = H / 8;   // 16-byte columns of a row
@@ -291,6 +302,8 @@ __global__ void __launch_bounds__(1024) permute_gather_small_kernel(
   }
 }
 
+constexpr int kScatterWarps = 8;   // warps placing a CTA's slots in the cooperative permutation
+
 // Any T, one cooperative launch of up to kPermuteMaxGrid CTAs of 1024 threads: routing (or given
 // ids), per-CTA expert histograms of contiguous token ranges, a grid-wide barrier, every CTA's
 // stable placement base per expert (the histograms of the CTAs before it plus the expert's
@@ -311,7 +324,9 @@ __global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
     int32_t* __restrict__ hist, int4* __restrict__ tiles, int32_t* __restrict__ meta, int tile_rows,
     unsigned long long* __restrict__ bar, int32_t* __restrict__ status) {
   __shared__ int s_cnt[kMaxE];   // this CTA's histogram, then its placement cursors
-  __shared__ uint2 s_topk[32][32];   // each warp's top-k scratch
+  // routing: each warp's top-k scratch; placement: per-warp expert counts, then cursors
+  __shared__ __align__(16) unsigned char s_raw[kScatterWarps * kMaxE * sizeof(int)];
+  uint2 (*s_topk)[32] = reinterpret_cast<uint2 (*)[32]>(s_raw);
   __shared__ int s_tot[kMaxE];   // expert counts (for the work list)
   __shared__ int s_off[kMaxE];   // expert offsets
   __shared__ int s_warp[32];
@@ -408,12 +423,38 @@ __global__ void __launch_bounds__(1024, 1) route_permute_large_kernel(
   }
   if (b == 0 && threadIdx.x == 0) offsets[E] = S;
   __syncthreads();
-  // stable placement of the CTA's slots (its own ids, written above or given)
-  if (warp == 0) {
+  // stable placement of the CTA's slots (its own ids, written above or given) by kScatterWarps
+  // warps, each a contiguous chunk: every warp counts its chunk's slots per expert, each expert's
+  // cursor is split into per-warp cursors in chunk order, and the warps place their chunks
+  {
     const int32_t* src = logits ? ids : ids_in;
-    warp_stable_scatter(src, t0 * k, (t1 - t0) * k, E, s_cnt, sorted_slot, slot_pos);
+    const int s_begin = t0 * k, n_sl = (t1 - t0) * k;
+    const int chunk = (n_sl + kScatterWarps - 1) / kScatterWarps;
+    const int c0 = min(n_sl, warp * chunk), c1 = min(n_sl, c0 + chunk);
+    int* wc = reinterpret_cast<int*>(s_raw);   // [kScatterWarps][E]
+    for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wc[i] = 0;
+    __syncthreads();
+    if (warp < kScatterWarps) {
+      for (int i = c0 + lane; i < c1; i += 32) {
+        const int ex = src[s_begin + i];
+        if (ex >= 0 && ex < E) atomicAdd(&wc[warp * E + ex], 1);
+      }
+    }
+    __syncthreads();
+    for (int ex = threadIdx.x; ex < E; ex += blockDim.x) {
+      int run = s_cnt[ex];
+      for (int w2 = 0; w2 < kScatterWarps; ++w2) {
+        const int cw = wc[w2 * E + ex];
+        wc[w2 * E + ex] = run;
+        run += cw;
+      }
+    }
+    __syncthreads();
+    if (warp < kScatterWarps && c1 > c0)
+      warp_stable_scatter(src, s_begin + c0, c1 - c0, E, wc + warp * E, sorted_slot, slot_pos);
   }
-  if (b == 0) write_tiles_block(E, S, T, has_shared, tile_rows, s_tot, s_off, tiles, meta, s_warp);
+  // (s_cnt is free: the placement reads its per-warp cursors)
+  if (b == 0) write_tiles_block(E, S, T, has_shared, tile_rows, s_tot, s_off, tiles, meta, s_warp, s_cnt);
 }
 
 __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __restrict__ offsets,
@@ -423,6 +464,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
                                                            int32_t* __restrict__ status) {
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE];
+  __shared__ int s_base[kMaxE];
   __shared__ int s_warp[32];
   __shared__ int s_bad;
   const int S = T * k;
@@ -439,7 +481,7 @@ __global__ void __launch_bounds__(1024) build_tiles_kernel(const int32_t* __rest
     if (threadIdx.x == 0) report_device_error(status, kDevBadIndex);
   }
   __syncthreads();
-  write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp);
+  write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp, s_base);
 }
 
 }  // namespace
