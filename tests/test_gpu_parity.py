@@ -38,6 +38,9 @@ SMALL = [
     (129, 256, 8, 2, 256, 0, "none", 109),
     (1000, 512, 64, 8, 256, 1, "zipf", 110),
     (700, 1024, 32, 6, 512, 1, "normal", 111),
+    # k = 16 on the tcgen05 arm with enough tokens that each thread of the compact-y combine's
+    # resident grid (one CTA per SM above 10 ranks) walks several (token, 8-column) units
+    (2000, 512, 64, 16, 256, 1, "zipf", 145),
 ]
 
 
@@ -131,7 +134,7 @@ def test_forward_deterministic_and_matches_stages(cuda_lib):
     tensor-core arm, which hands y to the combine as f16 of the raw accumulator, within one f16
     rounding of each weighted y value."""
     moe = cuda_lib
-    for case in (SMALL[2], SMALL[4], SMALL[5], SMALL[7], SMALL[12], SMALL[14], SMALL[15], SMALL[16]):
+    for case in (SMALL[2], SMALL[4], SMALL[5], SMALL[7], SMALL[12], SMALL[14], SMALL[15], SMALL[16], SMALL[17]):
         L = _small_layer(case)
         ms = moe_shape(moe, L.shape)
         gu, dn = L.gpu_weights(moe)
