@@ -190,9 +190,13 @@ moe_status_t moe_forward_routed(const uint16_t* x, const moe_nvfp4_weights_t* ro
  *     arm-0 shapes, so every arm-0 shape fits).
  *   - All calls on a device share the array: calls that overlap on the GPU (other streams or
  *     threads) race and corrupt each other; serialize them.
- *   - The first call on a device looks up the array's device address, and looks it up again
- *     after the device's context changed (a device reset); make the first call outside any
+ *   - The first call in a context looks up the array's device address (a caller that makes
+ *     another context current gets that context's own lookup); make the first call outside any
  *     CUDA stream capture.
+ *   - Not supported across a device reset.  The library carries its own copy of the CUDA
+ *     runtime, so a cudaDeviceReset (or a reset of the primary context) made by other code in
+ *     the process is not seen by it, and its kernels and this array are not reloaded: after such
+ *     a reset, unload the library (or restart the process) before calling it again.
  *   - Each call first clears the status word, the launch count and the decode kernel's counters
  *     on `stream` (an asynchronous memset).
  *     Device-side timeouts are not reported back by this call. */

@@ -17,9 +17,13 @@
 //    rejected).
 //  - All calls on a device share the one array.  Calls whose work overlaps on the GPU (two
 //    streams, or two host threads) race on it and produce garbage; serialize them.
-//  - The first call on a device looks up the array's device address (cudaGetSymbolAddress), and
-//    looks it up again when the device's context has changed (after a device reset).  Make that
-//    first call outside any CUDA stream capture.
+//  - The first call in a context looks up the array's device address (cudaGetSymbolAddress); a
+//    caller that makes another context current gets that context's own lookup.  Make that first
+//    call outside any CUDA stream capture.
+//  - A device reset is not supported: the library links its own static copy of the CUDA
+//    runtime, which does not see a cudaDeviceReset (or primary-context reset) made by other code
+//    in the process, so neither this array nor the library's kernels are reloaded after one.
+//    The library must be unloaded (or the process restarted) after such a reset.
 //  - Each call clears the status word, the launch counter and the decode kernel's other
 //    synchronisation words at the start (an asynchronous memset on the caller's stream, not an allocation), so a
 //    device-side timeout of one call does not poison the next; such a timeout is not reported
@@ -98,8 +102,8 @@ cudaError_t current_context_id(unsigned long long* id) {
 
 // Device address of the scratch array in the current context.  It is looked up once per device
 // with that device current (cudaGetSymbolAddress) and kept together with the id of the context it
-// was taken in: after a device reset the runtime creates a new context (a new id), in which the
-// module, and so the array, may sit at another address, and the lookup is then made again.
+// was taken in: when a caller makes another context current (the module, and so the array, sits
+// at another address there) the lookup is made again.
 void* scratch_address(cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {};
