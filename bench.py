@@ -577,8 +577,9 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     # its output out on their own streams (the copies in of call n+1 and out of call n-1 overlap
     # call n; device buffers double-buffered per layer); for decode batches, whose calls take
     # microseconds, the whole step's inputs (every layer's x and logits, back to back in one pinned
-    # buffer) move in one copy before its calls and its outputs in one copy after them, all on the
-    # calls' stream.
+    # buffer) move in one copy and its outputs in one copy, on their own streams: the copy in of
+    # step n+1 and the copy out of step n-1 overlap step n's calls (device buffers double-buffered
+    # per step).
     e2e_steps = min(steps, 200)
     overlap = min(L["T"] for L in layers) >= 64
     if overlap:
@@ -602,14 +603,14 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
                 buf[in_off[li]:in_off[li] + xb[li]].copy_(L["xs"][p].cpu().view(torch.uint8).reshape(-1))
                 buf[in_off[li] + xb[li]:in_off[li] + xb[li] + lb[li]].copy_(L["lgs"][p].cpu().view(torch.uint8).reshape(-1))
             hin.append(buf)
-        hout = torch.empty(sum(ob), dtype=torch.uint8).pin_memory()
-        din = torch.empty(sum(xb) + sum(lb), dtype=torch.uint8, device=device)
-        dout = torch.empty(sum(ob), dtype=torch.uint8, device=device)
-        dviews = [(din[in_off[li]:in_off[li] + xb[li]].view(torch.bfloat16).view(L["T"], H),
-                   din[in_off[li] + xb[li]:in_off[li] + xb[li] + lb[li]].view(torch.float32).view(L["T"], E),
-                   dout[out_off[li]:out_off[li] + ob[li]].view(torch.bfloat16).view(L["T"], H))
-                  for li, L in enumerate(layers)]
-    h2d_s, d2h_s = (torch.cuda.Stream(device), torch.cuda.Stream(device)) if overlap else (stream, stream)
+        hout = [torch.empty(sum(ob), dtype=torch.uint8).pin_memory() for _ in range(2)]
+        din = [torch.empty(sum(xb) + sum(lb), dtype=torch.uint8, device=device) for _ in range(2)]
+        dout = [torch.empty(sum(ob), dtype=torch.uint8, device=device) for _ in range(2)]
+        dviews = [[(din[b][in_off[li]:in_off[li] + xb[li]].view(torch.bfloat16).view(L["T"], H),
+                    din[b][in_off[li] + xb[li]:in_off[li] + xb[li] + lb[li]].view(torch.float32).view(L["T"], E),
+                    dout[b][out_off[li]:out_off[li] + ob[li]].view(torch.bfloat16).view(L["T"], H))
+                   for li, L in enumerate(layers)] for b in range(2)]
+    h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
     in_ready = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
     done = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
     out_read = [[torch.cuda.Event() for _ in range(2)] for _ in layers]
@@ -617,11 +618,20 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     def e2e_step(i):
         p, b = i % pool, i % 2
         if not overlap:
+            with torch.cuda.stream(h2d_s):
+                h2d_s.wait_event(done[0][b])          # the step two back has read these inputs
+                din[b].copy_(hin[p], non_blocking=True)
+                in_ready[0][b].record(h2d_s)
             with torch.cuda.stream(stream):
-                din.copy_(hin[p], non_blocking=True)
-                for (x, lg, out), L in zip(dviews, layers):
+                stream.wait_event(in_ready[0][b])
+                stream.wait_event(out_read[0][b])     # its outputs have been copied out
+                for (x, lg, out), L in zip(dviews[b], layers):
                     moe.forward(x, lg, L["gu"], L["dn"], L["ms"], L["ws"], out=out)
-                hout.copy_(dout, non_blocking=True)
+                done[0][b].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done[0][b])
+                hout[b].copy_(dout[b], non_blocking=True)
+                out_read[0][b].record(d2h_s)
             return
         for li, L in enumerate(layers):
             with torch.cuda.stream(h2d_s):
@@ -666,8 +676,9 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "method": ("moe_forward per layer call with pinned-host x/logits copied in and the output copied out "
                       "every call; " + ("copies on their own streams overlap the neighbouring calls' compute"
-                                        if overlap else "the step's inputs (every layer's) in one copy before its "
-                                        "calls and its outputs in one copy after them, on the calls' stream"))}
+                                        if overlap else "the step's inputs (every layer's) in one copy and its "
+                                        "outputs in one copy, on their own streams, overlapping the neighbouring "
+                                        "steps' calls"))}
     torch.cuda.synchronize(device)
 
     status = [moe.device_status(L["ws"]) for L in layers]
