@@ -573,15 +573,16 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
 
     # end to end through host buffers: every step copies its inputs in from pinned host memory,
     # runs the C-ABI calls and copies the results back to pinned memory, all inside the timed
-    # region.  For batches of 64 tokens and more every layer call copies its x and logits in and
-    # its output out on their own streams (the copies in of call n+1 and out of call n-1 overlap
-    # call n; device buffers double-buffered per layer); for decode batches, whose calls take
-    # microseconds, the whole step's inputs (every layer's x and logits, back to back in one pinned
-    # buffer) move in one copy and its outputs in one copy, on their own streams: the copy in of
-    # step n+1 and the copy out of step n-1 overlap step n's calls (device buffers double-buffered
-    # per step).
+    # region.  When a step moves more than 64 MB (the long prefill) every layer call copies its x
+    # and logits in and its output out on their own streams (the copies in of call n+1 and out of
+    # call n-1 overlap call n; device buffers double-buffered per layer); otherwise the whole step's
+    # inputs (every layer's x and logits, back to back in one pinned buffer) move in one copy and
+    # its outputs in one copy, on their own streams: the copy in of step n+1 and the copy out of
+    # step n-1 overlap step n's calls (device buffers double-buffered per step), with fewer host
+    # calls per step than the per-layer form (a 64-token layer's calls take microseconds).
     e2e_steps = min(steps, 200)
-    overlap = min(L["T"] for L in layers) >= 64
+    step_bytes = sum(L["T"] * (2 * H * 2 + E * 4) for L in layers)
+    overlap = step_bytes > (64 << 20)   # per-layer copies
     if overlap:
         hx = [[L["xs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
         hl = [[L["lgs"][p].cpu().pin_memory() for p in range(pool)] for L in layers]
@@ -675,10 +676,10 @@ def measure(moe, name, steps, warmup, pool, device, dist, world, warmup_seconds,
     e2e = {"value": replica_throughput(world, e2e_steps, tokens_per_step, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "method": ("moe_forward per layer call with pinned-host x/logits copied in and the output copied out "
-                      "every call; " + ("copies on their own streams overlap the neighbouring calls' compute"
-                                        if overlap else "the step's inputs (every layer's) in one copy and its "
-                                        "outputs in one copy, on their own streams, overlapping the neighbouring "
-                                        "steps' calls"))}
+                      "every call; copies on their own streams overlap the neighbouring calls' compute" if overlap else
+                      "moe_forward per layer call; every step's inputs (every layer's x and logits) copied in from "
+                      "pinned host memory in one copy and its outputs copied out in one copy, on their own streams, "
+                      "overlapping the neighbouring steps' calls")}
     torch.cuda.synchronize(device)
 
     status = [moe.device_status(L["ws"]) for L in layers]
