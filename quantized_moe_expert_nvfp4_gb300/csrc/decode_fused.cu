@@ -62,6 +62,7 @@ constexpr int kSlotBytes = 36 * 1024;
 constexpr int kDkMaxSlots = 8;
 constexpr int kFdMaxS = kFdMaxT * kMaxK;
 constexpr int kFdSmemLimit = 227 * 1024;
+constexpr int kFdMaxI = 1024;                 // intermediate size of the one-launch arm, at most
 constexpr uint64_t kFdTimeoutNs = 1000000000ull;
 constexpr int kRedCols = 16;                   // output columns per reduction block
 
@@ -577,21 +578,34 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
       // the group's rows of h as f16 scaled by 2^-e per row (e from the row's maximum over all I
       // columns, as for x): warp n stages token row n
       if (ok && warp < nt) {
+        // the row stays in registers between its maximum and its conversion (I <= kFdMaxI: at
+        // most kFdMaxI / 256 16-byte pieces per lane), one read of h from L2
+        constexpr int kMaxHv = kFdMaxI / 256;
+        const int nhv = I / 256;
         const uint4* src = reinterpret_cast<const uint4*>(a.h + static_cast<int64_t>(row0 + warp) * I);
+        uint4 hv[kMaxHv];
         float mx = 0.0f;
-        for (int c = lane; c < I / 8; c += 32) mx = absmax_bf16x8(mx, __ldcg(src + c));
+#pragma unroll
+        for (int i = 0; i < kMaxHv; ++i) {
+          if (i < nhv) {
+            hv[i] = __ldcg(src + i * 32 + lane);
+            mx = absmax_bf16x8(mx, hv[i]);
+          }
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         const int e = row_exponent(mx);
         const float inv = pow2i(-e);
         if (lane == 0) sm->hfac[warp] = pow2i(e);
         uint4* dst = reinterpret_cast<uint4*>(hb + warp * a.hb_pitch);
-        for (int c = lane; c < I / 8; c += 32) {
-          const uint4 hv = __ldcg(src + c);
-          dst[c] = make_uint4(f32x2_to_f16x2(bf16_lo(hv.x) * inv, bf16_hi(hv.x) * inv),
-                              f32x2_to_f16x2(bf16_lo(hv.y) * inv, bf16_hi(hv.y) * inv),
-                              f32x2_to_f16x2(bf16_lo(hv.z) * inv, bf16_hi(hv.z) * inv),
-                              f32x2_to_f16x2(bf16_lo(hv.w) * inv, bf16_hi(hv.w) * inv));
+#pragma unroll
+        for (int i = 0; i < kMaxHv; ++i) {
+          if (i < nhv) {
+            dst[i * 32 + lane] = make_uint4(f32x2_to_f16x2(bf16_lo(hv[i].x) * inv, bf16_hi(hv[i].x) * inv),
+                                            f32x2_to_f16x2(bf16_lo(hv[i].y) * inv, bf16_hi(hv[i].y) * inv),
+                                            f32x2_to_f16x2(bf16_lo(hv[i].z) * inv, bf16_hi(hv[i].z) * inv),
+                                            f32x2_to_f16x2(bf16_lo(hv[i].w) * inv, bf16_hi(hv[i].w) * inv));
+          }
         }
       }
       named_sync(1, kDkCThreads);
@@ -712,7 +726,7 @@ struct FdPlan {
 };
 
 bool fd_plan(const moe_shape_t& s, FdPlan* p) {
-  if (s.T < 1 || s.T > kFdMaxT || s.H % 512 || s.H > 4096 || s.I % 256 || s.I > 1024) return false;
+  if (s.T < 1 || s.T > kFdMaxT || s.H % 512 || s.H > 4096 || s.I % 256 || s.I > kFdMaxI) return false;
   // the 64 extra bytes per row put the 8 rows of an MMA's B loads in distinct banks
   p->x_pitch = 2 * s.H + 64;   // f16 rows of x (gate_up units)
   p->hb_pitch = 2 * s.I + 64;  // f16 rows of h (down units), in the same area
