@@ -685,36 +685,47 @@ __global__ void __launch_bounds__(kDkThreads, 1) decode_fused_kernel(const __gri
   }
   named_sync(1, kDkCThreads);
   if (*reinterpret_cast<volatile int*>(&sm->abort_flag)) return;
-  // columns in blocks of 16: thread (t, c4) sums token t's expert outputs over 4 columns in
-  // rank order, then adds the shared expert's
+  // columns in blocks of 16: warp w takes the tasks (token t, 4 columns c4) w, w + 16, ...; lane
+  // j < k loads rank j's 4 values of token t and lane k the shared expert's, all at once, and lane
+  // 0 sums them in rank order, then adds the shared expert's (the values reach it by shuffles)
+  const int cw = threadIdx.x >> 5;   // compute warp
   for (int b = blockIdx.x; b < H / kRedCols; b += gridDim.x) {
     const int col0 = b * kRedCols;
-    for (int task = threadIdx.x; task < T * 4; task += kDkCThreads) {
+    for (int task = cw; task < T * 4; task += kDkCompute) {
       const int t = task >> 2, c4 = task & 3;
+      float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float wv = 0.0f;
+      if (lane < k) {
+        wv = sm->w[t * k + lane];
+        v = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<int64_t>(sm->slot_pos[t * k + lane]) * H +
+                                                   col0 + 4 * c4));
+      } else if (lane == k && a.has_shared) {
+        v = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<int64_t>(S + t) * H + col0 + 4 * c4));
+      }
       float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
       for (int j = 0; j < k; ++j) {
-        const float wj = sm->w[t * k + j];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<int64_t>(sm->slot_pos[t * k + j]) * H +
-                                                                col0 + 4 * c4));
-        acc.x = fmaf(wj, v.x, acc.x);
-        acc.y = fmaf(wj, v.y, acc.y);
-        acc.z = fmaf(wj, v.z, acc.z);
-        acc.w = fmaf(wj, v.w, acc.w);
+        const float wj = __shfl_sync(0xffffffffu, wv, j);
+        acc.x = fmaf(wj, __shfl_sync(0xffffffffu, v.x, j), acc.x);
+        acc.y = fmaf(wj, __shfl_sync(0xffffffffu, v.y, j), acc.y);
+        acc.z = fmaf(wj, __shfl_sync(0xffffffffu, v.z, j), acc.z);
+        acc.w = fmaf(wj, __shfl_sync(0xffffffffu, v.w, j), acc.w);
       }
       if (a.has_shared) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(a.y + static_cast<int64_t>(S + t) * H + col0 + 4 * c4));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+        acc.x += __shfl_sync(0xffffffffu, v.x, k);
+        acc.y += __shfl_sync(0xffffffffu, v.y, k);
+        acc.z += __shfl_sync(0xffffffffu, v.z, k);
+        acc.w += __shfl_sync(0xffffffffu, v.w, k);
       }
-      const int64_t o = static_cast<int64_t>(t) * H + col0 + 4 * c4;
-      if (a.out_is_fp32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = acc;
-      } else {
-        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + o) =
-            make_uint2(static_cast<uint32_t>(f32_to_bf16_bits(acc.x)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.y)) << 16),
-                       static_cast<uint32_t>(f32_to_bf16_bits(acc.z)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.w)) << 16));
+      if (lane == 0) {
+        const int64_t o = static_cast<int64_t>(t) * H + col0 + 4 * c4;
+        if (a.out_is_fp32) {
+          *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o) = acc;
+        } else {
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + o) =
+              make_uint2(static_cast<uint32_t>(f32_to_bf16_bits(acc.x)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.y)) << 16),
+                         static_cast<uint32_t>(f32_to_bf16_bits(acc.z)) | (static_cast<uint32_t>(f32_to_bf16_bits(acc.w)) << 16));
+        }
       }
     }
   }
