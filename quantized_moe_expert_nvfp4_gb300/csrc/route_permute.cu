@@ -201,11 +201,13 @@ __global__ void __launch_bounds__(1024) permute_gather_small_kernel(
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot,
     int32_t* __restrict__ slot_pos, int4* __restrict__ tiles, int32_t* __restrict__ meta, int tile_rows,
     uint16_t* __restrict__ xf, float* __restrict__ xe, int32_t* __restrict__ status) {
+  constexpr int kPlaceWarps = 4;   // warps placing the batch's slots, a contiguous chunk each
   __shared__ int s_ids[kDecodeMaxT * kMaxK];
   __shared__ int s_pos[kDecodeMaxT * kMaxK];
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE];
   __shared__ int s_cur[kMaxE];
+  __shared__ int s_wc[kPlaceWarps * kMaxE];   // per-warp expert counts, then per-warp cursors
   __shared__ int s_warp[32];
   __shared__ float s_max[32];
   pdl_wait_then_release();
@@ -236,16 +238,36 @@ __global__ void __launch_bounds__(1024) permute_gather_small_kernel(
   }
   if (lead && threadIdx.x == 0) offsets[E] = S;
   __syncthreads();
-  // stable placement by warp 0, 32 slots a step: a slot goes after the earlier slots of its expert
-  if (warp == 0) {
+  // stable placement by kPlaceWarps warps, each a contiguous chunk of the slots: every warp counts
+  // its chunk per expert, each expert's offset is split into per-warp cursors in chunk order, and
+  // the warps place their chunks 32 slots a step (a slot goes after the earlier slots of its
+  // expert)
+  const int chunk = (S + kPlaceWarps - 1) / kPlaceWarps;
+  const int c0 = min(S, warp * chunk), c1 = min(S, c0 + chunk);
+  for (int i = threadIdx.x; i < kPlaceWarps * E; i += blockDim.x) s_wc[i] = 0;
+  __syncthreads();
+  if (warp < kPlaceWarps)
+    for (int i = c0 + lane; i < c1; i += 32) atomicAdd(&s_wc[warp * E + s_ids[i]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = s_cur[e];
+    for (int w2 = 0; w2 < kPlaceWarps; ++w2) {
+      const int cw = s_wc[w2 * E + e];
+      s_wc[w2 * E + e] = run;
+      run += cw;
+    }
+  }
+  __syncthreads();
+  if (warp < kPlaceWarps && c1 > c0) {
+    int* cur = s_wc + warp * E;
     const unsigned lt = (1u << lane) - 1u;
-    for (int b = 0; b < S; b += 32) {
+    for (int b = c0; b < c1; b += 32) {
       const int s = b + lane;
-      const int e = (s < S) ? s_ids[s] : -1;
+      const int e = (s < c1) ? s_ids[s] : -1;
       const unsigned same = __match_any_sync(kFull, e);
       const int rank = __popc(same & lt);
       if (e >= 0) {
-        const int pos = s_cur[e] + rank;
+        const int pos = cur[e] + rank;
         s_pos[s] = pos;
         if (lead) {
           sorted_slot[pos] = s;
@@ -253,10 +275,11 @@ __global__ void __launch_bounds__(1024) permute_gather_small_kernel(
         }
       }
       __syncwarp();
-      if (e >= 0 && rank == 0) s_cur[e] += __popc(same);
+      if (e >= 0 && rank == 0) cur[e] += __popc(same);
       __syncwarp();
     }
   }
+  // (s_cur is free: the placement reads its per-warp cursors)
   if (lead) write_tiles_block(E, S, T, has_shared, tile_rows, s_cnt, s_off, tiles, meta, s_warp, s_cur);
   __syncthreads();
   // this CTA's tokens: f16 rows scaled by the row's power of two, to every row that holds the token
