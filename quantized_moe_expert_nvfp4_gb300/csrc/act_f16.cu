@@ -98,14 +98,34 @@ __global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __
     p = S + t;
   }
   const uint4* s = reinterpret_cast<const uint4*>(src + static_cast<int64_t>(t) * K);
+  // a whole row handled by one warp with K <= 2048 stays in registers between its maximum and its
+  // conversion (one read of the row); otherwise the slice is read again after the maximum
+  constexpr int kHeld = 8;   // 16-byte pieces per lane held in registers
+  const bool held = slices == 1 && K % 256 == 0 && K <= 256 * kHeld;
+  uint4 hv[kHeld];
   float m = 0.0f;
-  for (int c = lane; c < K / 8; c += 32) {
-    const uint4 v = __ldg(s + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (held) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
-      m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    for (int i = 0; i < kHeld; ++i) {
+      if (i < K / 256) {
+        hv[i] = __ldg(s + i * 32 + lane);
+        const uint32_t w[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+          m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+        }
+      }
+    }
+  } else {
+    for (int c = lane; c < K / 8; c += 32) {
+      const uint4 v = __ldg(s + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+      }
     }
   }
 #pragma unroll
@@ -113,6 +133,26 @@ __global__ void __launch_bounds__(256) act_scatter_f16_kernel(const uint16_t* __
   const int e = (m > 0.0f && m <= 3.4e38f) ? max(ilogbf(m) - 14, -126) : 0;
   const float inv = __int_as_float((127 - e) << 23);
   if (p >= 0 && sl == 0) factor[p] = __int_as_float((127 + e) << 23);
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i) {
+      if (i < K / 256) {
+        const uint32_t w[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16) * inv, __uint_as_float(w[j] & 0xffff0000u) * inv);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int jj = 0; jj <= k; ++jj) {
+          const int pj = __shfl_sync(0xffffffffu, p, jj);
+          if (pj >= 0) reinterpret_cast<uint4*>(dst + static_cast<int64_t>(pj) * K)[i * 32 + lane] = ov;
+        }
+      }
+    }
+    return;
+  }
   const int per = K / 8 / slices;   // uint4 columns of this warp's slice
   for (int c = sl * per + lane; c < (sl + 1) * per; c += 32) {
     const uint4 v = __ldg(s + c);
