@@ -38,14 +38,33 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
     }
   }
   const uint4* s = reinterpret_cast<const uint4*>(src + srow * K);
+  // rows of K <= 2048 stay in registers between their maximum and their conversion (one read)
+  constexpr int kHeld = 8;   // 16-byte pieces per lane held in registers
+  const bool held = K % 256 == 0 && K <= 256 * kHeld;
+  uint4 hv[kHeld];
   float m = 0.0f;
-  for (int c = lane; c < K / 8; c += 32) {
-    const uint4 v = __ldg(s + c);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if (held) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
-      m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+    for (int i = 0; i < kHeld; ++i) {
+      if (i < K / 256) {
+        hv[i] = __ldg(s + i * 32 + lane);
+        const uint32_t w[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          m = fmaxf(m, fabsf(__uint_as_float(w[j] << 16)));
+          m = fmaxf(m, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+        }
+      }
+    }
+  } else {
+    for (int c = lane; c < K / 8; c += 32) {
+      const uint4 v = __ldg(s + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(w[i] & 0xffff0000u)));
+      }
     }
   }
 #pragma unroll
@@ -55,6 +74,22 @@ __global__ void __launch_bounds__(256) act_to_f16_kernel(const uint16_t* __restr
   const float inv = __int_as_float((127 - e) << 23);           // 2^-e, exactly
   if (lane == 0) factor[r] = __int_as_float((127 + e) << 23);  // the epilogue's 2^e
   uint4* d = reinterpret_cast<uint4*>(dst + r * K);
+  if (held) {
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i) {
+      if (i < K / 256) {
+        const uint32_t w[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half2 h = __floats2half2_rn(__uint_as_float(w[j] << 16) * inv, __uint_as_float(w[j] & 0xffff0000u) * inv);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        d[i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    return;
+  }
   for (int c = lane; c < K / 8; c += 32) {
     const uint4 v = __ldg(s + c);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
